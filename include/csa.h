@@ -1,0 +1,212 @@
+/*
+ * csa.h -- C ABI of the B300 (sm_103a) library for DeepSeek-V4 hybrid compressed attention.
+ *
+ * The method (as explained on "DeepSeek V4 技术大全", wineandchord.com, chapter "Hybrid
+ * Attention", and "DeepSeek-V4 技术解析", chang-wenbin.github.io, section 2.1):
+ *   CSA  compress every m = 4 tokens into one shared K=V entry (softmax-gated, overlapped over
+ *        2m rows), RMSNorm it and rotate its last 64 dims; score every closed entry with the
+ *        lightning indexer; keep the top-k per query; attend over those entries plus an
+ *        uncompressed 128-token window with a per-head sink logit.
+ *   HCA  compress every m' = 128 tokens (single stream) and attend densely over all closed
+ *        entries plus the same window and sink.
+ *
+ * Conventions shared by every call
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller, contiguous, row-major with
+ *     the last dimension fastest, and 16-byte aligned.  "bf16" is IEEE bfloat16, "e4m3" is OCP
+ *     FP8 E4M3.  Host pointers appear only where a comment says HOST.
+ *   - The library allocates no memory and keeps no global mutable state: it is re-entrant and
+ *     thread-safe.  Scratch memory is a caller-supplied workspace whose size the matching
+ *     *_workspace() query returns.
+ *   - Every call only enqueues kernels on `stream` and returns; nothing synchronises.
+ *   - Invalid or unsupported descriptors are rejected before any launch.  A failed launch
+ *     returns CSA_ERR_CUDA.  Device-detected problems (an index out of range) never trap: the
+ *     kernel skips the access and records the first problem in the workspace status word,
+ *     which csa_read_device_status() returns.
+ *   - Positions are explicit: q_pos[b][i] is the 0-based token index t of query i of sequence
+ *     b.  For decode, t is the index of the new token (the context length).
+ */
+#ifndef CSA_B300_H
+#define CSA_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* csa_stream_t;
+
+typedef enum {
+  CSA_OK = 0,
+  CSA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer */
+  CSA_ERR_UNSUPPORTED = 2,   /* valid request outside what the kernels implement */
+  CSA_ERR_WORKSPACE = 3,     /* workspace missing or smaller than *_workspace() */
+  CSA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+  CSA_ERR_DEVICE_CHECK = 5,  /* a kernel found an out-of-range index (see status word) */
+  CSA_ERR_TIMEOUT = 6        /* reserved: a bounded device-side wait gave up */
+} csa_status;
+
+/* Storage formats of compressed entries and indexer keys. */
+typedef enum {
+  CSA_FMT_BF16 = 0,
+  /* Mixed-precision cache row (the pages: RoPE dims stay BF16, the rest FP8), d = 512 only:
+   * 608 bytes = [0,448) e4m3 codes of dims 0..447 | [448,576) bf16 dims 448..511 |
+   * [576,604) seven fp32 scales, one per 64-dim block of the e4m3 part | [604,608) padding.
+   * value = code * scale. */
+  CSA_FMT_FP8_MIXED = 1,
+  /* Indexer keys: e4m3 codes [.., dI] plus one fp32 scale per row; value = code * scale. */
+  CSA_FMT_FP8_ROWSCALE = 2
+} csa_format;
+
+#define CSA_FP8_MIXED_ROW_BYTES 608
+
+/* ---------------------------------------------------------------------------------------------
+ * csa_compress -- token-level compressor (CSA overlapped or HCA single-stream).
+ *
+ * Source: "DeepSeek V4 技术大全", CSA path, the Softmax_row and C^Comp equations (overlapped
+ * 2m rows with biases B^a, B^b), and the HCA path, its S / C^Comp equations (m' rows, bias B);
+ * component table rows "query / KV RMSNorm" and "partial RoPE" (RMSNorm eps 1e-6, RoPE on the
+ * last 64 dims, compressed-branch base 160000).
+ *
+ * For entry i in [0, N), N = floor(T/m), channel c:
+ *   rows  = a-stream rows m*i .. m*i+m-1 with logits Za + bias_a[row - m*i]
+ *           plus, when overlap and i >= 1, b-stream rows m*(i-1) .. m*i-1 with Zb + bias_b[..]
+ *   out_i = sum_rows softmax_rows(logit)[c] * C[row][c]
+ * then, if flags has CSA_COMPRESS_NORM: out_i = out_i / sqrt(mean(out_i^2) + eps) * gamma,
+ * and if CSA_COMPRESS_ROPE: dims [d-r, d) rotated on adjacent pairs (2j, 2j+1) by angle
+ * (m*i + pos_shift) * inv_freq_j.
+ *
+ * Ca, Za: bf16 [B, T, d].  Cb, Zb: bf16 [B, T, d] when overlap = 1, else ignored (may be NULL).
+ * bias_a, bias_b: fp32 [m, d] or NULL (zero).  gamma: fp32 [d] or NULL (one).
+ * out: bf16 [B, N, d].
+ * Supported: d % 64 == 0 and 64 <= d <= 1024; 1 <= m <= 256; rope_dims even and <= d;
+ * out_fmt CSA_FMT_BF16.
+ * ------------------------------------------------------------------------------------------- */
+enum { CSA_COMPRESS_NORM = 1u, CSA_COMPRESS_ROPE = 2u };
+
+typedef struct {
+  int B, T, d, m;
+  int overlap;             /* 1: CSA (Cb, Zb used, block i-1 overlaps); 0: HCA single stream */
+  int rope_dims;           /* r; 0 = no rotation */
+  float rope_theta;        /* base used when inv_freq is NULL (160000 on the compressed branch) */
+  const float* inv_freq;   /* HOST pointer to r/2 values (e.g. a YaRN table) or NULL:
+                              inv_freq_j = theta^(-2j/r) */
+  int pos_shift;           /* entry i sits at position m*i + pos_shift */
+  float eps;               /* RMSNorm epsilon (1e-6) */
+  unsigned flags;          /* CSA_COMPRESS_NORM | CSA_COMPRESS_ROPE */
+  csa_format out_fmt;      /* CSA_FMT_BF16 */
+} csa_compress_desc;
+
+csa_status csa_compress(const csa_compress_desc* desc, const void* Ca, const void* Cb,
+                        const void* Za, const void* Zb, const float* bias_a, const float* bias_b,
+                        const float* gamma, void* out, csa_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * csa_index_topk -- lightning-indexer scores and per-query top-k selection.
+ *
+ * Source: "DeepSeek V4 技术大全", CSA path, the I_{t,s} and TopK equations:
+ *   I_{t,s} = sum_h w_{t,h} * ReLU(q^I_{t,h} . K^I_s)  for s < floor((t+1)/m)
+ *   idx_t   = TopK_k { I_{t,s} }
+ * Ties go to the smaller s.  When fewer than k entries are visible, all are returned and the
+ * row is padded with -1.  Output order inside a row: entries with score above the k-th score in
+ * increasing s, then the ties at the k-th score in increasing s.  The result depends only on
+ * the query's own inputs (batch-invariant) and is deterministic.
+ *
+ * qI: bf16 [B, Tq, n_heads, head_dim].  w: fp32 [B, Tq, n_heads].
+ * kI: bf16 [B, N, head_dim] (key_fmt CSA_FMT_BF16) or e4m3 [B, N, head_dim] with
+ *     kI_scale fp32 [B, N] (CSA_FMT_FP8_ROWSCALE).
+ * q_pos: int32 [B, Tq].  idx_out: int32 [B, Tq, k].
+ * score_out: fp32 [B, Tq, N] or NULL; when given, visible scores are written there and
+ *     invisible ones are -inf.
+ * workspace: device buffer of at least csa_index_topk_workspace(desc) bytes.
+ * Supported: head_dim 64 or 128; n_heads % 4 == 0 and <= 64; 1 <= k <= 2048; N <= 262144
+ * (larger N returns CSA_ERR_UNSUPPORTED).
+ * ------------------------------------------------------------------------------------------- */
+typedef struct {
+  int B, Tq, N, n_heads, head_dim, k, m;
+  csa_format key_fmt;      /* CSA_FMT_BF16 or CSA_FMT_FP8_ROWSCALE */
+} csa_index_desc;
+
+size_t csa_index_topk_workspace(const csa_index_desc* desc);
+
+csa_status csa_index_topk(const csa_index_desc* desc, const void* qI, const float* w,
+                          const void* kI, const float* kI_scale, const int32_t* q_pos,
+                          int32_t* idx_out, float* score_out, void* workspace, size_t ws_bytes,
+                          csa_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * csa_attend / hca_attend -- shared K=V multi-query attention with SWA window and sink.
+ *
+ * Source: "DeepSeek V4 技术大全", component table rows "Shared K=V MQA", "query / KV RMSNorm",
+ * "partial RoPE", "attention sink" (p = exp(z) / (exp(a_h) + sum exp(z))), "SWA"
+ * (W_t = {t-127 .. t}), the HCA visibility set j < floor((t+1)/m'), and the implementation
+ * note that the core-attention output gets a reverse rotation.
+ *
+ * Per query (b, i) at position t = q_pos[b][i], per head h:
+ *   q_hat = RoPE_t(RMSNorm(q[b,i,h]))               (if CSA_ATTEND_Q_NORM_ROPE; unit weight)
+ *   keys  = csa_attend: entries idx[b,i,0..k-1] (entries equal to -1 are skipped)
+ *           hca_attend: every entry j < min(N, floor((t+1)/m))
+ *           plus window rows win[b, u mod Wcap] for u in [max(0, t-window+1), t]
+ *   z_j   = scale * q_hat . key_j
+ *   out   = sum_j exp(z_j) key_j / (exp(sink[h]) + sum_j exp(z_j))
+ *   out[d-r:] rotated by -t                          (if CSA_ATTEND_OUT_UNROTATE)
+ *   lse   = log(exp(sink[h]) + sum_j exp(z_j))       (if CSA_ATTEND_WRITE_LSE)
+ *
+ * q: bf16 [B, Tq, H, d].  kv: bf16 [B, N, d] or FP8_MIXED rows [B, N, 608 bytes].
+ * idx: int32 [B, Tq, k] (csa_attend only).  win: bf16 [B, Wcap, d]; the caller keeps every
+ * window position of every query of the call in a distinct live slot (decode: a 128-slot ring;
+ * prefill from position 0: Wcap >= T).  sink: fp32 [H].  q_pos: int32 [B, Tq].
+ * out: bf16 [B, Tq, H, d].  lse: fp32 [B, Tq, H] or NULL.
+ * An idx entry outside [-1, N) is skipped and reported through the status word.
+ * Supported: d in {128, 512}; H % 16 == 0 and <= 128; kv_fmt FP8_MIXED needs d = 512;
+ * rope_dims even, <= d; window <= Wcap.
+ * ------------------------------------------------------------------------------------------- */
+enum { CSA_ATTEND_Q_NORM_ROPE = 1u, CSA_ATTEND_OUT_UNROTATE = 2u, CSA_ATTEND_WRITE_LSE = 4u };
+
+typedef struct {
+  int B, Tq, N, H, d;
+  int rope_dims;
+  int k;                   /* csa_attend: columns of idx; ignored by hca_attend */
+  int m;                   /* compression ratio (hca_attend visibility; csa_attend ignores it) */
+  int Wcap, window;        /* ring capacity and window length (128) */
+  float scale;             /* 0 => 1/sqrt(d) */
+  float rope_theta;        /* base used when inv_freq is NULL */
+  const float* inv_freq;   /* HOST pointer to rope_dims/2 values or NULL */
+  float eps;               /* RMSNorm epsilon for q */
+  csa_format kv_fmt;       /* CSA_FMT_BF16 or CSA_FMT_FP8_MIXED */
+  unsigned flags;          /* CSA_ATTEND_* */
+} csa_attend_desc;
+
+size_t csa_attend_workspace(const csa_attend_desc* desc);
+
+csa_status csa_attend(const csa_attend_desc* desc, const void* q, const void* kv,
+                      const int32_t* idx, const void* win, const float* sink,
+                      const int32_t* q_pos, void* out, float* lse, void* workspace,
+                      size_t ws_bytes, csa_stream_t stream);
+
+csa_status hca_attend(const csa_attend_desc* desc, const void* q, const void* kv,
+                      const void* win, const float* sink, const int32_t* q_pos, void* out,
+                      float* lse, void* workspace, size_t ws_bytes, csa_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Status helpers.
+ * csa_read_device_status: waits for `stream`, reads the status word at the start of a
+ * workspace that a previous call used, returns CSA_OK or CSA_ERR_DEVICE_CHECK, and (if
+ * detail != NULL, HOST pointer) stores the first offending value.  csa_clear_device_status
+ * enqueues a reset of that word.  csa_status_string never returns NULL.
+ * ------------------------------------------------------------------------------------------- */
+csa_status csa_read_device_status(const void* workspace, csa_stream_t stream, int32_t* detail);
+csa_status csa_clear_device_status(void* workspace, csa_stream_t stream);
+const char* csa_status_string(csa_status status);
+
+/* Number of kernel launches the library has enqueued in this process (all calls, all threads;
+ * an atomic counter kept for instrumentation, not part of any result). */
+uint64_t csa_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA_B300_H */

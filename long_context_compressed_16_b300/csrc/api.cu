@@ -1,0 +1,293 @@
+// Host side of the C ABI declared in include/csa.h: argument validation, workspace layout,
+// RoPE tables and kernel orchestration.  Nothing here allocates device memory.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+
+#include "common.cuh"
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+constexpr size_t kScoreChunkCap = size_t(256) << 20;   // bytes of fp32 scores per top-k pass
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline csa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
+
+bool make_rope(int r, float theta, const float* inv_freq, csa::RopeParams* rp) {
+  if (r < 0 || (r & 1) || r / 2 > csa::kMaxRopePairs) return false;
+  std::memset(rp, 0, sizeof(*rp));
+  rp->r = r;
+  for (int j = 0; j < r / 2; ++j) {
+    rp->inv_freq[j] = inv_freq ? static_cast<double>(inv_freq[j])
+                               : std::pow(static_cast<double>(theta), -2.0 * j / static_cast<double>(r));
+  }
+  return true;
+}
+
+void count(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
+
+// ---------------------------------------------------------------- indexer chunking
+struct IndexPlan {
+  int G;            // queries per group
+  long long groups; // total groups
+  long long chunk;  // groups per top-k pass
+  size_t score_bytes;
+};
+
+bool index_desc_ok(const csa_index_desc* d) {
+  if (!d) return false;
+  if (d->B < 0 || d->Tq < 0 || d->N < 0 || d->m < 1) return false;
+  if (d->n_heads < 1 || d->n_heads > 64) return false;
+  if (d->head_dim != 64 && d->head_dim != 128) return false;
+  if (d->k < 1 || d->k > 2048) return false;
+  if (d->key_fmt != CSA_FMT_BF16 && d->key_fmt != CSA_FMT_FP8_ROWSCALE) return false;
+  return true;
+}
+
+IndexPlan plan_index(const csa_index_desc* d) {
+  IndexPlan p;
+  p.G = d->Tq > 1 ? 4 : 1;
+  const long long gpb = (d->Tq + p.G - 1) / p.G;
+  p.groups = static_cast<long long>(d->B) * gpb;
+  const size_t per_group = static_cast<size_t>(p.G) * (d->N > 0 ? d->N : 1) * sizeof(float);
+  long long cg = static_cast<long long>(kScoreChunkCap / per_group);
+  if (cg < 1) cg = 1;
+  if (cg > 65535) cg = 65535;
+  p.chunk = p.groups < cg ? p.groups : cg;
+  p.score_bytes = static_cast<size_t>(p.chunk) * per_group;
+  return p;
+}
+
+// ---------------------------------------------------------------- attention planning
+bool attend_desc_ok(const csa_attend_desc* d, bool csa_mode) {
+  if (!d) return false;
+  if (d->B < 0 || d->Tq < 0 || d->N < 0) return false;
+  if (d->d != 128 && d->d != 512) return false;
+  if (d->H < 16 || d->H > 128 || (d->H % 16) != 0) return false;
+  if (d->rope_dims < 0 || d->rope_dims > d->d || d->rope_dims > 2 * csa::kMaxRopePairs || (d->rope_dims & 1))
+    return false;
+  if (csa_mode && (d->k < 1 || d->k > 65536)) return false;
+  if (!csa_mode && d->m < 1) return false;
+  if (d->window < 0 || d->window > d->Wcap || (d->window > 0 && d->Wcap < 1)) return false;
+  if (d->kv_fmt != CSA_FMT_BF16 && d->kv_fmt != CSA_FMT_FP8_MIXED) return false;
+  if (d->kv_fmt == CSA_FMT_FP8_MIXED && d->d != 512) return false;
+  if (!(d->scale >= 0.f) || !(d->eps >= 0.f)) return false;
+  return true;
+}
+
+struct AttendPlan {
+  int n_slots, split_slots, n_splits;
+  size_t partial_bytes;
+};
+
+AttendPlan plan_attend(const csa_attend_desc* d, bool csa_mode) {
+  AttendPlan p;
+  p.n_slots = (csa_mode ? d->k : d->N) + d->window;
+  if (p.n_slots < 1) p.n_slots = 1;
+  // Decode (one query per sequence) splits the slot range in fixed 256-slot pieces, merged by a
+  // second kernel; the split size never depends on the batch.  Prefill keeps one split per query.
+  p.split_slots = (d->Tq == 1) ? 256 : ((p.n_slots + 63) / 64) * 64;
+  p.n_splits = (p.n_slots + p.split_slots - 1) / p.split_slots;
+  if (p.n_splits < 1) p.n_splits = 1;
+  p.partial_bytes = csa::attend_partial_bytes(d->B * d->Tq, d->H, d->d, p.n_splits);
+  return p;
+}
+
+csa_status attend_common(const csa_attend_desc* d, bool csa_mode, const void* q, const void* kv,
+                         const int32_t* idx, const void* win, const float* sink, const int32_t* q_pos,
+                         void* out, float* lse, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!attend_desc_ok(d, csa_mode)) return CSA_ERR_INVALID_ARG;
+  const long long Q = static_cast<long long>(d->B) * d->Tq;
+  if (!ws) return CSA_ERR_WORKSPACE;
+  const AttendPlan plan = plan_attend(d, csa_mode);
+  if (ws_bytes < csa::kStatusBytes + plan.partial_bytes) return CSA_ERR_WORKSPACE;
+  if (!aligned16(ws)) return CSA_ERR_INVALID_ARG;
+  if (Q == 0) return CSA_OK;
+  if (Q > 2147483647LL) return CSA_ERR_UNSUPPORTED;
+  if (!q || !sink || !q_pos || !out) return CSA_ERR_INVALID_ARG;
+  if (!kv && (d->N > 0)) return CSA_ERR_INVALID_ARG;
+  if (csa_mode && !idx) return CSA_ERR_INVALID_ARG;
+  if (!win && d->window > 0) return CSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || (kv && !aligned16(kv)) || (win && !aligned16(win)) || !aligned16(out))
+    return CSA_ERR_INVALID_ARG;
+  if ((d->flags & CSA_ATTEND_WRITE_LSE) && !lse) return CSA_ERR_INVALID_ARG;
+
+  csa::AttendArgs a{};
+  a.q = q; a.kv = kv; a.idx = csa_mode ? idx : nullptr; a.win = win; a.sink = sink; a.q_pos = q_pos;
+  a.out = out; a.lse = (d->flags & CSA_ATTEND_WRITE_LSE) ? lse : nullptr;
+  a.status = static_cast<int32_t*>(ws);
+  a.partial = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + csa::kStatusBytes);
+  a.B = d->B; a.Tq = d->Tq; a.N = d->N; a.H = d->H; a.d = d->d; a.k = csa_mode ? d->k : 0;
+  a.m = csa_mode ? 1 : d->m;
+  a.Wcap = d->Wcap > 0 ? d->Wcap : 1; a.window = d->window;
+  a.fp8 = d->kv_fmt == CSA_FMT_FP8_MIXED;
+  a.q_norm_rope = (d->flags & CSA_ATTEND_Q_NORM_ROPE) != 0;
+  a.out_unrotate = (d->flags & CSA_ATTEND_OUT_UNROTATE) != 0;
+  a.scale = d->scale > 0.f ? d->scale : 1.0f / std::sqrt(static_cast<float>(d->d));
+  a.eps = d->eps;
+  a.n_slots = plan.n_slots; a.split_slots = plan.split_slots; a.n_splits = plan.n_splits;
+  if (!make_rope(d->rope_dims, d->rope_theta, d->inv_freq, &a.rp)) return CSA_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(ws, 0, 8, stream) != cudaSuccess) return CSA_ERR_CUDA;
+  int launches = 0;
+  const cudaError_t e = csa::launch_attend(a, stream, &launches);
+  count(launches);
+  if (e == cudaErrorInvalidValue) return CSA_ERR_UNSUPPORTED;
+  return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+csa_status csa_compress(const csa_compress_desc* d, const void* Ca, const void* Cb, const void* Za,
+                        const void* Zb, const float* bias_a, const float* bias_b, const float* gamma,
+                        void* out, csa_stream_t stream) {
+  if (!d) return CSA_ERR_INVALID_ARG;
+  if (d->B < 0 || d->T < 0 || d->m < 1 || d->m > 256) return CSA_ERR_INVALID_ARG;
+  if (d->d < 64 || d->d > 1024 || (d->d % 64) != 0) return CSA_ERR_UNSUPPORTED;
+  if (d->rope_dims < 0 || d->rope_dims > d->d || (d->rope_dims % 8) != 0 ||
+      d->rope_dims > 2 * csa::kMaxRopePairs)
+    return CSA_ERR_UNSUPPORTED;
+  if (d->out_fmt != CSA_FMT_BF16) return CSA_ERR_UNSUPPORTED;
+  if (!(d->eps >= 0.f)) return CSA_ERR_INVALID_ARG;
+  const int N = d->T / d->m;
+  if (static_cast<long long>(d->B) * N == 0) return CSA_OK;
+  if (!Ca || !Za || !out) return CSA_ERR_INVALID_ARG;
+  if (d->overlap && (!Cb || !Zb)) return CSA_ERR_INVALID_ARG;
+  if (!aligned16(Ca) || !aligned16(Za) || !aligned16(out) || (d->overlap && (!aligned16(Cb) || !aligned16(Zb))) ||
+      (bias_a && !aligned16(bias_a)) || (bias_b && !aligned16(bias_b)) || (gamma && !aligned16(gamma)))
+    return CSA_ERR_INVALID_ARG;
+  csa::CompressArgs a{};
+  a.Ca = Ca; a.Cb = d->overlap ? Cb : nullptr; a.Za = Za; a.Zb = d->overlap ? Zb : nullptr;
+  a.bias_a = bias_a; a.bias_b = d->overlap ? bias_b : nullptr; a.gamma = gamma; a.out = out;
+  a.B = d->B; a.T = d->T; a.d = d->d; a.m = d->m; a.N = N; a.overlap = d->overlap ? 1 : 0;
+  a.norm = (d->flags & CSA_COMPRESS_NORM) != 0;
+  a.rope = (d->flags & CSA_COMPRESS_ROPE) != 0 && d->rope_dims > 0;
+  a.pos_shift = d->pos_shift;
+  a.eps = d->eps;
+  if (!make_rope(d->rope_dims, d->rope_theta, d->inv_freq, &a.rp)) return CSA_ERR_INVALID_ARG;
+  int launches = 0;
+  const cudaError_t e = csa::launch_compress(a, reinterpret_cast<cudaStream_t>(stream), &launches);
+  count(launches);
+  return from_cuda(e);
+}
+
+size_t csa_index_topk_workspace(const csa_index_desc* d) {
+  if (!index_desc_ok(d)) return 0;
+  return csa::kStatusBytes + plan_index(d).score_bytes;
+}
+
+csa_status csa_index_topk(const csa_index_desc* d, const void* qI, const float* w, const void* kI,
+                          const float* kI_scale, const int32_t* q_pos, int32_t* idx_out, float* score_out,
+                          void* ws, size_t ws_bytes, csa_stream_t stream_) {
+  if (!index_desc_ok(d)) return CSA_ERR_INVALID_ARG;
+  if (d->N > 262144) return CSA_ERR_UNSUPPORTED;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const IndexPlan plan = plan_index(d);
+  if (!ws) return CSA_ERR_WORKSPACE;
+  if (ws_bytes < csa::kStatusBytes + (score_out ? 0 : plan.score_bytes)) return CSA_ERR_WORKSPACE;
+  if (!aligned16(ws)) return CSA_ERR_INVALID_ARG;
+  const long long Q = static_cast<long long>(d->B) * d->Tq;
+  if (Q == 0) return CSA_OK;
+  if (!qI || !w || !q_pos || !idx_out || (!kI && d->N > 0)) return CSA_ERR_INVALID_ARG;
+  const bool fp8 = d->key_fmt == CSA_FMT_FP8_ROWSCALE;
+  if (fp8 && !kI_scale && d->N > 0) return CSA_ERR_INVALID_ARG;
+  if (!aligned16(qI) || (kI && !aligned16(kI))) return CSA_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(ws, 0, 8, stream) != cudaSuccess) return CSA_ERR_CUDA;
+
+  csa::IndexArgs ia{};
+  ia.qI = qI; ia.w = w; ia.kI = kI; ia.kI_scale = kI_scale; ia.q_pos = q_pos;
+  ia.B = d->B; ia.Tq = d->Tq; ia.N = d->N; ia.nI = d->n_heads; ia.dI = d->head_dim; ia.m = d->m;
+  ia.fp8 = fp8 ? 1 : 0;
+  csa::TopkArgs ta{};
+  ta.q_pos = q_pos; ta.idx_out = idx_out; ta.status = static_cast<int32_t*>(ws);
+  ta.Tq = d->Tq; ta.N = d->N; ta.k = d->k; ta.m = d->m;
+
+  const long long gpb = (d->Tq + plan.G - 1) / plan.G;
+  int launches = 0;
+  cudaError_t e = cudaSuccess;
+  if (d->N == 0) {
+    // nothing visible anywhere: the selector only pads
+    ta.scores = nullptr; ta.q_begin = 0; ta.q_count = static_cast<int>(Q); ta.score_row_offset = 0;
+    e = csa::launch_topk(ta, stream, &launches);
+    count(launches);
+    return from_cuda(e);
+  }
+  const long long step = score_out ? 65535 : plan.chunk;
+  for (long long g0 = 0; g0 < plan.groups && e == cudaSuccess; g0 += step) {
+    const long long g1 = (g0 + step < plan.groups) ? g0 + step : plan.groups;
+    const long long q_first = (g0 / gpb) * d->Tq + (g0 % gpb) * plan.G;
+    const long long gl = g1 - 1;
+    const long long q_last = (gl / gpb) * d->Tq + (gl % gpb) * plan.G +
+                             ((d->Tq - (gl % gpb) * plan.G) < plan.G ? (d->Tq - (gl % gpb) * plan.G) : plan.G);
+    float* scores = score_out ? score_out
+                              : reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + csa::kStatusBytes);
+    ia.scores = scores;
+    ia.q_begin = static_cast<int>(g0);
+    ia.q_count = static_cast<int>(g1 - g0);
+    ia.score_row_offset = score_out ? 0 : static_cast<int>(q_first);
+    e = csa::launch_index_score_groups(ia, plan.G, score_out ? 1 : 0, stream, &launches);
+    if (e != cudaSuccess) break;
+    ta.scores = scores;
+    ta.q_begin = static_cast<int>(q_first);
+    ta.q_count = static_cast<int>(q_last - q_first);
+    ta.score_row_offset = ia.score_row_offset;
+    e = csa::launch_topk(ta, stream, &launches);
+  }
+  count(launches);
+  if (e == cudaErrorInvalidValue) return CSA_ERR_UNSUPPORTED;
+  return from_cuda(e);
+}
+
+size_t csa_attend_workspace(const csa_attend_desc* d) {
+  if (!attend_desc_ok(d, true)) return 0;
+  return csa::kStatusBytes + plan_attend(d, true).partial_bytes;
+}
+
+csa_status csa_attend(const csa_attend_desc* d, const void* q, const void* kv, const int32_t* idx,
+                      const void* win, const float* sink, const int32_t* q_pos, void* out, float* lse,
+                      void* ws, size_t ws_bytes, csa_stream_t stream) {
+  return attend_common(d, true, q, kv, idx, win, sink, q_pos, out, lse, ws, ws_bytes,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+csa_status hca_attend(const csa_attend_desc* d, const void* q, const void* kv, const void* win,
+                      const float* sink, const int32_t* q_pos, void* out, float* lse, void* ws,
+                      size_t ws_bytes, csa_stream_t stream) {
+  return attend_common(d, false, q, kv, nullptr, win, sink, q_pos, out, lse, ws, ws_bytes,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+csa_status csa_read_device_status(const void* ws, csa_stream_t stream, int32_t* detail) {
+  if (!ws) return CSA_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return CSA_ERR_CUDA;
+  int32_t h[2] = {0, 0};
+  if (cudaMemcpy(h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return CSA_ERR_CUDA;
+  if (detail) *detail = h[1];
+  return h[0] == 0 ? CSA_OK : CSA_ERR_DEVICE_CHECK;
+}
+
+csa_status csa_clear_device_status(void* ws, csa_stream_t stream) {
+  if (!ws) return CSA_ERR_INVALID_ARG;
+  return from_cuda(cudaMemsetAsync(ws, 0, 8, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char* csa_status_string(csa_status s) {
+  switch (s) {
+    case CSA_OK: return "ok";
+    case CSA_ERR_INVALID_ARG: return "invalid argument";
+    case CSA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case CSA_ERR_WORKSPACE: return "workspace missing or too small";
+    case CSA_ERR_CUDA: return "CUDA error";
+    case CSA_ERR_DEVICE_CHECK: return "device-side range check failed";
+    case CSA_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+uint64_t csa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

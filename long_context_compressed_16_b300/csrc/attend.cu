@@ -1,0 +1,517 @@
+// Shared K=V multi-query attention over the selected (CSA) or all closed (HCA) compressed entries
+// plus the uncompressed SWA window, with a per-head sink logit and the reverse rotation of the
+// output's RoPE dims ("DeepSeek V4 技术大全", component table rows Shared K=V MQA, query/KV
+// RMSNorm, partial RoPE, attention sink, SWA; the HCA visibility set; the reverse-rotation note).
+//
+// Per query the candidate rows are laid out as "slots": [0, K_q) entry slots (the idx row, or
+// entries 0..N_vis-1 for HCA) followed by `window` window slots (positions t-window+1 .. t).
+// A CTA owns one query, a group of 16*NG heads and one split of the slot range.  Rows are
+// gathered CK at a time with cp.async into a double-buffered shared-memory tile (FP8 rows are
+// widened to bf16 there); the heads x keys logits and the heads x d output run on the tensor
+// cores; the softmax is online in the log2 domain and the sink joins the normaliser at the end.
+// Split boundaries sit at fixed multiples of the split size in slot space, never depending on
+// the batch, and splits are merged by a second kernel in fixed order (batch-invariant decode).
+#include "common.cuh"
+
+namespace csa {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D, int NG, bool FP8>
+struct AttnCfg {
+  // keys per chunk: fixed per row format (never per head grouping), so the rounding of the
+  // probabilities, which follows the chunked running maximum, is identical for any batch size
+  static constexpr int CK = FP8 ? 32 : 64;
+  static constexpr int NKT = CK / 32;                         // n8 key tiles per warp (S phase)
+  static constexpr int HG = 16 * NG;                          // heads per CTA
+  static constexpr int THREADS = 128 * NG;
+  static constexpr int QS = D + 8;                            // padded smem row strides (bf16)
+  static constexpr int KS = D + 8;
+  static constexpr int PS = CK + 8;
+  static constexpr int ROWB = FP8 ? CSA_FP8_MIXED_ROW_BYTES : D * 2;   // global row bytes
+  static constexpr size_t q_off = 0;
+  static constexpr size_t k_off = q_off + size_t(HG) * QS * 2;
+  static constexpr size_t st_off = k_off + size_t(2) * CK * KS * 2;
+  static constexpr size_t p_off = st_off + (FP8 ? size_t(2) * CK * ROWB : 0);
+  static constexpr size_t red_off = p_off + size_t(HG) * PS * 2;
+  static constexpr size_t lsum_off = red_off + size_t(HG) * 4 * 4;
+  static constexpr size_t ptr_off = lsum_off + size_t(HG) * 4 * 4;
+  static constexpr size_t smem = ptr_off + size_t(2) * CK * 8;
+};
+
+__device__ __forceinline__ int slot_row(const AttendArgs& a, int b, long long qi, int t, int Kq, int s,
+                                        bool& win_row, int32_t* status) {
+  // returns the row index (entry index or ring slot) or -1 when the slot holds nothing
+  if (s < Kq) {
+    win_row = false;
+    if (a.idx == nullptr) return s;
+    const int e = a.idx[qi * a.k + s];
+    if (e == -1) return -1;
+    if (e < -1 || e >= a.N) {
+      report_error(status, CSA_ERR_DEVICE_CHECK, e);
+      return -1;
+    }
+    return e;
+  }
+  const int j = s - Kq;
+  if (j >= a.window) return -1;
+  win_row = true;
+  const int u = t - a.window + 1 + j;
+  if (u < 0) return -1;
+  return u % a.Wcap;
+}
+
+template <int D, int NG, bool FP8>
+__global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(AttendArgs a) {
+  using C = AttnCfg<D, NG, FP8>;
+  constexpr int CK = C::CK, NKT = C::NKT, HG = C::HG, QS = C::QS, KS = C::KS, PS = C::PS;
+  extern __shared__ __align__(16) unsigned char smem[];
+  __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(smem + C::q_off);
+  __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(smem + C::k_off);
+  unsigned char* St = smem + C::st_off;
+  __nv_bfloat16* Ps = reinterpret_cast<__nv_bfloat16*>(smem + C::p_off);
+  float* redmax = reinterpret_cast<float*>(smem + C::red_off);
+  float* lsum = reinterpret_cast<float*>(smem + C::lsum_off);
+  const unsigned char** rowptr = reinterpret_cast<const unsigned char**>(smem + C::ptr_off);
+
+  const int tid = threadIdx.x, lane = tid & 31, wall = tid >> 5;
+  const int g = wall >> 2, wq = wall & 3;
+  const int split = blockIdx.x;
+  const int h0 = blockIdx.y * HG;
+  const long long qi = blockIdx.z;
+  const int b = static_cast<int>(qi / a.Tq);
+  const int t = a.q_pos[qi];
+  const int nvis = n_visible(t, a.m, a.N);
+  const int Kq = (a.idx == nullptr) ? nvis : a.k;
+  const int nslots = Kq + a.window;
+  const int s_begin = split * a.split_slots;
+  const int s_end = min(nslots, s_begin + a.split_slots);
+  const int nchunks = s_end > s_begin ? (s_end - s_begin + CK - 1) / CK : 0;
+
+  // ---------------- prologue: q_hat = RoPE_t(RMSNorm(q)) -> bf16 in shared memory
+  {
+    constexpr int E = D / 32;   // elements per lane
+    const __nv_bfloat16* qsrc = static_cast<const __nv_bfloat16*>(a.q);
+    for (int hl = wall; hl < HG; hl += 4 * NG) {
+      const __nv_bfloat16* src = qsrc + ((qi * a.H) + h0 + hl) * static_cast<long long>(D) + lane * E;
+      float v[E];
+      if constexpr (E >= 8) {
+#pragma unroll
+        for (int c = 0; c < E; c += 8) {
+          const uint4 u = *reinterpret_cast<const uint4*>(src + c);
+          v[c + 0] = bf16lo(u.x); v[c + 1] = bf16hi(u.x);
+          v[c + 2] = bf16lo(u.y); v[c + 3] = bf16hi(u.y);
+          v[c + 4] = bf16lo(u.z); v[c + 5] = bf16hi(u.z);
+          v[c + 6] = bf16lo(u.w); v[c + 7] = bf16hi(u.w);
+        }
+      } else {
+        static_assert(E == 4, "d must be 128 or 512");
+        const uint2 u = *reinterpret_cast<const uint2*>(src);
+        v[0] = bf16lo(u.x); v[1] = bf16hi(u.x);
+        v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
+      }
+      if (a.q_norm_rope) {
+        float ss = 0.f;
+#pragma unroll
+        for (int c = 0; c < E; ++c) ss = fmaf(v[c], v[c], ss);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float inv = 1.0f / sqrtf(ss / static_cast<float>(D) + a.eps);
+#pragma unroll
+        for (int c = 0; c < E; ++c) v[c] *= inv;
+        const int cbase = lane * E;
+        if (cbase + E > D - a.rp.r) {
+#pragma unroll
+          for (int c = 0; c < E; c += 2) {
+            const int ch = cbase + c;
+            if (ch >= D - a.rp.r) {
+              float cs, sn;
+              rope_cos_sin(static_cast<double>(t), a.rp.inv_freq[(ch - (D - a.rp.r)) >> 1], cs, sn);
+              const float x0 = v[c], x1 = v[c + 1];
+              v[c] = x0 * cs - x1 * sn;
+              v[c + 1] = x0 * sn + x1 * cs;
+            }
+          }
+        }
+      }
+      __nv_bfloat16* dst = Qs + hl * QS + lane * E;
+      if constexpr (E >= 8) {
+#pragma unroll
+        for (int c = 0; c < E; c += 8) {
+          uint4 u;
+          u.x = pack_bf16x2(v[c + 0], v[c + 1]);
+          u.y = pack_bf16x2(v[c + 2], v[c + 3]);
+          u.z = pack_bf16x2(v[c + 4], v[c + 5]);
+          u.w = pack_bf16x2(v[c + 6], v[c + 7]);
+          *reinterpret_cast<uint4*>(dst + c) = u;
+        }
+      } else {
+        uint2 u;
+        u.x = pack_bf16x2(v[0], v[1]);
+        u.y = pack_bf16x2(v[2], v[3]);
+        *reinterpret_cast<uint2*>(dst) = u;
+      }
+    }
+  }
+
+  const unsigned char* kvb = static_cast<const unsigned char*>(a.kv);
+  const unsigned char* winb = static_cast<const unsigned char*>(a.win);
+  const unsigned char* dummy = static_cast<const unsigned char*>(a.q);   // source of zero-size copies
+
+  auto compute_ptrs = [&](int c, int buf) {
+    if (tid < CK) {
+      const int s = s_begin + c * CK + tid;
+      const unsigned char* p = nullptr;
+      if (s < s_end) {
+        bool isw = false;
+        const int r = slot_row(a, b, qi, t, Kq, s, isw, a.status);
+        if (r >= 0) {
+          p = isw ? winb + (static_cast<size_t>(b) * a.Wcap + r) * (D * 2)
+                  : kvb + (static_cast<size_t>(b) * a.N + r) * C::ROWB;
+          if (FP8 && isw) p = reinterpret_cast<const unsigned char*>(reinterpret_cast<uintptr_t>(p) | 1u);
+        }
+      }
+      rowptr[buf * CK + tid] = p;
+    }
+  };
+  // cp.async of chunk rows into Ks (bf16) or the FP8 staging area (window rows go straight to Ks)
+  auto issue_loads = [&](int buf) {
+    constexpr int CPR = D * 2 / 16;
+    for (int c = tid; c < CK * CPR; c += C::THREADS) {
+      const int r = c / CPR, q = c % CPR;
+      const unsigned char* p = rowptr[buf * CK + r];
+      __nv_bfloat16* kd = Ks + (buf * CK + r) * KS + q * 8;
+      if (!FP8) {
+        cp_async16(kd, p ? p + q * 16 : dummy, p != nullptr);
+      } else {
+        const bool isw = (reinterpret_cast<uintptr_t>(p) & 1u) != 0;
+        const unsigned char* pw = reinterpret_cast<const unsigned char*>(reinterpret_cast<uintptr_t>(p) & ~uintptr_t(1));
+        if (isw) {
+          cp_async16(kd, pw + q * 16, true);
+        } else if (q < C::ROWB / 16) {
+          cp_async16(St + (buf * CK + r) * C::ROWB + q * 16, p ? p + q * 16 : dummy, p != nullptr);
+        }
+      }
+    }
+  };
+
+  float m_run[2] = {-INFINITY, -INFINITY};
+  float l_run[2] = {0.f, 0.f};
+  constexpr int NO = D / 32;          // n8 tiles of output dims per warp (D/4 dims)
+  float oacc[NO][4];
+#pragma unroll
+  for (int i = 0; i < NO; ++i)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) oacc[i][c] = 0.f;
+  const float sl2 = a.scale * kLog2e;
+
+  if (nchunks > 0) {
+    compute_ptrs(0, 0);
+    __syncthreads();
+    issue_loads(0);
+    cp_async_commit();
+  }
+  for (int c = 0; c < nchunks; ++c) {
+    const int buf = c & 1;
+    if (c + 1 < nchunks) compute_ptrs(c + 1, buf ^ 1);
+    __syncthreads();                                   // (A)
+    if (c + 1 < nchunks) {
+      issue_loads(buf ^ 1);
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();                                   // (B)
+    if (FP8) {
+      // widen entry rows: dims [0,448) e4m3 * block scale, dims [448,512) bf16 copy
+      for (int idx = tid; idx < CK * (D / 8); idx += C::THREADS) {
+        const int r = idx / (D / 8), p8 = idx % (D / 8);
+        const unsigned char* p = rowptr[buf * CK + r];
+        if ((reinterpret_cast<uintptr_t>(p) & 1u) != 0) continue;     // window row, already bf16
+        const unsigned char* row = St + (buf * CK + r) * C::ROWB;
+        __nv_bfloat16* kd = Ks + (buf * CK + r) * KS + p8 * 8;
+        if (p8 < 56) {
+          const float sc = *reinterpret_cast<const float*>(row + 576 + (p8 >> 3) * 4);
+          const uint2 v = *reinterpret_cast<const uint2*>(row + p8 * 8);
+          float f[8];
+          e4m3x2_to_float2(static_cast<uint16_t>(v.x & 0xFFFF), f[0], f[1]);
+          e4m3x2_to_float2(static_cast<uint16_t>(v.x >> 16), f[2], f[3]);
+          e4m3x2_to_float2(static_cast<uint16_t>(v.y & 0xFFFF), f[4], f[5]);
+          e4m3x2_to_float2(static_cast<uint16_t>(v.y >> 16), f[6], f[7]);
+          uint4 o;
+          o.x = pack_bf16x2(f[0] * sc, f[1] * sc); o.y = pack_bf16x2(f[2] * sc, f[3] * sc);
+          o.z = pack_bf16x2(f[4] * sc, f[5] * sc); o.w = pack_bf16x2(f[6] * sc, f[7] * sc);
+          *reinterpret_cast<uint4*>(kd) = o;
+        } else {
+          *reinterpret_cast<uint4*>(kd) = *reinterpret_cast<const uint4*>(row + 448 + (p8 - 56) * 16);
+        }
+      }
+      __syncthreads();                                 // (B')
+    }
+    const __nv_bfloat16* Kb = Ks + buf * CK * KS;
+
+    // ---- S = Q K^T for heads [16g, 16g+16) x keys [wq*8*NKT, +8*NKT)
+    float sacc[NKT][4];
+#pragma unroll
+    for (int n = 0; n < NKT; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sacc[n][e] = 0.f;
+#pragma unroll 4
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t af[4];
+      ldmatrix_x4(af[0], af[1], af[2], af[3],
+                  smem_u32(Qs + (16 * g + (lane & 15)) * QS + ks * 16 + (lane >> 4) * 8));
+      if (NKT == 2) {
+        uint32_t b0, b1, b2, b3;
+        const int key = wq * 16 + (lane >> 4) * 8 + (lane & 7);
+        ldmatrix_x4(b0, b1, b2, b3, smem_u32(Kb + key * KS + ks * 16 + ((lane >> 3) & 1) * 8));
+        const uint32_t bb0[2] = {b0, b1}, bb1[2] = {b2, b3};
+        mma_bf16_16816(sacc[0], af, bb0);
+        mma_bf16_16816(sacc[NKT - 1], af, bb1);
+      } else {
+        uint32_t b0, b1;
+        const int key = wq * 8 + (lane & 7);
+        ldmatrix_x2(b0, b1, smem_u32(Kb + key * KS + ks * 16 + ((lane >> 3) & 1) * 8));
+        const uint32_t bb0[2] = {b0, b1};
+        mma_bf16_16816(sacc[0], af, bb0);
+      }
+    }
+    // ---- mask, scale to log2 domain, row max over this warp's keys
+    float cmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int n = 0; n < NKT; ++n) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = wq * 8 * NKT + n * 8 + 2 * (lane & 3) + (e & 1);
+        const bool ok = rowptr[buf * CK + key] != nullptr;
+        const float v = ok ? sacc[n][e] * sl2 : -INFINITY;
+        sacc[n][e] = v;
+        cmax[e >> 1] = fmaxf(cmax[e >> 1], v);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      cmax[r] = fmaxf(cmax[r], __shfl_xor_sync(0xffffffffu, cmax[r], 1));
+      cmax[r] = fmaxf(cmax[r], __shfl_xor_sync(0xffffffffu, cmax[r], 2));
+    }
+    if ((lane & 3) == 0) {
+      redmax[(16 * g + (lane >> 2)) * 4 + wq] = cmax[0];
+      redmax[(16 * g + (lane >> 2) + 8) * 4 + wq] = cmax[1];
+    }
+    __syncthreads();                                   // (C)
+    float alpha[2], muse[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const float* rm = redmax + (16 * g + (lane >> 2) + 8 * r) * 4;
+      const float mc = fmaxf(fmaxf(rm[0], rm[1]), fmaxf(rm[2], rm[3]));
+      const float mn = fmaxf(m_run[r], mc);
+      muse[r] = (mn == -INFINITY) ? 0.f : mn;
+      alpha[r] = exp2f(m_run[r] - muse[r]);
+      m_run[r] = mn;
+    }
+    // ---- P = exp2(s - m), partial row sums, P (bf16) to shared memory
+    float psum[2] = {0.f, 0.f};
+#pragma unroll
+    for (int n = 0; n < NKT; ++n) {
+      const float p0 = exp2f(sacc[n][0] - muse[0]);
+      const float p1 = exp2f(sacc[n][1] - muse[0]);
+      const float p2 = exp2f(sacc[n][2] - muse[1]);
+      const float p3 = exp2f(sacc[n][3] - muse[1]);
+      psum[0] += p0 + p1;
+      psum[1] += p2 + p3;
+      const int key = wq * 8 * NKT + n * 8 + 2 * (lane & 3);
+      const int hr = 16 * g + (lane >> 2);
+      *reinterpret_cast<uint32_t*>(Ps + hr * PS + key) = pack_bf16x2(p0, p1);
+      *reinterpret_cast<uint32_t*>(Ps + (hr + 8) * PS + key) = pack_bf16x2(p2, p3);
+    }
+    l_run[0] = l_run[0] * alpha[0] + psum[0];
+    l_run[1] = l_run[1] * alpha[1] + psum[1];
+#pragma unroll
+    for (int i = 0; i < NO; ++i) {
+      oacc[i][0] *= alpha[0]; oacc[i][1] *= alpha[0];
+      oacc[i][2] *= alpha[1]; oacc[i][3] *= alpha[1];
+    }
+    __syncthreads();                                   // (D)
+    // ---- O += P V for heads [16g,16g+16) x dims [wq*D/4, +D/4)
+#pragma unroll
+    for (int kk = 0; kk < CK / 16; ++kk) {
+      uint32_t pa[4];
+      ldmatrix_x4(pa[0], pa[1], pa[2], pa[3],
+                  smem_u32(Ps + (16 * g + (lane & 15)) * PS + kk * 16 + (lane >> 4) * 8));
+#pragma unroll
+      for (int np = 0; np < NO / 2; ++np) {
+        uint32_t v0, v1, v2, v3;
+        const int key = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int dim = wq * (D / 4) + np * 16 + (lane >> 4) * 8;
+        ldmatrix_x4_trans(v0, v1, v2, v3, smem_u32(Kb + key * KS + dim));
+        const uint32_t vb0[2] = {v0, v1}, vb1[2] = {v2, v3};
+        mma_bf16_16816(oacc[2 * np], pa, vb0);
+        mma_bf16_16816(oacc[2 * np + 1], pa, vb1);
+      }
+    }
+  }
+
+  // ---------------- epilogue: total row sums, sink, normalise / write partials
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 1);
+    l_run[r] += __shfl_xor_sync(0xffffffffu, l_run[r], 2);
+  }
+  __syncthreads();
+  if ((lane & 3) == 0) {
+    lsum[(16 * g + (lane >> 2)) * 4 + wq] = l_run[0];
+    lsum[(16 * g + (lane >> 2) + 8) * 4 + wq] = l_run[1];
+  }
+  __syncthreads();
+  float ltot[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const float* ls = lsum + (16 * g + (lane >> 2) + 8 * r) * 4;
+    ltot[r] = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+  }
+  const int Q = a.B * a.Tq;
+  if (a.n_splits == 1) {
+    float fac[2], linv[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int h = h0 + 16 * g + (lane >> 2) + 8 * r;
+      const float a2 = a.sink[h] * kLog2e;
+      const float M = fmaxf(m_run[r], a2);
+      fac[r] = (m_run[r] == -INFINITY) ? 0.f : exp2f(m_run[r] - M);
+      const float L = ltot[r] * fac[r] + exp2f(a2 - M);
+      linv[r] = 1.0f / L;
+      if (a.lse != nullptr && wq == 0 && (lane & 3) == 0) a.lse[qi * a.H + h] = (M + log2f(L)) * kLn2;
+    }
+    __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(a.out);
+#pragma unroll
+    for (int i = 0; i < NO; ++i) {
+      const int dim = wq * (D / 4) + i * 8 + 2 * (lane & 3);
+      float cs = 1.f, sn = 0.f;
+      const bool rot = a.out_unrotate && dim >= D - a.rp.r;
+      if (rot) rope_cos_sin(-static_cast<double>(t), a.rp.inv_freq[(dim - (D - a.rp.r)) >> 1], cs, sn);
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int h = h0 + 16 * g + (lane >> 2) + 8 * r;
+        float x0 = oacc[i][2 * r] * fac[r] * linv[r];
+        float x1 = oacc[i][2 * r + 1] * fac[r] * linv[r];
+        if (rot) {
+          const float y0 = x0 * cs - x1 * sn, y1 = x0 * sn + x1 * cs;
+          x0 = y0; x1 = y1;
+        }
+        *reinterpret_cast<uint32_t*>(outp + (qi * a.H + h) * static_cast<long long>(D) + dim) =
+            pack_bf16x2(x0, x1);
+      }
+    }
+  } else {
+    // partial: O (relative to m_run, log2 domain) and (m, l) per (query, split, head)
+    float* po = a.partial;
+    float* pml = a.partial + static_cast<size_t>(Q) * a.n_splits * a.H * D;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int h = h0 + 16 * g + (lane >> 2) + 8 * r;
+      const size_t rowi = (static_cast<size_t>(qi) * a.n_splits + split) * a.H + h;
+      if (wq == 0 && (lane & 3) == 0) {
+        pml[rowi * 2 + 0] = m_run[r];
+        pml[rowi * 2 + 1] = ltot[r];
+      }
+#pragma unroll
+      for (int i = 0; i < NO; ++i) {
+        const int dim = wq * (D / 4) + i * 8 + 2 * (lane & 3);
+        *reinterpret_cast<float2*>(po + rowi * D + dim) = make_float2(oacc[i][2 * r], oacc[i][2 * r + 1]);
+      }
+    }
+  }
+}
+
+// Merge split partials: out = sum_s O_s 2^(m_s - M) / (sum_s l_s 2^(m_s - M) + 2^(a_h - M)).
+template <int D>
+__global__ void __launch_bounds__(128) k_attend_combine(AttendArgs a) {
+  const long long qi = blockIdx.x;
+  const int h = blockIdx.y;
+  const int S = a.n_splits;
+  const int Q = a.B * a.Tq;
+  const float* po = a.partial;
+  const float* pml = a.partial + static_cast<size_t>(Q) * S * a.H * D;
+  const float a2 = a.sink[h] * kLog2e;
+  float M = a2;
+  for (int s = 0; s < S; ++s) M = fmaxf(M, pml[((qi * S + s) * a.H + h) * 2]);
+  float L = exp2f(a2 - M);
+  for (int s = 0; s < S; ++s) {
+    const size_t ri = (static_cast<size_t>(qi) * S + s) * a.H + h;
+    const float ms = pml[ri * 2];
+    if (ms != -INFINITY) L = fmaf(pml[ri * 2 + 1], exp2f(ms - M), L);
+  }
+  const float linv = 1.0f / L;
+  const int t = a.q_pos[qi];
+  __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(a.out);
+  for (int dim = threadIdx.x * 2; dim < D; dim += 256) {
+    float x0 = 0.f, x1 = 0.f;
+    for (int s = 0; s < S; ++s) {
+      const size_t ri = (static_cast<size_t>(qi) * S + s) * a.H + h;
+      const float ms = pml[ri * 2];
+      if (ms == -INFINITY) continue;
+      const float f = exp2f(ms - M);
+      const float2 v = *reinterpret_cast<const float2*>(po + ri * D + dim);
+      x0 = fmaf(v.x, f, x0);
+      x1 = fmaf(v.y, f, x1);
+    }
+    x0 *= linv;
+    x1 *= linv;
+    if (a.out_unrotate && dim >= D - a.rp.r) {
+      float cs, sn;
+      rope_cos_sin(-static_cast<double>(t), a.rp.inv_freq[(dim - (D - a.rp.r)) >> 1], cs, sn);
+      const float y0 = x0 * cs - x1 * sn, y1 = x0 * sn + x1 * cs;
+      x0 = y0; x1 = y1;
+    }
+    *reinterpret_cast<uint32_t*>(outp + (qi * a.H + h) * static_cast<long long>(D) + dim) = pack_bf16x2(x0, x1);
+  }
+  if (a.lse != nullptr && threadIdx.x == 0) a.lse[qi * a.H + h] = (M + log2f(L)) * kLn2;
+}
+
+template <int D, int NG, bool FP8>
+cudaError_t launch_t(const AttendArgs& a, cudaStream_t s, int* launches) {
+  using C = AttnCfg<D, NG, FP8>;
+  cudaError_t e = cudaFuncSetAttribute(k_attend<D, NG, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(C::smem));
+  if (e != cudaSuccess) return e;
+  const int Q = a.B * a.Tq;
+  dim3 grid(a.n_splits, a.H / C::HG, Q);
+  k_attend<D, NG, FP8><<<grid, C::THREADS, C::smem, s>>>(a);
+  ++*launches;
+  e = cudaGetLastError();
+  if (e != cudaSuccess || a.n_splits == 1) return e;
+  k_attend_combine<D><<<dim3(Q, a.H), 128, 0, s>>>(a);
+  ++*launches;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t attend_partial_bytes(int Q, int H, int d, int n_splits) {
+  if (n_splits <= 1) return 0;
+  return static_cast<size_t>(Q) * n_splits * H * (d + 2) * sizeof(float);
+}
+
+cudaError_t launch_attend(const AttendArgs& a, cudaStream_t s, int* launches) {
+  const int Q = a.B * a.Tq;
+  if (Q == 0) return cudaSuccess;
+  // 64 heads per CTA when there is enough parallelism, otherwise 16 (identical numerics)
+  int sms = 148;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const bool wide = (a.H % 64 == 0) && (static_cast<long long>(Q) * a.n_splits * (a.H / 64) >= 2LL * sms);
+  if (a.d == 512) {
+    if (a.fp8) return wide ? launch_t<512, 4, true>(a, s, launches) : launch_t<512, 1, true>(a, s, launches);
+    return wide ? launch_t<512, 4, false>(a, s, launches) : launch_t<512, 1, false>(a, s, launches);
+  }
+  if (a.d == 128 && !a.fp8) {
+    return wide ? launch_t<128, 4, false>(a, s, launches) : launch_t<128, 1, false>(a, s, launches);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace csa

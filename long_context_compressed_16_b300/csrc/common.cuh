@@ -1,0 +1,171 @@
+// Internal helpers shared by the library's kernels (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "../../include/csa.h"
+
+namespace csa {
+
+constexpr int kMaxRopePairs = 64;   // rope_dims <= 128
+
+// RoPE frequencies are computed on the host in double and passed by value.
+struct RopeParams {
+  int r;                    // rotated dims (even), the last r dims of each vector
+  double inv_freq[kMaxRopePairs];
+};
+
+// Status word at the start of every workspace: {code, detail, pad, pad}.
+constexpr size_t kStatusBytes = 256;
+
+// Closed compressed blocks visible to position t: s < floor((t+1)/m), clipped to [0, N].
+__host__ __device__ __forceinline__ int n_visible(int t, int m, int N) {
+  const long long v = (static_cast<long long>(t) + 1) / m;
+  return v <= 0 ? 0 : (v >= N ? N : static_cast<int>(v));
+}
+
+__device__ __forceinline__ void report_error(int32_t* status, int32_t code, int32_t detail) {
+  if (status == nullptr) return;
+  if (atomicCAS(status, 0, code) == 0) status[1] = detail;
+}
+
+// cos/sin of pos * inv_freq.  The product and its reduction modulo 2*pi run in double so that
+// positions up to 2^20 and beyond keep full fp32 accuracy in the angle.
+__device__ __forceinline__ void rope_cos_sin(double pos, double inv_freq, float& c, float& s) {
+  const double kTwoPi = 6.283185307179586476925286766559;
+  const double kInvTwoPi = 0.15915494309189533576888376337251;
+  double a = pos * inv_freq;
+  double n = floor(a * kInvTwoPi);
+  double red = fma(-n, kTwoPi, a);
+  sincosf(static_cast<float>(red), &s, &c);
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// e4m3 pair -> two floats (exact) via the hardware f16x2 conversion.
+__device__ __forceinline__ void e4m3x2_to_float2(uint16_t v, float& lo, float& hi) {
+  uint32_t h2;
+  asm("{cvt.rn.f16x2.e4m3x2 %0, %1;}" : "=r"(h2) : "h"(v));
+  __half2 hh = *reinterpret_cast<__half2*>(&h2);
+  float2 f = __half22float2(hh);
+  lo = f.x;
+  hi = f.y;
+}
+
+// ------------------------------------------------------------------ warp-level MMA (bf16)
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                            uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+__device__ __forceinline__ void ldmatrix_x2(uint32_t& r0, uint32_t& r1, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n"
+               : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                                  uint32_t& r3, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+// D = A(16x16, row) * B(16x8, col) + D, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, const uint32_t* b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// ------------------------------------------------------------------ cp.async
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
+  const int n = valid ? 16 : 0;   // src-size 0 => the 16 bytes are zero-filled
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n"
+               :: "r"(smem_u32(smem)), "l"(gmem), "r"(n));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" :: "n"(N)); }
+
+}  // namespace csa
+
+// ------------------------------------------------------------------ launchers (internal)
+namespace csa {
+
+struct CompressArgs {
+  const void *Ca, *Cb, *Za, *Zb;
+  const float *bias_a, *bias_b, *gamma;
+  void* out;
+  int B, T, d, m, N, overlap, norm, rope;
+  int pos_shift;
+  float eps;
+  RopeParams rp;
+};
+cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s, int* launches);
+
+struct IndexArgs {
+  const void* qI;
+  const float* w;
+  const void* kI;
+  const float* kI_scale;
+  const int32_t* q_pos;
+  float* scores;            // score rows of N floats
+  int B, Tq, N, nI, dI, m, fp8;
+  int q_begin, q_count;     // range of query GROUPS (G consecutive queries of one sequence)
+  int score_row_offset;     // flattened query q (= b*Tq + i) owns score row q - score_row_offset
+};
+// Scores for the query groups [q_begin, q_begin + q_count).  fill_invisible: also write -inf
+// for every s in [N_vis, N) so that the rows are complete.
+cudaError_t launch_index_score_groups(const IndexArgs& a, int G, int fill_invisible, cudaStream_t s,
+                                      int* launches);
+
+struct TopkArgs {
+  const float* scores;
+  const int32_t* q_pos;
+  int32_t* idx_out;
+  int32_t* status;
+  int Tq, N, k, m;
+  int q_begin, q_count;
+  int score_row_offset;
+};
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s, int* launches);
+
+struct AttendArgs {
+  const void* q;
+  const void* kv;
+  const int32_t* idx;       // nullptr => dense (HCA)
+  const void* win;
+  const float* sink;
+  const int32_t* q_pos;
+  void* out;
+  float* lse;
+  float* partial;           // workspace for split partials
+  int32_t* status;
+  int B, Tq, N, H, d, k, m, Wcap, window, fp8;
+  int q_norm_rope, out_unrotate;
+  float scale, eps;
+  int n_slots;              // slots per query (k + window, or N + window)
+  int split_slots;          // slots per split (multiple of the chunk size)
+  int n_splits;
+  RopeParams rp;
+};
+size_t attend_partial_bytes(int Q, int H, int d, int n_splits);
+cudaError_t launch_attend(const AttendArgs& a, cudaStream_t s, int* launches);
+
+}  // namespace csa

@@ -1,0 +1,57 @@
+"""Shared test helpers: move library tensors to oracle inputs and apply the parity bars.
+
+Bars (the method's stated tolerances): outputs max-abs <= 2e-2 and relative L2 <= 5e-3 against
+the fp64 oracle; top-k sets exact except entries whose oracle score lies within 1e-3 relative
+of the k-th score; -1 padding exact."""
+import numpy as np
+import torch
+
+from oracle import csa_oracle as O
+
+MAX_ABS = 2e-2
+REL_L2 = 5e-3
+TIE_REL = 1e-3
+
+
+def bits16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> fp64 through the oracle's own decoder; fp32 tensors convert exactly."""
+    if t.dtype == torch.bfloat16:
+        return O.bf16_to_f64(bits16(t))
+    return t.detach().cpu().to(torch.float64).numpy()
+
+
+def assert_close(gpu_bf16: torch.Tensor, ref: np.ndarray, what: str, max_abs=MAX_ABS, rel_l2=REL_L2):
+    g = f64(gpu_bf16) if isinstance(gpu_bf16, torch.Tensor) else np.asarray(gpu_bf16, dtype=np.float64)
+    assert g.shape == ref.shape, (what, g.shape, ref.shape)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite output"
+    d = g - ref
+    ma = float(np.max(np.abs(d))) if d.size else 0.0
+    rl = float(np.linalg.norm(d) / max(np.linalg.norm(ref), 1e-30)) if d.size else 0.0
+    assert ma <= max_abs and rl <= rel_l2, f"{what}: max-abs {ma:.3e} (bar {max_abs}), rel-L2 {rl:.3e} (bar {rel_l2})"
+    return ma, rl
+
+
+def check_topk_row(g: np.ndarray, scores: np.ndarray, nvis: int, k: int, what: str):
+    """g: GPU idx row [k]; scores: oracle fp64 scores of the visible entries [nvis]."""
+    if nvis <= k:
+        assert sorted(g[:nvis].tolist()) == list(range(nvis)), f"{what}: not all visible entries taken"
+        assert np.all(g[nvis:] == -1), f"{what}: bad padding"
+        return 0
+    assert np.all((g >= 0) & (g < nvis)), f"{what}: index out of range"
+    assert len(set(g.tolist())) == k, f"{what}: duplicate indices"
+    order = np.lexsort((np.arange(nvis), -scores))
+    ref = set(order[:k].tolist())
+    Ik = scores[order[k - 1]]
+    diff = set(g.tolist()) ^ ref
+    for s in diff:
+        assert abs(scores[s] - Ik) <= TIE_REL * abs(Ik), (
+            f"{what}: entry {s} score {scores[s]!r} vs k-th {Ik!r} differs beyond the near-tie band")
+    return len(diff)
+
+
+def nvis_of(t, m, N):
+    return O.n_visible(int(t), m, N)

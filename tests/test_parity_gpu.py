@@ -1,0 +1,398 @@
+"""GPU parity: each C-ABI call against the fp64 oracle on the same seeded inputs.
+
+Every call gets inputs that come from the seeded generator or from the oracle itself (never from
+the CUDA path): the attention calls receive the oracle's own top-k sets, the indexer receives
+the oracle's compressed keys rounded to bf16 by the oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from long_context_compressed_16_b300 import capi as C
+from long_context_compressed_16_b300 import pipeline as P
+from long_context_compressed_16_b300 import synth as S
+from oracle import csa_oracle as O
+from tests.helpers import assert_close, check_topk_row, f64, nvis_of
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+THETA = 160000.0
+
+
+def _oracle_compress(inp, names, m, d, rope=True, overlap=True, **kw):
+    Ca, Cb, Za, Zb = (f64(inp[n]) for n in names) if overlap else (f64(inp[names[0]]), None,
+                                                                     f64(inp[names[1]]), None)
+    return O.compress(Ca, Za, m, Cb=Cb, Zb=Zb, rope_on=rope, rope_dims=64 if rope else 0, theta=THETA, **kw)
+
+
+def _to_dev_bf16(x64: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(O.bf16_round(x64).view(np.int16)).view(torch.bfloat16).to(DEV)
+
+
+# ------------------------------------------------------------------------------------------------ compress
+
+@pytest.mark.parametrize("B,T,d,m,overlap,rope,bias", [
+    (1, 2048, 128, 4, True, True, False),       # tiny workload main stream
+    (1, 2048, 64, 4, True, False, False),       # tiny workload indexer keys (RMSNorm, no RoPE)
+    (2, 2050, 512, 4, True, True, True),        # ragged tail, batch 2, biases and gamma
+    (1, 1000, 128, 1, True, True, True),        # m = 1 (two-row logistic mix)
+    (2, 4096 + 77, 512, 128, False, True, True),  # HCA, ragged
+    (1, 640, 1024, 8, True, True, False),       # widest supported row
+])
+def test_compress_parity(B, T, d, m, overlap, rope, bias):
+    g = torch.Generator().manual_seed(T + d)
+    names = ("Ca", "Cb", "Za", "Zb")
+    inp = {n: S.normal_bf16((B, T, d), 7, S.TID[n], DEV) for n in names}
+    ba = bb = gam = None
+    kw = {}
+    if bias:
+        ba = torch.randn(m, d, generator=g).float().to(DEV)
+        bb = torch.randn(m, d, generator=g).float().to(DEV)
+        gam = (1 + 0.1 * torch.randn(d, generator=g)).float().to(DEV)
+        kw = dict(bias_a=ba.double().cpu().numpy(), bias_b=bb.double().cpu().numpy() if overlap else None,
+                  gamma=gam.double().cpu().numpy())
+    out = P.compress(inp["Ca"], inp["Za"], m, Cb=inp["Cb"] if overlap else None, Zb=inp["Zb"] if overlap else None,
+                     bias_a=ba, bias_b=bb if overlap else None, gamma=gam, rope=rope,
+                     rope_dims=64 if rope else 0, theta=THETA)
+    torch.cuda.synchronize()
+    if overlap:
+        ref = O.compress(f64(inp["Ca"]), f64(inp["Za"]), m, Cb=f64(inp["Cb"]), Zb=f64(inp["Zb"]), rope_on=rope,
+                         rope_dims=64 if rope else 0, theta=THETA, **kw)
+    else:
+        ref = O.compress(f64(inp["Ca"]), f64(inp["Za"]), m, rope_on=rope, rope_dims=64 if rope else 0, theta=THETA,
+                         **{k: v for k, v in kw.items() if k != "bias_b"})
+    assert_close(out, ref, f"compress B{B} T{T} d{d} m{m}")
+
+
+def test_compress_degenerate_sizes():
+    x = S.normal_bf16((1, 3, 128), 0, 1, DEV)
+    out = P.compress(x, x, 4, Cb=x, Zb=x)             # T < m: no closed block
+    assert out.shape == (1, 0, 128)
+    x = S.normal_bf16((0, 64, 128), 0, 1, DEV)
+    assert P.compress(x, x, 4, Cb=x, Zb=x).shape == (0, 16, 128)
+
+
+def test_compress_full_size_prefill_streams():
+    """The 65536-token prefill chunk: main stream d=512 and indexer stream d=128, every entry."""
+    w = S.WORKLOADS["csa_prefill_t65536"]
+    inp = S.make_inputs(S.scaled(w), DEV)
+    kv = P.compress(inp["Ca"], inp["Za"], 4, Cb=inp["Cb"], Zb=inp["Zb"], theta=THETA)
+    kI = P.compress(inp["Ca_I"], inp["Za_I"], 4, Cb=inp["Cb_I"], Zb=inp["Zb_I"], rope=False, rope_dims=0)
+    torch.cuda.synchronize()
+    ref = _oracle_compress(inp, ("Ca", "Cb", "Za", "Zb"), 4, 512)
+    assert_close(kv, ref, "compress T=65536 d=512")
+    ref = _oracle_compress(inp, ("Ca_I", "Cb_I", "Za_I", "Zb_I"), 4, 128, rope=False)
+    assert_close(kI, ref, "compress T=65536 d=128 (indexer keys)")
+
+
+# ------------------------------------------------------------------------------------------------ indexer + top-k
+
+def _index_case(qI, w, kI, q_pos, m, k, kI_scale=None, with_scores=True, sample=None):
+    B, Tq = qI.shape[:2]
+    N = kI.shape[1]
+    sc = torch.empty((B, Tq, N), dtype=torch.float32, device=DEV) if with_scores else None
+    idx = P.index_topk(qI, w, kI, q_pos, m, k, kI_scale=kI_scale, score_out=sc)
+    torch.cuda.synchronize()
+    qpos = q_pos.cpu().numpy()
+    gi = idx.cpu().numpy()
+    gs = sc.cpu().numpy() if with_scores else None
+    pairs = sample if sample is not None else [(b, t) for b in range(B) for t in range(Tq)]
+    near = 0
+    for b in range(B):
+        rows = [t for (bb, t) in pairs if bb == b]
+        if not rows:
+            continue
+        if kI_scale is None:
+            kb = f64(kI[b:b + 1])
+        else:
+            kb = O.e4m3_to_f64(kI[b:b + 1].cpu().numpy()) * kI_scale[b:b + 1].cpu().double().numpy()[..., None]
+        qb = f64(qI[b:b + 1, rows])
+        wb = f64(w[b:b + 1, rows])
+        ref = O.index_scores(qb, wb, kb, [qpos[b, rows]], m)
+        for j, t in enumerate(rows):
+            nv = nvis_of(qpos[b, t], m, N)
+            if with_scores:
+                row_ref = ref[0, j]
+                tol = 1e-5 * max(1.0, float(np.max(np.abs(row_ref[:nv])))) if nv else 1e-6
+                assert np.all(np.abs(gs[b, t, :nv] - row_ref[:nv]) <= tol), f"scores b{b} t{t}"
+                assert np.all(np.isneginf(gs[b, t, nv:])), f"invisible scores b{b} t{t}"
+            near += check_topk_row(gi[b, t], ref[0, j, :nv], nv, k, f"topk b{b} t{t}")
+    return near
+
+
+def test_index_topk_tiny_prefill_all_queries():
+    w = S.WORKLOADS["tiny_csa_prefill_t2048"]
+    inp = S.make_inputs(w, DEV)
+    kI64 = _oracle_compress(inp, ("Ca_I", "Cb_I", "Za_I", "Zb_I"), 4, 64, rope=False)
+    kI = _to_dev_bf16(kI64)
+    _index_case(inp["qI"], inp["w"], kI, inp["q_pos"], 4, w.k)
+
+
+@pytest.mark.parametrize("B,Tq,N,nI,dI,k,m", [
+    (2, 37, 1000, 20, 128, 48, 4),     # ragged tiles, heads not a multiple of 16, prefill groups
+    (3, 1, 129, 64, 128, 512, 4),      # k > N visible: take all + pad
+    (1, 9, 300, 64, 64, 7, 4),         # dI = 64
+    (2, 1, 5000, 8, 128, 2048, 4),     # largest k
+])
+def test_index_topk_shapes(B, Tq, N, nI, dI, k, m):
+    qI = S.normal_bf16((B, Tq, nI, dI), 3, S.TID["qI"], DEV)
+    w = S.uniform_f64((B, Tq, nI), 3, S.TID["w"], DEV).float()
+    kI = S.normal_bf16((B, N, dI), 3, S.TID["kI"], DEV)
+    gen = torch.Generator().manual_seed(N)
+    q_pos = torch.randint(0, 4 * N + 8, (B, Tq), generator=gen).int()
+    q_pos[0, 0] = 2          # a query with nothing visible
+    _index_case(qI, w, kI, q_pos.to(DEV), m, k)
+
+
+def test_index_topk_no_entries():
+    qI = S.normal_bf16((2, 3, 8, 64), 1, 1, DEV)
+    w = torch.ones((2, 3, 8), device=DEV)
+    kI = torch.empty((2, 0, 64), dtype=torch.bfloat16, device=DEV)
+    q_pos = torch.full((2, 3), 100, dtype=torch.int32, device=DEV)
+    idx = P.index_topk(qI, w, kI, q_pos, 4, 5)
+    assert torch.all(idx == -1)
+
+
+def test_index_topk_decode_128k_full():
+    w = S.WORKLOADS["csa_decode_128k_b32"]
+    inp = S.make_inputs(w, DEV)
+    _index_case(inp["qI"], inp["w"], inp["kI"], inp["q_pos"], 4, w.k)
+
+
+def test_index_topk_decode_1m_fp8_full():
+    w = S.WORKLOADS["csa_decode_1m_b4_fp8"]
+    inp = S.make_inputs(w, DEV)
+    _index_case(inp["qI"], inp["w"], inp["kI"], inp["q_pos"], 4, w.k, kI_scale=inp["kI_scale"])
+
+
+# ------------------------------------------------------------------------------------------------ attention
+
+def _oracle_attend_rows(inp, idx_np, m, window, pairs, fp8=False, dense=False, **kw):
+    """Oracle outputs for (b, t) pairs, decoding only the kv rows each query uses."""
+    q_pos = inp["q_pos"].cpu().numpy()
+    N = inp["kv"].shape[1]
+    outs, lses = [], []
+    for b, t in pairs:
+        pos = int(q_pos[b, t])
+        if dense:
+            ents = list(range(nvis_of(pos, m, N)))
+        else:
+            ents = [int(e) for e in idx_np[b, t] if e >= 0]
+        rows = inp["kv"][b, ents] if ents else inp["kv"][b, :0]
+        kvr = O.fp8_mixed_row_to_f64(rows.cpu().numpy()) if fp8 else f64(rows)
+        win = f64(inp["win"][b])
+        o, l = O.attend_query(f64(inp["q"][b, t]), pos, kvr, range(len(ents)), win, window,
+                              f64(inp["sink"]), theta=THETA, **kw)
+        outs.append(o)
+        lses.append(l)
+    return np.stack(outs), np.stack(lses)
+
+
+def _oracle_topk(inp, m, k, pairs):
+    """The oracle's own top-k rows for the given queries (fp64 scores over the generator's keys)."""
+    q_pos = inp["q_pos"].cpu().numpy()
+    N = inp["kI"].shape[1]
+    B, Tq = inp["q"].shape[:2]
+    idx = np.full((B, Tq, k), -1, dtype=np.int64)
+    for b in sorted({p[0] for p in pairs}):
+        rows = [t for (bb, t) in pairs if bb == b]
+        if "kI_scale" in inp:
+            kb = O.e4m3_to_f64(inp["kI"][b:b + 1].cpu().numpy()) * inp["kI_scale"][b:b + 1].cpu().double().numpy()[..., None]
+        else:
+            kb = f64(inp["kI"][b:b + 1])
+        sc = O.index_scores(f64(inp["qI"][b:b + 1, rows]), f64(inp["w"][b:b + 1, rows]), kb, [q_pos[b, rows]], m)
+        sel = O.topk_select(sc, [q_pos[b, rows]], m, k)
+        for j, t in enumerate(rows):
+            idx[b, t] = sel[0, j]
+    return idx
+
+
+def _decode_attend_case(name, fp8=False):
+    w = S.WORKLOADS[name]
+    inp = S.make_inputs(w, DEV)
+    pairs = [(b, 0) for b in range(w.B)]
+    idx_np = _oracle_topk(inp, w.m, w.k, pairs)
+    idx = torch.from_numpy(idx_np.astype(np.int32)).to(DEV)
+    out, lse, ws = P.csa_attend(inp["q"], inp["kv"], idx, inp["win"], inp["sink"], inp["q_pos"], fp8=fp8,
+                                want_lse=True)
+    torch.cuda.synchronize()
+    assert C.csa_read_device_status(ws)[0] == C.CSA_OK
+    ref, lref = _oracle_attend_rows(inp, idx_np, w.m, w.window, pairs, fp8=fp8)
+    assert_close(out[:, 0], ref, name)
+    assert np.allclose(lse[:, 0].cpu().numpy(), lref, atol=2e-3, rtol=1e-4)
+
+
+def test_attend_decode_128k_full():
+    _decode_attend_case("csa_decode_128k_b32")
+
+
+def test_attend_decode_1m_fp8_full():
+    _decode_attend_case("csa_decode_1m_b4_fp8", fp8=True)
+
+
+def test_attend_tiny_prefill_all_queries():
+    w = S.WORKLOADS["tiny_csa_prefill_t2048"]
+    inp = S.make_inputs(w, DEV)
+    kI64 = _oracle_compress(inp, ("Ca_I", "Cb_I", "Za_I", "Zb_I"), 4, 64, rope=False)
+    kv64 = _oracle_compress(inp, ("Ca", "Cb", "Za", "Zb"), 4, 128)
+    inp["kI"] = _to_dev_bf16(kI64)
+    inp["kv"] = _to_dev_bf16(kv64)
+    pairs = [(0, t) for t in range(w.T)]
+    idx_np = _oracle_topk(inp, 4, w.k, pairs)
+    idx = torch.from_numpy(idx_np.astype(np.int32)).to(DEV)
+    out, lse, _ = P.csa_attend(inp["q"], inp["kv"], idx, inp["win"], inp["sink"], inp["q_pos"], want_lse=True)
+    torch.cuda.synchronize()
+    ref, lref = _oracle_attend_rows(inp, idx_np, 4, w.window, pairs)
+    assert_close(out[0], ref, "tiny prefill attend")
+    assert np.allclose(lse[0].cpu().numpy(), lref, atol=2e-3, rtol=1e-4)
+
+
+def test_attend_hca_decode_1m_full():
+    w = S.WORKLOADS["hca_decode_1m_b8"]
+    inp = S.make_inputs(w, DEV)
+    out, lse, _ = P.hca_attend(inp["q"], inp["kv"], inp["win"], inp["sink"], inp["q_pos"], m=128, want_lse=True)
+    torch.cuda.synchronize()
+    pairs = [(b, 0) for b in range(w.B)]
+    ref, lref = _oracle_attend_rows(inp, None, 128, w.window, pairs, dense=True)
+    assert_close(out[:, 0], ref, "hca decode")
+    assert np.allclose(lse[:, 0].cpu().numpy(), lref, atol=2e-3, rtol=1e-4)
+
+
+def test_attend_hca_prefill_sampled():
+    w = S.WORKLOADS["hca_prefill_t32768"]
+    inp = S.make_inputs(w, DEV)
+    kv = P.compress(inp["C"], inp["Z"], 128, theta=THETA)
+    out, _, _ = P.hca_attend(inp["q"], kv, inp["win"], inp["sink"], inp["q_pos"], m=128)
+    torch.cuda.synchronize()
+    kv64 = O.compress(f64(inp["C"]), f64(inp["Z"]), 128, theta=THETA)
+    assert_close(kv, kv64, "hca prefill compress")
+    inp["kv"] = _to_dev_bf16(kv64)
+    out2, _, _ = P.hca_attend(inp["q"], inp["kv"], inp["win"], inp["sink"], inp["q_pos"], m=128)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    ts = sorted(set([0, 1, 126, 127, 128, 129, 255, 256, 4095, w.T - 1] + rng.integers(0, w.T, 54).tolist()))
+    pairs = [(0, t) for t in ts]
+    ref, _ = _oracle_attend_rows(inp, None, 128, w.window, pairs, dense=True)
+    assert_close(out2[0, ts], ref, "hca prefill attend (sampled)")
+
+
+@pytest.mark.parametrize("flags", [(True, True), (False, False), (True, False)])
+def test_attend_flags_and_edges(flags):
+    """Small decode-like case: -1 pads, windows clipped at 0, ring wrap, sink, flags off, lse."""
+    qnr, unrot = flags
+    B, H, d, N, k, Wcap = 3, 32, 512, 300, 40, 160
+    q = S.normal_bf16((B, 1, H, d), 11, 1, DEV)
+    kv = S.normal_bf16((B, N, d), 11, 2, DEV)
+    win = S.normal_bf16((B, Wcap, d), 11, 3, DEV)
+    sink = (S.normal_f64((H,), 11, 4) * 3).float().to(DEV)
+    q_pos = torch.tensor([[5], [1199], [1000]], dtype=torch.int32, device=DEV)   # t=5: window clipped
+    rng = np.random.default_rng(0)
+    idx_np = np.full((B, 1, k), -1)
+    for b in range(B):
+        nv = nvis_of(int(q_pos[b, 0]), 4, N)
+        sel = rng.permutation(nv)[:k - 3]
+        idx_np[b, 0, :sel.size] = sel
+    idx = torch.from_numpy(idx_np.astype(np.int32)).to(DEV)
+    out, lse, _ = P.csa_attend(q, kv, idx, win, sink, q_pos, q_norm_rope=qnr, out_unrotate=unrot, want_lse=True)
+    torch.cuda.synchronize()
+    inp = dict(q=q, kv=kv, win=win, sink=sink, q_pos=q_pos)
+    ref, lref = _oracle_attend_rows(inp, idx_np, 4, 128, [(b, 0) for b in range(B)], q_norm_rope=qnr,
+                                    out_unrotate=unrot)
+    if not qnr:   # without the norm the logits are ~sqrt(d) larger: compare the unscaled case loosely
+        assert_close(out[:, 0], ref, "flags off", max_abs=3e-2, rel_l2=2e-2)
+    else:
+        assert_close(out[:, 0], ref, f"flags {flags}")
+        assert np.allclose(lse[:, 0].cpu().numpy(), lref, atol=2e-3, rtol=1e-4)
+
+
+def test_attend_bad_index_is_reported_and_skipped():
+    B, H, d, N, k = 1, 16, 128, 64, 8
+    q = S.normal_bf16((B, 1, H, d), 12, 1, DEV)
+    kv = S.normal_bf16((B, N, d), 12, 2, DEV)
+    win = S.normal_bf16((B, 128, d), 12, 3, DEV)
+    sink = torch.zeros(H, device=DEV)
+    q_pos = torch.tensor([[256]], dtype=torch.int32, device=DEV)
+    good = np.array([[[3, 9, 27, 40, 41, -1, 60, 2]]])
+    bad = good.copy()
+    bad[0, 0, 5] = N + 5
+    out_b, _, ws = P.csa_attend(q, kv, torch.from_numpy(bad.astype(np.int32)).to(DEV), win, sink, q_pos)
+    st, detail = C.csa_read_device_status(ws)
+    assert st == C.CSA_ERR_DEVICE_CHECK and detail == N + 5
+    out_g, _, ws2 = P.csa_attend(q, kv, torch.from_numpy(good.astype(np.int32)).to(DEV), win, sink, q_pos)
+    assert C.csa_read_device_status(ws2)[0] == C.CSA_OK
+    assert torch.equal(out_b, out_g)
+
+
+# ------------------------------------------------------------------------------------------------ whole path
+
+def test_prefill_chain_small_end_to_end():
+    """compress -> index/top-k -> attend on the GPU against the same chain in the oracle (which
+    stores its compressed caches in bf16).  Top-k sets follow the near-tie rule; outputs are
+    compared on every query whose selected set matches the oracle's exactly."""
+    w = S.scaled(S.WORKLOADS["csa_prefill_t65536"], T=2048, N=512)
+    inp = S.make_inputs(w, DEV)
+    kv = P.compress(inp["Ca"], inp["Za"], 4, Cb=inp["Cb"], Zb=inp["Zb"], theta=THETA)
+    kI = P.compress(inp["Ca_I"], inp["Za_I"], 4, Cb=inp["Cb_I"], Zb=inp["Zb_I"], rope=False, rope_dims=0)
+    idx = P.index_topk(inp["qI"], inp["w"], kI, inp["q_pos"], 4, w.k)
+    out, _, _ = P.csa_attend(inp["q"], kv, idx, inp["win"], inp["sink"], inp["q_pos"])
+    torch.cuda.synchronize()
+    kv64 = O.bf16_to_f64(O.bf16_round(_oracle_compress(inp, ("Ca", "Cb", "Za", "Zb"), 4, 512)))
+    kI64 = O.bf16_to_f64(O.bf16_round(_oracle_compress(inp, ("Ca_I", "Cb_I", "Za_I", "Zb_I"), 4, 128, rope=False)))
+    rng = np.random.default_rng(1)
+    ts = sorted(set([0, 3, 4, 127, 128, 2047] + rng.integers(0, w.T, 40).tolist()))
+    qpos = inp["q_pos"].cpu().numpy()
+    sc = O.index_scores(f64(inp["qI"][:, ts]), f64(inp["w"][:, ts]), kI64, [qpos[0, ts]], 4)
+    sel = O.topk_select(sc, [qpos[0, ts]], 4, w.k)
+    gi = idx.cpu().numpy()
+    same = []
+    for j, t in enumerate(ts):
+        nv = nvis_of(t, 4, w.N)
+        n = check_topk_row(gi[0, t], sc[0, j, :nv], nv, w.k, f"chain t{t}")
+        if n == 0:
+            same.append((j, t))
+    assert len(same) >= len(ts) // 2
+    for j, t in same:
+        o, _ = O.attend_query(f64(inp["q"][0, t]), t, kv64[0], sel[0, j], f64(inp["win"][0]), 128,
+                              f64(inp["sink"]), theta=THETA)
+        assert_close(out[0, t], o, f"chain attend t{t}")
+
+
+def test_batch_invariance_and_determinism():
+    """The same sequence decoded alone or inside a batch of 32 gives bit-identical indices and
+    outputs; two runs are bit-identical."""
+    w = S.WORKLOADS["csa_decode_128k_b32"]
+    inp = S.make_inputs(S.scaled(w, B=8, N=8192), DEV)
+    args = (inp["qI"], inp["w"], inp["kI"], inp["q_pos"], 4, 512)
+    idx_a = P.index_topk(*args)
+    idx_b = P.index_topk(*args)
+    out_a, _, _ = P.csa_attend(inp["q"], inp["kv"], idx_a, inp["win"], inp["sink"], inp["q_pos"])
+    out_b, _, _ = P.csa_attend(inp["q"], inp["kv"], idx_a, inp["win"], inp["sink"], inp["q_pos"])
+    assert torch.equal(idx_a, idx_b) and torch.equal(out_a, out_b)
+    b = 5
+    one = lambda t: t[b:b + 1].contiguous()
+    idx_1 = P.index_topk(one(inp["qI"]), one(inp["w"]), one(inp["kI"]), one(inp["q_pos"]), 4, 512)
+    out_1, _, _ = P.csa_attend(one(inp["q"]), one(inp["kv"]), idx_1, one(inp["win"]), inp["sink"], one(inp["q_pos"]))
+    assert torch.equal(idx_1[0], idx_a[b]) and torch.equal(out_1[0], out_a[b])
+
+
+def test_gpu_path_is_causal():
+    """Perturbing every input after position t leaves outputs at positions <= t bit-identical."""
+    w = S.WORKLOADS["tiny_csa_prefill_t2048"]
+    inp = S.make_inputs(w, DEV)
+
+    def run(d):
+        kv = P.compress(d["Ca"], d["Za"], 4, Cb=d["Cb"], Zb=d["Zb"], theta=THETA)
+        kI = P.compress(d["Ca_I"], d["Za_I"], 4, Cb=d["Cb_I"], Zb=d["Zb_I"], rope=False, rope_dims=0)
+        idx = P.index_topk(d["qI"], d["w"], kI, d["q_pos"], 4, w.k)
+        return P.csa_attend(d["q"], kv, idx, d["win"], d["sink"], d["q_pos"])[0]
+
+    ref = run(inp)
+    t = 1234
+    pert = {k: v.clone() for k, v in inp.items()}
+    for k in ("Ca", "Cb", "Za", "Zb", "Ca_I", "Cb_I", "Za_I", "Zb_I", "q", "qI", "w", "win"):
+        x = pert[k]
+        x[:, t + 1:] = (torch.randn_like(x[:, t + 1:].float()) * 3).to(x.dtype)
+    out = run(pert)
+    assert torch.equal(out[:, :t + 1], ref[:, :t + 1])
+    assert not torch.equal(out[:, t + 1:], ref[:, t + 1:])
