@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--workload", default="csa_decode_128k_b32", choices=DECODE_WORKLOADS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--quick", action="store_true",
+                    help="time exactly one block of K steps; no clock sampling, e2e or CPU leg (for profilers)")
     return ap.parse_args()
 
 
@@ -284,6 +286,8 @@ def run_ours(args):
     blocks.append(timed_block(K))
     est = time.time() - tw0
     n_more = max(0, min(50, math.ceil(1.5 / max(est, 1e-3)) - 1))   # keep >= ~1.5 s under the clock sampler
+    if args.quick:
+        n_more = 0
     for _ in range(n_more):
         blocks.append(timed_block(K))
     t_clock1 = time.time()
@@ -320,7 +324,7 @@ def run_ours(args):
         e2e_step()
     torch.cuda.synchronize()
     e_t = []
-    for i in range(K):
+    for i in range(0 if args.quick else K):
         flush.fill_(i & 0xFF)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -328,13 +332,17 @@ def run_ours(args):
         e1.record(stream)
         e_t.append((e0, e1))
     torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e_t) / K
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e_t) / K if e_t else float("nan")
     sampler.stop()
     clocks = sampler.summary(t_clock0, t_clock1)
     if world > 1:
         tt = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = tt.item()
+
+    st_i, _ = C.csa_read_device_status(ws_i, sptr)
+    st_a, _ = C.csa_read_device_status(ws_a, sptr)
+    dev_status = {"csa_index_topk": C.status_string(st_i), "csa_attend": C.status_string(st_a)}
 
     # ---------------- roofline of the dominant call (indexer scores + top-k)
     hbm, peak_kind = peaks()
@@ -348,7 +356,7 @@ def run_ours(args):
     value = world * B / (t_step * 1e-3)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
         host = host_copy(inp, 0, B)
         n, dt = oracle_sample(w, host, B, args.cpu_seconds)
         cpu = {"value": n / dt, "unit": "query-tok/s", "cores": blas_threads(), "kind": "oracle",
@@ -375,6 +383,7 @@ def run_ours(args):
         "e2e": {"value": world * B / (e2e_ms * 1e-3), "unit": "query-tok/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
+        "device_status": dev_status,
         "clocks": clocks,
     }
     print(json.dumps(line))

@@ -179,7 +179,10 @@ typedef struct {
   unsigned flags;          /* CSA_ATTEND_* */
 } csa_attend_desc;
 
+/* Workspace bytes for csa_attend / hca_attend with this descriptor (0 if it is invalid).  The two
+ * differ: a dense HCA query visits up to N + window rows, a CSA query k + window. */
 size_t csa_attend_workspace(const csa_attend_desc* desc);
+size_t hca_attend_workspace(const csa_attend_desc* desc);
 
 csa_status csa_attend(const csa_attend_desc* desc, const void* q, const void* kv,
                       const int32_t* idx, const void* win, const float* sink,

@@ -35,7 +35,7 @@ CSA_ATTEND_OUT_UNROTATE = 2
 CSA_ATTEND_WRITE_LSE = 4
 
 EXPORTS = ("csa_compress", "csa_index_topk_workspace", "csa_index_topk", "csa_attend_workspace",
-           "csa_attend", "hca_attend", "csa_read_device_status", "csa_clear_device_status",
+           "hca_attend_workspace", "csa_attend", "hca_attend", "csa_read_device_status", "csa_clear_device_status",
            "csa_status_string", "csa_launch_count")
 
 
@@ -76,6 +76,8 @@ def _load() -> ctypes.CDLL:
     lib.csa_index_topk.restype = c_int
     lib.csa_attend_workspace.argtypes = [POINTER(csa_attend_desc)]
     lib.csa_attend_workspace.restype = c_size_t
+    lib.hca_attend_workspace.argtypes = [POINTER(csa_attend_desc)]
+    lib.hca_attend_workspace.restype = c_size_t
     lib.csa_attend.argtypes = [POINTER(csa_attend_desc), vp, vp, vp, vp, vp, vp, vp, vp, vp, c_size_t, vp]
     lib.csa_attend.restype = c_int
     lib.hca_attend.argtypes = [POINTER(csa_attend_desc), vp, vp, vp, vp, vp, vp, vp, vp, c_size_t, vp]
@@ -155,6 +157,10 @@ def csa_index_topk(desc, qI, w, kI, kI_scale, q_pos, idx_out, score_out, workspa
 
 def csa_attend_workspace(desc) -> int:
     return lib.csa_attend_workspace(ctypes.byref(desc))
+
+
+def hca_attend_workspace(desc) -> int:
+    return lib.hca_attend_workspace(ctypes.byref(desc))
 
 
 def csa_attend(desc, q, kv, idx, win, sink, q_pos, out, lse, workspace, ws_bytes=None, stream=None) -> int:

@@ -247,6 +247,11 @@ size_t csa_attend_workspace(const csa_attend_desc* d) {
   return csa::kStatusBytes + plan_attend(d, true).partial_bytes;
 }
 
+size_t hca_attend_workspace(const csa_attend_desc* d) {
+  if (!attend_desc_ok(d, false)) return 0;
+  return csa::kStatusBytes + plan_attend(d, false).partial_bytes;
+}
+
 csa_status csa_attend(const csa_attend_desc* d, const void* q, const void* kv, const int32_t* idx,
                       const void* win, const float* sink, const int32_t* q_pos, void* out, float* lse,
                       void* ws, size_t ws_bytes, csa_stream_t stream) {

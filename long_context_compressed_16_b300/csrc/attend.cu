@@ -32,14 +32,19 @@ struct AttnCfg {
   static constexpr int KS = D + 8;
   static constexpr int PS = CK + 8;
   static constexpr int ROWB = FP8 ? CSA_FP8_MIXED_ROW_BYTES : D * 2;   // global row bytes
+  // FP8 rows: 8 blocks of 64 dims (7 e4m3 blocks with their own scale + the bf16 RoPE block)
+  static constexpr int NB = FP8 ? D / 64 : 1;
+  static constexpr int QPARTS = FP8 ? 2 : 1;                  // FP8: q_hat = hi + lo (two bf16)
   static constexpr size_t q_off = 0;
-  static constexpr size_t k_off = q_off + size_t(HG) * QS * 2;
+  static constexpr size_t k_off = q_off + size_t(QPARTS) * HG * QS * 2;
   static constexpr size_t st_off = k_off + size_t(2) * CK * KS * 2;
   static constexpr size_t p_off = st_off + (FP8 ? size_t(2) * CK * ROWB : 0);
-  static constexpr size_t red_off = p_off + size_t(HG) * PS * 2;
+  static constexpr size_t sc_off = p_off + size_t(NB) * HG * PS * 2;
+  static constexpr size_t red_off = sc_off + (FP8 ? size_t(2) * CK * NB * 4 : 0);
   static constexpr size_t lsum_off = red_off + size_t(HG) * 4 * 4;
   static constexpr size_t ptr_off = lsum_off + size_t(HG) * 4 * 4;
   static constexpr size_t smem = ptr_off + size_t(2) * CK * 8;
+  static_assert(!FP8 || (NG == 1 && D == 512), "the FP8 cache path runs 16 heads per CTA, d = 512");
 };
 
 __device__ __forceinline__ int slot_row(const AttendArgs& a, int b, long long qi, int t, int Kq, int s,
@@ -73,6 +78,7 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
   __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(smem + C::k_off);
   unsigned char* St = smem + C::st_off;
   __nv_bfloat16* Ps = reinterpret_cast<__nv_bfloat16*>(smem + C::p_off);
+  float* bscale = reinterpret_cast<float*>(smem + C::sc_off);      // FP8: [2][CK][NB] row block scales
   float* redmax = reinterpret_cast<float*>(smem + C::red_off);
   float* lsum = reinterpret_cast<float*>(smem + C::lsum_off);
   const unsigned char** rowptr = reinterpret_cast<const unsigned char**>(smem + C::ptr_off);
@@ -147,6 +153,15 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
           u.z = pack_bf16x2(v[c + 4], v[c + 5]);
           u.w = pack_bf16x2(v[c + 6], v[c + 7]);
           *reinterpret_cast<uint4*>(dst + c) = u;
+          if constexpr (FP8) {
+            // residual part: q_hat - bf16(q_hat), so that hi + lo carries ~16 significant bits
+            uint4 r;
+            r.x = pack_bf16x2(v[c + 0] - bf16lo(u.x), v[c + 1] - bf16hi(u.x));
+            r.y = pack_bf16x2(v[c + 2] - bf16lo(u.y), v[c + 3] - bf16hi(u.y));
+            r.z = pack_bf16x2(v[c + 4] - bf16lo(u.z), v[c + 5] - bf16hi(u.z));
+            r.w = pack_bf16x2(v[c + 6] - bf16lo(u.w), v[c + 7] - bf16hi(u.w));
+            *reinterpret_cast<uint4*>(dst + HG * QS + c) = r;
+          }
         }
       } else {
         uint2 u;
@@ -227,15 +242,22 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
     }
     __syncthreads();                                   // (B)
     if (FP8) {
-      // widen entry rows: dims [0,448) e4m3 * block scale, dims [448,512) bf16 copy
+      // entry rows: e4m3 codes -> bf16 (exact) and the seven block scales to shared memory (the
+      // RoPE block keeps scale 1); window rows arrived as bf16 and take scale 1 in every block
       for (int idx = tid; idx < CK * (D / 8); idx += C::THREADS) {
         const int r = idx / (D / 8), p8 = idx % (D / 8);
         const unsigned char* p = rowptr[buf * CK + r];
-        if ((reinterpret_cast<uintptr_t>(p) & 1u) != 0) continue;     // window row, already bf16
+        const bool isw = (reinterpret_cast<uintptr_t>(p) & 1u) != 0;
         const unsigned char* row = St + (buf * CK + r) * C::ROWB;
+        if ((p8 & 7) == 0) {
+          const int blk = p8 >> 3;
+          float sc = 1.f;
+          if (!isw && blk < 7) sc = (p != nullptr) ? *reinterpret_cast<const float*>(row + 576 + blk * 4) : 0.f;
+          bscale[(buf * CK + r) * C::NB + blk] = sc;
+        }
+        if (isw) continue;
         __nv_bfloat16* kd = Ks + (buf * CK + r) * KS + p8 * 8;
         if (p8 < 56) {
-          const float sc = *reinterpret_cast<const float*>(row + 576 + (p8 >> 3) * 4);
           const uint2 v = *reinterpret_cast<const uint2*>(row + p8 * 8);
           float f[8];
           e4m3x2_to_float2(static_cast<uint16_t>(v.x & 0xFFFF), f[0], f[1]);
@@ -243,8 +265,8 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
           e4m3x2_to_float2(static_cast<uint16_t>(v.y & 0xFFFF), f[4], f[5]);
           e4m3x2_to_float2(static_cast<uint16_t>(v.y >> 16), f[6], f[7]);
           uint4 o;
-          o.x = pack_bf16x2(f[0] * sc, f[1] * sc); o.y = pack_bf16x2(f[2] * sc, f[3] * sc);
-          o.z = pack_bf16x2(f[4] * sc, f[5] * sc); o.w = pack_bf16x2(f[6] * sc, f[7] * sc);
+          o.x = pack_bf16x2(f[0], f[1]); o.y = pack_bf16x2(f[2], f[3]);
+          o.z = pack_bf16x2(f[4], f[5]); o.w = pack_bf16x2(f[6], f[7]);
           *reinterpret_cast<uint4*>(kd) = o;
         } else {
           *reinterpret_cast<uint4*>(kd) = *reinterpret_cast<const uint4*>(row + 448 + (p8 - 56) * 16);
@@ -260,24 +282,54 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
     for (int n = 0; n < NKT; ++n)
 #pragma unroll
       for (int e = 0; e < 4; ++e) sacc[n][e] = 0.f;
+    if constexpr (!FP8) {
 #pragma unroll 4
-    for (int ks = 0; ks < D / 16; ++ks) {
-      uint32_t af[4];
-      ldmatrix_x4(af[0], af[1], af[2], af[3],
-                  smem_u32(Qs + (16 * g + (lane & 15)) * QS + ks * 16 + (lane >> 4) * 8));
-      if (NKT == 2) {
-        uint32_t b0, b1, b2, b3;
-        const int key = wq * 16 + (lane >> 4) * 8 + (lane & 7);
-        ldmatrix_x4(b0, b1, b2, b3, smem_u32(Kb + key * KS + ks * 16 + ((lane >> 3) & 1) * 8));
-        const uint32_t bb0[2] = {b0, b1}, bb1[2] = {b2, b3};
-        mma_bf16_16816(sacc[0], af, bb0);
-        mma_bf16_16816(sacc[NKT - 1], af, bb1);
-      } else {
-        uint32_t b0, b1;
-        const int key = wq * 8 + (lane & 7);
-        ldmatrix_x2(b0, b1, smem_u32(Kb + key * KS + ks * 16 + ((lane >> 3) & 1) * 8));
-        const uint32_t bb0[2] = {b0, b1};
-        mma_bf16_16816(sacc[0], af, bb0);
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t af[4];
+        ldmatrix_x4(af[0], af[1], af[2], af[3],
+                    smem_u32(Qs + (16 * g + (lane & 15)) * QS + ks * 16 + (lane >> 4) * 8));
+        if (NKT == 2) {
+          uint32_t b0, b1, b2, b3;
+          const int key = wq * 16 + (lane >> 4) * 8 + (lane & 7);
+          ldmatrix_x4(b0, b1, b2, b3, smem_u32(Kb + key * KS + ks * 16 + ((lane >> 3) & 1) * 8));
+          const uint32_t bb0[2] = {b0, b1}, bb1[2] = {b2, b3};
+          mma_bf16_16816(sacc[0], af, bb0);
+          mma_bf16_16816(sacc[NKT - 1], af, bb1);
+        } else {
+          uint32_t b0, b1;
+          const int key = wq * 8 + (lane & 7);
+          ldmatrix_x2(b0, b1, smem_u32(Kb + key * KS + ks * 16 + ((lane >> 3) & 1) * 8));
+          const uint32_t bb0[2] = {b0, b1};
+          mma_bf16_16816(sacc[0], af, bb0);
+        }
+      }
+    } else {
+      // z = sum_b scale_{j,b} * (q_hat_b . code_{j,b}), q_hat = hi + lo, each block in fp32
+      const float* scb = bscale + buf * CK * C::NB;
+      const int kc0 = wq * 8 + 2 * (lane & 3);
+#pragma unroll 1
+      for (int blk = 0; blk < C::NB; ++blk) {
+        float pacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kq = 0; kq < 4; ++kq) {
+          const int ks = blk * 4 + kq;
+          uint32_t ah[4], al[4];
+          ldmatrix_x4(ah[0], ah[1], ah[2], ah[3],
+                      smem_u32(Qs + (lane & 15) * QS + ks * 16 + (lane >> 4) * 8));
+          ldmatrix_x4(al[0], al[1], al[2], al[3],
+                      smem_u32(Qs + HG * QS + (lane & 15) * QS + ks * 16 + (lane >> 4) * 8));
+          uint32_t b0, b1;
+          const int key = wq * 8 + (lane & 7);
+          ldmatrix_x2(b0, b1, smem_u32(Kb + key * KS + ks * 16 + ((lane >> 3) & 1) * 8));
+          const uint32_t bb0[2] = {b0, b1};
+          mma_bf16_16816(pacc, ah, bb0);
+          mma_bf16_16816(pacc, al, bb0);
+        }
+        const float s0 = scb[kc0 * C::NB + blk], s1 = scb[(kc0 + 1) * C::NB + blk];
+        sacc[0][0] = fmaf(pacc[0], s0, sacc[0][0]);
+        sacc[0][1] = fmaf(pacc[1], s1, sacc[0][1]);
+        sacc[0][2] = fmaf(pacc[2], s0, sacc[0][2]);
+        sacc[0][3] = fmaf(pacc[3], s1, sacc[0][3]);
       }
     }
     // ---- mask, scale to log2 domain, row max over this warp's keys
@@ -325,8 +377,19 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
       psum[1] += p2 + p3;
       const int key = wq * 8 * NKT + n * 8 + 2 * (lane & 3);
       const int hr = 16 * g + (lane >> 2);
-      *reinterpret_cast<uint32_t*>(Ps + hr * PS + key) = pack_bf16x2(p0, p1);
-      *reinterpret_cast<uint32_t*>(Ps + (hr + 8) * PS + key) = pack_bf16x2(p2, p3);
+      if constexpr (!FP8) {
+        *reinterpret_cast<uint32_t*>(Ps + hr * PS + key) = pack_bf16x2(p0, p1);
+        *reinterpret_cast<uint32_t*>(Ps + (hr + 8) * PS + key) = pack_bf16x2(p2, p3);
+      } else {
+        const float* scb = bscale + buf * CK * C::NB;
+#pragma unroll
+        for (int blk = 0; blk < C::NB; ++blk) {
+          const float s0 = scb[key * C::NB + blk], s1 = scb[(key + 1) * C::NB + blk];
+          __nv_bfloat16* pb = Ps + blk * HG * PS;
+          *reinterpret_cast<uint32_t*>(pb + hr * PS + key) = pack_bf16x2(p0 * s0, p1 * s1);
+          *reinterpret_cast<uint32_t*>(pb + (hr + 8) * PS + key) = pack_bf16x2(p2 * s0, p3 * s1);
+        }
+      }
     }
     l_run[0] = l_run[0] * alpha[0] + psum[0];
     l_run[1] = l_run[1] * alpha[1] + psum[1];
@@ -339,9 +402,15 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
     // ---- O += P V for heads [16g,16g+16) x dims [wq*D/4, +D/4)
 #pragma unroll
     for (int kk = 0; kk < CK / 16; ++kk) {
-      uint32_t pa[4];
+      uint32_t pa[4], pb2[4] = {0u, 0u, 0u, 0u};
+      const __nv_bfloat16* P0 = FP8 ? Ps + (wq * 2) * HG * PS : Ps;
       ldmatrix_x4(pa[0], pa[1], pa[2], pa[3],
-                  smem_u32(Ps + (16 * g + (lane & 15)) * PS + kk * 16 + (lane >> 4) * 8));
+                  smem_u32(P0 + (16 * g + (lane & 15)) * PS + kk * 16 + (lane >> 4) * 8));
+      if constexpr (FP8) {
+        const __nv_bfloat16* P1 = Ps + (wq * 2 + 1) * HG * PS;
+        ldmatrix_x4(pb2[0], pb2[1], pb2[2], pb2[3],
+                    smem_u32(P1 + (16 * g + (lane & 15)) * PS + kk * 16 + (lane >> 4) * 8));
+      }
 #pragma unroll
       for (int np = 0; np < NO / 2; ++np) {
         uint32_t v0, v1, v2, v3;
@@ -349,8 +418,9 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
         const int dim = wq * (D / 4) + np * 16 + (lane >> 4) * 8;
         ldmatrix_x4_trans(v0, v1, v2, v3, smem_u32(Kb + key * KS + dim));
         const uint32_t vb0[2] = {v0, v1}, vb1[2] = {v2, v3};
-        mma_bf16_16816(oacc[2 * np], pa, vb0);
-        mma_bf16_16816(oacc[2 * np + 1], pa, vb1);
+        const uint32_t* A = (FP8 && np >= NO / 4) ? pb2 : pa;   // FP8: dims of the warp's second block
+        mma_bf16_16816(oacc[2 * np], A, vb0);
+        mma_bf16_16816(oacc[2 * np + 1], A, vb1);
       }
     }
   }
@@ -505,7 +575,7 @@ cudaError_t launch_attend(const AttendArgs& a, cudaStream_t s, int* launches) {
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const bool wide = (a.H % 64 == 0) && (static_cast<long long>(Q) * a.n_splits * (a.H / 64) >= 2LL * sms);
   if (a.d == 512) {
-    if (a.fp8) return wide ? launch_t<512, 4, true>(a, s, launches) : launch_t<512, 1, true>(a, s, launches);
+    if (a.fp8) return launch_t<512, 1, true>(a, s, launches);
     return wide ? launch_t<512, 4, false>(a, s, launches) : launch_t<512, 1, false>(a, s, launches);
   }
   if (a.d == 128 && !a.fp8) {

@@ -93,9 +93,18 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk(TopkArgs a, int CS, int cap
     uint32_t* h = hist + (p & 1) * 2048;
     for (int i = tid; i < 2048; i += TK_THREADS) h[i] = 0;
     __syncthreads();
-    for (int i = tid; i < L; i += TK_THREADS) {
-      const uint32_t kk = keys[i];
-      if ((kk & pmask) == prefix) atomicAdd(&h[(kk >> shift) & (nb - 1)], 1u);
+    // warp-aggregated histogram: the scores of one query crowd into a few leading-digit bins, so
+    // lanes that hit the same bin are merged with a match before one atomic per distinct bin
+    const int rounds = (L + TK_THREADS - 1) / TK_THREADS;
+    for (int rd = 0; rd < rounds; ++rd) {
+      const int i = rd * TK_THREADS + tid;
+      uint32_t bin = 0xFFFFFFFFu;
+      if (i < L) {
+        const uint32_t kk = keys[i];
+        if ((kk & pmask) == prefix) bin = (kk >> shift) & static_cast<uint32_t>(nb - 1);
+      }
+      const unsigned grp = __match_any_sync(0xffffffffu, bin);
+      if (bin != 0xFFFFFFFFu && (tid & 31) == __ffs(grp) - 1) atomicAdd(&h[bin], static_cast<uint32_t>(__popc(grp)));
     }
     cluster.sync();
     // thread tid owns the bins at descending positions 2*tid and 2*tid+1

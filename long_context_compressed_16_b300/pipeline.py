@@ -80,7 +80,7 @@ def _attend(csa_mode, q, kv, idx, win, sink, q_pos, m, window, rope_dims, theta,
     if want_lse and lse is None:
         lse = torch.empty((B, Tq, H), dtype=torch.float32, device=q.device)
     if workspace is None:
-        workspace = _ws(C.csa_attend_workspace(desc), q.device)
+        workspace = _ws(C.csa_attend_workspace(desc) if csa_mode else C.hca_attend_workspace(desc), q.device)
     if csa_mode:
         st = C.csa_attend(desc, q, kv, idx, win, sink, q_pos, out, lse, workspace, stream=stream)
     else:
