@@ -103,6 +103,7 @@ csa_status attend_common(const csa_attend_desc* d, bool csa_mode, const void* q,
   const long long Q = static_cast<long long>(d->B) * d->Tq;
   if (!ws) return CSA_ERR_WORKSPACE;
   const AttendPlan plan = plan_attend(d, csa_mode);
+  if (plan.n_splits > 65535) return CSA_ERR_UNSUPPORTED;
   if (ws_bytes < csa::kStatusBytes + plan.partial_bytes) return CSA_ERR_WORKSPACE;
   if (!aligned16(ws)) return CSA_ERR_INVALID_ARG;
   if (Q == 0) return CSA_OK;

@@ -6,8 +6,8 @@
 // Per query the candidate rows are laid out as "slots": [0, K_q) entry slots (the idx row, or
 // entries 0..N_vis-1 for HCA) followed by `window` window slots (positions t-window+1 .. t).
 // A CTA owns one query, a group of 16*NG heads and one split of the slot range.  Rows are
-// gathered CK at a time with cp.async into a double-buffered shared-memory tile (FP8 rows are
-// widened to bf16 there); the heads x keys logits and the heads x d output run on the tensor
+// gathered CK at a time with cp.async into a double-buffered shared-memory tile; the heads x keys
+// logits and the heads x d output run on the tensor
 // cores; the softmax is online in the log2 domain and the sink joins the normaliser at the end.
 // Split boundaries sit at fixed multiples of the split size in slot space, never depending on
 // the batch, and splits are merged by a second kernel in fixed order (batch-invariant decode).
@@ -32,9 +32,11 @@ struct AttnCfg {
   static constexpr int KS = D + 8;
   static constexpr int PS = CK + 8;
   static constexpr int ROWB = FP8 ? CSA_FP8_MIXED_ROW_BYTES : D * 2;   // global row bytes
-  // FP8 rows: 8 blocks of 64 dims (7 e4m3 blocks with their own scale + the bf16 RoPE block)
+  // FP8 rows: 8 blocks of 64 dims (7 e4m3 blocks with their own scale + the bf16 RoPE block).
+  // That path multiplies in fp16: e4m3 codes and the bf16 parts are exact in fp16, the query is
+  // split into fp16 hi + lo, and block scales are applied in fp32.
   static constexpr int NB = FP8 ? D / 64 : 1;
-  static constexpr int QPARTS = FP8 ? 2 : 1;                  // FP8: q_hat = hi + lo (two bf16)
+  static constexpr int QPARTS = FP8 ? 2 : 1;
   static constexpr size_t q_off = 0;
   static constexpr size_t k_off = q_off + size_t(QPARTS) * HG * QS * 2;
   static constexpr size_t st_off = k_off + size_t(2) * CK * KS * 2;
@@ -85,9 +87,9 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
 
   const int tid = threadIdx.x, lane = tid & 31, wall = tid >> 5;
   const int g = wall >> 2, wq = wall & 3;
-  const int split = blockIdx.x;
+  const int split = blockIdx.z;
   const int h0 = blockIdx.y * HG;
-  const long long qi = blockIdx.z;
+  const long long qi = blockIdx.x;
   const int b = static_cast<int>(qi / a.Tq);
   const int t = a.q_pos[qi];
   const int nvis = n_visible(t, a.m, a.N);
@@ -144,7 +146,21 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
         }
       }
       __nv_bfloat16* dst = Qs + hl * QS + lane * E;
-      if constexpr (E >= 8) {
+      if constexpr (FP8) {
+#pragma unroll
+        for (int c = 0; c < E; c += 8) {
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int p2 = 0; p2 < 4; ++p2) {
+            const float x0 = v[c + 2 * p2], x1 = v[c + 2 * p2 + 1];
+            hw[p2] = pack_half2(x0, x1);
+            const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hw[p2]));
+            lw[p2] = pack_half2(x0 - hf.x, x1 - hf.y);        // residual: hi + lo ~ 22 significant bits
+          }
+          *reinterpret_cast<uint4*>(dst + c) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(dst + HG * QS + c) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+      } else if constexpr (E >= 8) {
 #pragma unroll
         for (int c = 0; c < E; c += 8) {
           uint4 u;
@@ -153,15 +169,6 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
           u.z = pack_bf16x2(v[c + 4], v[c + 5]);
           u.w = pack_bf16x2(v[c + 6], v[c + 7]);
           *reinterpret_cast<uint4*>(dst + c) = u;
-          if constexpr (FP8) {
-            // residual part: q_hat - bf16(q_hat), so that hi + lo carries ~16 significant bits
-            uint4 r;
-            r.x = pack_bf16x2(v[c + 0] - bf16lo(u.x), v[c + 1] - bf16hi(u.x));
-            r.y = pack_bf16x2(v[c + 2] - bf16lo(u.y), v[c + 3] - bf16hi(u.y));
-            r.z = pack_bf16x2(v[c + 4] - bf16lo(u.z), v[c + 5] - bf16hi(u.z));
-            r.w = pack_bf16x2(v[c + 6] - bf16lo(u.w), v[c + 7] - bf16hi(u.w));
-            *reinterpret_cast<uint4*>(dst + HG * QS + c) = r;
-          }
         }
       } else {
         uint2 u;
@@ -242,8 +249,9 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
     }
     __syncthreads();                                   // (B)
     if (FP8) {
-      // entry rows: e4m3 codes -> bf16 (exact) and the seven block scales to shared memory (the
-      // RoPE block keeps scale 1); window rows arrived as bf16 and take scale 1 in every block
+      // fp16 tile: entry rows take their e4m3 codes (exact) and the bf16 RoPE block; window rows,
+      // cp.async'ed as bf16, are converted in place; block scales go to shared memory (window
+      // rows and the RoPE block use scale 1)
       for (int idx = tid; idx < CK * (D / 8); idx += C::THREADS) {
         const int r = idx / (D / 8), p8 = idx % (D / 8);
         const unsigned char* p = rowptr[buf * CK + r];
@@ -255,22 +263,19 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
           if (!isw && blk < 7) sc = (p != nullptr) ? *reinterpret_cast<const float*>(row + 576 + blk * 4) : 0.f;
           bscale[(buf * CK + r) * C::NB + blk] = sc;
         }
-        if (isw) continue;
         __nv_bfloat16* kd = Ks + (buf * CK + r) * KS + p8 * 8;
-        if (p8 < 56) {
-          const uint2 v = *reinterpret_cast<const uint2*>(row + p8 * 8);
-          float f[8];
-          e4m3x2_to_float2(static_cast<uint16_t>(v.x & 0xFFFF), f[0], f[1]);
-          e4m3x2_to_float2(static_cast<uint16_t>(v.x >> 16), f[2], f[3]);
-          e4m3x2_to_float2(static_cast<uint16_t>(v.y & 0xFFFF), f[4], f[5]);
-          e4m3x2_to_float2(static_cast<uint16_t>(v.y >> 16), f[6], f[7]);
-          uint4 o;
-          o.x = pack_bf16x2(f[0], f[1]); o.y = pack_bf16x2(f[2], f[3]);
-          o.z = pack_bf16x2(f[4], f[5]); o.w = pack_bf16x2(f[6], f[7]);
-          *reinterpret_cast<uint4*>(kd) = o;
+        uint4 src;
+        if (isw || p8 >= 56) {
+          src = isw ? *reinterpret_cast<const uint4*>(kd)
+                    : *reinterpret_cast<const uint4*>(row + 448 + (p8 - 56) * 16);
+          src = make_uint4(pack_half2(bf16lo(src.x), bf16hi(src.x)), pack_half2(bf16lo(src.y), bf16hi(src.y)),
+                           pack_half2(bf16lo(src.z), bf16hi(src.z)), pack_half2(bf16lo(src.w), bf16hi(src.w)));
         } else {
-          *reinterpret_cast<uint4*>(kd) = *reinterpret_cast<const uint4*>(row + 448 + (p8 - 56) * 16);
+          const uint2 v = *reinterpret_cast<const uint2*>(row + p8 * 8);
+          src = make_uint4(e4m3x2_to_half2(static_cast<uint16_t>(v.x & 0xFFFF)), e4m3x2_to_half2(static_cast<uint16_t>(v.x >> 16)),
+                           e4m3x2_to_half2(static_cast<uint16_t>(v.y & 0xFFFF)), e4m3x2_to_half2(static_cast<uint16_t>(v.y >> 16)));
         }
+        *reinterpret_cast<uint4*>(kd) = src;
       }
       __syncthreads();                                 // (B')
     }
@@ -304,7 +309,7 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
         }
       }
     } else {
-      // z = sum_b scale_{j,b} * (q_hat_b . code_{j,b}), q_hat = hi + lo, each block in fp32
+      // z = sum_b scale_{j,b} * (q_hat_b . code_{j,b}), q_hat = hi + lo (fp16), each block in fp32
       const float* scb = bscale + buf * CK * C::NB;
       const int kc0 = wq * 8 + 2 * (lane & 3);
 #pragma unroll 1
@@ -322,8 +327,8 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
           const int key = wq * 8 + (lane & 7);
           ldmatrix_x2(b0, b1, smem_u32(Kb + key * KS + ks * 16 + ((lane >> 3) & 1) * 8));
           const uint32_t bb0[2] = {b0, b1};
-          mma_bf16_16816(pacc, ah, bb0);
-          mma_bf16_16816(pacc, al, bb0);
+          mma_f16_16816(pacc, ah, bb0);
+          mma_f16_16816(pacc, al, bb0);
         }
         const float s0 = scb[kc0 * C::NB + blk], s1 = scb[(kc0 + 1) * C::NB + blk];
         sacc[0][0] = fmaf(pacc[0], s0, sacc[0][0]);
@@ -386,8 +391,9 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
         for (int blk = 0; blk < C::NB; ++blk) {
           const float s0 = scb[key * C::NB + blk], s1 = scb[(key + 1) * C::NB + blk];
           __nv_bfloat16* pb = Ps + blk * HG * PS;
-          *reinterpret_cast<uint32_t*>(pb + hr * PS + key) = pack_bf16x2(p0 * s0, p1 * s1);
-          *reinterpret_cast<uint32_t*>(pb + (hr + 8) * PS + key) = pack_bf16x2(p2 * s0, p3 * s1);
+          // p * scale * 2^8 stays in fp16's normal range; the 2^-8 is taken back after the loop
+          *reinterpret_cast<uint32_t*>(pb + hr * PS + key) = pack_half2(p0 * s0 * 256.f, p1 * s1 * 256.f);
+          *reinterpret_cast<uint32_t*>(pb + (hr + 8) * PS + key) = pack_half2(p2 * s0 * 256.f, p3 * s1 * 256.f);
         }
       }
     }
@@ -418,11 +424,22 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
         const int dim = wq * (D / 4) + np * 16 + (lane >> 4) * 8;
         ldmatrix_x4_trans(v0, v1, v2, v3, smem_u32(Kb + key * KS + dim));
         const uint32_t vb0[2] = {v0, v1}, vb1[2] = {v2, v3};
-        const uint32_t* A = (FP8 && np >= NO / 4) ? pb2 : pa;   // FP8: dims of the warp's second block
-        mma_bf16_16816(oacc[2 * np], A, vb0);
-        mma_bf16_16816(oacc[2 * np + 1], A, vb1);
+        if constexpr (FP8) {
+          const uint32_t* A = (np >= NO / 4) ? pb2 : pa;   // dims of the warp's second block
+          mma_f16_16816(oacc[2 * np], A, vb0);
+          mma_f16_16816(oacc[2 * np + 1], A, vb1);
+        } else {
+          mma_bf16_16816(oacc[2 * np], pa, vb0);
+          mma_bf16_16816(oacc[2 * np + 1], pa, vb1);
+        }
       }
     }
+  }
+  if constexpr (FP8) {
+#pragma unroll
+    for (int i = 0; i < NO; ++i)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) oacc[i][c] *= (1.0f / 256.0f);
   }
 
   // ---------------- epilogue: total row sums, sink, normalise / write partials
@@ -549,7 +566,7 @@ cudaError_t launch_t(const AttendArgs& a, cudaStream_t s, int* launches) {
                                        static_cast<int>(C::smem));
   if (e != cudaSuccess) return e;
   const int Q = a.B * a.Tq;
-  dim3 grid(a.n_splits, a.H / C::HG, Q);
+  dim3 grid(Q, a.H / C::HG, a.n_splits);
   k_attend<D, NG, FP8><<<grid, C::THREADS, C::smem, s>>>(a);
   ++*launches;
   e = cudaGetLastError();

@@ -175,7 +175,8 @@ __global__ void __launch_bounds__(TK_THREADS) k_topk(TopkArgs a, int CS, int cap
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s, int* launches) {
   if (a.q_count == 0) return cudaSuccess;
-  int CS = (a.N + 4095) / 4096;
+  // one CTA holds up to 32768 candidates in shared memory; longer rows spread over a cluster
+  int CS = (a.N + kMaxSlice - 1) / kMaxSlice;
   if (CS < 1) CS = 1;
   if (CS > 8) CS = 8;
   const int cap = ((a.N + CS - 1) / CS + 3) & ~3;   // keeps the 64-bit scan slots 8-byte aligned
