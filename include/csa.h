@@ -1,7 +1,7 @@
 /*
  * csa.h -- C ABI of the B300 (sm_103a) library for DeepSeek-V4 hybrid compressed attention.
  *
- * The method (as explained on "DeepSeek V4 技术大全", wineandchord.com, chapter "Hybrid
+ * The method (as explained on "DeepSeek V4 模型技术大全", wineandchord.com, chapter "Hybrid
  * Attention", and "DeepSeek-V4 技术解析", chang-wenbin.github.io, section 2.1):
  *   CSA  compress every m = 4 tokens into one shared K=V entry (softmax-gated, overlapped over
  *        2m rows), RMSNorm it and rotate its last 64 dims; score every closed entry with the
@@ -65,7 +65,7 @@ typedef enum {
 /* ---------------------------------------------------------------------------------------------
  * csa_compress -- token-level compressor (CSA overlapped or HCA single-stream).
  *
- * Source: "DeepSeek V4 技术大全", CSA path, the Softmax_row and C^Comp equations (overlapped
+ * Source: "DeepSeek V4 模型技术大全", CSA path, the Softmax_row and C^Comp equations (overlapped
  * 2m rows with biases B^a, B^b), and the HCA path, its S / C^Comp equations (m' rows, bias B);
  * component table rows "query / KV RMSNorm" and "partial RoPE" (RMSNorm eps 1e-6, RoPE on the
  * last 64 dims, compressed-branch base 160000).
@@ -106,7 +106,7 @@ csa_status csa_compress(const csa_compress_desc* desc, const void* Ca, const voi
 /* ---------------------------------------------------------------------------------------------
  * csa_index_topk -- lightning-indexer scores and per-query top-k selection.
  *
- * Source: "DeepSeek V4 技术大全", CSA path, the I_{t,s} and TopK equations:
+ * Source: "DeepSeek V4 模型技术大全", CSA path, the I_{t,s} and TopK equations:
  *   I_{t,s} = sum_h w_{t,h} * ReLU(q^I_{t,h} . K^I_s)  for s < floor((t+1)/m)
  *   idx_t   = TopK_k { I_{t,s} }
  * Ties go to the smaller s.  When fewer than k entries are visible, all are returned and the
@@ -139,7 +139,7 @@ csa_status csa_index_topk(const csa_index_desc* desc, const void* qI, const floa
 /* ---------------------------------------------------------------------------------------------
  * csa_attend / hca_attend -- shared K=V multi-query attention with SWA window and sink.
  *
- * Source: "DeepSeek V4 技术大全", component table rows "Shared K=V MQA", "query / KV RMSNorm",
+ * Source: "DeepSeek V4 模型技术大全", component table rows "Shared K=V MQA", "query / KV RMSNorm",
  * "partial RoPE", "attention sink" (p = exp(z) / (exp(a_h) + sum exp(z))), "SWA"
  * (W_t = {t-127 .. t}), the HCA visibility set j < floor((t+1)/m'), and the implementation
  * note that the core-attention output gets a reverse rotation.

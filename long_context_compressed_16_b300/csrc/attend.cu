@@ -1,6 +1,6 @@
 // Shared K=V multi-query attention over the selected (CSA) or all closed (HCA) compressed entries
 // plus the uncompressed SWA window, with a per-head sink logit and the reverse rotation of the
-// output's RoPE dims ("DeepSeek V4 技术大全", component table rows Shared K=V MQA, query/KV
+// output's RoPE dims ("DeepSeek V4 模型技术大全", component table rows Shared K=V MQA, query/KV
 // RMSNorm, partial RoPE, attention sink, SWA; the HCA visibility set; the reverse-rotation note).
 //
 // Per query the candidate rows are laid out as "slots": [0, K_q) entry slots (the idx row, or

@@ -1,5 +1,5 @@
 // Token-level compressor: softmax-gated weighted sum over m (HCA) or 2m overlapped (CSA) rows,
-// fused with RMSNorm and partial RoPE.  ("DeepSeek V4 技术大全", CSA path, Softmax_row and
+// fused with RMSNorm and partial RoPE.  ("DeepSeek V4 模型技术大全", CSA path, Softmax_row and
 // C^Comp equations; HCA path, S and C^Comp equations.)
 //
 // Pure HBM stream: every input row is read exactly once (entry i owns a-block i and b-block i-1),

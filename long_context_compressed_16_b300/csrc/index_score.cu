@@ -1,5 +1,5 @@
 // Lightning-indexer scores I_{t,s} = sum_h w_{t,h} ReLU(q^I_{t,h} . K^I_s), s < floor((t+1)/m)
-// ("DeepSeek V4 技术大全", CSA path, the I_{t,s} equation).
+// ("DeepSeek V4 模型技术大全", CSA path, the I_{t,s} equation).
 //
 // One CTA scores a tile of 128 keys for a group of G queries of the same sequence.  The key tile
 // is staged once in shared memory (cp.async, zero-filled past N; e4m3 keys are widened to bf16,

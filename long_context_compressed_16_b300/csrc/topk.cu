@@ -1,4 +1,4 @@
-// Per-query top-k over the visible indexer scores ("DeepSeek V4 技术大全", CSA path, the TopK_k
+// Per-query top-k over the visible indexer scores ("DeepSeek V4 模型技术大全", CSA path, the TopK_k
 // equation), ties to the smaller entry index.
 //
 // Radix select on order-preserving 32-bit keys of the fp32 scores, three digit passes

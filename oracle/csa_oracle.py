@@ -1,7 +1,7 @@
 """Oracle for DeepSeek-V4 hybrid compressed attention (CSA / HCA) -- TEST INFRASTRUCTURE ONLY.
 
 A plain, slow, fp64 NumPy restatement of what the method computes, written from the
-equations of "DeepSeek V4 技术大全" (wineandchord.com), chapter "Hybrid Attention":
+equations of "DeepSeek V4 模型技术大全" (wineandchord.com), chapter "Hybrid Attention":
 the CSA compressor (the overlapped-softmax equations), the lightning indexer and
 top-k (the I_{t,s} and TopK equations), the HCA compressor and visibility set, the
 attention sink, the SWA window set and the partial-RoPE / RMSNorm table rows.
