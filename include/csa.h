@@ -137,6 +137,34 @@ csa_status csa_index_topk(const csa_index_desc* desc, const void* qI, const floa
                           csa_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * csa_index_topk_noalloc -- csa_index_topk for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart: this is a library convenience.  Some callers cannot call
+ * cudaMalloc when they need a selection, e.g. code running inside a host callback or an
+ * allocator hook, or a plug-in whose host hands it only input and output buffers.  This call
+ * computes exactly what csa_index_topk computes (same arguments, same results, bit for bit) but
+ * takes no workspace: its scratch is one fixed array of CSA_NOALLOC_SCRATCH_BYTES in device
+ * memory, declared by the library, which every GPU that loads the library keeps until the
+ * process exits.  The call allocates nothing and frees nothing.
+ *
+ * Limits and behaviour:
+ *   - Requests whose csa_index_topk_workspace() exceeds CSA_NOALLOC_SCRATCH_BYTES return
+ *     CSA_ERR_UNSUPPORTED before any CUDA call (decode at N = 262144 fits up to B = 7; a
+ *     prefill chunk fits while Tq * N * 4 bytes, rounded up to 4-query groups, stays under it).
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *     with that device current and caches it; make that first call before any stream capture.
+ *   - Every call on a device shares the one array and it keeps the last call's contents: calls
+ *     that may overlap on the GPU (other streams, other threads) race and must be serialised by
+ *     the caller.  The status word in the array is not readable by the caller.
+ * Errors are otherwise those of csa_index_topk.
+ * ------------------------------------------------------------------------------------------- */
+#define CSA_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+csa_status csa_index_topk_noalloc(const csa_index_desc* desc, const void* qI, const float* w,
+                                  const void* kI, const float* kI_scale, const int32_t* q_pos,
+                                  int32_t* idx_out, float* score_out, csa_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
  * csa_attend / hca_attend -- shared K=V multi-query attention with SWA window and sink.
  *
  * Source: "DeepSeek V4 模型技术大全", component table rows "Shared K=V MQA", "query / KV RMSNorm",

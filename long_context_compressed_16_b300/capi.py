@@ -27,6 +27,7 @@ CSA_FMT_BF16 = 0
 CSA_FMT_FP8_MIXED = 1
 CSA_FMT_FP8_ROWSCALE = 2
 CSA_FP8_MIXED_ROW_BYTES = 608
+CSA_NOALLOC_SCRATCH_BYTES = 8 << 20
 # flags
 CSA_COMPRESS_NORM = 1
 CSA_COMPRESS_ROPE = 2
@@ -36,7 +37,7 @@ CSA_ATTEND_WRITE_LSE = 4
 
 EXPORTS = ("csa_compress", "csa_index_topk_workspace", "csa_index_topk", "csa_attend_workspace",
            "hca_attend_workspace", "csa_attend", "hca_attend", "csa_read_device_status", "csa_clear_device_status",
-           "csa_status_string", "csa_launch_count")
+           "csa_status_string", "csa_launch_count", "csa_index_topk_noalloc")
 
 
 class csa_compress_desc(ctypes.Structure):
@@ -74,6 +75,8 @@ def _load() -> ctypes.CDLL:
     lib.csa_index_topk_workspace.restype = c_size_t
     lib.csa_index_topk.argtypes = [POINTER(csa_index_desc), vp, vp, vp, vp, vp, vp, vp, vp, c_size_t, vp]
     lib.csa_index_topk.restype = c_int
+    lib.csa_index_topk_noalloc.argtypes = [POINTER(csa_index_desc), vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.csa_index_topk_noalloc.restype = c_int
     lib.csa_attend_workspace.argtypes = [POINTER(csa_attend_desc)]
     lib.csa_attend_workspace.restype = c_size_t
     lib.hca_attend_workspace.argtypes = [POINTER(csa_attend_desc)]
@@ -153,6 +156,13 @@ def csa_index_topk(desc, qI, w, kI, kI_scale, q_pos, idx_out, score_out, workspa
     n = _nbytes(workspace) if ws_bytes is None else ws_bytes
     return lib.csa_index_topk(ctypes.byref(desc), _p(qI), _p(w), _p(kI), _p(kI_scale), _p(q_pos), _p(idx_out),
                               _p(score_out), _p(workspace), n, _stream(stream))
+
+
+def csa_index_topk_noalloc(desc, qI, w, kI, kI_scale, q_pos, idx_out, score_out, stream=None) -> int:
+    """csa_index_topk without a workspace argument: the library's fixed device scratch array is
+    used instead (for callers that cannot allocate device memory; see include/csa.h)."""
+    return lib.csa_index_topk_noalloc(ctypes.byref(desc), _p(qI), _p(w), _p(kI), _p(kI_scale), _p(q_pos),
+                                      _p(idx_out), _p(score_out), _stream(stream))
 
 
 def csa_attend_workspace(desc) -> int:
