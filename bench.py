@@ -5,7 +5,8 @@
 A step is one pass of the decode hot path over one batch: csa_index_topk (lightning-indexer
 scores over every visible compressed entry, then the per-query top-k) followed by csa_attend
 (shared K=V MQA over the selected entries + 128-token window + sink).  Inputs are seeded
-synthetic tensors resident in HBM; L2 is flushed (256 MiB write) before every timed step.
+synthetic tensors resident in HBM; every step reads more than the L2 holds (the indexer keys
+alone are 256 MiB), so no flush runs between steps.
 Under torchrun each rank decodes its own batch (weak scaling, no collective on the data path).
 `--impl reference` times the fp64 oracle on the host cores on a bounded sample of the same
 workload (there is no other implementation of the method to run)."""
@@ -240,7 +241,6 @@ def run_ours(args):
         C.check(C.csa_attend(adesc, inp["q"], inp["kv"], idx, inp["win"], inp["sink"], inp["q_pos"], out, None,
                              ws_a, stream=sptr), "csa_attend")
 
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
@@ -262,7 +262,6 @@ def run_ours(args):
         torch.cuda.synchronize()
         n0 = C.csa_launch_count()
         for i in range(K):
-            flush.fill_(i & 0xFF)
             evs[i][0].record(stream)
             C.check(C.csa_index_topk(idesc, inp["qI"], inp["w"], inp["kI"], kI_scale, inp["q_pos"], idx, None, ws_i,
                                      stream=sptr), "csa_index_topk")
@@ -325,7 +324,6 @@ def run_ours(args):
     torch.cuda.synchronize()
     e_t = []
     for i in range(0 if args.quick else K):
-        flush.fill_(i & 0xFF)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         e2e_step()
@@ -348,6 +346,9 @@ def run_ours(args):
     hbm, peak_kind = peaks()
     key_row = w.dI * (1 if fp8 else 2) + (4 if fp8 else 0)
     idx_bytes = B * (N * key_row + w.nI * w.dI * 2 + w.nI * 4 + k * 4)
+    row_bytes = 608 if fp8 else w.d * 2
+    att_bytes = B * ((k + w.window) * row_bytes + 2 * w.H * w.d * 2 + k * 4)
+    step_bytes = idx_bytes + att_bytes
     achieved = idx_bytes / (t_idx * 1e-3) / 1e9
     tr = TRAFFIC.get(args.workload, {})
     traffic = None
@@ -373,7 +374,7 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "B": B, "N": N, "context_tokens": w.m * N, "k": k, "H": w.H, "d": w.d,
                    "indexer_heads": w.nI, "indexer_dim": w.dI, "window": w.window, "kv_format": "fp8_mixed" if fp8 else "bf16",
-                   "l2": "flushed before every timed step (256 MiB write)", "timed_blocks": len(blocks),
+                   "l2": f"inputs larger than L2: {step_bytes / 2**20:.0f} MiB read per step (126 MB L2), no flush", "timed_blocks": len(blocks),
                    "parallelism": f"dp{world}"},
         "breakdown_ms": {"csa_index_topk": t_idx, "csa_attend": t_att},
         "roofline": {"bound": "hbm", "kernel": "csa_index_topk (k_index_score + k_topk)", "achieved": achieved,

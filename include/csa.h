@@ -45,7 +45,7 @@ typedef enum {
   CSA_ERR_WORKSPACE = 3,     /* workspace missing or smaller than *_workspace() */
   CSA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
   CSA_ERR_DEVICE_CHECK = 5,  /* a kernel found an out-of-range index (see status word) */
-  CSA_ERR_TIMEOUT = 6        /* reserved: a bounded device-side wait gave up */
+  CSA_ERR_TIMEOUT = 6        /* a bounded device-side wait gave up (see status word) */
 } csa_status;
 
 /* Storage formats of compressed entries and indexer keys. */
@@ -110,9 +110,9 @@ csa_status csa_compress(const csa_compress_desc* desc, const void* Ca, const voi
  *   I_{t,s} = sum_h w_{t,h} * ReLU(q^I_{t,h} . K^I_s)  for s < floor((t+1)/m)
  *   idx_t   = TopK_k { I_{t,s} }
  * Ties go to the smaller s.  When fewer than k entries are visible, all are returned and the
- * row is padded with -1.  Output order inside a row: entries with score above the k-th score in
- * increasing s, then the ties at the k-th score in increasing s.  The result depends only on
- * the query's own inputs (batch-invariant) and is deterministic.
+ * row is padded with -1.  Output order inside a row: the selected entries in increasing s,
+ * then the -1 padding.  The result depends only on the query's own inputs (batch-invariant)
+ * and is deterministic.
  *
  * qI: bf16 [B, Tq, n_heads, head_dim].  w: fp32 [B, Tq, n_heads].
  * kI: bf16 [B, N, head_dim] (key_fmt CSA_FMT_BF16) or e4m3 [B, N, head_dim] with
@@ -121,7 +121,7 @@ csa_status csa_compress(const csa_compress_desc* desc, const void* Ca, const voi
  * score_out: fp32 [B, Tq, N] or NULL; when given, visible scores are written there and
  *     invisible ones are -inf.
  * workspace: device buffer of at least csa_index_topk_workspace(desc) bytes.
- * Supported: head_dim 64 or 128; n_heads % 4 == 0 and <= 64; 1 <= k <= 2048; N <= 262144
+ * Supported: head_dim 64 or 128; 1 <= n_heads <= 64; 1 <= k <= 2048; N <= 262144
  * (larger N returns CSA_ERR_UNSUPPORTED).
  * ------------------------------------------------------------------------------------------- */
 typedef struct {

@@ -31,10 +31,11 @@ void count(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_o
 
 // ---------------------------------------------------------------- indexer chunking
 struct IndexPlan {
-  int G;            // queries per group
-  long long groups; // total groups
-  long long chunk;  // groups per top-k pass
-  size_t score_bytes;
+  int G;             // queries per group
+  long long groups;  // total groups
+  long long chunk;   // groups per score + top-k pass
+  size_t score_bytes;  // fp32 score rows of one chunk (rounded up to 256 bytes)
+  size_t cand_bytes;   // two-stage top-k candidates of one chunk (0 for rows <= one slice)
 };
 
 bool index_desc_ok(const csa_index_desc* d) {
@@ -47,17 +48,31 @@ bool index_desc_ok(const csa_index_desc* d) {
   return true;
 }
 
+inline size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
 IndexPlan plan_index(const csa_index_desc* d) {
   IndexPlan p;
-  p.G = d->Tq > 1 ? 4 : 1;
+  p.G = csa::index_grouping(d->n_heads, d->Tq).G;
   const long long gpb = (d->Tq + p.G - 1) / p.G;
   p.groups = static_cast<long long>(d->B) * gpb;
-  const size_t per_group = static_cast<size_t>(p.G) * (d->N > 0 ? d->N : 1) * sizeof(float);
-  long long cg = static_cast<long long>(kScoreChunkCap / per_group);
+  const size_t per_group_scores = static_cast<size_t>(p.G) * (d->N > 0 ? d->N : 1) * sizeof(float);
+  long long cg = static_cast<long long>(kScoreChunkCap / per_group_scores);
   if (cg < 1) cg = 1;
-  if (cg > 65535) cg = 65535;
   p.chunk = p.groups < cg ? p.groups : cg;
-  p.score_bytes = static_cast<size_t>(p.chunk) * per_group;
+  if (p.chunk < 1) p.chunk = 1;
+  p.score_bytes = round256(static_cast<size_t>(p.chunk) * per_group_scores);
+  // candidate bytes of the largest selector launch: the slicing depends on the launch's query
+  // count, and launches of 128 queries or more select in one stage, so the largest need is among
+  // 1..128 queries
+  size_t cand = 0;
+  const long long q_total = static_cast<long long>(d->B) * d->Tq;
+  const long long q_cap = static_cast<long long>(p.chunk) * p.G;
+  const long long q_max = q_total < q_cap ? q_total : q_cap;
+  for (long long q = 1; q <= q_max && q <= 128; ++q) {
+    const size_t c = csa::topk_candidate_bytes(static_cast<int>(q), d->N, d->k);
+    if (c > cand) cand = c;
+  }
+  p.cand_bytes = round256(cand);
   return p;
 }
 
@@ -88,8 +103,9 @@ AttendPlan plan_attend(const csa_attend_desc* d, bool csa_mode) {
   p.n_slots = (csa_mode ? d->k : d->N) + d->window;
   if (p.n_slots < 1) p.n_slots = 1;
   // Decode (one query per sequence) splits the slot range in fixed 256-slot pieces, merged by a
-  // second kernel; the split size never depends on the batch.  Prefill keeps one split per query.
-  p.split_slots = (d->Tq == 1) ? 256 : ((p.n_slots + 63) / 64) * 64;
+  // second kernel (192 slots: three 64-row chunks); the split size never depends on the batch.
+  // Prefill keeps one split per query.
+  p.split_slots = (d->Tq == 1) ? 192 : ((p.n_slots + 63) / 64) * 64;
   p.n_splits = (p.n_slots + p.split_slots - 1) / p.split_slots;
   if (p.n_splits < 1) p.n_splits = 1;
   p.partial_bytes = csa::attend_partial_bytes(d->B * d->Tq, d->H, d->d, p.n_splits);
@@ -178,7 +194,8 @@ csa_status csa_compress(const csa_compress_desc* d, const void* Ca, const void* 
 
 size_t csa_index_topk_workspace(const csa_index_desc* d) {
   if (!index_desc_ok(d)) return 0;
-  return csa::kStatusBytes + plan_index(d).score_bytes;
+  const IndexPlan p = plan_index(d);
+  return csa::kStatusBytes + p.score_bytes + p.cand_bytes;
 }
 
 csa_status csa_index_topk(const csa_index_desc* d, const void* qI, const float* w, const void* kI,
@@ -189,7 +206,7 @@ csa_status csa_index_topk(const csa_index_desc* d, const void* qI, const float* 
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const IndexPlan plan = plan_index(d);
   if (!ws) return CSA_ERR_WORKSPACE;
-  if (ws_bytes < csa::kStatusBytes + (score_out ? 0 : plan.score_bytes)) return CSA_ERR_WORKSPACE;
+  if (ws_bytes < csa::kStatusBytes + (score_out ? 0 : plan.score_bytes) + plan.cand_bytes) return CSA_ERR_WORKSPACE;
   if (!aligned16(ws)) return CSA_ERR_INVALID_ARG;
   const long long Q = static_cast<long long>(d->B) * d->Tq;
   if (Q == 0) return CSA_OK;
@@ -203,40 +220,43 @@ csa_status csa_index_topk(const csa_index_desc* d, const void* qI, const float* 
   ia.qI = qI; ia.w = w; ia.kI = kI; ia.kI_scale = kI_scale; ia.q_pos = q_pos;
   ia.B = d->B; ia.Tq = d->Tq; ia.N = d->N; ia.nI = d->n_heads; ia.dI = d->head_dim; ia.m = d->m;
   ia.fp8 = fp8 ? 1 : 0;
+  ia.status = static_cast<int32_t*>(ws);
+  const csa::IndexGrouping grouping = csa::index_grouping(d->n_heads, d->Tq);
   csa::TopkArgs ta{};
   ta.q_pos = q_pos; ta.idx_out = idx_out; ta.status = static_cast<int32_t*>(ws);
   ta.Tq = d->Tq; ta.N = d->N; ta.k = d->k; ta.m = d->m;
 
   const long long gpb = (d->Tq + plan.G - 1) / plan.G;
+  unsigned char* wsb = static_cast<unsigned char*>(ws);
+  void* cand = plan.cand_bytes ? wsb + csa::kStatusBytes + (score_out ? 0 : plan.score_bytes) : nullptr;
   int launches = 0;
   cudaError_t e = cudaSuccess;
   if (d->N == 0) {
     // nothing visible anywhere: the selector only pads
     ta.scores = nullptr; ta.q_begin = 0; ta.q_count = static_cast<int>(Q); ta.score_row_offset = 0;
-    e = csa::launch_topk(ta, stream, &launches);
+    e = csa::launch_topk(ta, cand, stream, &launches);
     count(launches);
     return from_cuda(e);
   }
-  const long long step = score_out ? 65535 : plan.chunk;
+  const long long step = plan.chunk;
   for (long long g0 = 0; g0 < plan.groups && e == cudaSuccess; g0 += step) {
     const long long g1 = (g0 + step < plan.groups) ? g0 + step : plan.groups;
     const long long q_first = (g0 / gpb) * d->Tq + (g0 % gpb) * plan.G;
     const long long gl = g1 - 1;
     const long long q_last = (gl / gpb) * d->Tq + (gl % gpb) * plan.G +
                              ((d->Tq - (gl % gpb) * plan.G) < plan.G ? (d->Tq - (gl % gpb) * plan.G) : plan.G);
-    float* scores = score_out ? score_out
-                              : reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + csa::kStatusBytes);
+    float* scores = score_out ? score_out : reinterpret_cast<float*>(wsb + csa::kStatusBytes);
     ia.scores = scores;
     ia.q_begin = static_cast<int>(g0);
     ia.q_count = static_cast<int>(g1 - g0);
     ia.score_row_offset = score_out ? 0 : static_cast<int>(q_first);
-    e = csa::launch_index_score_groups(ia, plan.G, score_out ? 1 : 0, stream, &launches);
+    e = csa::launch_index_score_groups(ia, grouping, score_out ? 1 : 0, stream, &launches);
     if (e != cudaSuccess) break;
     ta.scores = scores;
     ta.q_begin = static_cast<int>(q_first);
     ta.q_count = static_cast<int>(q_last - q_first);
     ta.score_row_offset = ia.score_row_offset;
-    e = csa::launch_topk(ta, stream, &launches);
+    e = csa::launch_topk(ta, cand, stream, &launches);
   }
   count(launches);
   if (e == cudaErrorInvalidValue) return CSA_ERR_UNSUPPORTED;

@@ -45,7 +45,8 @@ struct AttnCfg {
   static constexpr size_t red_off = sc_off + (FP8 ? size_t(2) * CK * NB * 4 : 0);
   static constexpr size_t lsum_off = red_off + size_t(HG) * 4 * 4;
   static constexpr size_t ptr_off = lsum_off + size_t(HG) * 4 * 4;
-  static constexpr size_t smem = ptr_off + size_t(2) * CK * 8;
+  static constexpr size_t rope_off = ptr_off + size_t(2) * CK * 8;   // float2 [kMaxRopePairs]
+  static constexpr size_t smem = rope_off + size_t(kMaxRopePairs) * 8;
   static_assert(!FP8 || (NG == 1 && D == 512), "the FP8 cache path runs 16 heads per CTA, d = 512");
 };
 
@@ -84,6 +85,7 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
   float* redmax = reinterpret_cast<float*>(smem + C::red_off);
   float* lsum = reinterpret_cast<float*>(smem + C::lsum_off);
   const unsigned char** rowptr = reinterpret_cast<const unsigned char**>(smem + C::ptr_off);
+  float2* rope_tab = reinterpret_cast<float2*>(smem + C::rope_off);   // (cos, sin) of t * inv_freq_j
 
   const int tid = threadIdx.x, lane = tid & 31, wall = tid >> 5;
   const int g = wall >> 2, wq = wall & 3;
@@ -98,86 +100,6 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
   const int s_begin = split * a.split_slots;
   const int s_end = min(nslots, s_begin + a.split_slots);
   const int nchunks = s_end > s_begin ? (s_end - s_begin + CK - 1) / CK : 0;
-
-  // ---------------- prologue: q_hat = RoPE_t(RMSNorm(q)) -> bf16 in shared memory
-  {
-    constexpr int E = D / 32;   // elements per lane
-    const __nv_bfloat16* qsrc = static_cast<const __nv_bfloat16*>(a.q);
-    for (int hl = wall; hl < HG; hl += 4 * NG) {
-      const __nv_bfloat16* src = qsrc + ((qi * a.H) + h0 + hl) * static_cast<long long>(D) + lane * E;
-      float v[E];
-      if constexpr (E >= 8) {
-#pragma unroll
-        for (int c = 0; c < E; c += 8) {
-          const uint4 u = *reinterpret_cast<const uint4*>(src + c);
-          v[c + 0] = bf16lo(u.x); v[c + 1] = bf16hi(u.x);
-          v[c + 2] = bf16lo(u.y); v[c + 3] = bf16hi(u.y);
-          v[c + 4] = bf16lo(u.z); v[c + 5] = bf16hi(u.z);
-          v[c + 6] = bf16lo(u.w); v[c + 7] = bf16hi(u.w);
-        }
-      } else {
-        static_assert(E == 4, "d must be 128 or 512");
-        const uint2 u = *reinterpret_cast<const uint2*>(src);
-        v[0] = bf16lo(u.x); v[1] = bf16hi(u.x);
-        v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
-      }
-      if (a.q_norm_rope) {
-        float ss = 0.f;
-#pragma unroll
-        for (int c = 0; c < E; ++c) ss = fmaf(v[c], v[c], ss);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        const float inv = 1.0f / sqrtf(ss / static_cast<float>(D) + a.eps);
-#pragma unroll
-        for (int c = 0; c < E; ++c) v[c] *= inv;
-        const int cbase = lane * E;
-        if (cbase + E > D - a.rp.r) {
-#pragma unroll
-          for (int c = 0; c < E; c += 2) {
-            const int ch = cbase + c;
-            if (ch >= D - a.rp.r) {
-              float cs, sn;
-              rope_cos_sin(static_cast<double>(t), a.rp.inv_freq[(ch - (D - a.rp.r)) >> 1], cs, sn);
-              const float x0 = v[c], x1 = v[c + 1];
-              v[c] = x0 * cs - x1 * sn;
-              v[c + 1] = x0 * sn + x1 * cs;
-            }
-          }
-        }
-      }
-      __nv_bfloat16* dst = Qs + hl * QS + lane * E;
-      if constexpr (FP8) {
-#pragma unroll
-        for (int c = 0; c < E; c += 8) {
-          uint32_t hw[4], lw[4];
-#pragma unroll
-          for (int p2 = 0; p2 < 4; ++p2) {
-            const float x0 = v[c + 2 * p2], x1 = v[c + 2 * p2 + 1];
-            hw[p2] = pack_half2(x0, x1);
-            const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hw[p2]));
-            lw[p2] = pack_half2(x0 - hf.x, x1 - hf.y);        // residual: hi + lo ~ 22 significant bits
-          }
-          *reinterpret_cast<uint4*>(dst + c) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(dst + HG * QS + c) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-        }
-      } else if constexpr (E >= 8) {
-#pragma unroll
-        for (int c = 0; c < E; c += 8) {
-          uint4 u;
-          u.x = pack_bf16x2(v[c + 0], v[c + 1]);
-          u.y = pack_bf16x2(v[c + 2], v[c + 3]);
-          u.z = pack_bf16x2(v[c + 4], v[c + 5]);
-          u.w = pack_bf16x2(v[c + 6], v[c + 7]);
-          *reinterpret_cast<uint4*>(dst + c) = u;
-        }
-      } else {
-        uint2 u;
-        u.x = pack_bf16x2(v[0], v[1]);
-        u.y = pack_bf16x2(v[2], v[3]);
-        *reinterpret_cast<uint2*>(dst) = u;
-      }
-    }
-  }
 
   const unsigned char* kvb = static_cast<const unsigned char*>(a.kv);
   const unsigned char* winb = static_cast<const unsigned char*>(a.win);
@@ -230,12 +152,101 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
     for (int c = 0; c < 4; ++c) oacc[i][c] = 0.f;
   const float sl2 = a.scale * kLog2e;
 
+  // the first chunk's row gather is in flight while the query block is prepared
   if (nchunks > 0) {
     compute_ptrs(0, 0);
     __syncthreads();
     issue_loads(0);
     cp_async_commit();
   }
+
+  // ---------------- prologue: q_hat = RoPE_t(RMSNorm(q)) -> bf16 in shared memory.  The query's
+  // rotation angles are shared by all heads: one (cos, sin) table per CTA.
+  if (tid < a.rp.r / 2) {
+    float cs, sn;
+    rope_cos_sin(static_cast<double>(t), a.rp.inv_freq[tid], cs, sn);
+    rope_tab[tid] = make_float2(cs, sn);
+  }
+  __syncthreads();
+  {
+    constexpr int E = D / 32;   // elements per lane
+    const __nv_bfloat16* qsrc = static_cast<const __nv_bfloat16*>(a.q);
+    for (int hl = wall; hl < HG; hl += 4 * NG) {
+      const __nv_bfloat16* src = qsrc + ((qi * a.H) + h0 + hl) * static_cast<long long>(D) + lane * E;
+      float v[E];
+      if constexpr (E >= 8) {
+#pragma unroll
+        for (int c = 0; c < E; c += 8) {
+          const uint4 u = *reinterpret_cast<const uint4*>(src + c);
+          v[c + 0] = bf16lo(u.x); v[c + 1] = bf16hi(u.x);
+          v[c + 2] = bf16lo(u.y); v[c + 3] = bf16hi(u.y);
+          v[c + 4] = bf16lo(u.z); v[c + 5] = bf16hi(u.z);
+          v[c + 6] = bf16lo(u.w); v[c + 7] = bf16hi(u.w);
+        }
+      } else {
+        static_assert(E == 4, "d must be 128 or 512");
+        const uint2 u = *reinterpret_cast<const uint2*>(src);
+        v[0] = bf16lo(u.x); v[1] = bf16hi(u.x);
+        v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
+      }
+      if (a.q_norm_rope) {
+        float ss = 0.f;
+#pragma unroll
+        for (int c = 0; c < E; ++c) ss = fmaf(v[c], v[c], ss);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float inv = 1.0f / sqrtf(ss / static_cast<float>(D) + a.eps);
+#pragma unroll
+        for (int c = 0; c < E; ++c) v[c] *= inv;
+        const int cbase = lane * E;
+        if (cbase + E > D - a.rp.r) {
+#pragma unroll
+          for (int c = 0; c < E; c += 2) {
+            const int ch = cbase + c;
+            if (ch >= D - a.rp.r) {
+              const float2 cssn = rope_tab[(ch - (D - a.rp.r)) >> 1];
+              const float cs = cssn.x, sn = cssn.y;
+              const float x0 = v[c], x1 = v[c + 1];
+              v[c] = x0 * cs - x1 * sn;
+              v[c + 1] = x0 * sn + x1 * cs;
+            }
+          }
+        }
+      }
+      __nv_bfloat16* dst = Qs + hl * QS + lane * E;
+      if constexpr (FP8) {
+#pragma unroll
+        for (int c = 0; c < E; c += 8) {
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int p2 = 0; p2 < 4; ++p2) {
+            const float x0 = v[c + 2 * p2], x1 = v[c + 2 * p2 + 1];
+            hw[p2] = pack_half2(x0, x1);
+            const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hw[p2]));
+            lw[p2] = pack_half2(x0 - hf.x, x1 - hf.y);        // residual: hi + lo ~ 22 significant bits
+          }
+          *reinterpret_cast<uint4*>(dst + c) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(dst + HG * QS + c) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+      } else if constexpr (E >= 8) {
+#pragma unroll
+        for (int c = 0; c < E; c += 8) {
+          uint4 u;
+          u.x = pack_bf16x2(v[c + 0], v[c + 1]);
+          u.y = pack_bf16x2(v[c + 2], v[c + 3]);
+          u.z = pack_bf16x2(v[c + 4], v[c + 5]);
+          u.w = pack_bf16x2(v[c + 6], v[c + 7]);
+          *reinterpret_cast<uint4*>(dst + c) = u;
+        }
+      } else {
+        uint2 u;
+        u.x = pack_bf16x2(v[0], v[1]);
+        u.y = pack_bf16x2(v[2], v[3]);
+        *reinterpret_cast<uint2*>(dst) = u;
+      }
+    }
+  }
+
   for (int c = 0; c < nchunks; ++c) {
     const int buf = c & 1;
     if (c + 1 < nchunks) compute_ptrs(c + 1, buf ^ 1);
@@ -479,7 +490,11 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
       const int dim = wq * (D / 4) + i * 8 + 2 * (lane & 3);
       float cs = 1.f, sn = 0.f;
       const bool rot = a.out_unrotate && dim >= D - a.rp.r;
-      if (rot) rope_cos_sin(-static_cast<double>(t), a.rp.inv_freq[(dim - (D - a.rp.r)) >> 1], cs, sn);
+      if (rot) {                      // rotation by -t: (cos, -sin) of the query's angles
+        const float2 cssn = rope_tab[(dim - (D - a.rp.r)) >> 1];
+        cs = cssn.x;
+        sn = -cssn.y;
+      }
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const int h = h0 + 16 * g + (lane >> 2) + 8 * r;
@@ -514,49 +529,68 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
   }
 }
 
-// Merge split partials: out = sum_s O_s 2^(m_s - M) / (sum_s l_s 2^(m_s - M) + 2^(a_h - M)).
+// Merge split partials: out = sum_s O_s 2^(m_s - M) / (sum_s l_s 2^(m_s - M) + 2^(a_h - M)),
+// M = max(a_h, max_s m_s), in fixed split order.  One CTA per (query, pair of heads), 128 threads
+// per head: the two heads' merge factors and the query's rotation table are computed once in
+// shared memory, then each thread merges dim pairs of its head.
+constexpr int kCombineHeads = 2;
+
 template <int D>
-__global__ void __launch_bounds__(128) k_attend_combine(AttendArgs a) {
+__global__ void __launch_bounds__(128 * kCombineHeads) k_attend_combine(AttendArgs a) {
+  extern __shared__ float csm[];
   const long long qi = blockIdx.x;
-  const int h = blockIdx.y;
-  const int S = a.n_splits;
+  const int h0 = blockIdx.y * kCombineHeads;
+  const int S = a.n_splits, H = a.H;
   const int Q = a.B * a.Tq;
+  float* fac = csm;                                                               // [2][S]
+  float2* tab = reinterpret_cast<float2*>(csm + ((kCombineHeads * S + 1) & ~1));  // [r/2]
   const float* po = a.partial;
-  const float* pml = a.partial + static_cast<size_t>(Q) * S * a.H * D;
-  const float a2 = a.sink[h] * kLog2e;
-  float M = a2;
-  for (int s = 0; s < S; ++s) M = fmaxf(M, pml[((qi * S + s) * a.H + h) * 2]);
-  float L = exp2f(a2 - M);
-  for (int s = 0; s < S; ++s) {
-    const size_t ri = (static_cast<size_t>(qi) * S + s) * a.H + h;
-    const float ms = pml[ri * 2];
-    if (ms != -INFINITY) L = fmaf(pml[ri * 2 + 1], exp2f(ms - M), L);
-  }
-  const float linv = 1.0f / L;
+  const float* pml = a.partial + static_cast<size_t>(Q) * S * H * D;
   const int t = a.q_pos[qi];
+  const int tid = threadIdx.x;
+  if (tid < a.rp.r / 2) {
+    float cs, sn;
+    rope_cos_sin(static_cast<double>(t), a.rp.inv_freq[tid], cs, sn);
+    tab[tid] = make_float2(cs, -sn);                                              // rotation by -t
+  }
+  if (tid < kCombineHeads) {
+    const int h = h0 + tid;
+    const float a2 = a.sink[h] * kLog2e;
+    float M = a2;
+    for (int s = 0; s < S; ++s) M = fmaxf(M, pml[((qi * S + s) * H + h) * 2]);
+    float L = exp2f(a2 - M);
+    for (int s = 0; s < S; ++s) {
+      const size_t ri = (static_cast<size_t>(qi) * S + s) * H + h;
+      const float ms = pml[ri * 2];
+      if (ms != -INFINITY) L = fmaf(pml[ri * 2 + 1], exp2f(ms - M), L);
+    }
+    const float linv = 1.0f / L;
+    for (int s = 0; s < S; ++s) {
+      const float ms = pml[((qi * S + s) * H + h) * 2];
+      fac[tid * S + s] = (ms == -INFINITY) ? 0.f : exp2f(ms - M) * linv;
+    }
+    if (a.lse != nullptr) a.lse[qi * H + h] = (M + log2f(L)) * kLn2;
+  }
+  __syncthreads();
+  const int hl = tid / 128;
+  const int h = h0 + hl;
   __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(a.out);
-  for (int dim = threadIdx.x * 2; dim < D; dim += 256) {
+  for (int pr = tid % 128; pr < D / 2; pr += 128) {
+    const int dim = pr * 2;
     float x0 = 0.f, x1 = 0.f;
     for (int s = 0; s < S; ++s) {
-      const size_t ri = (static_cast<size_t>(qi) * S + s) * a.H + h;
-      const float ms = pml[ri * 2];
-      if (ms == -INFINITY) continue;
-      const float f = exp2f(ms - M);
-      const float2 v = *reinterpret_cast<const float2*>(po + ri * D + dim);
+      const float f = fac[hl * S + s];         // 0 for a split without rows (its partial is zeros)
+      const float2 v = *reinterpret_cast<const float2*>(po + ((static_cast<size_t>(qi) * S + s) * H + h) * D + dim);
       x0 = fmaf(v.x, f, x0);
       x1 = fmaf(v.y, f, x1);
     }
-    x0 *= linv;
-    x1 *= linv;
     if (a.out_unrotate && dim >= D - a.rp.r) {
-      float cs, sn;
-      rope_cos_sin(-static_cast<double>(t), a.rp.inv_freq[(dim - (D - a.rp.r)) >> 1], cs, sn);
-      const float y0 = x0 * cs - x1 * sn, y1 = x0 * sn + x1 * cs;
+      const float2 cssn = tab[(dim - (D - a.rp.r)) >> 1];
+      const float y0 = x0 * cssn.x - x1 * cssn.y, y1 = x0 * cssn.y + x1 * cssn.x;
       x0 = y0; x1 = y1;
     }
-    *reinterpret_cast<uint32_t*>(outp + (qi * a.H + h) * static_cast<long long>(D) + dim) = pack_bf16x2(x0, x1);
+    *reinterpret_cast<uint32_t*>(outp + (qi * H + h) * static_cast<long long>(D) + dim) = pack_bf16x2(x0, x1);
   }
-  if (a.lse != nullptr && threadIdx.x == 0) a.lse[qi * a.H + h] = (M + log2f(L)) * kLn2;
 }
 
 template <int D, int NG, bool FP8>
@@ -571,7 +605,13 @@ cudaError_t launch_t(const AttendArgs& a, cudaStream_t s, int* launches) {
   ++*launches;
   e = cudaGetLastError();
   if (e != cudaSuccess || a.n_splits == 1) return e;
-  k_attend_combine<D><<<dim3(Q, a.H), 128, 0, s>>>(a);
+  const size_t csmem =
+      (static_cast<size_t>((kCombineHeads * a.n_splits + 1) & ~1) + 2 * kMaxRopePairs) * sizeof(float);
+  if (csmem > 48 * 1024) {
+    e = cudaFuncSetAttribute(k_attend_combine<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(csmem));
+    if (e != cudaSuccess) return e;
+  }
+  k_attend_combine<D><<<dim3(Q, a.H / kCombineHeads), 128 * kCombineHeads, csmem, s>>>(a);
   ++*launches;
   return cudaGetLastError();
 }
@@ -586,11 +626,12 @@ size_t attend_partial_bytes(int Q, int H, int d, int n_splits) {
 cudaError_t launch_attend(const AttendArgs& a, cudaStream_t s, int* launches) {
   const int Q = a.B * a.Tq;
   if (Q == 0) return cudaSuccess;
-  // 64 heads per CTA when there is enough parallelism, otherwise 16 (identical numerics)
+  // 64 heads per CTA (each gathered row read once) when that still gives work to at least half
+  // of the SMs, otherwise 16 heads per CTA; the numerics are identical
   int sms = 148;
   int dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const bool wide = (a.H % 64 == 0) && (static_cast<long long>(Q) * a.n_splits * (a.H / 64) >= 2LL * sms);
+  const bool wide = (a.H % 64 == 0) && (2LL * Q * a.n_splits * (a.H / 64) >= sms);
   if (a.d == 512) {
     if (a.fp8) return launch_t<512, 1, true>(a, s, launches);
     return wide ? launch_t<512, 4, false>(a, s, launches) : launch_t<512, 1, false>(a, s, launches);

@@ -147,14 +147,33 @@ struct IndexArgs {
   const float* kI_scale;
   const int32_t* q_pos;
   float* scores;            // score rows of N floats
+  int32_t* status;          // workspace status word (bounded-wait timeouts)
   int B, Tq, N, nI, dI, m, fp8;
   int q_begin, q_count;     // range of query GROUPS (G consecutive queries of one sequence)
   int score_row_offset;     // flattened query q (= b*Tq + i) owns score row q - score_row_offset
 };
+
+// How the indexer packs queries into one tensor-core N dimension: heads padded to NHP (a power
+// of two >= 16), G consecutive queries of one sequence per group, NCOL = G * NHP <= 256 columns.
+struct IndexGrouping {
+  int NHP, G, NCOL;
+};
+inline IndexGrouping index_grouping(int nI, int Tq) {
+  IndexGrouping g;
+  int nhp = 16;
+  while (nhp < nI) nhp <<= 1;
+  int G = 1;
+  while (G < Tq && G * nhp < 256) G <<= 1;
+  g.NHP = nhp;
+  g.G = G;
+  g.NCOL = G * nhp;
+  return g;
+}
+
 // Scores for the query groups [q_begin, q_begin + q_count).  fill_invisible: also write -inf
 // for every s in [N_vis, N) so that the rows are complete.
-cudaError_t launch_index_score_groups(const IndexArgs& a, int G, int fill_invisible, cudaStream_t s,
-                                      int* launches);
+cudaError_t launch_index_score_groups(const IndexArgs& a, const IndexGrouping& gr, int fill_invisible,
+                                      cudaStream_t s, int* launches);
 
 struct TopkArgs {
   const float* scores;
@@ -165,7 +184,12 @@ struct TopkArgs {
   int q_begin, q_count;
   int score_row_offset;
 };
-cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s, int* launches);
+// Rows longer than one selection slice are selected in two stages; the first writes
+// topk_candidate_bytes(Q, N, k) bytes of (key, index) candidates for a launch over Q queries to
+// cand_ws (8-byte aligned), which may be null when that size is 0.
+int topk_slices(int Q, int N, int k);
+size_t topk_candidate_bytes(int Q, int N, int k);
+cudaError_t launch_topk(const TopkArgs& a, void* cand_ws, cudaStream_t s, int* launches);
 
 struct AttendArgs {
   const void* q;
@@ -187,6 +211,7 @@ struct AttendArgs {
   RopeParams rp;
 };
 size_t attend_partial_bytes(int Q, int H, int d, int n_splits);
+
 cudaError_t launch_attend(const AttendArgs& a, cudaStream_t s, int* launches);
 
 }  // namespace csa

@@ -1,225 +1,539 @@
 // Lightning-indexer scores I_{t,s} = sum_h w_{t,h} ReLU(q^I_{t,h} . K^I_s), s < floor((t+1)/m)
-// ("DeepSeek V4 模型技术大全", CSA path, the I_{t,s} equation).
+// ("DeepSeek V4 模型技术大全", CSA path, the I_{t,s} equation), on the 5th-generation tensor cores.
 //
-// One CTA scores a tile of 128 keys for a group of G queries of the same sequence.  The key tile
-// is staged once in shared memory (cp.async, zero-filled past N; e4m3 keys are widened to bf16,
-// which is exact) and multiplied by each query's [heads x dI] block on the tensor cores
-// (keys as M, heads as N, dI as K).  The ReLU / w-weighted head sum is the MMA epilogue: the
-// heads of one key live in one lane quad, so the sum is two shuffles.
+// The contraction runs with keys as the MMA's M dimension (128 keys per tile) and the (query,
+// head) pairs of a group of G queries as N (G x padded heads <= 256), K = head_dim.  The fp32
+// accumulator lives in tensor memory, one TMEM lane per key, so the ReLU / w-weighted head sum is
+// a per-thread loop over TMEM columns with no cross-lane reduction.
+//
+// One persistent CTA per SM, warp-specialised:
+//   warp 0        TMA producer: key tiles (3-D tensor map, 128-byte swizzle, zero fill past N)
+//                 into a ring of shared-memory stages, and each group's query block
+//   warp 1        owns the TMEM allocation; one lane issues tcgen05.mma (M=128, N=G*heads,
+//                 K=16 per instruction) and tcgen05.commit to release stages and publish results
+//   warps 4..     epilogue: tcgen05.ld of the accumulator (double-buffered in TMEM), ReLU,
+//                 weighting, head sum, optional FP8 row scale, coalesced score stores
+//   FP8 keys only: converter warps widen each staged e4m3 tile to bf16 (exact) in the swizzled
+//                 operand layout
+// Work is a static split of (group, tile) pairs that all roles walk identically; every score is
+// one MMA chain over the same K order, so results do not depend on the batch or the split.
+// Every wait is bounded: a stuck pipeline sets CSA_ERR_TIMEOUT in the status word and the CTA
+// drains its own copies, frees its tensor memory and returns.
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace csa {
 
 namespace {
 
-constexpr int KT = 128;         // keys per tile
-constexpr int NTHREADS = 128;   // 4 warps x 32 keys
+constexpr int KT = 128;                 // keys per tile = MMA M
+constexpr int kMaxSmem = 232448;        // dynamic shared memory per block on sm_100-class parts
 
-template <int DI, bool FP8>
-struct IndexSmem {
-  static constexpr int KS = DI + 8;                       // padded row (bf16 elements)
-  static constexpr size_t k_bytes = size_t(KT) * KS * 2;
-  static constexpr size_t stage_bytes = FP8 ? size_t(KT) * DI : 0;
-  __host__ __device__ static size_t q_bytes(int G, int NH) { return size_t(G) * NH * KS * 2; }
-  __host__ __device__ static size_t total(int G, int NH) {
-    return k_bytes + stage_bytes + q_bytes(G, NH) + size_t(G) * NH * 4 + KT * 4;
+template <int DI, int NCOL, bool FP8>
+struct Cfg {
+  static constexpr int NREG = DI / 64;                    // 128-byte swizzle regions per row
+  static constexpr int KEY_REGION = KT * 128;
+  static constexpr int STAGE_BYTES = NREG * KEY_REGION;   // bf16 key operand per stage
+  static constexpr int STAGED_BYTES = FP8 ? KT * DI : 0;  // e4m3 staging per stage
+  static constexpr int Q_REGION = NCOL * 128;
+  static constexpr int Q_BYTES = NREG * Q_REGION;
+  static constexpr int QB = NCOL >= 256 ? 1 : 2;          // query-block buffers
+  static constexpr int EW = NCOL > 128 ? 8 : 4;           // epilogue warps
+  static constexpr int CW = FP8 ? 4 : 0;                  // converter warps
+  static constexpr int THREADS = 32 * (4 + EW + CW);
+  static constexpr int W_FLOATS = EW * NCOL;              // per-epilogue-warp copy of the head weights
+  static constexpr int MISC = 1024;                       // barriers, TMEM address, flags
+  static constexpr int FIXED = 1024 /*alignment slack*/ + QB * Q_BYTES + W_FLOATS * 4 + MISC;
+  static constexpr int S_RAW = (kMaxSmem - FIXED) / (STAGE_BYTES + STAGED_BYTES);
+  static constexpr int STAGES = S_RAW > 6 ? 6 : S_RAW;
+  static constexpr int SMEM = FIXED + STAGES * (STAGE_BYTES + STAGED_BYTES);
+  static constexpr int ACC = NCOL <= 128 ? 4 : 2;            // accumulator buffers in tensor memory
+  static constexpr int TMEM_COLS = (ACC * NCOL) <= 32 ? 32 : (ACC * NCOL) <= 64 ? 64 : (ACC * NCOL) <= 128 ? 128
+                                   : (ACC * NCOL) <= 256 ? 256 : 512;
+  static_assert(STAGES >= 2, "shared memory too small for two stages");
+  static_assert(SMEM <= kMaxSmem, "shared memory budget");
+  static_assert(NCOL % 16 == 0 && NCOL >= 16 && NCOL <= 256, "UMMA N for M = 128");
+};
+
+struct TcParams {
+  int G, NHP;               // queries per group, padded heads per query
+  int mode;                 // 0: flattened (group, tile) space split evenly; 1: whole groups, snake order
+  int tiles_max;            // ceil(N / KT)
+  long long F;              // groups * tiles_max (mode 0)
+  int fill_invisible;
+};
+
+struct GroupInfo {
+  int b, i0, nq, nt;
+};
+
+__device__ __forceinline__ GroupInfo group_info(const IndexArgs& a, const TcParams& p, int g) {
+  GroupInfo gi;
+  const int ga = a.q_begin + g;
+  const int gpb = (a.Tq + p.G - 1) / p.G;
+  gi.b = ga / gpb;
+  gi.i0 = (ga % gpb) * p.G;
+  gi.nq = min(p.G, a.Tq - gi.i0);
+  int maxvis = 0;
+  for (int j = 0; j < gi.nq; ++j)
+    maxvis = max(maxvis, n_visible(a.q_pos[static_cast<size_t>(gi.b) * a.Tq + gi.i0 + j], a.m, a.N));
+  gi.nt = p.fill_invisible ? p.tiles_max : (maxvis + KT - 1) / KT;
+  return gi;
+}
+
+// Walks this CTA's (group, tile) pairs; every role runs its own copy and sees the same sequence.
+struct Walker {
+  long long f, f_end;       // mode 0
+  int round;                // mode 1
+  int g, t;
+  GroupInfo gi;
+
+  __device__ void init(const TcParams& p, int ngroups) {
+    const long long P = gridDim.x, c = blockIdx.x;
+    if (p.mode == 0) {
+      f = c * p.F / P;
+      f_end = (c + 1) * p.F / P;
+    }
+    round = 0;
+    g = -1;
+    t = 0;
+    (void)ngroups;
+  }
+
+  // Advances to the next pair; returns false when the CTA has no more work.  new_group is set
+  // when the pair belongs to a different group than the previous one.
+  __device__ bool next(const IndexArgs& a, const TcParams& p, int ngroups, bool& new_group) {
+    new_group = false;
+    if (p.mode == 0) {
+      while (f < f_end) {
+        const int gg = static_cast<int>(f / p.tiles_max);
+        const int tt = static_cast<int>(f % p.tiles_max);
+        if (gg != g) {
+          g = gg;
+          gi = group_info(a, p, g);
+          new_group = true;
+        }
+        if (tt < gi.nt) {
+          t = tt;
+          ++f;
+          return true;
+        }
+        f = static_cast<long long>(gg + 1) * p.tiles_max;
+      }
+      return false;
+    }
+    if (g >= 0 && t + 1 < gi.nt) {
+      ++t;
+      return true;
+    }
+    const int P = gridDim.x, c = blockIdx.x;
+    for (;;) {
+      const long long base = static_cast<long long>(round) * P;
+      if (base >= ngroups) return false;
+      const long long gg = base + ((round & 1) ? (P - 1 - c) : c);
+      ++round;
+      if (gg >= ngroups) continue;
+      g = static_cast<int>(gg);
+      gi = group_info(a, p, g);
+      if (gi.nt == 0) continue;
+      t = 0;
+      new_group = true;
+      return true;
+    }
   }
 };
 
-template <int DI, bool FP8>
-__global__ void __launch_bounds__(NTHREADS) k_index_score(IndexArgs a, int G, int NH, int g_begin,
-                                                          int fill_invisible) {
-  using S = IndexSmem<DI, FP8>;
-  constexpr int KS = S::KS;
-  extern __shared__ __align__(16) unsigned char smem[];
-  __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(smem);
-  unsigned char* stage = smem + S::k_bytes;
-  __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(smem + S::k_bytes + S::stage_bytes);
-  float* Ws = reinterpret_cast<float*>(smem + S::k_bytes + S::stage_bytes + S::q_bytes(G, NH));
-  float* kscale = Ws + G * NH;
-
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  const int tile = blockIdx.x;
-  const int grp = g_begin + blockIdx.y;
-  const int gpb = (a.Tq + G - 1) / G;
-  const int b = grp / gpb;
-  const int i0 = (grp % gpb) * G;
-  const int nq = min(G, a.Tq - i0);
-  const int key0 = tile * KT;
-
-  int maxvis = 0;
-  for (int j = 0; j < nq; ++j) {
-    const int t = a.q_pos[static_cast<size_t>(b) * a.Tq + i0 + j];
-    maxvis = max(maxvis, n_visible(t, a.m, a.N));
-  }
-  if (key0 >= maxvis) {
-    if (fill_invisible) {
-      for (int j = 0; j < nq; ++j) {
-        const long long row = static_cast<long long>(b) * a.Tq + i0 + j - a.score_row_offset;
-        float* dst = a.scores + row * a.N;
-        for (int s = key0 + tid; s < min(a.N, key0 + KT); s += NTHREADS) dst[s] = -INFINITY;
-      }
-    }
-    return;
-  }
-
-  // ---- stage the key tile
-  const size_t krow0 = static_cast<size_t>(b) * a.N + key0;
-  if (!FP8) {
-    constexpr int CPR = DI * 2 / 16;   // 16-byte chunks per row
-    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(a.kI);
-    for (int c = tid; c < KT * CPR; c += NTHREADS) {
-      const int r = c / CPR, q = c % CPR;
-      const bool ok = key0 + r < a.N;
-      const __nv_bfloat16* g = src + (krow0 + (ok ? r : 0)) * DI + q * 8;
-      cp_async16(Ks + r * KS + q * 8, g, ok);
-    }
-  } else {
-    constexpr int CPR = DI / 16;
-    const unsigned char* src = static_cast<const unsigned char*>(a.kI);
-    for (int c = tid; c < KT * CPR; c += NTHREADS) {
-      const int r = c / CPR, q = c % CPR;
-      const bool ok = key0 + r < a.N;
-      const unsigned char* g = src + (krow0 + (ok ? r : 0)) * DI + q * 16;
-      cp_async16(stage + r * DI + q * 16, g, ok);
-    }
-    for (int r = tid; r < KT; r += NTHREADS)
-      kscale[r] = (key0 + r < a.N) ? a.kI_scale[krow0 + r] : 0.f;
-  }
-  // ---- stage the group's queries (rows >= nI are zero) and weights
-  {
-    constexpr int CPR = DI * 2 / 16;
-    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(a.qI);
-    for (int c = tid; c < G * NH * CPR; c += NTHREADS) {
-      const int row = c / CPR, q = c % CPR;
-      const int j = row / NH, h = row % NH;
-      const bool ok = (j < nq) && (h < a.nI);
-      const size_t qrow = (static_cast<size_t>(b) * a.Tq + i0 + (ok ? j : 0)) * a.nI + (ok ? h : 0);
-      cp_async16(Qs + row * KS + q * 8, src + qrow * DI + q * 8, ok);
-    }
-    for (int c = tid; c < G * NH; c += NTHREADS) {
-      const int j = c / NH, h = c % NH;
-      Ws[c] = (j < nq && h < a.nI) ? a.w[(static_cast<size_t>(b) * a.Tq + i0 + j) * a.nI + h] : 0.f;
-    }
-  }
-  cp_async_commit();
-  cp_async_wait<0>();
-  __syncthreads();
-  if (FP8) {
-    // widen e4m3 -> bf16 (exact: every e4m3 value is a bf16 value)
-    for (int c = tid; c < KT * DI / 8; c += NTHREADS) {
-      const int r = c / (DI / 8), q = c % (DI / 8);
-      const uint2 v = *reinterpret_cast<const uint2*>(stage + r * DI + q * 8);
-      float f[8];
-      e4m3x2_to_float2(static_cast<uint16_t>(v.x & 0xFFFF), f[0], f[1]);
-      e4m3x2_to_float2(static_cast<uint16_t>(v.x >> 16), f[2], f[3]);
-      e4m3x2_to_float2(static_cast<uint16_t>(v.y & 0xFFFF), f[4], f[5]);
-      e4m3x2_to_float2(static_cast<uint16_t>(v.y >> 16), f[6], f[7]);
-      uint4 o;
-      o.x = pack_bf16x2(f[0], f[1]); o.y = pack_bf16x2(f[2], f[3]);
-      o.z = pack_bf16x2(f[4], f[5]); o.w = pack_bf16x2(f[6], f[7]);
-      *reinterpret_cast<uint4*>(Ks + r * KS + q * 8) = o;
-    }
-    __syncthreads();
-  }
-
-  const int NT = NH / 8;   // n8 tiles of heads (even, <= 8)
-  for (int j = 0; j < nq; ++j) {
-    const int t = a.q_pos[static_cast<size_t>(b) * a.Tq + i0 + j];
-    const int nvis = n_visible(t, a.m, a.N);
-    const __nv_bfloat16* Qj = Qs + static_cast<size_t>(j) * NH * KS;
-    float acc[2][8][4];
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[mt][nt][c] = 0.f;
-
-#pragma unroll
-    for (int ks = 0; ks < DI / 16; ++ks) {
-      uint32_t af[2][4];
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-        const int row = warp * 32 + mt * 16 + (lane & 15);
-        const int col = ks * 16 + (lane >> 4) * 8;
-        ldmatrix_x4(af[mt][0], af[mt][1], af[mt][2], af[mt][3], smem_u32(Ks + row * KS + col));
-      }
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        if (np * 2 < NT) {
-          uint32_t b0, b1, b2, b3;
-          const int h = np * 16 + (lane >> 4) * 8 + (lane & 7);
-          const int col = ks * 16 + ((lane >> 3) & 1) * 8;
-          ldmatrix_x4(b0, b1, b2, b3, smem_u32(Qj + h * KS + col));
-          const uint32_t bb0[2] = {b0, b1};
-          const uint32_t bb1[2] = {b2, b3};
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt) {
-            mma_bf16_16816(acc[mt][2 * np], af[mt], bb0);
-            mma_bf16_16816(acc[mt][2 * np + 1], af[mt], bb1);
-          }
-        }
-      }
-    }
-    // epilogue: ReLU, head weights, sum over heads (quad), write
-    const float* Wj = Ws + j * NH;
-    const long long row = static_cast<long long>(b) * a.Tq + i0 + j - a.score_row_offset;
-    float* dst = a.scores + row * a.N;
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-      float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        if (nt < NT) {
-          const int h = nt * 8 + 2 * (lane & 3);
-          const float w0 = Wj[h], w1 = Wj[h + 1];
-          s0 = fmaf(w0, fmaxf(acc[mt][nt][0], 0.f), s0);
-          s0 = fmaf(w1, fmaxf(acc[mt][nt][1], 0.f), s0);
-          s1 = fmaf(w0, fmaxf(acc[mt][nt][2], 0.f), s1);
-          s1 = fmaf(w1, fmaxf(acc[mt][nt][3], 0.f), s1);
-        }
-      }
-      s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
-      s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
-      s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
-      s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
-      if ((lane & 3) == 0) {
-        const int r0 = warp * 32 + mt * 16 + (lane >> 2);
-        const int r1 = r0 + 8;
-        if (FP8) { s0 *= kscale[r0]; s1 *= kscale[r1]; }
-        const int k0 = key0 + r0, k1 = key0 + r1;
-        if (k0 < a.N && (k0 < nvis || fill_invisible)) dst[k0] = k0 < nvis ? s0 : -INFINITY;
-        if (k1 < a.N && (k1 < nvis || fill_invisible)) dst[k1] = k1 < nvis ? s1 : -INFINITY;
-      }
-    }
-  }
+// e4m3 x4 (one 32-bit word) -> bf16 x4 (two 32-bit words), exact: every e4m3 value is a bf16 value.
+// The hardware widening to f16 is exact; an f16 with 3 significant mantissa bits maps to bf16 by
+// re-biasing the exponent (15 -> 127) and dropping 3 zero mantissa bits.  Zeros keep their sign.
+__device__ __forceinline__ uint32_t half2_to_bf162_exact(uint32_t h2) {
+  const uint32_t mag = h2 & 0x7FFF7FFFu;
+  uint32_t r = (h2 & 0x80008000u) | ((mag >> 3) & 0x0FFF0FFFu);
+  const uint32_t nz_lo = (mag & 0x0000FFFFu) ? 0x00003800u : 0u;
+  const uint32_t nz_hi = (mag & 0xFFFF0000u) ? 0x38000000u : 0u;
+  return r + nz_lo + nz_hi;
 }
 
-template <int DI, bool FP8>
-cudaError_t launch_t(const IndexArgs& a, int G, int fill_invisible, cudaStream_t s, int* launches) {
-  // heads padded to a multiple of 16 (zero q rows, zero weights) so B fragments load in pairs
-  const int NH = (a.nI + 15) / 16 * 16;
-  const size_t smem = IndexSmem<DI, FP8>::total(G, NH);
-  cudaError_t e = cudaFuncSetAttribute(k_index_score<DI, FP8>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+template <int DI, int NCOL, bool FP8>
+__global__ void __launch_bounds__(Cfg<DI, NCOL, FP8>::THREADS, 1)
+k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+              const TcParams p) {
+  using C = Cfg<DI, NCOL, FP8>;
+  constexpr int S = C::STAGES;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // TMA destinations and the 128-byte swizzle atoms need 1024-byte alignment of the shared-window
+  // offset (not of the generic address)
+  unsigned char* smem = smem_raw + ((1024u - (tc::sptr(smem_raw) & 1023u)) & 1023u);
+  unsigned char* qbuf = smem;                                         // QB x Q_BYTES
+  unsigned char* kbuf = qbuf + C::QB * C::Q_BYTES;                    // S x STAGE_BYTES
+  unsigned char* sbuf = kbuf + S * C::STAGE_BYTES;                    // S x STAGED_BYTES (FP8)
+  float* wsm = reinterpret_cast<float*>(sbuf + S * C::STAGED_BYTES);  // [EW][NCOL]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(wsm + C::W_FLOATS);
+  uint64_t* full = bars;              // [S] operand ready (TMA bytes, or converters)
+  uint64_t* empty = full + S;         // [S] operand consumed (MMA commit)
+  uint64_t* sfull = empty + S;        // [S] e4m3 staging landed (TMA)
+  uint64_t* sempty = sfull + S;       // [S] e4m3 staging consumed (converters)
+  uint64_t* qfull = sempty + S;       // [2]
+  uint64_t* qempty = qfull + 2;       // [2]
+  uint64_t* accfull = qempty + 2;     // [ACC]
+  uint64_t* accempty = accfull + 4;   // [ACC]
+  uint64_t* drain = accempty + 4;     // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ngroups = a.q_count;
+
+  // alignment the TMA / tensor-core path relies on; a violation is reported, never executed
+  {
+    const uint32_t bad = (tc::sptr(smem) & 1023u) | (tc::sptr(bars) & 7u) |
+                         static_cast<uint32_t>(reinterpret_cast<uintptr_t>(&kmap) & 63u) |
+                         static_cast<uint32_t>(reinterpret_cast<uintptr_t>(&qmap) & 63u);
+    if (bad != 0u) {
+      if (threadIdx.x == 0) report_error(a.status, CSA_ERR_DEVICE_CHECK, -1000 - static_cast<int>(bad));
+      return;
+    }
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      tc::mbar_init(&full[s], FP8 ? C::CW * 32 : 1);
+      tc::mbar_init(&empty[s], 1);
+      tc::mbar_init(&sfull[s], 1);
+      tc::mbar_init(&sempty[s], C::CW * 32 > 0 ? C::CW * 32 : 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&qfull[i], 1);
+      tc::mbar_init(&qempty[i], 1);
+    }
+    for (int i = 0; i < C::ACC; ++i) {
+      tc::mbar_init(&accfull[i], 1);
+      tc::mbar_init(&accempty[i], C::EW * 32);
+    }
+    tc::mbar_init(drain, 1);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::prefetch_tensormap(&kmap);
+    tc::prefetch_tensormap(&qmap);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto fail = [&](int where) {
+    *abort_flag = 1;
+    report_error(a.status, CSA_ERR_TIMEOUT, where);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int pend_parity[S];          // parity of the last load issued into each stage, -1 if none
+    int qpend[2] = {-1, -1};
+    for (int s = 0; s < S; ++s) pend_parity[s] = -1;
+    if (lane == 0) {
+      Walker wk;
+      wk.init(p, ngroups);
+      long long n = 0;
+      int gc = -1;
+      bool nw;
+      bool ok = true;
+      while (ok && wk.next(a, p, ngroups, nw)) {
+        if (nw) {
+          ++gc;
+          const int qb = gc % C::QB;
+          if (!tc::mbar_wait(&qempty[qb], ((gc / C::QB) & 1) ^ 1, abort_flag)) { fail(1); ok = false; break; }
+          tc::mbar_arrive_expect_tx(&qfull[qb], C::Q_BYTES);
+          const int z = wk.gi.b * a.Tq + wk.gi.i0;
+          for (int r = 0; r < C::NREG; ++r)
+            tc::tma_load_3d(qbuf + qb * C::Q_BYTES + r * C::Q_REGION, &qmap, r * 64, 0, z, &qfull[qb]);
+          qpend[qb] = (gc / C::QB) & 1;
+        }
+        const int s = static_cast<int>(n % S);
+        const uint32_t ph = static_cast<uint32_t>((n / S) & 1);
+        if (FP8) {
+          if (!tc::mbar_wait(&sempty[s], ph ^ 1, abort_flag)) { fail(2); ok = false; break; }
+          tc::mbar_arrive_expect_tx(&sfull[s], C::STAGED_BYTES);
+          tc::tma_load_3d(sbuf + s * C::STAGED_BYTES, &kmap, 0, wk.t * KT, wk.gi.b, &sfull[s]);
+        } else {
+          if (!tc::mbar_wait(&empty[s], ph ^ 1, abort_flag)) { fail(2); ok = false; break; }
+          tc::mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+          for (int r = 0; r < C::NREG; ++r)
+            tc::tma_load_3d(kbuf + s * C::STAGE_BYTES + r * C::KEY_REGION, &kmap, r * 64, wk.t * KT, wk.gi.b, &full[s]);
+        }
+        pend_parity[s] = static_cast<int>(ph);
+        ++n;
+      }
+      // drain: every copy this CTA issued has landed before the CTA may exit
+      for (int s = 0; s < S; ++s)
+        if (pend_parity[s] >= 0 && !tc::mbar_wait(FP8 ? &sfull[s] : &full[s], pend_parity[s], nullptr))
+          report_error(a.status, CSA_ERR_TIMEOUT, 9);
+      for (int i = 0; i < 2; ++i)
+        if (qpend[i] >= 0 && !tc::mbar_wait(&qfull[i], qpend[i], nullptr))
+          report_error(a.status, CSA_ERR_TIMEOUT, 9);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = tc::umma_idesc_bf16(KT, NCOL);
+    Walker wk;
+    wk.init(p, ngroups);
+    long long n = 0;
+    int gc = -1;
+    bool nw;
+    bool issued = false;
+    int ncommit_empty[S];              // commits issued to each barrier (lane 0)
+    int ncommit_q[2] = {0, 0};
+    for (int s = 0; s < S; ++s) ncommit_empty[s] = 0;
+    while (wk.next(a, p, ngroups, nw)) {
+      if (nw) {
+        ++gc;
+        if (gc >= 1 && lane == 0) {
+          tc::umma_commit(&qempty[(gc - 1) % C::QB]);
+          ++ncommit_q[(gc - 1) % C::QB];
+        }
+        if (!tc::mbar_wait(&qfull[gc % C::QB], (gc / C::QB) & 1, abort_flag)) { fail(3); break; }
+      }
+      const int s = static_cast<int>(n % S);
+      const uint32_t ph = static_cast<uint32_t>((n / S) & 1);
+      const int acc = static_cast<int>(n % C::ACC);
+      if (!tc::mbar_wait(&full[s], ph, abort_flag)) { fail(4); break; }
+      if (!tc::mbar_wait(&accempty[acc], ((n / C::ACC) & 1) ^ 1, abort_flag)) { fail(5); break; }
+      tc::tc_fence_after();
+      if (lane == 0) {
+        const uint32_t kaddr = tc::sptr(kbuf + s * C::STAGE_BYTES);
+        const uint32_t qaddr = tc::sptr(qbuf + (gc % C::QB) * C::Q_BYTES);
+#pragma unroll
+        for (int k = 0; k < DI / 16; ++k) {
+          const int r = k >> 2, off = (k & 3) * 32;
+          const uint64_t ad = tc::umma_desc_sw128(kaddr + r * C::KEY_REGION + off);
+          const uint64_t bd = tc::umma_desc_sw128(qaddr + r * C::Q_REGION + off);
+          tc::umma_bf16(tmem + acc * NCOL, ad, bd, idesc, k > 0 ? 1u : 0u);
+        }
+        tc::umma_commit(&empty[s]);
+        tc::umma_commit(&accfull[acc]);
+        ++ncommit_empty[s];
+        issued = true;
+      }
+      __syncwarp();
+      ++n;
+    }
+    // drain: all MMAs this thread issued have completed, and every arrival their commits
+    // trigger has landed, before tensor memory is released and the CTA's shared memory reused
+    if (lane == 0 && issued) {
+      tc::umma_commit(drain);
+      if (!tc::mbar_wait(drain, 0, nullptr)) report_error(a.status, CSA_ERR_TIMEOUT, 10);
+    }
+    if (lane == 0) {
+      for (int s = 0; s < S; ++s)
+        if (ncommit_empty[s] > 0 && !tc::mbar_wait(&empty[s], (ncommit_empty[s] - 1) & 1, nullptr))
+          report_error(a.status, CSA_ERR_TIMEOUT, 11);
+      for (int i = 0; i < 2; ++i)
+        if (ncommit_q[i] > 0 && !tc::mbar_wait(&qempty[i], (ncommit_q[i] - 1) & 1, nullptr))
+          report_error(a.status, CSA_ERR_TIMEOUT, 11);
+    }
+    __syncwarp();
+  } else if (warp >= 4 && warp < 4 + C::EW) {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 4;
+    const int quarter = warp & 3;                 // TMEM lanes [32*quarter, +32)
+    const int half = ew >> 2;                     // column split when EW = 8
+    constexpr int SPLIT = C::EW / 4;
+    const int NHP = p.NHP, G = p.G;
+    const int qs_per = (G + SPLIT - 1) / SPLIT;
+    const int j_lo = half * qs_per, j_hi = min(G, j_lo + qs_per);
+    float* wb = wsm + ew * NCOL;                  // this warp's copy of the group's head weights
+    Walker wk;
+    wk.init(p, ngroups);
+    long long n = 0;
+    bool nw;
+    while (wk.next(a, p, ngroups, nw)) {
+      if (nw) {
+        __syncwarp();
+        for (int c = j_lo * NHP + lane; c < j_hi * NHP; c += 32) {
+          const int j = c / NHP, h = c % NHP;
+          float v = 0.f;
+          if (j < wk.gi.nq && h < a.nI)
+            v = a.w[(static_cast<size_t>(wk.gi.b) * a.Tq + wk.gi.i0 + j) * a.nI + h];
+          wb[c] = v;
+        }
+        __syncwarp();
+      }
+      const int acc = static_cast<int>(n % C::ACC);
+      if (!tc::mbar_wait(&accfull[acc], (n / C::ACC) & 1, abort_flag)) { fail(6); break; }
+      tc::tc_fence_after();
+      const int key = wk.t * KT + quarter * 32 + lane;
+      float kscale = 1.f;
+      if (FP8 && key < a.N) kscale = a.kI_scale[static_cast<size_t>(wk.gi.b) * a.N + key];
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * NCOL;
+      for (int j = j_lo; j < j_hi; ++j) {
+        // four independent partial sums (fixed order: sum = (p0 + p1) + (p2 + p3))
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        if (NHP == 16) {
+          float v[16];
+          tc::tmem_ld16_wait(tbase + j * NHP, v);
+#pragma unroll
+          for (int h = 0; h < 16; ++h) ps[h & 3] = fmaf(wb[j * NHP + h], fmaxf(v[h], 0.f), ps[h & 3]);
+        } else {
+          for (int c0 = 0; c0 < NHP; c0 += 32) {
+            float v[32];
+            tc::tmem_ld32_wait(tbase + j * NHP + c0, v);
+#pragma unroll
+            for (int h = 0; h < 32; ++h) ps[h & 3] = fmaf(wb[j * NHP + c0 + h], fmaxf(v[h], 0.f), ps[h & 3]);
+          }
+        }
+        const float sum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        if (j < wk.gi.nq && key < a.N) {
+          const size_t qi = static_cast<size_t>(wk.gi.b) * a.Tq + wk.gi.i0 + j;
+          const int nv = n_visible(a.q_pos[qi], a.m, a.N);
+          float* dst = a.scores + (static_cast<long long>(qi) - a.score_row_offset) * a.N;
+          if (key < nv) dst[key] = sum * kscale;
+          else if (p.fill_invisible) dst[key] = -INFINITY;
+        }
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(&accempty[acc]);
+      ++n;
+    }
+  } else if (FP8 && warp >= 4 + C::EW) {
+    // ------------------------------------------------------------ e4m3 -> bf16 converters
+    const int ctid = threadIdx.x - 32 * (4 + C::EW);
+    Walker wk;
+    wk.init(p, ngroups);
+    long long n = 0;
+    bool nw;
+    constexpr int CPR = DI / 8;                   // 8-element chunks per row
+    while (wk.next(a, p, ngroups, nw)) {
+      const int s = static_cast<int>(n % S);
+      const uint32_t ph = static_cast<uint32_t>((n / S) & 1);
+      if (!tc::mbar_wait(&sfull[s], ph, abort_flag)) { fail(7); break; }
+      if (!tc::mbar_wait(&empty[s], ph ^ 1, abort_flag)) { fail(8); break; }
+      const unsigned char* src = sbuf + s * C::STAGED_BYTES;
+      unsigned char* dst = kbuf + s * C::STAGE_BYTES;
+      for (int c = ctid; c < KT * CPR; c += C::CW * 32) {
+        const int r = c / CPR, cc = c % CPR;
+        const uint2 v = *reinterpret_cast<const uint2*>(src + r * DI + cc * 8);
+        uint4 o;
+        o.x = half2_to_bf162_exact(e4m3x2_to_half2(static_cast<uint16_t>(v.x & 0xFFFF)));
+        o.y = half2_to_bf162_exact(e4m3x2_to_half2(static_cast<uint16_t>(v.x >> 16)));
+        o.z = half2_to_bf162_exact(e4m3x2_to_half2(static_cast<uint16_t>(v.y & 0xFFFF)));
+        o.w = half2_to_bf162_exact(e4m3x2_to_half2(static_cast<uint16_t>(v.y >> 16)));
+        const int region = cc >> 3, chunk = cc & 7;
+        *reinterpret_cast<uint4*>(dst + region * C::KEY_REGION + r * 128 + ((chunk ^ (r & 7)) << 4)) = o;
+      }
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(&full[s]);
+      tc::mbar_arrive(&sempty[s]);
+      ++n;
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == 1) tc::tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+bool make_map_3d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base, uint64_t d0, uint64_t d1,
+                 uint64_t d2, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * esize, d0 * d1 * esize};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n;
+}
+
+template <int DI, int NCOL, bool FP8>
+cudaError_t launch_t(const IndexArgs& a, const IndexGrouping& gr, int fill_invisible, cudaStream_t s,
+                     int* launches) {
+  using C = Cfg<DI, NCOL, FP8>;
+  CUtensorMap kmap, qmap;
+  bool ok;
+  if (FP8)
+    ok = make_map_3d(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.kI, DI, a.N, a.B, DI, KT, 1,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
+  else
+    ok = make_map_3d(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.kI, DI, a.N, a.B, 64, KT, 1,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_map_3d(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.qI, DI, a.nI,
+                         static_cast<uint64_t>(a.B) * a.Tq, 64, gr.NHP, gr.G, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return cudaErrorInvalidValue;
+  TcParams p;
+  p.G = gr.G;
+  p.NHP = gr.NHP;
+  p.tiles_max = (a.N + KT - 1) / KT;
+  p.fill_invisible = fill_invisible;
+  const int sms = sm_count();
+  const long long groups = a.q_count;
+  p.mode = groups >= 4LL * sms ? 1 : 0;
+  p.F = groups * p.tiles_max;
+  long long grid = sms;
+  if (p.mode == 0 && p.F < grid) grid = p.F;
+  if (grid < 1) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(k_index_score<DI, NCOL, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.N + KT - 1) / KT, a.q_count);
-  k_index_score<DI, FP8><<<grid, NTHREADS, smem, s>>>(a, G, NH, a.q_begin, fill_invisible);
+  k_index_score<DI, NCOL, FP8><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, s>>>(a, kmap, qmap, p);
   ++*launches;
   return cudaGetLastError();
 }
 
+template <int DI, bool FP8>
+cudaError_t launch_di(const IndexArgs& a, const IndexGrouping& gr, int fill, cudaStream_t s, int* launches) {
+  switch (gr.NCOL) {
+    case 16: return launch_t<DI, 16, FP8>(a, gr, fill, s, launches);
+    case 32: return launch_t<DI, 32, FP8>(a, gr, fill, s, launches);
+    case 64: return launch_t<DI, 64, FP8>(a, gr, fill, s, launches);
+    case 128: return launch_t<DI, 128, FP8>(a, gr, fill, s, launches);
+    case 256: return launch_t<DI, 256, FP8>(a, gr, fill, s, launches);
+  }
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
-// a.q_begin / a.q_count: range of query GROUPS (G consecutive queries of one sequence).
-cudaError_t launch_index_score_groups(const IndexArgs& a, int G, int fill_invisible, cudaStream_t s,
-                                      int* launches) {
-  if (a.dI == 128) return a.fp8 ? launch_t<128, true>(a, G, fill_invisible, s, launches)
-                                : launch_t<128, false>(a, G, fill_invisible, s, launches);
-  if (a.dI == 64) return a.fp8 ? launch_t<64, true>(a, G, fill_invisible, s, launches)
-                               : launch_t<64, false>(a, G, fill_invisible, s, launches);
+// a.q_begin / a.q_count: range of query GROUPS (gr.G consecutive queries of one sequence).
+cudaError_t launch_index_score_groups(const IndexArgs& a, const IndexGrouping& gr, int fill_invisible,
+                                      cudaStream_t s, int* launches) {
+  if (a.q_count <= 0 || a.N <= 0) return cudaSuccess;
+  if (a.dI == 128) return a.fp8 ? launch_di<128, true>(a, gr, fill_invisible, s, launches)
+                                : launch_di<128, false>(a, gr, fill_invisible, s, launches);
+  if (a.dI == 64) return a.fp8 ? launch_di<64, true>(a, gr, fill_invisible, s, launches)
+                               : launch_di<64, false>(a, gr, fill_invisible, s, launches);
   return cudaErrorInvalidValue;
 }
 

@@ -1,32 +1,40 @@
 // Per-query top-k over the visible indexer scores ("DeepSeek V4 模型技术大全", CSA path, the TopK_k
 // equation), ties to the smaller entry index.
 //
-// Radix select on order-preserving 32-bit keys of the fp32 scores, three digit passes
-// (11 / 11 / 10 bits).  One thread-block cluster of CS CTAs owns one query: each CTA keeps a
-// contiguous slice of the candidates in shared memory, builds its digit histogram with shared
-// atomics, and every CTA sums the CS histograms through distributed shared memory, so all CTAs
-// agree on the digit without a second kernel.  The final compaction writes, in increasing entry
-// index, the entries above the k-th score and then the ties taken in increasing index, so the
-// output is deterministic and depends only on the query's own scores.
-#include <cooperative_groups.h>
-
+// Radix select on order-preserving 32-bit keys of the fp32 scores, one CTA per slice of at most
+// 32768 candidates, everything in that CTA's shared memory (no clusters, no inter-CTA waits).
+// The first 11-bit digit starts at the highest bit where the slice's largest and smallest keys
+// differ (the bits above are common to all of them), so the histogram spreads over the scores'
+// actual range; each pass narrows the threshold bin, and the search stops once the threshold bin
+// is taken whole or all 32 bits are fixed.  The selected set is written in increasing entry
+// index: entries above the threshold bin and, inside it, the smallest indices first.
+//
+// Rows longer than one slice run in two stages: every slice writes its own top-k (key, index)
+// candidates in index order, and a merge CTA selects the top-k of the concatenation.  This is
+// exact: an entry of the row's top-k is also in its slice's top-k (with the same smaller-index
+// rule for ties), and the concatenated candidates stay in increasing index order.
+// The result depends only on the query's own scores (batch-invariant and deterministic).
 #include "common.cuh"
 
 namespace csa {
 
 namespace {
 
-namespace cg = cooperative_groups;
+constexpr int kSlice = 32768;        // longest slice per CTA (128 KB of keys in shared memory)
+constexpr int kMinSlice = 4096;      // slices are not split below this length
+constexpr int kMergeCap = 16384;     // candidates one merge CTA holds (keys + indices: 128 KB)
+constexpr int kTargetCtas = 128;     // split rows until the first stage has about this many CTAs
+constexpr int kDigit = 11;
+constexpr int kBins = 1 << kDigit;
+constexpr uint32_t kNoIndex = 0xFFFFFFFFu;
 
-constexpr int TK_THREADS = 1024;
-constexpr int kMaxSlice = 32768;     // candidates held per CTA (128 KB of keys)
-
+// Order-preserving key of a score; -0 and +0 map to the same key (equal scores tie by index).
 __device__ __forceinline__ uint32_t order_key(float f) {
-  const uint32_t u = __float_as_uint(f);
+  const uint32_t u = __float_as_uint(f + 0.0f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive block-wide scan of 64-bit sums.  ws: 33 slots of shared memory.
+// Exclusive block-wide scan of 64-bit values.  ws: 33 slots of shared memory.
 __device__ __forceinline__ unsigned long long block_excl_scan(unsigned long long v, unsigned long long* ws,
                                                               unsigned long long* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -40,14 +48,14 @@ __device__ __forceinline__ unsigned long long block_excl_scan(unsigned long long
   if (lane == 31) ws[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    unsigned long long x = lane < nwarps ? ws[lane] : 0ull;
+    const unsigned long long x = lane < nwarps ? ws[lane] : 0ull;
     unsigned long long xi = x;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const unsigned long long y = __shfl_up_sync(0xffffffffu, xi, o);
       if (lane >= o) xi += y;
     }
-    ws[lane] = xi - x;          // exclusive prefix of warp totals
+    ws[lane] = xi - x;
     if (lane == 31) ws[32] = xi;
   }
   __syncthreads();
@@ -57,150 +65,352 @@ __device__ __forceinline__ unsigned long long block_excl_scan(unsigned long long
   return r;
 }
 
-__global__ void __launch_bounds__(TK_THREADS) k_topk(TopkArgs a, int CS, int cap) {
-  extern __shared__ __align__(16) uint32_t tsm[];
-  uint32_t* keys = tsm;                                       // [cap]
-  uint32_t* hist = tsm + cap;                                 // [2][2048]
-  unsigned long long* ws = reinterpret_cast<unsigned long long*>(hist + 4096);   // [33]
-  uint32_t* xchg = reinterpret_cast<uint32_t*>(ws + 34);     // [0] gt count, [1] eq count, [2..3] sel
+struct TkSmem {
+  uint32_t* keys;              // [cap]
+  uint32_t* idx;               // [cap] (merge stage) or nullptr (index = base + position)
+  uint32_t* hist;              // [kBins]
+  uint32_t* red;               // [64]
+  unsigned long long* ws;      // [34]
+  uint32_t* xchg;              // [8]
+};
 
-  cg::cluster_group cluster = cg::this_cluster();
-  const int rank = static_cast<int>(cluster.block_rank());
-  const int tid = threadIdx.x;
-  const long long qi = a.q_begin + blockIdx.x / CS;          // flattened query index
-  const int t = a.q_pos[qi];
-  const int n = n_visible(t, a.m, a.N);
-  int32_t* out = a.idx_out + qi * a.k;
-
-  if (n <= a.k) {      // every visible entry is selected; no cluster communication
-    if (rank == 0)
-      for (int i = tid; i < a.k; i += TK_THREADS) out[i] = i < n ? i : -1;
-    return;
+// Block-wide top-k of keys[0, L) (L > k), written in increasing position order through emit(pos,
+// j) for the j-th selected element, j in [0, k).
+template <int NT, typename Emit>
+__device__ void select_block(const TkSmem& sm, int L, int k, Emit emit) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t kmax = 0u, kmin = 0xFFFFFFFFu;
+  for (int i = tid; i < L; i += NT) {
+    const uint32_t kk = sm.keys[i];
+    kmax = max(kmax, kk);
+    kmin = min(kmin, kk);
   }
-
-  const float* row = a.scores + (qi - a.score_row_offset) * static_cast<long long>(a.N);
-  const int lo = static_cast<int>(static_cast<long long>(n) * rank / CS);
-  const int hi = static_cast<int>(static_cast<long long>(n) * (rank + 1) / CS);
-  const int L = hi - lo;
-  for (int i = tid; i < L; i += TK_THREADS) keys[i] = order_key(row[lo + i]);
-
-  if (tid == 0) { xchg[2] = 0; xchg[3] = 0; }
-  uint32_t prefix = 0, pmask = 0;
-  int remaining = a.k;
-  for (int p = 0; p < 3; ++p) {
-    const int shift = p == 0 ? 21 : (p == 1 ? 10 : 0);
-    const int nb = p == 2 ? 1024 : 2048;
-    uint32_t* h = hist + (p & 1) * 2048;
-    for (int i = tid; i < 2048; i += TK_THREADS) h[i] = 0;
-    __syncthreads();
-    // warp-aggregated histogram: the scores of one query crowd into a few leading-digit bins, so
-    // lanes that hit the same bin are merged with a match before one atomic per distinct bin
-    const int rounds = (L + TK_THREADS - 1) / TK_THREADS;
-    for (int rd = 0; rd < rounds; ++rd) {
-      const int i = rd * TK_THREADS + tid;
-      uint32_t bin = 0xFFFFFFFFu;
-      if (i < L) {
-        const uint32_t kk = keys[i];
-        if ((kk & pmask) == prefix) bin = (kk >> shift) & static_cast<uint32_t>(nb - 1);
-      }
-      const unsigned grp = __match_any_sync(0xffffffffu, bin);
-      if (bin != 0xFFFFFFFFu && (tid & 31) == __ffs(grp) - 1) atomicAdd(&h[bin], static_cast<uint32_t>(__popc(grp)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+  }
+  if (lane == 0) {
+    sm.red[warp] = kmax;
+    sm.red[32 + warp] = kmin;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t mx = lane < NT / 32 ? sm.red[lane] : 0u;
+    uint32_t mn = lane < NT / 32 ? sm.red[32 + lane] : 0xFFFFFFFFu;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
     }
-    cluster.sync();
-    // thread tid owns the bins at descending positions 2*tid and 2*tid+1
-    const int bA = nb - 1 - 2 * tid, bB = nb - 2 - 2 * tid;
-    uint32_t cA = 0, cB = 0;
-    for (int r = 0; r < CS; ++r) {
-      const uint32_t* rh = cluster.map_shared_rank(h, r);
-      if (bA >= 0) cA += rh[bA];
-      if (bB >= 0) cB += rh[bB];
+    if (lane == 0) {
+      sm.xchg[5] = mx;
+      sm.xchg[6] = mn;
+    }
+  }
+  __syncthreads();
+  const uint32_t gmax = sm.xchg[5], gmin = sm.xchg[6];
+  // bits at and above `pos` are common to every key of the list
+  int pos = (gmax == gmin) ? 0 : 32 - __clz(gmax ^ gmin);
+  uint32_t prefix = pos >= 32 ? 0u : (gmax >> pos) << pos;
+  int remaining = k;
+  int cmp_shift = pos;
+  while (pos > 0) {
+    const int nbits = pos < kDigit ? pos : kDigit;
+    const int shift = pos - nbits;
+    const uint32_t dmask = (1u << nbits) - 1u;
+    const uint32_t hmask = pos >= 32 ? 0u : ~((1u << pos) - 1u);
+    for (int i = tid; i < kBins; i += NT) sm.hist[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < L; i += NT) {
+      const uint32_t kk = sm.keys[i];
+      if ((kk & hmask) == prefix) atomicAdd(&sm.hist[(kk >> shift) & dmask], 1u);
+    }
+    __syncthreads();
+    // thread tid owns the PER bins at descending positions [PER*tid, PER*tid + PER)
+    constexpr int PER = kBins / NT;
+    const int nb = 1 << nbits;
+    uint32_t c[PER];
+    uint32_t csum = 0;
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int bin = nb - 1 - (PER * tid + u);
+      c[u] = bin >= 0 ? sm.hist[bin] : 0u;
+      csum += c[u];
     }
     unsigned long long tot;
-    const unsigned long long above = block_excl_scan(cA + cB, ws, &tot);
+    unsigned long long above = block_excl_scan(csum, sm.ws, &tot);
     const unsigned long long rem = static_cast<unsigned long long>(remaining);
-    if (bA >= 0 && above < rem && rem <= above + cA) {
-      xchg[2] = static_cast<uint32_t>(bA);
-      xchg[3] = static_cast<uint32_t>(rem - above);
-    } else if (bB >= 0 && above + cA < rem && rem <= above + cA + cB) {
-      xchg[2] = static_cast<uint32_t>(bB);
-      xchg[3] = static_cast<uint32_t>(rem - above - cA);
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      if (above < rem && rem <= above + c[u]) {
+        sm.xchg[2] = static_cast<uint32_t>(nb - 1 - (PER * tid + u));
+        sm.xchg[3] = static_cast<uint32_t>(rem - above);
+        sm.xchg[4] = c[u];
+      }
+      above += c[u];
     }
     __syncthreads();
-    prefix |= xchg[2] << shift;
-    pmask |= static_cast<uint32_t>(nb - 1) << shift;
-    remaining = static_cast<int>(xchg[3]);
+    prefix |= (sm.xchg[2] & dmask) << shift;
+    remaining = static_cast<int>(min(sm.xchg[3], static_cast<uint32_t>(remaining)));
+    const uint32_t bin_count = sm.xchg[4];
+    pos = shift;
+    cmp_shift = shift;
     __syncthreads();
+    if (bin_count == static_cast<uint32_t>(remaining)) break;   // the threshold bin is taken whole
   }
-  const uint32_t thr = prefix;     // key of the k-th largest score; `remaining` ties are taken
-
-  // counts per thread over a contiguous run of the slice (keeps index order)
-  const int per = (L + TK_THREADS - 1) / TK_THREADS;
-  const int i_lo = min(L, tid * per), i_hi = min(L, i_lo + per);
+  // selected: key >> cmp_shift above thr, or equal to it among the first `remaining` positions.
+  // Each warp owns a contiguous range and walks it 32 consecutive keys at a time (conflict-free
+  // shared-memory reads); ballots give every lane its rank inside the range, so the output keeps
+  // increasing position order.
+  const uint32_t thr = cmp_shift >= 32 ? 0u : prefix >> cmp_shift;
+  constexpr int NW = NT / 32;
+  const int per_w = ((L + NW - 1) / NW + 31) & ~31;
+  const int w_lo = min(L, warp * per_w), w_hi = min(L, w_lo + per_w);
+  const uint32_t lt_mask = (1u << lane) - 1u;
   uint32_t gt = 0, eq = 0;
-  for (int i = i_lo; i < i_hi; ++i) {
-    const uint32_t kk = keys[i];
-    gt += kk > thr;
-    eq += kk == thr;
+  for (int base = w_lo; base < w_hi; base += 32) {
+    const int i = base + lane;
+    uint32_t kt = 0;
+    const bool in = i < w_hi;
+    if (in) kt = cmp_shift >= 32 ? 0u : sm.keys[i] >> cmp_shift;
+    gt += __popc(__ballot_sync(0xffffffffu, in && kt > thr));
+    eq += __popc(__ballot_sync(0xffffffffu, in && kt == thr));
   }
   unsigned long long tot;
-  const unsigned long long ex = block_excl_scan((static_cast<unsigned long long>(gt) << 32) | eq, ws, &tot);
-  if (tid == 0) {
-    xchg[0] = static_cast<uint32_t>(tot >> 32);
-    xchg[1] = static_cast<uint32_t>(tot & 0xFFFFFFFFu);
+  // one value per warp enters the scan (lanes other than 0 contribute zero)
+  const unsigned long long ex = block_excl_scan(lane == 0 ? (static_cast<unsigned long long>(gt) << 32) | eq : 0ull,
+                                                sm.ws, &tot);
+  const unsigned long long exw = __shfl_sync(0xffffffffu, ex, 0);
+  uint32_t g_before = static_cast<uint32_t>(exw >> 32);
+  uint32_t e_before = static_cast<uint32_t>(exw & 0xFFFFFFFFu);
+  const uint32_t rem = static_cast<uint32_t>(remaining);
+  for (int base = w_lo; base < w_hi; base += 32) {
+    const int i = base + lane;
+    uint32_t kt = 0;
+    const bool in = i < w_hi;
+    if (in) kt = cmp_shift >= 32 ? 0u : sm.keys[i] >> cmp_shift;
+    const uint32_t mg = __ballot_sync(0xffffffffu, in && kt > thr);
+    const uint32_t me = __ballot_sync(0xffffffffu, in && kt == thr);
+    const uint32_t g_rank = g_before + __popc(mg & lt_mask);
+    const uint32_t e_rank = e_before + __popc(me & lt_mask);
+    bool take = false;
+    if (in && kt > thr) take = true;
+    if (in && kt == thr) take = e_rank < rem;
+    if (take) {
+      const uint32_t j = g_rank + min(e_rank, rem);
+      if (j < static_cast<uint32_t>(k)) emit(i, static_cast<int>(j));
+    }
+    g_before += __popc(mg);
+    e_before += __popc(me);
   }
-  cluster.sync();
-  uint32_t gt_off = 0, eq_off = 0;
-  for (int r = 0; r < rank; ++r) {
-    const uint32_t* rx = cluster.map_shared_rank(xchg, r);
-    gt_off += rx[0];
-    eq_off += rx[1];
-  }
-  uint32_t g_rank = gt_off + static_cast<uint32_t>(ex >> 32);
-  uint32_t e_rank = eq_off + static_cast<uint32_t>(ex & 0xFFFFFFFFu);
-  const uint32_t base_eq = static_cast<uint32_t>(a.k - min(remaining, a.k));
-  for (int i = i_lo; i < i_hi; ++i) {
-    const uint32_t kk = keys[i];
-    if (kk > thr) {
-      if (g_rank < base_eq) out[g_rank] = lo + i;
-      ++g_rank;
-    } else if (kk == thr) {
-      if (e_rank < static_cast<uint32_t>(remaining)) out[base_eq + e_rank] = lo + i;
-      ++e_rank;
+}
+
+// keys[i] = order_key(src[i]) for i < L, eight independent loads in flight per thread.
+template <int NT>
+__device__ __forceinline__ void load_keys(uint32_t* keys, const float* src, int L) {
+  constexpr int U = 8;
+  for (int base = 0; base < L; base += NT * U) {
+    float v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * NT + threadIdx.x;
+      v[u] = i < L ? __ldg(src + i) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * NT + threadIdx.x;
+      if (i < L) keys[i] = order_key(v[u]);
     }
   }
-  cluster.sync();   // no CTA leaves while another may still read its shared memory
+}
+
+__device__ __forceinline__ TkSmem carve(uint32_t* base, int cap, bool with_idx) {
+  TkSmem s;
+  s.keys = base;
+  s.idx = with_idx ? base + cap : nullptr;
+  s.hist = base + cap * (with_idx ? 2 : 1);
+  s.red = s.hist + kBins;
+  s.ws = reinterpret_cast<unsigned long long*>(s.red + 64);
+  s.xchg = reinterpret_cast<uint32_t*>(s.ws + 34);
+  return s;
+}
+
+// Stage 1: one CTA per (query, slice of slice_len candidates).  S == 1 writes the final row;
+// S > 1 writes the slice's k candidates (key << 32 | index, index order, unused slots
+// (0, kNoIndex)) to cand.
+template <int NT>
+__global__ void __launch_bounds__(NT) k_topk_slice(TopkArgs a, int S, int slice_len, int cap,
+                                                   unsigned long long* cand) {
+  extern __shared__ __align__(16) uint32_t tsm[];
+  const TkSmem sm = carve(tsm, cap, false);
+  const int tid = threadIdx.x;
+  const long long qrel = blockIdx.x / S;
+  const int sl = static_cast<int>(blockIdx.x % S);
+  const long long qi = a.q_begin + qrel;
+  const int n = n_visible(a.q_pos[qi], a.m, a.N);
+  const int k = a.k;
+  const int lo = sl * slice_len;
+  const int L = max(0, min(n, lo + slice_len) - lo);
+  if (S == 1) {
+    int32_t* out = a.idx_out + qi * k;
+    if (n <= k) {
+      for (int i = tid; i < k; i += NT) out[i] = i < n ? i : -1;
+      return;
+    }
+    if (L > cap) {                       // cannot happen with a valid launch; never index past cap
+      if (tid == 0) report_error(a.status, CSA_ERR_DEVICE_CHECK, L);
+      return;
+    }
+    const float* row = a.scores + (qi - a.score_row_offset) * static_cast<long long>(a.N);
+    load_keys<NT>(sm.keys, row + lo, L);
+    __syncthreads();
+    select_block<NT>(sm, L, k, [&](int i, int j) { out[j] = lo + i; });
+    return;
+  }
+  unsigned long long* crow = cand + (qrel * S + sl) * static_cast<long long>(k);
+  if (L <= k) {
+    const float* row = a.scores + (qi - a.score_row_offset) * static_cast<long long>(a.N);
+    for (int i = tid; i < k; i += NT)
+      crow[i] = i < L ? (static_cast<unsigned long long>(order_key(row[lo + i])) << 32) | static_cast<uint32_t>(lo + i)
+                      : static_cast<unsigned long long>(kNoIndex);
+    return;
+  }
+  if (L > cap) {
+    if (tid == 0) report_error(a.status, CSA_ERR_DEVICE_CHECK, L);
+    return;
+  }
+  const float* row = a.scores + (qi - a.score_row_offset) * static_cast<long long>(a.N);
+  load_keys<NT>(sm.keys, row + lo, L);
+  __syncthreads();
+  select_block<NT>(sm, L, k, [&](int i, int j) {
+    crow[j] = (static_cast<unsigned long long>(sm.keys[i]) << 32) | static_cast<uint32_t>(lo + i);
+  });
+}
+
+// Stage 2: one CTA per query merges the S * k candidates of its slices.
+template <int NT>
+__global__ void __launch_bounds__(NT) k_topk_merge(TopkArgs a, int S, int cap, const unsigned long long* cand) {
+  extern __shared__ __align__(16) uint32_t tsm[];
+  const TkSmem sm = carve(tsm, cap, true);
+  const int tid = threadIdx.x;
+  const long long qrel = blockIdx.x;
+  const long long qi = a.q_begin + qrel;
+  const int k = a.k;
+  int32_t* out = a.idx_out + qi * k;
+  const int n = n_visible(a.q_pos[qi], a.m, a.N);
+  if (n <= k) {
+    for (int i = tid; i < k; i += NT) out[i] = i < n ? i : -1;
+    return;
+  }
+  const int total = S * k;
+  if (total > cap) {
+    if (tid == 0) report_error(a.status, CSA_ERR_DEVICE_CHECK, total);
+    return;
+  }
+  // compact the valid candidates (they are already in increasing index order); each warp owns a
+  // contiguous range read 32 consecutive candidates at a time
+  const unsigned long long* crow = cand + qrel * static_cast<long long>(total);
+  const int lane = tid & 31, warp = tid >> 5;
+  constexpr int NW = NT / 32;
+  const int per_w = ((total + NW - 1) / NW + 31) & ~31;
+  const int w_lo = min(total, warp * per_w), w_hi = min(total, w_lo + per_w);
+  uint32_t cnt = 0;
+  for (int base = w_lo; base < w_hi; base += 32) {
+    const int i = base + lane;
+    const bool valid = i < w_hi && static_cast<uint32_t>(crow[i] & 0xFFFFFFFFull) != kNoIndex;
+    cnt += __popc(__ballot_sync(0xffffffffu, valid));
+  }
+  unsigned long long tot;
+  const unsigned long long exs = block_excl_scan(lane == 0 ? cnt : 0u, sm.ws, &tot);
+  uint32_t p = static_cast<uint32_t>(__shfl_sync(0xffffffffu, exs, 0));
+  for (int base = w_lo; base < w_hi; base += 32) {
+    const int i = base + lane;
+    unsigned long long c = 0;
+    bool valid = false;
+    if (i < w_hi) {
+      c = crow[i];
+      valid = static_cast<uint32_t>(c & 0xFFFFFFFFull) != kNoIndex;
+    }
+    const uint32_t m = __ballot_sync(0xffffffffu, valid);
+    const uint32_t q = p + __popc(m & ((1u << lane) - 1u));
+    if (valid && q < static_cast<uint32_t>(cap)) {
+      sm.keys[q] = static_cast<uint32_t>(c >> 32);
+      sm.idx[q] = static_cast<uint32_t>(c & 0xFFFFFFFFull);
+    }
+    p += __popc(m);
+  }
+  __syncthreads();
+  const int L = static_cast<int>(min(tot, static_cast<unsigned long long>(cap)));
+  if (L <= k) {                          // fewer valid candidates than k (n > k makes this rare)
+    for (int i = tid; i < k; i += NT) out[i] = i < L ? static_cast<int32_t>(sm.idx[i]) : -1;
+    return;
+  }
+  select_block<NT>(sm, L, k, [&](int i, int j) { out[j] = static_cast<int32_t>(sm.idx[i]); });
+}
+
+size_t slice_smem(int cap, bool with_idx) {
+  return static_cast<size_t>(cap) * 4 * (with_idx ? 2 : 1) + kBins * 4 + 64 * 4 + 34 * 8 + 8 * 4;
 }
 
 }  // namespace
 
-cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s, int* launches) {
-  if (a.q_count == 0) return cudaSuccess;
-  // one CTA holds up to 32768 candidates in shared memory; longer rows spread over a cluster
-  int CS = (a.N + kMaxSlice - 1) / kMaxSlice;
-  if (CS < 1) CS = 1;
-  if (CS > 8) CS = 8;
-  const int cap = ((a.N + CS - 1) / CS + 3) & ~3;   // keeps the 64-bit scan slots 8-byte aligned
-  if (cap > kMaxSlice) return cudaErrorInvalidValue;
-  const size_t smem = static_cast<size_t>(cap) * 4 + 4096 * 4 + 34 * 8 + 16;
-  cudaError_t e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+// Slice length for Q queries of N candidates: one slice when the batch alone fills the GPU,
+// otherwise halved (down to kMinSlice) until about kTargetCtas first-stage CTAs run, as long as
+// the merge still holds every candidate.  Depends only on (Q, N, k), never on the device.
+int topk_slice_len(int Q, int N, int k) {
+  int len = kSlice;
+  auto slices = [&](int l) { return (N + l - 1) / l; };
+  while (len > kMinSlice && static_cast<long long>(Q) * slices(len) < kTargetCtas && slices(len / 2) > 1 &&
+         static_cast<long long>(slices(len / 2)) * k <= kMergeCap)
+    len /= 2;
+  return len;
+}
+
+int topk_slices(int Q, int N, int k) {
+  const int len = topk_slice_len(Q, N, k);
+  return N <= len ? 1 : (N + len - 1) / len;
+}
+
+size_t topk_candidate_bytes(int Q, int N, int k) {
+  const int S = topk_slices(Q, N, k);
+  return S > 1 ? static_cast<size_t>(Q) * S * k * sizeof(unsigned long long) : 0;
+}
+
+template <int NT>
+cudaError_t launch_slice(const TopkArgs& a, int S, int len, int cap, unsigned long long* cand, cudaStream_t s) {
+  const size_t smem = slice_smem(cap, false);
+  cudaError_t e = cudaFuncSetAttribute(k_topk_slice<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(a.q_count) * CS, 1, 1);
-  cfg.blockDim = dim3(TK_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CS;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, k_topk, a, CS, cap);
-  ++*launches;
-  if (e != cudaSuccess) return e;
+  k_topk_slice<NT><<<static_cast<unsigned>(a.q_count) * S, NT, smem, s>>>(a, S, len, cap, cand);
   return cudaGetLastError();
+}
+
+template <int NT>
+cudaError_t launch_merge(const TopkArgs& a, int S, int cap, const unsigned long long* cand, cudaStream_t s) {
+  const size_t smem = slice_smem(cap, true);
+  cudaError_t e = cudaFuncSetAttribute(k_topk_merge<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  k_topk_merge<NT><<<static_cast<unsigned>(a.q_count), NT, smem, s>>>(a, S, cap, cand);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const TopkArgs& a, void* cand_ws, cudaStream_t s, int* launches) {
+  if (a.q_count == 0) return cudaSuccess;
+  const int len = topk_slice_len(a.q_count, a.N, a.k);
+  const int S = topk_slices(a.q_count, a.N, a.k);
+  if (S > 1 && (cand_ws == nullptr || static_cast<long long>(S) * a.k > kMergeCap)) return cudaErrorInvalidValue;
+  const int cap1 = S == 1 ? ((a.N + 3) & ~3) : len;
+  unsigned long long* cand = static_cast<unsigned long long*>(cand_ws);
+  cudaError_t e = launch_slice<1024>(a, S, len, cap1, cand, s);
+  ++*launches;
+  if (e != cudaSuccess || S == 1) return e;
+  const int cap2 = (S * a.k + 3) & ~3;
+  e = launch_merge<1024>(a, S, cap2, cand, s);
+  ++*launches;
+  return e;
 }
 
 }  // namespace csa

@@ -120,9 +120,9 @@ def _adesc(**kw):
 
 
 def test_attend_validation_and_workspace():
-    # decode splits 640 slots into 256-slot pieces: partial results per split live in the workspace
+    # decode splits 640 slots into 192-slot pieces: partial results per split live in the workspace
     ws = C.lib.csa_attend_workspace(ctypes.byref(_adesc(k=512)))
-    assert ws == 256 + 2 * 3 * 64 * (512 + 2) * 4
+    assert ws == 256 + 2 * 4 * 64 * (512 + 2) * 4
     assert C.lib.csa_attend_workspace(ctypes.byref(_adesc(Tq=8, k=512))) == 256     # prefill: one split
 
     def call(desc, ws_bytes=1 << 30, **p):
