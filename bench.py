@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--workload", default="csa_decode_128k_b32", choices=DECODE_WORKLOADS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-prefill", action="store_true", help="skip the 65536-token prefill leg")
+    ap.add_argument("--prefill-steps", type=int, default=3)
     ap.add_argument("--quick", action="store_true",
                     help="time exactly one block of K steps; no clock sampling, e2e or CPU leg (for profilers)")
     return ap.parse_args()
@@ -204,6 +206,82 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+# ------------------------------------------------------------------------------------------ prefill leg
+def prefill_flops(w):
+    """Algorithmic tensor work of one prefill chunk: indexer 2*nI*dI per visible (query, entry)
+    pair; attention 4*H*d per (query, head, attended row) over min(k, N_vis) entries + window."""
+    vis = [min(w.N, (t + 1) // w.m) for t in range(w.T)]
+    idx_flops = sum(vis) * 2 * w.nI * w.dI
+    rows = sum(min(w.k, v) + min(w.window, t + 1) for t, v in enumerate(vis))
+    att_flops = rows * 4 * w.H * w.d
+    return idx_flops, att_flops
+
+
+def run_prefill(args, dev, stream):
+    """One CSA prefill chunk (T = 65536) through the four calls, timed per call with CUDA events."""
+    import torch
+    from long_context_compressed_16_b300 import capi as C
+    from long_context_compressed_16_b300 import pipeline as P
+    from long_context_compressed_16_b300 import synth as S
+
+    w = S.WORKLOADS["csa_prefill_t65536"]
+    inp = S.make_inputs(w, dev)
+    sptr = stream.cuda_stream
+    kv = torch.empty((1, w.N, w.d), dtype=torch.bfloat16, device=dev)
+    kI = torch.empty((1, w.N, w.dI), dtype=torch.bfloat16, device=dev)
+    idx = torch.empty((1, w.T, w.k), dtype=torch.int32, device=dev)
+    out = torch.empty((1, w.T, w.H, w.d), dtype=torch.bfloat16, device=dev)
+    idesc = P.index_desc(1, w.T, w.N, w.nI, w.dI, w.k, w.m)
+    adesc = P.attend_desc(1, w.T, w.N, w.H, w.d, k=w.k, m=w.m, Wcap=w.T, window=w.window)
+    ws_i = torch.empty(max(256, C.csa_index_topk_workspace(idesc)), dtype=torch.uint8, device=dev)
+    ws_a = torch.empty(max(256, C.csa_attend_workspace(adesc)), dtype=torch.uint8, device=dev)
+
+    def step(evs=None):
+        rec = (lambda i: evs[i].record(stream)) if evs else (lambda i: None)
+        rec(0)
+        P.compress(inp["Ca"], inp["Za"], w.m, Cb=inp["Cb"], Zb=inp["Zb"], out=kv, stream=sptr)
+        P.compress(inp["Ca_I"], inp["Za_I"], w.m, Cb=inp["Cb_I"], Zb=inp["Zb_I"], rope=False, rope_dims=0, out=kI,
+                   stream=sptr)
+        rec(1)
+        C.check(C.csa_index_topk(idesc, inp["qI"], inp["w"], kI, None, inp["q_pos"], idx, None, ws_i, stream=sptr),
+                "csa_index_topk")
+        rec(2)
+        C.check(C.csa_attend(adesc, inp["q"], kv, idx, inp["win"], inp["sink"], inp["q_pos"], out, None, ws_a,
+                             stream=sptr), "csa_attend")
+        rec(3)
+
+    step()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(max(1, args.prefill_steps)):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        step(evs)
+        torch.cuda.synchronize()
+        times.append([evs[i].elapsed_time(evs[i + 1]) for i in range(3)])
+    comp, ind, att = (statistics.median(x[i] for x in times) for i in range(3))
+    total = comp + ind + att
+    idx_flops, att_flops = prefill_flops(w)
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        pk = json.load(f)
+    peak = pk.get("bf16_tflops_sustained", 1386.7)
+    ind_tf = idx_flops / (ind * 1e-3) / 1e12
+    att_tf = att_flops / (att * 1e-3) / 1e12
+    comp_bytes = w.T * (4 * w.d + 4 * w.dI) * 2 + w.N * (w.d + w.dI) * 2
+    del inp, kv, kI, idx, out, ws_i, ws_a
+    torch.cuda.empty_cache()
+    return {
+        "workload": "csa_prefill_t65536", "tok_per_s": w.T / (total * 1e-3), "ms_per_chunk": total,
+        "steps": len(times),
+        "breakdown_ms": {"csa_compress_x2": comp, "csa_index_topk": ind, "csa_attend": att},
+        "indexer_tensor": {"achieved": ind_tf, "peak": peak, "unit": "TFLOP/s", "frac": ind_tf / peak,
+                           "flops_per_launch": idx_flops, "peak_kind": "measured sustained",
+                           "note": "scores (tcgen05) + top-k of all 65536 queries; flops are the score contraction"},
+        "attend_tensor": {"achieved": att_tf, "peak": peak, "unit": "TFLOP/s", "frac": att_tf / peak,
+                          "flops_per_launch": att_flops},
+        "compress_hbm": {"achieved": comp_bytes / (comp * 1e-3) / 1e9, "unit": "GB/s", "bytes": comp_bytes},
+    }
+
+
 # ------------------------------------------------------------------------------------------ our arm
 def run_ours(args):
     import torch
@@ -356,6 +434,10 @@ def run_ours(args):
         traffic = tr["bytes_per_launch"]
     value = world * B / (t_step * 1e-3)
 
+    prefill = None
+    if not args.quick and not args.no_prefill:
+        prefill = run_prefill(args, dev, stream)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
         host = host_copy(inp, 0, B)
@@ -384,6 +466,7 @@ def run_ours(args):
         "e2e": {"value": world * B / (e2e_ms * 1e-3), "unit": "query-tok/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
+        "prefill": prefill,
         "device_status": dev_status,
         "clocks": clocks,
     }

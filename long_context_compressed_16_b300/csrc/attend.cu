@@ -605,10 +605,17 @@ cudaError_t launch_t(const AttendArgs& a, cudaStream_t s, int* launches) {
   ++*launches;
   e = cudaGetLastError();
   if (e != cudaSuccess || a.n_splits == 1) return e;
+  return launch_attend_combine(a, s, launches);
+}
+
+template <int D>
+cudaError_t launch_combine_t(const AttendArgs& a, cudaStream_t s, int* launches) {
+  const int Q = a.B * a.Tq;
   const size_t csmem =
       (static_cast<size_t>((kCombineHeads * a.n_splits + 1) & ~1) + 2 * kMaxRopePairs) * sizeof(float);
   if (csmem > 48 * 1024) {
-    e = cudaFuncSetAttribute(k_attend_combine<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(csmem));
+    cudaError_t e = cudaFuncSetAttribute(k_attend_combine<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(csmem));
     if (e != cudaSuccess) return e;
   }
   k_attend_combine<D><<<dim3(Q, a.H / kCombineHeads), 128 * kCombineHeads, csmem, s>>>(a);
@@ -617,6 +624,13 @@ cudaError_t launch_t(const AttendArgs& a, cudaStream_t s, int* launches) {
 }
 
 }  // namespace
+
+cudaError_t launch_attend_combine(const AttendArgs& a, cudaStream_t s, int* launches) {
+  if (a.n_splits <= 1 || a.B * a.Tq == 0) return cudaSuccess;
+  if (a.d == 512) return launch_combine_t<512>(a, s, launches);
+  if (a.d == 128) return launch_combine_t<128>(a, s, launches);
+  return cudaErrorInvalidValue;
+}
 
 size_t attend_partial_bytes(int Q, int H, int d, int n_splits) {
   if (n_splits <= 1) return 0;
@@ -632,6 +646,7 @@ cudaError_t launch_attend(const AttendArgs& a, cudaStream_t s, int* launches) {
   int dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const bool wide = (a.H % 64 == 0) && (2LL * Q * a.n_splits * (a.H / 64) >= sms);
+  if (attend_tc_supported(a)) return launch_attend_tc(a, s, launches);
   if (a.d == 512) {
     if (a.fp8) return launch_t<512, 1, true>(a, s, launches);
     return wide ? launch_t<512, 4, false>(a, s, launches) : launch_t<512, 1, false>(a, s, launches);

@@ -211,6 +211,11 @@ struct AttendArgs {
   RopeParams rp;
 };
 size_t attend_partial_bytes(int Q, int H, int d, int n_splits);
+// Split merge (second kernel) for n_splits > 1.
+cudaError_t launch_attend_combine(const AttendArgs& a, cudaStream_t s, int* launches);
+// Tensor-core (tcgen05) attention for 512-dim bf16 rows and multiples of 64 heads.
+bool attend_tc_supported(const AttendArgs& a);
+cudaError_t launch_attend_tc(const AttendArgs& a, cudaStream_t s, int* launches);
 
 cudaError_t launch_attend(const AttendArgs& a, cudaStream_t s, int* launches);
 

@@ -280,33 +280,33 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = tc::umma_idesc_bf16(KT, NCOL);
-    Walker wk;
-    wk.init(p, ngroups);
-    long long n = 0;
-    int gc = -1;
-    bool nw;
-    bool issued = false;
-    int ncommit_empty[S];              // commits issued to each barrier (lane 0)
-    int ncommit_q[2] = {0, 0};
-    for (int s = 0; s < S; ++s) ncommit_empty[s] = 0;
-    while (wk.next(a, p, ngroups, nw)) {
-      if (nw) {
-        ++gc;
-        if (gc >= 1 && lane == 0) {
-          tc::umma_commit(&qempty[(gc - 1) % C::QB]);
-          ++ncommit_q[(gc - 1) % C::QB];
+    // ------------------------------------------------------------ MMA issuer (lane 0 only)
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::umma_idesc_bf16(KT, NCOL);
+      Walker wk;
+      wk.init(p, ngroups);
+      long long n = 0;
+      int gc = -1;
+      bool nw;
+      bool issued = false;
+      int ncommit_empty[S];              // commits issued to each barrier
+      int ncommit_q[2] = {0, 0};
+      for (int s = 0; s < S; ++s) ncommit_empty[s] = 0;
+      while (wk.next(a, p, ngroups, nw)) {
+        if (nw) {
+          ++gc;
+          if (gc >= 1) {
+            tc::umma_commit(&qempty[(gc - 1) % C::QB]);
+            ++ncommit_q[(gc - 1) % C::QB];
+          }
+          if (!tc::mbar_wait(&qfull[gc % C::QB], (gc / C::QB) & 1, abort_flag)) { fail(3); break; }
         }
-        if (!tc::mbar_wait(&qfull[gc % C::QB], (gc / C::QB) & 1, abort_flag)) { fail(3); break; }
-      }
-      const int s = static_cast<int>(n % S);
-      const uint32_t ph = static_cast<uint32_t>((n / S) & 1);
-      const int acc = static_cast<int>(n % C::ACC);
-      if (!tc::mbar_wait(&full[s], ph, abort_flag)) { fail(4); break; }
-      if (!tc::mbar_wait(&accempty[acc], ((n / C::ACC) & 1) ^ 1, abort_flag)) { fail(5); break; }
-      tc::tc_fence_after();
-      if (lane == 0) {
+        const int s = static_cast<int>(n % S);
+        const uint32_t ph = static_cast<uint32_t>((n / S) & 1);
+        const int acc = static_cast<int>(n % C::ACC);
+        if (!tc::mbar_wait(&full[s], ph, abort_flag)) { fail(4); break; }
+        if (!tc::mbar_wait(&accempty[acc], ((n / C::ACC) & 1) ^ 1, abort_flag)) { fail(5); break; }
+        tc::tc_fence_after();
         const uint32_t kaddr = tc::sptr(kbuf + s * C::STAGE_BYTES);
         const uint32_t qaddr = tc::sptr(qbuf + (gc % C::QB) * C::Q_BYTES);
 #pragma unroll
@@ -320,17 +320,14 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
         tc::umma_commit(&accfull[acc]);
         ++ncommit_empty[s];
         issued = true;
+        ++n;
       }
-      __syncwarp();
-      ++n;
-    }
-    // drain: all MMAs this thread issued have completed, and every arrival their commits
-    // trigger has landed, before tensor memory is released and the CTA's shared memory reused
-    if (lane == 0 && issued) {
-      tc::umma_commit(drain);
-      if (!tc::mbar_wait(drain, 0, nullptr)) report_error(a.status, CSA_ERR_TIMEOUT, 10);
-    }
-    if (lane == 0) {
+      // drain: all MMAs issued here have completed, and every arrival their commits trigger has
+      // landed, before tensor memory is released and the CTA's shared memory reused
+      if (issued) {
+        tc::umma_commit(drain);
+        if (!tc::mbar_wait(drain, 0, nullptr)) report_error(a.status, CSA_ERR_TIMEOUT, 10);
+      }
       for (int s = 0; s < S; ++s)
         if (ncommit_empty[s] > 0 && !tc::mbar_wait(&empty[s], (ncommit_empty[s] - 1) & 1, nullptr))
           report_error(a.status, CSA_ERR_TIMEOUT, 11);
@@ -366,7 +363,9 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
         __syncwarp();
       }
       const int acc = static_cast<int>(n % C::ACC);
-      if (!tc::mbar_wait(&accfull[acc], (n / C::ACC) & 1, abort_flag)) { fail(6); break; }
+      // the warp leaves together: a wait that gave up on any lane ends the loop for all lanes
+      const bool got = tc::mbar_wait(&accfull[acc], (n / C::ACC) & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) { fail(6); break; }
       tc::tc_fence_after();
       const int key = wk.t * KT + quarter * 32 + lane;
       float kscale = 1.f;

@@ -278,11 +278,13 @@ def test_attend_hca_prefill_sampled():
     assert_close(out2[0, ts], ref, "hca prefill attend (sampled)")
 
 
-@pytest.mark.parametrize("flags", [(True, True), (False, False), (True, False)])
-def test_attend_flags_and_edges(flags):
-    """Small decode-like case: -1 pads, windows clipped at 0, ring wrap, sink, flags off, lse."""
+@pytest.mark.parametrize("flags,H", [((True, True), 32), ((False, False), 32), ((True, False), 32),
+                                     ((True, True), 64), ((False, False), 128), ((True, False), 64)])
+def test_attend_flags_and_edges(flags, H):
+    """Small decode-like case: -1 pads, windows clipped at 0, ring wrap, sink, flags off, lse.
+    32 heads run the warp-MMA kernel, multiples of 64 heads the tensor-memory kernel."""
     qnr, unrot = flags
-    B, H, d, N, k, Wcap = 3, 32, 512, 300, 40, 160
+    B, d, N, k, Wcap = 3, 512, 300, 40, 160
     q = S.normal_bf16((B, 1, H, d), 11, 1, DEV)
     kv = S.normal_bf16((B, N, d), 11, 2, DEV)
     win = S.normal_bf16((B, Wcap, d), 11, 3, DEV)
@@ -304,8 +306,9 @@ def test_attend_flags_and_edges(flags):
     assert_lse(lse[:, 0], lref, "lse")
 
 
-def test_attend_bad_index_is_reported_and_skipped():
-    B, H, d, N, k = 1, 16, 128, 64, 8
+@pytest.mark.parametrize("H,d", [(16, 128), (64, 512)])
+def test_attend_bad_index_is_reported_and_skipped(H, d):
+    B, N, k = 1, 64, 8
     q = S.normal_bf16((B, 1, H, d), 12, 1, DEV)
     kv = S.normal_bf16((B, N, d), 12, 2, DEV)
     win = S.normal_bf16((B, 128, d), 12, 3, DEV)
@@ -320,6 +323,38 @@ def test_attend_bad_index_is_reported_and_skipped():
     out_g, _, ws2 = P.csa_attend(q, kv, torch.from_numpy(good.astype(np.int32)).to(DEV), win, sink, q_pos)
     assert C.csa_read_device_status(ws2)[0] == C.CSA_OK
     assert torch.equal(out_b, out_g)
+
+
+def test_attend_tc_prefill_rows_and_large_logits():
+    """Prefill-shaped call (one split per query, 640 rows in 10 chunks) where late entries have much
+    larger logits, so a head's maximum grows by more than 2^8 between chunks (the kernel then
+    rescales its accumulator in tensor memory).  The query is the oracle's own normalised and
+    rotated q_hat rounded to bf16 and passed with the query preprocessing off, so both sides use
+    identical logits and the comparison isolates the attention arithmetic."""
+    B, T, H, d, N, k = 1, 96, 64, 512, 200, 512
+    q_pos = (torch.arange(T, dtype=torch.int32) * 8 + 7)[None]
+    q_raw = S.normal_f64((B, T, H, d), 13, 1).numpy()
+    inv = O.rope_inv_freq(THETA, 64)
+    qhat = np.stack([O.rope(O.rmsnorm(q_raw[0, t]), float(q_pos[0, t]), inv, 64) for t in range(T)])[None]
+    q = _to_dev_bf16(qhat)
+    kv64 = S.normal_f64((B, N, d), 13, 2, DEV)
+    kv64[:, 150:] *= 4.0                              # late entries give much larger logits
+    kv = S.f64_to_bf16(kv64)
+    win = S.normal_bf16((B, 1024, d), 13, 3, DEV)     # ring of 1024 slots covers positions <= 767
+    sink = S.normal_f64((H,), 13, 4).float().to(DEV)
+    q_pos = q_pos.to(DEV)
+    idx_np = np.full((B, T, k), -1, dtype=np.int32)
+    for t in range(T):
+        nv = nvis_of(int(q_pos[0, t]), 4, N)
+        idx_np[0, t, :nv] = np.arange(nv)             # small logits first, the large ones chunks later
+    idx = torch.from_numpy(idx_np).to(DEV)
+    out, lse, _ = P.csa_attend(q, kv, idx, win, sink, q_pos, q_norm_rope=False, want_lse=True)
+    torch.cuda.synchronize()
+    inp = dict(q=q, kv=kv, win=win, sink=sink, q_pos=q_pos)
+    ts = list(range(0, T, 5)) + [T - 1]
+    ref, lref = _oracle_attend_rows(inp, idx_np, 4, 128, [(0, t) for t in ts], q_norm_rope=False)
+    assert_close(out[0, ts], ref, "tc prefill rows")
+    assert_lse(lse[0, ts], lref, "lse")
 
 
 # ------------------------------------------------------------------------------------------------ whole path
