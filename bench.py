@@ -2,9 +2,10 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
-A step is one pass of the decode hot path over one batch: csa_index_topk (lightning-indexer
-scores over every visible compressed entry, then the per-query top-k) followed by csa_attend
-(shared K=V MQA over the selected entries + 128-token window + sink).  Inputs are seeded
+A step is one pass of the decode hot path over one batch: csa_index_score (lightning-indexer
+scores over every visible compressed entry), csa_topk (the per-query top-k of those scores) and
+csa_attend (shared K=V MQA over the selected entries + 128-token window + sink), with CUDA events
+between the calls so the dominant score kernel is timed on its own.  Inputs are seeded
 synthetic tensors resident in HBM; every step reads more than the L2 holds (the indexer keys
 alone are 256 MiB), so no flush runs between steps.
 Under torchrun each rank decodes its own batch (weak scaling, no collective on the data path).
@@ -233,8 +234,10 @@ def run_prefill(args, dev, stream):
     out = torch.empty((1, w.T, w.H, w.d), dtype=torch.bfloat16, device=dev)
     idesc = P.index_desc(1, w.T, w.N, w.nI, w.dI, w.k, w.m)
     adesc = P.attend_desc(1, w.T, w.N, w.H, w.d, k=w.k, m=w.m, Wcap=w.T, window=w.window)
-    ws_i = torch.empty(max(256, C.csa_index_topk_workspace(idesc)), dtype=torch.uint8, device=dev)
-    ws_a = torch.empty(max(256, C.csa_attend_workspace(adesc)), dtype=torch.uint8, device=dev)
+    ws_s = torch.zeros(max(256, C.csa_index_score_workspace(idesc)), dtype=torch.uint8, device=dev)
+    ws_t = torch.zeros(max(256, C.csa_topk_workspace(idesc)), dtype=torch.uint8, device=dev)
+    ws_a = torch.zeros(max(256, C.csa_attend_workspace(adesc)), dtype=torch.uint8, device=dev)
+    scores = torch.empty((1, w.T, w.N), dtype=torch.float32, device=dev)       # 4 GiB, visible part written
 
     def step(evs=None):
         rec = (lambda i: evs[i].record(stream)) if evs else (lambda i: None)
@@ -243,23 +246,25 @@ def run_prefill(args, dev, stream):
         P.compress(inp["Ca_I"], inp["Za_I"], w.m, Cb=inp["Cb_I"], Zb=inp["Zb_I"], rope=False, rope_dims=0, out=kI,
                    stream=sptr)
         rec(1)
-        C.check(C.csa_index_topk(idesc, inp["qI"], inp["w"], kI, None, inp["q_pos"], idx, None, ws_i, stream=sptr),
-                "csa_index_topk")
+        C.check(C.csa_index_score(idesc, inp["qI"], inp["w"], kI, None, inp["q_pos"], scores, ws_s, stream=sptr),
+                "csa_index_score")
         rec(2)
+        C.check(C.csa_topk(idesc, scores, inp["q_pos"], idx, ws_t, stream=sptr), "csa_topk")
+        rec(3)
         C.check(C.csa_attend(adesc, inp["q"], kv, idx, inp["win"], inp["sink"], inp["q_pos"], out, None, ws_a,
                              stream=sptr), "csa_attend")
-        rec(3)
+        rec(4)
 
     step()
     torch.cuda.synchronize()
     times = []
     for _ in range(max(1, args.prefill_steps)):
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
         step(evs)
         torch.cuda.synchronize()
-        times.append([evs[i].elapsed_time(evs[i + 1]) for i in range(3)])
-    comp, ind, att = (statistics.median(x[i] for x in times) for i in range(3))
-    total = comp + ind + att
+        times.append([evs[i].elapsed_time(evs[i + 1]) for i in range(4)])
+    comp, ind, topk, att = (statistics.median(x[i] for x in times) for i in range(4))
+    total = comp + ind + topk + att
     idx_flops, att_flops = prefill_flops(w)
     with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
         pk = json.load(f)
@@ -267,15 +272,15 @@ def run_prefill(args, dev, stream):
     ind_tf = idx_flops / (ind * 1e-3) / 1e12
     att_tf = att_flops / (att * 1e-3) / 1e12
     comp_bytes = w.T * (4 * w.d + 4 * w.dI) * 2 + w.N * (w.d + w.dI) * 2
-    del inp, kv, kI, idx, out, ws_i, ws_a
+    del inp, kv, kI, idx, out, ws_s, ws_t, ws_a, scores
     torch.cuda.empty_cache()
     return {
         "workload": "csa_prefill_t65536", "tok_per_s": w.T / (total * 1e-3), "ms_per_chunk": total,
         "steps": len(times),
-        "breakdown_ms": {"csa_compress_x2": comp, "csa_index_topk": ind, "csa_attend": att},
+        "breakdown_ms": {"csa_compress_x2": comp, "csa_index_score": ind, "csa_topk": topk, "csa_attend": att},
         "indexer_tensor": {"achieved": ind_tf, "peak": peak, "unit": "TFLOP/s", "frac": ind_tf / peak,
                            "flops_per_launch": idx_flops, "peak_kind": "measured sustained",
-                           "note": "scores (tcgen05) + top-k of all 65536 queries; flops are the score contraction"},
+                           "note": "k_index_score alone (tcgen05), flops of the causal score contraction"},
         "attend_tensor": {"achieved": att_tf, "peak": peak, "unit": "TFLOP/s", "frac": att_tf / peak,
                           "flops_per_launch": att_flops},
         "compress_hbm": {"achieved": comp_bytes / (comp * 1e-3) / 1e9, "unit": "GB/s", "bytes": comp_bytes},
@@ -305,22 +310,55 @@ def run_ours(args):
     fp8 = w.fp8
     idesc = P.index_desc(B, 1, N, w.nI, w.dI, k, w.m, fp8=fp8)
     adesc = P.attend_desc(B, 1, N, w.H, w.d, k=k, m=w.m, Wcap=w.window, window=w.window, fp8=fp8)
-    ws_i = torch.empty(max(256, C.csa_index_topk_workspace(idesc)), dtype=torch.uint8, device=dev)
-    ws_a = torch.empty(max(256, C.csa_attend_workspace(adesc)), dtype=torch.uint8, device=dev)
+    ws_s = torch.zeros(max(256, C.csa_index_score_workspace(idesc)), dtype=torch.uint8, device=dev)
+    ws_t = torch.zeros(max(256, C.csa_topk_workspace(idesc)), dtype=torch.uint8, device=dev)
+    ws_a = torch.zeros(max(256, C.csa_attend_workspace(adesc)), dtype=torch.uint8, device=dev)
+    scores = torch.empty((B, 1, N), dtype=torch.float32, device=dev)
     idx = torch.empty((B, 1, k), dtype=torch.int32, device=dev)
     out = torch.empty((B, 1, w.H, w.d), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
     kI_scale = inp.get("kI_scale")
 
-    def step():
-        C.check(C.csa_index_topk(idesc, inp["qI"], inp["w"], inp["kI"], kI_scale, inp["q_pos"], idx, None, ws_i,
-                                 stream=sptr), "csa_index_topk")
-        C.check(C.csa_attend(adesc, inp["q"], inp["kv"], idx, inp["win"], inp["sink"], inp["q_pos"], out, None,
-                             ws_a, stream=sptr), "csa_attend")
+    def call_score(qI, wts, q_pos, sp):
+        C.check(C.csa_index_score(idesc, qI, wts, inp["kI"], kI_scale, q_pos, scores, ws_s, stream=sp),
+                "csa_index_score")
+
+    def call_topk(q_pos, sp):
+        C.check(C.csa_topk(idesc, scores, q_pos, idx, ws_t, stream=sp), "csa_topk")
+
+    def call_attend(q, q_pos, sp):
+        C.check(C.csa_attend(adesc, q, inp["kv"], idx, inp["win"], inp["sink"], q_pos, out, None, ws_a, stream=sp),
+                "csa_attend")
+
+    def run_calls(qI, wts, q, q_pos):
+        call_score(qI, wts, q_pos, sptr)
+        call_topk(q_pos, sptr)
+        call_attend(q, q_pos, sptr)
 
     for _ in range(max(3, args.warmup)):
-        step()
+        run_calls(inp["qI"], inp["w"], inp["q"], inp["q_pos"])
+    torch.cuda.synchronize()
+    # The device-timed steps replay one CUDA graph per step (the three calls captured once), so
+    # the host's launch overhead stays off the device timeline; the e2e leg below uses plain calls.
+    # Each call is also captured alone and replayed back to back for the per-call breakdown and
+    # for the dominant kernel's roofline.
+    calls = (lambda sp: call_score(inp["qI"], inp["w"], inp["q_pos"], sp), lambda sp: call_topk(inp["q_pos"], sp),
+             lambda sp: call_attend(inp["q"], inp["q_pos"], sp))
+
+    def capture(fns):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for fn in fns:
+                fn(torch.cuda.current_stream().cuda_stream)
+        return g
+
+    n0 = C.csa_launch_count()
+    g_step = capture(calls)
+    launches_per_step = C.csa_launch_count() - n0
+    g_parts = [capture([fn]) for fn in calls]
+    for _ in range(max(3, args.warmup)):
+        g_step.replay()
     torch.cuda.synchronize()
 
     gpu_id = "0"
@@ -333,28 +371,31 @@ def run_ours(args):
     time.sleep(0.3)
 
     def timed_block(K):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-                torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
-        n0 = C.csa_launch_count()
         for i in range(K):
             evs[i][0].record(stream)
-            C.check(C.csa_index_topk(idesc, inp["qI"], inp["w"], inp["kI"], kI_scale, inp["q_pos"], idx, None, ws_i,
-                                     stream=sptr), "csa_index_topk")
+            g_step.replay()
             evs[i][1].record(stream)
-            C.check(C.csa_attend(adesc, inp["q"], inp["kv"], idx, inp["win"], inp["sink"], inp["q_pos"], out, None,
-                                 ws_a, stream=sptr), "csa_attend")
-            evs[i][2].record(stream)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
-        launches = C.csa_launch_count() - n0
-        t_step = sum(e[0].elapsed_time(e[2]) for e in evs) / K
-        t_idx = sum(e[0].elapsed_time(e[1]) for e in evs) / K
-        t_att = sum(e[1].elapsed_time(e[2]) for e in evs) / K
-        return t_step, t_idx, t_att, launches
+        return sum(e[0].elapsed_time(e[1]) for e in evs) / K
+
+    def parts_block(K):
+        out_ms = []
+        for g in g_parts:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(K):
+                g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            out_ms.append(e0.elapsed_time(e1) / K)
+        return out_ms
 
     K = args.steps
     t_clock0 = time.time()
@@ -368,12 +409,14 @@ def run_ours(args):
     for _ in range(n_more):
         blocks.append(timed_block(K))
     t_clock1 = time.time()
-    med = sorted(blocks, key=lambda x: x[0])[len(blocks) // 2]
-    t_step, t_idx, t_att, launches = med
+    t_step = sorted(blocks)[len(blocks) // 2]
+    parts = [parts_block(K) for _ in range(1 if args.quick else 3)]
+    t_score, t_topk, t_att = (sorted(p[j] for p in parts)[len(parts) // 2] for j in range(3))
+    launches = K * launches_per_step
     if world > 1:
-        tt = torch.tensor([t_step, t_idx, t_att], device=dev, dtype=torch.float64)
+        tt = torch.tensor([t_step, t_score, t_topk, t_att], device=dev, dtype=torch.float64)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_step, t_idx, t_att = tt.tolist()
+        t_step, t_score, t_topk, t_att = tt.tolist()
 
     # ---------------- end to end through the public API: per-step inputs from pinned host memory
     h_q = inp["q"].cpu().pin_memory()
@@ -391,9 +434,7 @@ def run_ours(args):
         d_qI.copy_(h_qI, non_blocking=True)
         d_w.copy_(h_w, non_blocking=True)
         d_pos.copy_(h_pos, non_blocking=True)
-        C.check(C.csa_index_topk(idesc, d_qI, d_w, inp["kI"], kI_scale, d_pos, idx, None, ws_i, stream=sptr), "idx")
-        C.check(C.csa_attend(adesc, d_q, inp["kv"], idx, inp["win"], inp["sink"], d_pos, out, None, ws_a,
-                             stream=sptr), "att")
+        run_calls(d_qI, d_w, d_q, d_pos)
         h_out.copy_(out, non_blocking=True)
         h_idx.copy_(idx, non_blocking=True)
 
@@ -416,18 +457,17 @@ def run_ours(args):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = tt.item()
 
-    st_i, _ = C.csa_read_device_status(ws_i, sptr)
-    st_a, _ = C.csa_read_device_status(ws_a, sptr)
-    dev_status = {"csa_index_topk": C.status_string(st_i), "csa_attend": C.status_string(st_a)}
+    dev_status = {name: C.status_string(C.csa_read_device_status(ws, sptr)[0])
+                  for name, ws in (("csa_index_score", ws_s), ("csa_topk", ws_t), ("csa_attend", ws_a))}
 
-    # ---------------- roofline of the dominant call (indexer scores + top-k)
+    # ---------------- roofline of the dominant kernel (indexer scores), timed alone between events
     hbm, peak_kind = peaks()
     key_row = w.dI * (1 if fp8 else 2) + (4 if fp8 else 0)
-    idx_bytes = B * (N * key_row + w.nI * w.dI * 2 + w.nI * 4 + k * 4)
+    score_bytes = B * (N * key_row + w.nI * w.dI * 2 + w.nI * 4 + N * 4)     # keys, q, w in; scores out
     row_bytes = 608 if fp8 else w.d * 2
     att_bytes = B * ((k + w.window) * row_bytes + 2 * w.H * w.d * 2 + k * 4)
-    step_bytes = idx_bytes + att_bytes
-    achieved = idx_bytes / (t_idx * 1e-3) / 1e9
+    step_bytes = B * (N * key_row + w.nI * w.dI * 2 + w.nI * 4 + k * 4) + att_bytes   # method's bytes per step
+    achieved = score_bytes / (t_score * 1e-3) / 1e9
     tr = TRAFFIC.get(args.workload, {})
     traffic = None
     if tr.get("bytes_per_launch") and tr.get("source_sha") == source_sha("index_score.cu"):
@@ -457,11 +497,15 @@ def run_ours(args):
         "config": {"workload": args.workload, "B": B, "N": N, "context_tokens": w.m * N, "k": k, "H": w.H, "d": w.d,
                    "indexer_heads": w.nI, "indexer_dim": w.dI, "window": w.window, "kv_format": "fp8_mixed" if fp8 else "bf16",
                    "l2": f"inputs larger than L2: {step_bytes / 2**20:.0f} MiB read per step (126 MB L2), no flush", "timed_blocks": len(blocks),
+                   "timing": "step: one CUDA graph of the three calls per step, CUDA events around each replay; "
+                             "breakdown and roofline: each call's graph replayed K times back to back",
                    "parallelism": f"dp{world}"},
-        "breakdown_ms": {"csa_index_topk": t_idx, "csa_attend": t_att},
-        "roofline": {"bound": "hbm", "kernel": "csa_index_topk (k_index_score + k_topk)", "achieved": achieved,
+        "breakdown_ms": {"csa_index_score": t_score, "csa_topk": t_topk, "csa_attend": t_att},
+        "roofline": {"bound": "hbm", "kernel": "k_index_score", "achieved": achieved,
                      "peak": hbm, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": traffic, "algorithmic_bytes_per_launch": idx_bytes},
+                     "traffic": traffic, "algorithmic_bytes_per_launch": score_bytes,
+                     "step": {"algorithmic_bytes": step_bytes, "achieved": step_bytes / (t_step * 1e-3) / 1e9,
+                              "frac": step_bytes / (t_step * 1e-3) / 1e9 / hbm}},
         "cpu_baseline": cpu,
         "e2e": {"value": world * B / (e2e_ms * 1e-3), "unit": "query-tok/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

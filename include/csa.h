@@ -19,9 +19,13 @@
  *     *_workspace() query returns.
  *   - Every call only enqueues kernels on `stream` and returns; nothing synchronises.
  *   - Invalid or unsupported descriptors are rejected before any launch.  A failed launch
- *     returns CSA_ERR_CUDA.  Device-detected problems (an index out of range) never trap: the
- *     kernel skips the access and records the first problem in the workspace status word,
- *     which csa_read_device_status() returns.
+ *     returns CSA_ERR_CUDA.  Device-detected problems (an index out of range, a bounded wait
+ *     that gave up) never trap: the kernel skips the access or returns, and records the first
+ *     problem in the status word at the start of the workspace, which csa_read_device_status()
+ *     returns.  The status word is sticky: calls never reset it, so it holds the first problem
+ *     since it was last cleared (csa_clear_device_status).  A workspace must start with its
+ *     first 8 bytes zero (clear it once, or allocate it zero-filled).  Keeping the reset out of
+ *     the calls keeps a step's kernels back to back on the stream.
  *   - Positions are explicit: q_pos[b][i] is the 0-based token index t of query i of sequence
  *     b.  For decode, t is the index of the new token (the context length).
  */
@@ -137,6 +141,30 @@ csa_status csa_index_topk(const csa_index_desc* desc, const void* qI, const floa
                           csa_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * csa_index_score / csa_topk -- the two halves of csa_index_topk as separate calls.
+ *
+ * Same sources and conventions as csa_index_topk.  csa_index_score writes the visible scores
+ * I_{t,s}, s < floor((t+1)/m), into score_out fp32 [B, Tq, N] and leaves the rest of each row
+ * untouched; its workspace needs only the status header (csa_index_score_workspace).
+ * csa_topk reads scores fp32
+ * [B, Tq, N] (only the entries s < floor((t+1)/m) of each row, so the others may hold anything)
+ * and writes idx_out exactly as csa_index_topk would for those scores; workspace:
+ * csa_topk_workspace(desc) bytes.  csa_index_score followed by csa_topk on the same stream gives
+ * the same idx_out as csa_index_topk, bit for bit.  Both reject what csa_index_topk rejects;
+ * csa_topk ignores qI / head settings of the descriptor except for validation.
+ * ------------------------------------------------------------------------------------------- */
+size_t csa_index_score_workspace(const csa_index_desc* desc);
+
+csa_status csa_index_score(const csa_index_desc* desc, const void* qI, const float* w,
+                           const void* kI, const float* kI_scale, const int32_t* q_pos,
+                           float* score_out, void* workspace, size_t ws_bytes, csa_stream_t stream);
+
+size_t csa_topk_workspace(const csa_index_desc* desc);
+
+csa_status csa_topk(const csa_index_desc* desc, const float* scores, const int32_t* q_pos,
+                    int32_t* idx_out, void* workspace, size_t ws_bytes, csa_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
  * csa_index_topk_noalloc -- csa_index_topk for callers that cannot allocate device memory.
  *
  * The pages have no counterpart: this is a library convenience.  Some callers cannot call
@@ -224,7 +252,8 @@ csa_status hca_attend(const csa_attend_desc* desc, const void* q, const void* kv
 /* ---------------------------------------------------------------------------------------------
  * Status helpers.
  * csa_read_device_status: waits for `stream`, reads the status word at the start of a
- * workspace that a previous call used, returns CSA_OK or CSA_ERR_DEVICE_CHECK, and (if
+ * workspace that a previous call used, returns CSA_OK, CSA_ERR_DEVICE_CHECK (a range check
+ * failed) or CSA_ERR_TIMEOUT (a bounded device-side wait gave up), and (if
  * detail != NULL, HOST pointer) stores the first offending value.  csa_clear_device_status
  * enqueues a reset of that word.  csa_status_string never returns NULL.
  * ------------------------------------------------------------------------------------------- */
@@ -235,6 +264,23 @@ const char* csa_status_string(csa_status status);
 /* Number of kernel launches the library has enqueued in this process (all calls, all threads;
  * an atomic counter kept for instrumentation, not part of any result). */
 uint64_t csa_launch_count(void);
+
+/* ---------------------------------------------------------------------------------------------
+ * csa_selftest_bounded_wait -- exercises the library's failure path on purpose.
+ *
+ * No counterpart in the pages: a diagnostic of the library itself.  Every wait inside the
+ * library's kernels is bounded; a wait that is never satisfied gives up after its limit, writes
+ * CSA_ERR_TIMEOUT to the workspace status word and the kernel returns, leaving the CUDA context
+ * usable.  This call launches one small kernel whose wait nothing can complete (an mbarrier no
+ * thread arrives on), with the given limit, so a caller can check that path end to end:
+ * afterwards csa_read_device_status returns CSA_ERR_TIMEOUT and the detail holds the time the
+ * wait took, in microseconds.
+ * workspace: at least 256 bytes, 16-byte aligned (its status word is the only thing written).
+ * limit_ns: 1000 .. 2000000000.  Returns CSA_ERR_INVALID_ARG / CSA_ERR_WORKSPACE for bad
+ * arguments, CSA_ERR_CUDA if the launch fails, else CSA_OK (the timeout itself is reported
+ * through the status word).
+ * ------------------------------------------------------------------------------------------- */
+csa_status csa_selftest_bounded_wait(void* workspace, size_t ws_bytes, int64_t limit_ns, csa_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -37,7 +37,8 @@ CSA_ATTEND_WRITE_LSE = 4
 
 EXPORTS = ("csa_compress", "csa_index_topk_workspace", "csa_index_topk", "csa_attend_workspace",
            "hca_attend_workspace", "csa_attend", "hca_attend", "csa_read_device_status", "csa_clear_device_status",
-           "csa_status_string", "csa_launch_count", "csa_index_topk_noalloc")
+           "csa_status_string", "csa_launch_count", "csa_index_topk_noalloc", "csa_index_score_workspace",
+           "csa_index_score", "csa_topk_workspace", "csa_topk", "csa_selftest_bounded_wait")
 
 
 class csa_compress_desc(ctypes.Structure):
@@ -77,6 +78,14 @@ def _load() -> ctypes.CDLL:
     lib.csa_index_topk.restype = c_int
     lib.csa_index_topk_noalloc.argtypes = [POINTER(csa_index_desc), vp, vp, vp, vp, vp, vp, vp, vp]
     lib.csa_index_topk_noalloc.restype = c_int
+    lib.csa_index_score_workspace.argtypes = [POINTER(csa_index_desc)]
+    lib.csa_index_score_workspace.restype = c_size_t
+    lib.csa_index_score.argtypes = [POINTER(csa_index_desc), vp, vp, vp, vp, vp, vp, vp, c_size_t, vp]
+    lib.csa_index_score.restype = c_int
+    lib.csa_topk_workspace.argtypes = [POINTER(csa_index_desc)]
+    lib.csa_topk_workspace.restype = c_size_t
+    lib.csa_topk.argtypes = [POINTER(csa_index_desc), vp, vp, vp, vp, c_size_t, vp]
+    lib.csa_topk.restype = c_int
     lib.csa_attend_workspace.argtypes = [POINTER(csa_attend_desc)]
     lib.csa_attend_workspace.restype = c_size_t
     lib.hca_attend_workspace.argtypes = [POINTER(csa_attend_desc)]
@@ -91,6 +100,8 @@ def _load() -> ctypes.CDLL:
     lib.csa_clear_device_status.restype = c_int
     lib.csa_status_string.argtypes = [c_int]
     lib.csa_status_string.restype = ctypes.c_char_p
+    lib.csa_selftest_bounded_wait.argtypes = [vp, c_size_t, ctypes.c_int64, vp]
+    lib.csa_selftest_bounded_wait.restype = c_int
     lib.csa_launch_count.argtypes = []
     lib.csa_launch_count.restype = c_uint64
     return lib
@@ -165,6 +176,25 @@ def csa_index_topk_noalloc(desc, qI, w, kI, kI_scale, q_pos, idx_out, score_out,
                                       _p(idx_out), _p(score_out), _stream(stream))
 
 
+def csa_index_score_workspace(desc) -> int:
+    return lib.csa_index_score_workspace(ctypes.byref(desc))
+
+
+def csa_index_score(desc, qI, w, kI, kI_scale, q_pos, score_out, workspace, ws_bytes=None, stream=None) -> int:
+    n = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return lib.csa_index_score(ctypes.byref(desc), _p(qI), _p(w), _p(kI), _p(kI_scale), _p(q_pos), _p(score_out),
+                               _p(workspace), n, _stream(stream))
+
+
+def csa_topk_workspace(desc) -> int:
+    return lib.csa_topk_workspace(ctypes.byref(desc))
+
+
+def csa_topk(desc, scores, q_pos, idx_out, workspace, ws_bytes=None, stream=None) -> int:
+    n = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return lib.csa_topk(ctypes.byref(desc), _p(scores), _p(q_pos), _p(idx_out), _p(workspace), n, _stream(stream))
+
+
 def csa_attend_workspace(desc) -> int:
     return lib.csa_attend_workspace(ctypes.byref(desc))
 
@@ -193,6 +223,11 @@ def csa_read_device_status(workspace, stream=None):
 
 def csa_clear_device_status(workspace, stream=None) -> int:
     return lib.csa_clear_device_status(_p(workspace), _stream(stream))
+
+
+def csa_selftest_bounded_wait(workspace, limit_ns, ws_bytes=None, stream=None) -> int:
+    n = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return lib.csa_selftest_bounded_wait(_p(workspace), n, int(limit_ns), _stream(stream))
 
 
 def csa_launch_count() -> int:

@@ -29,6 +29,14 @@ bool make_rope(int r, float theta, const float* inv_freq, csa::RopeParams* rp) {
 
 void count(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
 
+}  // namespace
+
+namespace csa {
+void note_launches(int n) { count(n); }
+}  // namespace csa
+
+namespace {
+
 // ---------------------------------------------------------------- indexer chunking
 struct IndexPlan {
   int G;             // queries per group
@@ -147,7 +155,6 @@ csa_status attend_common(const csa_attend_desc* d, bool csa_mode, const void* q,
   a.eps = d->eps;
   a.n_slots = plan.n_slots; a.split_slots = plan.split_slots; a.n_splits = plan.n_splits;
   if (!make_rope(d->rope_dims, d->rope_theta, d->inv_freq, &a.rp)) return CSA_ERR_INVALID_ARG;
-  if (cudaMemsetAsync(ws, 0, 8, stream) != cudaSuccess) return CSA_ERR_CUDA;
   int launches = 0;
   const cudaError_t e = csa::launch_attend(a, stream, &launches);
   count(launches);
@@ -214,7 +221,6 @@ csa_status csa_index_topk(const csa_index_desc* d, const void* qI, const float* 
   const bool fp8 = d->key_fmt == CSA_FMT_FP8_ROWSCALE;
   if (fp8 && !kI_scale && d->N > 0) return CSA_ERR_INVALID_ARG;
   if (!aligned16(qI) || (kI && !aligned16(kI))) return CSA_ERR_INVALID_ARG;
-  if (cudaMemsetAsync(ws, 0, 8, stream) != cudaSuccess) return CSA_ERR_CUDA;
 
   csa::IndexArgs ia{};
   ia.qI = qI; ia.w = w; ia.kI = kI; ia.kI_scale = kI_scale; ia.q_pos = q_pos;
@@ -263,6 +269,77 @@ csa_status csa_index_topk(const csa_index_desc* d, const void* qI, const float* 
   return from_cuda(e);
 }
 
+size_t csa_index_score_workspace(const csa_index_desc* d) {
+  if (!index_desc_ok(d)) return 0;
+  return csa::kStatusBytes;
+}
+
+csa_status csa_index_score(const csa_index_desc* d, const void* qI, const float* w, const void* kI,
+                           const float* kI_scale, const int32_t* q_pos, float* score_out, void* ws,
+                           size_t ws_bytes, csa_stream_t stream_) {
+  if (!index_desc_ok(d)) return CSA_ERR_INVALID_ARG;
+  if (d->N > 262144) return CSA_ERR_UNSUPPORTED;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (!ws) return CSA_ERR_WORKSPACE;
+  if (ws_bytes < csa::kStatusBytes) return CSA_ERR_WORKSPACE;
+  if (!aligned16(ws)) return CSA_ERR_INVALID_ARG;
+  const long long Q = static_cast<long long>(d->B) * d->Tq;
+  if (Q == 0 || d->N == 0) return CSA_OK;
+  if (!qI || !w || !q_pos || !kI || !score_out) return CSA_ERR_INVALID_ARG;
+  const bool fp8 = d->key_fmt == CSA_FMT_FP8_ROWSCALE;
+  if (fp8 && !kI_scale) return CSA_ERR_INVALID_ARG;
+  if (!aligned16(qI) || !aligned16(kI)) return CSA_ERR_INVALID_ARG;
+  const IndexPlan plan = plan_index(d);
+  if (plan.groups > 2147483647LL) return CSA_ERR_UNSUPPORTED;
+  csa::IndexArgs ia{};
+  ia.qI = qI; ia.w = w; ia.kI = kI; ia.kI_scale = kI_scale; ia.q_pos = q_pos;
+  ia.B = d->B; ia.Tq = d->Tq; ia.N = d->N; ia.nI = d->n_heads; ia.dI = d->head_dim; ia.m = d->m;
+  ia.fp8 = fp8 ? 1 : 0;
+  ia.status = static_cast<int32_t*>(ws);
+  ia.scores = score_out;
+  ia.q_begin = 0;
+  ia.q_count = static_cast<int>(plan.groups);
+  ia.score_row_offset = 0;
+  int launches = 0;
+  const cudaError_t e =
+      csa::launch_index_score_groups(ia, csa::index_grouping(d->n_heads, d->Tq), 0, stream, &launches);
+  count(launches);
+  if (e == cudaErrorInvalidValue) return CSA_ERR_UNSUPPORTED;
+  return from_cuda(e);
+}
+
+size_t csa_topk_workspace(const csa_index_desc* d) {
+  if (!index_desc_ok(d)) return 0;
+  const long long Q = static_cast<long long>(d->B) * d->Tq;
+  if (Q > 2147483647LL) return 0;
+  return csa::kStatusBytes + round256(csa::topk_candidate_bytes(static_cast<int>(Q), d->N, d->k));
+}
+
+csa_status csa_topk(const csa_index_desc* d, const float* scores, const int32_t* q_pos, int32_t* idx_out,
+                    void* ws, size_t ws_bytes, csa_stream_t stream_) {
+  if (!index_desc_ok(d)) return CSA_ERR_INVALID_ARG;
+  if (d->N > 262144) return CSA_ERR_UNSUPPORTED;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (!ws) return CSA_ERR_WORKSPACE;
+  const long long Q = static_cast<long long>(d->B) * d->Tq;
+  if (Q > 2147483647LL) return CSA_ERR_UNSUPPORTED;
+  const size_t cand = round256(csa::topk_candidate_bytes(static_cast<int>(Q), d->N, d->k));
+  if (ws_bytes < csa::kStatusBytes + cand) return CSA_ERR_WORKSPACE;
+  if (!aligned16(ws)) return CSA_ERR_INVALID_ARG;
+  if (Q == 0) return CSA_OK;
+  if (!q_pos || !idx_out || (!scores && d->N > 0)) return CSA_ERR_INVALID_ARG;
+  csa::TopkArgs ta{};
+  ta.scores = scores; ta.q_pos = q_pos; ta.idx_out = idx_out; ta.status = static_cast<int32_t*>(ws);
+  ta.Tq = d->Tq; ta.N = d->N; ta.k = d->k; ta.m = d->m;
+  ta.q_begin = 0; ta.q_count = static_cast<int>(Q); ta.score_row_offset = 0;
+  int launches = 0;
+  const cudaError_t e =
+      csa::launch_topk(ta, cand ? static_cast<unsigned char*>(ws) + csa::kStatusBytes : nullptr, stream, &launches);
+  count(launches);
+  if (e == cudaErrorInvalidValue) return CSA_ERR_UNSUPPORTED;
+  return from_cuda(e);
+}
+
 size_t csa_attend_workspace(const csa_attend_desc* d) {
   if (!attend_desc_ok(d, true)) return 0;
   return csa::kStatusBytes + plan_attend(d, true).partial_bytes;
@@ -293,7 +370,8 @@ csa_status csa_read_device_status(const void* ws, csa_stream_t stream, int32_t* 
   int32_t h[2] = {0, 0};
   if (cudaMemcpy(h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return CSA_ERR_CUDA;
   if (detail) *detail = h[1];
-  return h[0] == 0 ? CSA_OK : CSA_ERR_DEVICE_CHECK;
+  if (h[0] == 0) return CSA_OK;
+  return h[0] == CSA_ERR_TIMEOUT ? CSA_ERR_TIMEOUT : CSA_ERR_DEVICE_CHECK;
 }
 
 csa_status csa_clear_device_status(void* ws, csa_stream_t stream) {

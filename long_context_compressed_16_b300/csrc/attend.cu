@@ -86,6 +86,8 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
   float* lsum = reinterpret_cast<float*>(smem + C::lsum_off);
   const unsigned char** rowptr = reinterpret_cast<const unsigned char**>(smem + C::ptr_off);
   float2* rope_tab = reinterpret_cast<float2*>(smem + C::rope_off);   // (cos, sin) of t * inv_freq_j
+  grid_dep_wait();
+  grid_dep_launch();
 
   const int tid = threadIdx.x, lane = tid & 31, wall = tid >> 5;
   const int g = wall >> 2, wq = wall & 3;
@@ -538,6 +540,8 @@ constexpr int kCombineHeads = 2;
 template <int D>
 __global__ void __launch_bounds__(128 * kCombineHeads) k_attend_combine(AttendArgs a) {
   extern __shared__ float csm[];
+  grid_dep_wait();
+  grid_dep_launch();
   const long long qi = blockIdx.x;
   const int h0 = blockIdx.y * kCombineHeads;
   const int S = a.n_splits, H = a.H;
@@ -601,9 +605,8 @@ cudaError_t launch_t(const AttendArgs& a, cudaStream_t s, int* launches) {
   if (e != cudaSuccess) return e;
   const int Q = a.B * a.Tq;
   dim3 grid(Q, a.H / C::HG, a.n_splits);
-  k_attend<D, NG, FP8><<<grid, C::THREADS, C::smem, s>>>(a);
+  e = launch_k(k_attend<D, NG, FP8>, grid, dim3(C::THREADS), C::smem, s, a);
   ++*launches;
-  e = cudaGetLastError();
   if (e != cudaSuccess || a.n_splits == 1) return e;
   return launch_attend_combine(a, s, launches);
 }
@@ -618,9 +621,10 @@ cudaError_t launch_combine_t(const AttendArgs& a, cudaStream_t s, int* launches)
                                          static_cast<int>(csmem));
     if (e != cudaSuccess) return e;
   }
-  k_attend_combine<D><<<dim3(Q, a.H / kCombineHeads), 128 * kCombineHeads, csmem, s>>>(a);
+  const cudaError_t e = launch_k(k_attend_combine<D>, dim3(Q, a.H / kCombineHeads), dim3(128 * kCombineHeads), csmem,
+                                 s, a);
   ++*launches;
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace
@@ -646,7 +650,6 @@ cudaError_t launch_attend(const AttendArgs& a, cudaStream_t s, int* launches) {
   int dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const bool wide = (a.H % 64 == 0) && (2LL * Q * a.n_splits * (a.H / 64) >= sms);
-  if (attend_tc_supported(a)) return launch_attend_tc(a, s, launches);
   if (a.d == 512) {
     if (a.fp8) return launch_t<512, 1, true>(a, s, launches);
     return wide ? launch_t<512, 4, false>(a, s, launches) : launch_t<512, 1, false>(a, s, launches);

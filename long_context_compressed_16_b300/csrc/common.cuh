@@ -20,10 +20,37 @@ struct RopeParams {
 // Status word at the start of every workspace: {code, detail, pad, pad}.
 constexpr size_t kStatusBytes = 256;
 
+// Adds to the library's count of kernel launches (csa_launch_count).
+void note_launches(int n);
+
 // Closed compressed blocks visible to position t: s < floor((t+1)/m), clipped to [0, N].
 __host__ __device__ __forceinline__ int n_visible(int t, int m, int N) {
   const long long v = (static_cast<long long>(t) + 1) / m;
   return v <= 0 ? 0 : (v >= N ? N : static_cast<int>(v));
+}
+
+// Programmatic dependent launch.  Every kernel is launched with programmatic stream
+// serialization (launch_k), so its CTAs may be scheduled while the previous kernel on the stream
+// is still finishing; grid_dep_wait() then blocks until that kernel has completed and its memory
+// writes are visible.  Each kernel calls grid_dep_wait() before its first global-memory access
+// (read or write), and grid_dep_launch() right after it: the next kernel's CTAs may then take
+// SM resources as this kernel's CTAs retire, which hides the launch gap between them.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 
 __device__ __forceinline__ void report_error(int32_t* status, int32_t code, int32_t detail) {
@@ -213,9 +240,7 @@ struct AttendArgs {
 size_t attend_partial_bytes(int Q, int H, int d, int n_splits);
 // Split merge (second kernel) for n_splits > 1.
 cudaError_t launch_attend_combine(const AttendArgs& a, cudaStream_t s, int* launches);
-// Tensor-core (tcgen05) attention for 512-dim bf16 rows and multiples of 64 heads.
-bool attend_tc_supported(const AttendArgs& a);
-cudaError_t launch_attend_tc(const AttendArgs& a, cudaStream_t s, int* launches);
+
 
 cudaError_t launch_attend(const AttendArgs& a, cudaStream_t s, int* launches);
 

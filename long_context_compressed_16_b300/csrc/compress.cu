@@ -25,6 +25,8 @@ __device__ __forceinline__ uint4 ldg_nc(const void* p) {
 
 __global__ void __launch_bounds__(256) k_compress(CompressArgs a, int RS, int EPC) {
   extern __shared__ float smem[];
+  grid_dep_wait();
+  grid_dep_launch();
   const int TPE = a.d >> 3;
   const int tid = threadIdx.x;
   const int cg = tid % TPE;
@@ -209,9 +211,9 @@ cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s, int* launches
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  k_compress<<<static_cast<unsigned>(blocks), threads, smem, s>>>(a, RS, EPC);
+  const cudaError_t e = launch_k(k_compress, dim3(static_cast<unsigned>(blocks)), dim3(threads), smem, s, a, RS, EPC);
   ++*launches;
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace csa

@@ -28,6 +28,12 @@ namespace {
 
 constexpr int KT = 128;                 // keys per tile = MMA M
 constexpr int kMaxSmem = 232448;        // dynamic shared memory per block on sm_100-class parts
+#ifndef CSA_IDX_MAX_STAGES
+#define CSA_IDX_MAX_STAGES 6            // key-tile stages in flight per CTA (capped by shared memory)
+#endif
+#ifndef CSA_IDX_WALK_CHUNK
+#define CSA_IDX_WALK_CHUNK 0            // > 0: CTAs take chunks of this many tiles round-robin
+#endif
 
 template <int DI, int NCOL, bool FP8>
 struct Cfg {
@@ -38,14 +44,19 @@ struct Cfg {
   static constexpr int Q_REGION = NCOL * 128;
   static constexpr int Q_BYTES = NREG * Q_REGION;
   static constexpr int QB = NCOL >= 256 ? 1 : 2;          // query-block buffers
-  static constexpr int EW = NCOL > 128 ? 8 : 4;           // epilogue warps
+  static constexpr int EW = 8;                            // epilogue warps: two sets of four
+  // NCOL <= 128: the two sets take alternate tiles; wider: they split the group's queries
+  static constexpr bool TSPLIT = NCOL <= 128;
+  static constexpr int ACC_ARRIVALS = 32 * (TSPLIT ? EW / 2 : EW);   // epilogue threads per tile
   static constexpr int CW = FP8 ? 4 : 0;                  // converter warps
   static constexpr int THREADS = 32 * (4 + EW + CW);
   static constexpr int W_FLOATS = EW * NCOL;              // per-epilogue-warp copy of the head weights
+  static constexpr int GMAX = 16;                         // queries per group (NCOL / 16 heads at most)
+  static constexpr int NV_INTS = EW * GMAX;               // per-epilogue-warp visible counts of the group
   static constexpr int MISC = 1024;                       // barriers, TMEM address, flags
-  static constexpr int FIXED = 1024 /*alignment slack*/ + QB * Q_BYTES + W_FLOATS * 4 + MISC;
+  static constexpr int FIXED = 1024 /*alignment slack*/ + QB * Q_BYTES + W_FLOATS * 4 + NV_INTS * 4 + MISC;
   static constexpr int S_RAW = (kMaxSmem - FIXED) / (STAGE_BYTES + STAGED_BYTES);
-  static constexpr int STAGES = S_RAW > 6 ? 6 : S_RAW;
+  static constexpr int STAGES = S_RAW > CSA_IDX_MAX_STAGES ? CSA_IDX_MAX_STAGES : S_RAW;
   static constexpr int SMEM = FIXED + STAGES * (STAGE_BYTES + STAGED_BYTES);
   static constexpr int ACC = NCOL <= 128 ? 4 : 2;            // accumulator buffers in tensor memory
   static constexpr int TMEM_COLS = (ACC * NCOL) <= 32 ? 32 : (ACC * NCOL) <= 64 ? 64 : (ACC * NCOL) <= 128 ? 128
@@ -57,7 +68,9 @@ struct Cfg {
 
 struct TcParams {
   int G, NHP;               // queries per group, padded heads per query
-  int mode;                 // 0: flattened (group, tile) space split evenly; 1: whole groups, snake order
+  int mode;                 // 0: flattened (group, tile) space split evenly; 1: whole groups, snake order;
+                            // 2: chunks of `chunk` tiles of the flattened space, round-robin over CTAs
+  int chunk;
   int tiles_max;            // ceil(N / KT)
   long long F;              // groups * tiles_max (mode 0)
   int fill_invisible;
@@ -93,6 +106,8 @@ struct Walker {
     if (p.mode == 0) {
       f = c * p.F / P;
       f_end = (c + 1) * p.F / P;
+    } else {
+      f = f_end = 0;
     }
     round = 0;
     g = -1;
@@ -104,6 +119,30 @@ struct Walker {
   // when the pair belongs to a different group than the previous one.
   __device__ bool next(const IndexArgs& a, const TcParams& p, int ngroups, bool& new_group) {
     new_group = false;
+    if (p.mode == 2) {
+      for (;;) {
+        while (f < f_end) {
+          const int gg = static_cast<int>(f / p.tiles_max);
+          const int tt = static_cast<int>(f % p.tiles_max);
+          if (gg != g) {
+            g = gg;
+            gi = group_info(a, p, g);
+            new_group = true;
+          }
+          if (tt < gi.nt) {
+            t = tt;
+            ++f;
+            return true;
+          }
+          f = static_cast<long long>(gg + 1) * p.tiles_max;
+        }
+        const long long ci = static_cast<long long>(blockIdx.x) + static_cast<long long>(round) * gridDim.x;
+        ++round;
+        f = ci * p.chunk;
+        if (f >= p.F) return false;
+        f_end = f + p.chunk < p.F ? f + p.chunk : p.F;
+      }
+    }
     if (p.mode == 0) {
       while (f < f_end) {
         const int gg = static_cast<int>(f / p.tiles_max);
@@ -143,6 +182,11 @@ struct Walker {
   }
 };
 
+// How many of the first n round-robin items (item j goes to slot j % P) went to slot i.
+__device__ __forceinline__ long long issued_into(long long n, int i, int P) {
+  return n > i ? (n - 1 - i) / P + 1 : 0;
+}
+
 // e4m3 x4 (one 32-bit word) -> bf16 x4 (two 32-bit words), exact: every e4m3 value is a bf16 value.
 // The hardware widening to f16 is exact; an f16 with 3 significant mantissa bits maps to bf16 by
 // re-biasing the exponent (15 -> 127) and dropping 3 zero mantissa bits.  Zeros keep their sign.
@@ -168,7 +212,8 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
   unsigned char* kbuf = qbuf + C::QB * C::Q_BYTES;                    // S x STAGE_BYTES
   unsigned char* sbuf = kbuf + S * C::STAGE_BYTES;                    // S x STAGED_BYTES (FP8)
   float* wsm = reinterpret_cast<float*>(sbuf + S * C::STAGED_BYTES);  // [EW][NCOL]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(wsm + C::W_FLOATS);
+  int* nvsm = reinterpret_cast<int*>(wsm + C::W_FLOATS);                // [EW][GMAX]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(nvsm + C::NV_INTS);
   uint64_t* full = bars;              // [S] operand ready (TMA bytes, or converters)
   uint64_t* empty = full + S;         // [S] operand consumed (MMA commit)
   uint64_t* sfull = empty + S;        // [S] e4m3 staging landed (TMA)
@@ -183,6 +228,8 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ngroups = a.q_count;
+  grid_dep_wait();
+  grid_dep_launch();
 
   // alignment the TMA / tensor-core path relies on; a violation is reported, never executed
   {
@@ -208,7 +255,7 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
     }
     for (int i = 0; i < C::ACC; ++i) {
       tc::mbar_init(&accfull[i], 1);
-      tc::mbar_init(&accempty[i], C::EW * 32);
+      tc::mbar_init(&accempty[i], C::ACC_ARRIVALS);
     }
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -234,13 +281,11 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    int pend_parity[S];          // parity of the last load issued into each stage, -1 if none
-    int qpend[2] = {-1, -1};
-    for (int s = 0; s < S; ++s) pend_parity[s] = -1;
     if (lane == 0) {
       Walker wk;
       wk.init(p, ngroups);
-      long long n = 0;
+      long long n = 0;           // key-tile loads issued (load j went to stage j % S, phase j / S)
+      int nq = 0;                // query-block loads issued (load j went to buffer j % QB)
       int gc = -1;
       bool nw;
       bool ok = true;
@@ -253,7 +298,7 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
           const int z = wk.gi.b * a.Tq + wk.gi.i0;
           for (int r = 0; r < C::NREG; ++r)
             tc::tma_load_3d(qbuf + qb * C::Q_BYTES + r * C::Q_REGION, &qmap, r * 64, 0, z, &qfull[qb]);
-          qpend[qb] = (gc / C::QB) & 1;
+          ++nq;
         }
         const int s = static_cast<int>(n % S);
         const uint32_t ph = static_cast<uint32_t>((n / S) & 1);
@@ -267,16 +312,20 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
           for (int r = 0; r < C::NREG; ++r)
             tc::tma_load_3d(kbuf + s * C::STAGE_BYTES + r * C::KEY_REGION, &kmap, r * 64, wk.t * KT, wk.gi.b, &full[s]);
         }
-        pend_parity[s] = static_cast<int>(ph);
         ++n;
       }
-      // drain: every copy this CTA issued has landed before the CTA may exit
-      for (int s = 0; s < S; ++s)
-        if (pend_parity[s] >= 0 && !tc::mbar_wait(FP8 ? &sfull[s] : &full[s], pend_parity[s], nullptr))
+      // drain: every copy this CTA issued has landed before the CTA may exit (the last phase of
+      // each barrier follows from the issue counts; no per-stage arrays in local memory)
+      for (int s = 0; s < S; ++s) {
+        const long long cnt = issued_into(n, s, S);
+        if (cnt > 0 && !tc::mbar_wait(FP8 ? &sfull[s] : &full[s], static_cast<uint32_t>((cnt - 1) & 1), nullptr))
           report_error(a.status, CSA_ERR_TIMEOUT, 9);
-      for (int i = 0; i < 2; ++i)
-        if (qpend[i] >= 0 && !tc::mbar_wait(&qfull[i], qpend[i], nullptr))
+      }
+      for (int i = 0; i < C::QB; ++i) {
+        const long long cnt = issued_into(nq, i, C::QB);
+        if (cnt > 0 && !tc::mbar_wait(&qfull[i], static_cast<uint32_t>((cnt - 1) & 1), nullptr))
           report_error(a.status, CSA_ERR_TIMEOUT, 9);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -289,16 +338,10 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
       int gc = -1;
       bool nw;
       bool issued = false;
-      int ncommit_empty[S];              // commits issued to each barrier
-      int ncommit_q[2] = {0, 0};
-      for (int s = 0; s < S; ++s) ncommit_empty[s] = 0;
-      while (wk.next(a, p, ngroups, nw)) {
+      while (wk.next(a, p, ngroups, nw)) {     // tile n's commit goes to empty[n % S]
         if (nw) {
           ++gc;
-          if (gc >= 1) {
-            tc::umma_commit(&qempty[(gc - 1) % C::QB]);
-            ++ncommit_q[(gc - 1) % C::QB];
-          }
+          if (gc >= 1) tc::umma_commit(&qempty[(gc - 1) % C::QB]);   // group j's commit: qempty[j % QB]
           if (!tc::mbar_wait(&qfull[gc % C::QB], (gc / C::QB) & 1, abort_flag)) { fail(3); break; }
         }
         const int s = static_cast<int>(n % S);
@@ -318,7 +361,6 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
         }
         tc::umma_commit(&empty[s]);
         tc::umma_commit(&accfull[acc]);
-        ++ncommit_empty[s];
         issued = true;
         ++n;
       }
@@ -328,30 +370,38 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
         tc::umma_commit(drain);
         if (!tc::mbar_wait(drain, 0, nullptr)) report_error(a.status, CSA_ERR_TIMEOUT, 10);
       }
-      for (int s = 0; s < S; ++s)
-        if (ncommit_empty[s] > 0 && !tc::mbar_wait(&empty[s], (ncommit_empty[s] - 1) & 1, nullptr))
+      for (int s = 0; s < S; ++s) {
+        const long long cnt = issued_into(n, s, S);
+        if (cnt > 0 && !tc::mbar_wait(&empty[s], static_cast<uint32_t>((cnt - 1) & 1), nullptr))
           report_error(a.status, CSA_ERR_TIMEOUT, 11);
-      for (int i = 0; i < 2; ++i)
-        if (ncommit_q[i] > 0 && !tc::mbar_wait(&qempty[i], (ncommit_q[i] - 1) & 1, nullptr))
+      }
+      const int nqc = gc > 0 ? gc : 0;           // groups 0 .. gc-1 had their commit
+      for (int i = 0; i < C::QB; ++i) {
+        const long long cnt = issued_into(nqc, i, C::QB);
+        if (cnt > 0 && !tc::mbar_wait(&qempty[i], static_cast<uint32_t>((cnt - 1) & 1), nullptr))
           report_error(a.status, CSA_ERR_TIMEOUT, 11);
+      }
     }
     __syncwarp();
   } else if (warp >= 4 && warp < 4 + C::EW) {
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 4;
     const int quarter = warp & 3;                 // TMEM lanes [32*quarter, +32)
-    const int half = ew >> 2;                     // column split when EW = 8
-    constexpr int SPLIT = C::EW / 4;
+    const int set = ew >> 2;                      // warp set: its tile parity or its query half
+    const int half = C::TSPLIT ? 0 : set;
+    constexpr int SPLIT = C::TSPLIT ? 1 : 2;
     const int NHP = p.NHP, G = p.G;
     const int qs_per = (G + SPLIT - 1) / SPLIT;
     const int j_lo = half * qs_per, j_hi = min(G, j_lo + qs_per);
     float* wb = wsm + ew * NCOL;                  // this warp's copy of the group's head weights
+    int* nvb = nvsm + ew * C::GMAX;               // and of its queries' visible entry counts
     Walker wk;
     wk.init(p, ngroups);
     long long n = 0;
     bool nw;
     while (wk.next(a, p, ngroups, nw)) {
       if (nw) {
+        // per-group values are read from global memory once per group, not once per tile
         __syncwarp();
         for (int c = j_lo * NHP + lane; c < j_hi * NHP; c += 32) {
           const int j = c / NHP, h = c % NHP;
@@ -360,37 +410,58 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
             v = a.w[(static_cast<size_t>(wk.gi.b) * a.Tq + wk.gi.i0 + j) * a.nI + h];
           wb[c] = v;
         }
+        for (int j = j_lo + lane; j < j_hi; j += 32)
+          nvb[j] = j < wk.gi.nq ? n_visible(a.q_pos[static_cast<size_t>(wk.gi.b) * a.Tq + wk.gi.i0 + j], a.m, a.N)
+                                : 0;
         __syncwarp();
       }
+      if (C::TSPLIT && static_cast<int>(n & 1) != set) {   // the other set's tile
+        ++n;
+        continue;
+      }
       const int acc = static_cast<int>(n % C::ACC);
+      const int key = wk.t * KT + quarter * 32 + lane;
+      float kscale = 1.f;                         // issued before the wait so its latency overlaps it
+      if (FP8 && key < a.N) kscale = a.kI_scale[static_cast<size_t>(wk.gi.b) * a.N + key];
       // the warp leaves together: a wait that gave up on any lane ends the loop for all lanes
       const bool got = tc::mbar_wait(&accfull[acc], (n / C::ACC) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, got)) { fail(6); break; }
       tc::tc_fence_after();
-      const int key = wk.t * KT + quarter * 32 + lane;
-      float kscale = 1.f;
-      if (FP8 && key < a.N) kscale = a.kI_scale[static_cast<size_t>(wk.gi.b) * a.N + key];
       const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * NCOL;
       for (int j = j_lo; j < j_hi; ++j) {
         // four independent partial sums (fixed order: sum = (p0 + p1) + (p2 + p3))
+        // head h always feeds partial sum h % 4, in increasing h, whatever the load width
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        auto accum = [&](const float* v, const float* wrow, int cnt) {
+          const float4* w4 = reinterpret_cast<const float4*>(wrow);
+#pragma unroll
+          for (int h = 0; h < cnt; h += 4) {
+            const float4 ww = w4[h >> 2];
+            ps[0] = fmaf(ww.x, fmaxf(v[h], 0.f), ps[0]);
+            ps[1] = fmaf(ww.y, fmaxf(v[h + 1], 0.f), ps[1]);
+            ps[2] = fmaf(ww.z, fmaxf(v[h + 2], 0.f), ps[2]);
+            ps[3] = fmaf(ww.w, fmaxf(v[h + 3], 0.f), ps[3]);
+          }
+        };
         if (NHP == 16) {
           float v[16];
           tc::tmem_ld16_wait(tbase + j * NHP, v);
-#pragma unroll
-          for (int h = 0; h < 16; ++h) ps[h & 3] = fmaf(wb[j * NHP + h], fmaxf(v[h], 0.f), ps[h & 3]);
+          accum(v, wb + j * NHP, 16);
+        } else if (NHP == 32) {
+          float v[32];
+          tc::tmem_ld32_wait(tbase + j * NHP, v);
+          accum(v, wb + j * NHP, 32);
         } else {
-          for (int c0 = 0; c0 < NHP; c0 += 32) {
-            float v[32];
-            tc::tmem_ld32_wait(tbase + j * NHP + c0, v);
-#pragma unroll
-            for (int h = 0; h < 32; ++h) ps[h & 3] = fmaf(wb[j * NHP + c0 + h], fmaxf(v[h], 0.f), ps[h & 3]);
+          for (int c0 = 0; c0 < NHP; c0 += 64) {
+            float v[64];
+            tc::tmem_ld64_wait(tbase + j * NHP + c0, v);
+            accum(v, wb + j * NHP + c0, 64);
           }
         }
         const float sum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
         if (j < wk.gi.nq && key < a.N) {
           const size_t qi = static_cast<size_t>(wk.gi.b) * a.Tq + wk.gi.i0 + j;
-          const int nv = n_visible(a.q_pos[qi], a.m, a.N);
+          const int nv = nvb[j];
           float* dst = a.scores + (static_cast<long long>(qi) - a.score_row_offset) * a.N;
           if (key < nv) dst[key] = sum * kscale;
           else if (p.fill_invisible) dst[key] = -INFINITY;
@@ -442,32 +513,11 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
 
 // ------------------------------------------------------------------ host side
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = []() -> EncodeTiledFn {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    return reinterpret_cast<EncodeTiledFn>(f);
-  }();
-  return fn;
-}
-
 bool make_map_3d(CUtensorMap* map, CUtensorMapDataType dt, int esize, const void* base, uint64_t d0, uint64_t d1,
                  uint64_t d2, uint32_t b0, uint32_t b1, uint32_t b2, CUtensorMapSwizzle sw) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[3] = {d0, d1, d2};
-  const cuuint64_t strides[2] = {d0 * esize, d0 * d1 * esize};
-  const cuuint32_t box[3] = {b0, b1, b2};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint64_t dims[3] = {d0, d1, d2};
+  const uint32_t box[3] = {b0, b1, b2};
+  return tc::make_tensor_map(map, dt, 3, base, esize, dims, box, sw);
 }
 
 int sm_count() {
@@ -498,17 +548,19 @@ cudaError_t launch_t(const IndexArgs& a, const IndexGrouping& gr, int fill_invis
   p.fill_invisible = fill_invisible;
   const int sms = sm_count();
   const long long groups = a.q_count;
-  p.mode = groups >= 4LL * sms ? 1 : 0;
+  p.mode = groups >= 4LL * sms ? 1 : (CSA_IDX_WALK_CHUNK > 0 ? 2 : 0);
+  p.chunk = CSA_IDX_WALK_CHUNK > 0 ? CSA_IDX_WALK_CHUNK : 1;
   p.F = groups * p.tiles_max;
   long long grid = sms;
-  if (p.mode == 0 && p.F < grid) grid = p.F;
+  if (p.mode != 1 && p.F < grid) grid = p.F;
   if (grid < 1) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(k_index_score<DI, NCOL, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM);
   if (e != cudaSuccess) return e;
-  k_index_score<DI, NCOL, FP8><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM, s>>>(a, kmap, qmap, p);
+  e = launch_k(k_index_score<DI, NCOL, FP8>, dim3(static_cast<unsigned>(grid)), dim3(C::THREADS),
+               static_cast<size_t>(C::SMEM), s, a, kmap, qmap, p);
   ++*launches;
-  return cudaGetLastError();
+  return e;
 }
 
 template <int DI, bool FP8>

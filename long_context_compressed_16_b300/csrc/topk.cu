@@ -3,11 +3,14 @@
 //
 // Radix select on order-preserving 32-bit keys of the fp32 scores, one CTA per slice of at most
 // 32768 candidates, everything in that CTA's shared memory (no clusters, no inter-CTA waits).
-// The first 11-bit digit starts at the highest bit where the slice's largest and smallest keys
+// The first 8-bit digit starts at the highest bit where the slice's largest and smallest keys
 // differ (the bits above are common to all of them), so the histogram spreads over the scores'
 // actual range; each pass narrows the threshold bin, and the search stops once the threshold bin
-// is taken whole or all 32 bits are fixed.  The selected set is written in increasing entry
-// index: entries above the threshold bin and, inside it, the smallest indices first.
+// is taken whole or all 32 bits are fixed.  A pass costs two block barriers: every thread adds
+// its keys to a 256-bin shared histogram, then one warp scans the bins from the top, finds the
+// threshold bin and clears the histogram for the next pass.  The selected set is written in
+// increasing entry index: entries above the threshold bin and, inside it, the smallest indices
+// first.
 //
 // Rows longer than one slice run in two stages: every slice writes its own top-k (key, index)
 // candidates in index order, and a merge CTA selects the top-k of the concatenation.  This is
@@ -23,9 +26,17 @@ namespace {
 constexpr int kSlice = 32768;        // longest slice per CTA (128 KB of keys in shared memory)
 constexpr int kMinSlice = 4096;      // slices are not split below this length
 constexpr int kMergeCap = 16384;     // candidates one merge CTA holds (keys + indices: 128 KB)
-constexpr int kTargetCtas = 128;     // split rows until the first stage has about this many CTAs
-constexpr int kDigit = 11;
-constexpr int kBins = 1 << kDigit;
+#ifndef CSA_TOPK_TARGET_CTAS
+#define CSA_TOPK_TARGET_CTAS 128
+#endif
+#ifndef CSA_TOPK_SLICE_NT
+#define CSA_TOPK_SLICE_NT 1024
+#endif
+constexpr int kTargetCtas = CSA_TOPK_TARGET_CTAS;   // split rows until the first stage has about this many CTAs
+constexpr int kMergeRounds = 16;     // 32-candidate rounds per merge warp (registers per thread)
+constexpr int kDigit = 8;
+constexpr int kBins = 1 << kDigit;          // one warp scans them: kBins / 32 per lane
+constexpr int kBinsPerLane = kBins / 32;
 constexpr uint32_t kNoIndex = 0xFFFFFFFFu;
 
 // Order-preserving key of a score; -0 and +0 map to the same key (equal scores tie by index).
@@ -75,41 +86,11 @@ struct TkSmem {
 };
 
 // Block-wide top-k of keys[0, L) (L > k), written in increasing position order through emit(pos,
-// j) for the j-th selected element, j in [0, k).
+// j) for the j-th selected element, j in [0, k).  gmax / gmin: the largest and smallest key of
+// the list.  sm.hist must be all zero on entry; it is all zero again on return.
 template <int NT, typename Emit>
-__device__ void select_block(const TkSmem& sm, int L, int k, Emit emit) {
+__device__ void select_block(const TkSmem& sm, int L, int k, uint32_t gmax, uint32_t gmin, Emit emit) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t kmax = 0u, kmin = 0xFFFFFFFFu;
-  for (int i = tid; i < L; i += NT) {
-    const uint32_t kk = sm.keys[i];
-    kmax = max(kmax, kk);
-    kmin = min(kmin, kk);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
-    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
-  }
-  if (lane == 0) {
-    sm.red[warp] = kmax;
-    sm.red[32 + warp] = kmin;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t mx = lane < NT / 32 ? sm.red[lane] : 0u;
-    uint32_t mn = lane < NT / 32 ? sm.red[32 + lane] : 0xFFFFFFFFu;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    }
-    if (lane == 0) {
-      sm.xchg[5] = mx;
-      sm.xchg[6] = mn;
-    }
-  }
-  __syncthreads();
-  const uint32_t gmax = sm.xchg[5], gmin = sm.xchg[6];
   // bits at and above `pos` are common to every key of the list
   int pos = (gmax == gmin) ? 0 : 32 - __clz(gmax ^ gmin);
   uint32_t prefix = pos >= 32 ? 0u : (gmax >> pos) << pos;
@@ -120,35 +101,43 @@ __device__ void select_block(const TkSmem& sm, int L, int k, Emit emit) {
     const int shift = pos - nbits;
     const uint32_t dmask = (1u << nbits) - 1u;
     const uint32_t hmask = pos >= 32 ? 0u : ~((1u << pos) - 1u);
-    for (int i = tid; i < kBins; i += NT) sm.hist[i] = 0u;
-    __syncthreads();
     for (int i = tid; i < L; i += NT) {
       const uint32_t kk = sm.keys[i];
       if ((kk & hmask) == prefix) atomicAdd(&sm.hist[(kk >> shift) & dmask], 1u);
     }
     __syncthreads();
-    // thread tid owns the PER bins at descending positions [PER*tid, PER*tid + PER)
-    constexpr int PER = kBins / NT;
-    const int nb = 1 << nbits;
-    uint32_t c[PER];
-    uint32_t csum = 0;
+    if (warp == 0) {
+      // lane owns kBinsPerLane bins at descending positions; clears them for the next pass
+      const int nb = 1 << nbits;
+      uint32_t c[kBinsPerLane];
+      uint32_t csum = 0;
 #pragma unroll
-    for (int u = 0; u < PER; ++u) {
-      const int bin = nb - 1 - (PER * tid + u);
-      c[u] = bin >= 0 ? sm.hist[bin] : 0u;
-      csum += c[u];
-    }
-    unsigned long long tot;
-    unsigned long long above = block_excl_scan(csum, sm.ws, &tot);
-    const unsigned long long rem = static_cast<unsigned long long>(remaining);
-#pragma unroll
-    for (int u = 0; u < PER; ++u) {
-      if (above < rem && rem <= above + c[u]) {
-        sm.xchg[2] = static_cast<uint32_t>(nb - 1 - (PER * tid + u));
-        sm.xchg[3] = static_cast<uint32_t>(rem - above);
-        sm.xchg[4] = c[u];
+      for (int u = 0; u < kBinsPerLane; ++u) {
+        const int bin = nb - 1 - (kBinsPerLane * lane + u);
+        c[u] = 0u;
+        if (bin >= 0) {
+          c[u] = sm.hist[bin];
+          sm.hist[bin] = 0u;
+        }
+        csum += c[u];
       }
-      above += c[u];
+      uint32_t incl = csum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      uint32_t above = incl - csum;
+      const uint32_t rem = static_cast<uint32_t>(remaining);
+#pragma unroll
+      for (int u = 0; u < kBinsPerLane; ++u) {
+        if (above < rem && rem <= above + c[u]) {
+          sm.xchg[2] = static_cast<uint32_t>(nb - 1 - (kBinsPerLane * lane + u));
+          sm.xchg[3] = rem - above;
+          sm.xchg[4] = c[u];
+        }
+        above += c[u];
+      }
     }
     __syncthreads();
     prefix |= (sm.xchg[2] & dmask) << shift;
@@ -156,7 +145,8 @@ __device__ void select_block(const TkSmem& sm, int L, int k, Emit emit) {
     const uint32_t bin_count = sm.xchg[4];
     pos = shift;
     cmp_shift = shift;
-    __syncthreads();
+    // xchg is rewritten only after the next pass's first barrier, which every thread reaches
+    // after these reads
     if (bin_count == static_cast<uint32_t>(remaining)) break;   // the threshold bin is taken whole
   }
   // selected: key >> cmp_shift above thr, or equal to it among the first `remaining` positions.
@@ -206,10 +196,36 @@ __device__ void select_block(const TkSmem& sm, int L, int k, Emit emit) {
   }
 }
 
-// keys[i] = order_key(src[i]) for i < L, eight independent loads in flight per thread.
+// Block-wide max and min of per-thread values; every thread gets both.  Ends with a barrier.
 template <int NT>
-__device__ __forceinline__ void load_keys(uint32_t* keys, const float* src, int L) {
-  constexpr int U = 8;
+__device__ __forceinline__ void block_minmax(const TkSmem& sm, uint32_t& kmax, uint32_t& kmin) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+    kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+  }
+  if (lane == 0) {
+    sm.red[warp] = kmax;
+    sm.red[32 + warp] = kmin;
+  }
+  __syncthreads();
+  uint32_t mx = lane < NT / 32 ? sm.red[lane] : 0u;
+  uint32_t mn = lane < NT / 32 ? sm.red[32 + lane] : 0xFFFFFFFFu;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+  }
+  kmax = mx;
+  kmin = mn;
+}
+
+// keys[i] = order_key(src[i]) for i < L, eight independent loads in flight per thread; returns
+// this thread's largest and smallest key through kmax / kmin.
+template <int NT>
+__device__ __forceinline__ void load_keys(uint32_t* keys, const float* src, int L, uint32_t& kmax, uint32_t& kmin) {
+  constexpr int U = NT >= 1024 ? 8 : (NT >= 512 ? 16 : 32);   // loads in flight per thread
   for (int base = 0; base < L; base += NT * U) {
     float v[U];
 #pragma unroll
@@ -220,9 +236,18 @@ __device__ __forceinline__ void load_keys(uint32_t* keys, const float* src, int 
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int i = base + u * NT + threadIdx.x;
-      if (i < L) keys[i] = order_key(v[u]);
+      if (i < L) {
+        const uint32_t kk = order_key(v[u]);
+        keys[i] = kk;
+        kmax = max(kmax, kk);
+        kmin = min(kmin, kk);
+      }
     }
   }
+}
+
+__device__ __forceinline__ void clear_hist(const TkSmem& sm) {
+  for (int i = threadIdx.x; i < kBins; i += blockDim.x) sm.hist[i] = 0u;
 }
 
 __device__ __forceinline__ TkSmem carve(uint32_t* base, int cap, bool with_idx) {
@@ -243,6 +268,8 @@ template <int NT>
 __global__ void __launch_bounds__(NT) k_topk_slice(TopkArgs a, int S, int slice_len, int cap,
                                                    unsigned long long* cand) {
   extern __shared__ __align__(16) uint32_t tsm[];
+  grid_dep_wait();
+  grid_dep_launch();
   const TkSmem sm = carve(tsm, cap, false);
   const int tid = threadIdx.x;
   const long long qrel = blockIdx.x / S;
@@ -263,9 +290,11 @@ __global__ void __launch_bounds__(NT) k_topk_slice(TopkArgs a, int S, int slice_
       return;
     }
     const float* row = a.scores + (qi - a.score_row_offset) * static_cast<long long>(a.N);
-    load_keys<NT>(sm.keys, row + lo, L);
-    __syncthreads();
-    select_block<NT>(sm, L, k, [&](int i, int j) { out[j] = lo + i; });
+    uint32_t kmax = 0u, kmin = 0xFFFFFFFFu;
+    clear_hist(sm);
+    load_keys<NT>(sm.keys, row + lo, L, kmax, kmin);
+    block_minmax<NT>(sm, kmax, kmin);
+    select_block<NT>(sm, L, k, kmax, kmin, [&](int i, int j) { out[j] = lo + i; });
     return;
   }
   unsigned long long* crow = cand + (qrel * S + sl) * static_cast<long long>(k);
@@ -281,9 +310,11 @@ __global__ void __launch_bounds__(NT) k_topk_slice(TopkArgs a, int S, int slice_
     return;
   }
   const float* row = a.scores + (qi - a.score_row_offset) * static_cast<long long>(a.N);
-  load_keys<NT>(sm.keys, row + lo, L);
-  __syncthreads();
-  select_block<NT>(sm, L, k, [&](int i, int j) {
+  uint32_t kmax = 0u, kmin = 0xFFFFFFFFu;
+  clear_hist(sm);
+  load_keys<NT>(sm.keys, row + lo, L, kmax, kmin);
+  block_minmax<NT>(sm, kmax, kmin);
+  select_block<NT>(sm, L, k, kmax, kmin, [&](int i, int j) {
     crow[j] = (static_cast<unsigned long long>(sm.keys[i]) << 32) | static_cast<uint32_t>(lo + i);
   });
 }
@@ -292,6 +323,8 @@ __global__ void __launch_bounds__(NT) k_topk_slice(TopkArgs a, int S, int slice_
 template <int NT>
 __global__ void __launch_bounds__(NT) k_topk_merge(TopkArgs a, int S, int cap, const unsigned long long* cand) {
   extern __shared__ __align__(16) uint32_t tsm[];
+  grid_dep_wait();
+  grid_dep_launch();
   const TkSmem sm = carve(tsm, cap, true);
   const int tid = threadIdx.x;
   const long long qrel = blockIdx.x;
@@ -309,44 +342,54 @@ __global__ void __launch_bounds__(NT) k_topk_merge(TopkArgs a, int S, int cap, c
     return;
   }
   // compact the valid candidates (they are already in increasing index order); each warp owns a
-  // contiguous range read 32 consecutive candidates at a time
+  // contiguous range, read 32 consecutive candidates at a time, all of them loaded up front so the
+  // loads overlap
   const unsigned long long* crow = cand + qrel * static_cast<long long>(total);
   const int lane = tid & 31, warp = tid >> 5;
   constexpr int NW = NT / 32;
+  constexpr int UMAX = kMergeRounds;                // 32-candidate rounds per warp at most
   const int per_w = ((total + NW - 1) / NW + 31) & ~31;
   const int w_lo = min(total, warp * per_w), w_hi = min(total, w_lo + per_w);
-  uint32_t cnt = 0;
-  for (int base = w_lo; base < w_hi; base += 32) {
-    const int i = base + lane;
-    const bool valid = i < w_hi && static_cast<uint32_t>(crow[i] & 0xFFFFFFFFull) != kNoIndex;
-    cnt += __popc(__ballot_sync(0xffffffffu, valid));
+  if (per_w > UMAX * 32) {               // cannot happen: the launch picks NT >= total / UMAX
+    if (tid == 0) report_error(a.status, CSA_ERR_DEVICE_CHECK, per_w);
+    return;
   }
+  unsigned long long c[UMAX];
+#pragma unroll
+  for (int u = 0; u < UMAX; ++u) {
+    const int i = w_lo + u * 32 + lane;
+    c[u] = i < w_hi ? crow[i] : static_cast<unsigned long long>(kNoIndex);
+  }
+  uint32_t cnt = 0;
+#pragma unroll
+  for (int u = 0; u < UMAX; ++u)
+    cnt += __popc(__ballot_sync(0xffffffffu, static_cast<uint32_t>(c[u] & 0xFFFFFFFFull) != kNoIndex));
+  clear_hist(sm);
   unsigned long long tot;
   const unsigned long long exs = block_excl_scan(lane == 0 ? cnt : 0u, sm.ws, &tot);
   uint32_t p = static_cast<uint32_t>(__shfl_sync(0xffffffffu, exs, 0));
-  for (int base = w_lo; base < w_hi; base += 32) {
-    const int i = base + lane;
-    unsigned long long c = 0;
-    bool valid = false;
-    if (i < w_hi) {
-      c = crow[i];
-      valid = static_cast<uint32_t>(c & 0xFFFFFFFFull) != kNoIndex;
-    }
+  uint32_t kmax = 0u, kmin = 0xFFFFFFFFu;
+#pragma unroll
+  for (int u = 0; u < UMAX; ++u) {
+    const bool valid = static_cast<uint32_t>(c[u] & 0xFFFFFFFFull) != kNoIndex;
     const uint32_t m = __ballot_sync(0xffffffffu, valid);
     const uint32_t q = p + __popc(m & ((1u << lane) - 1u));
     if (valid && q < static_cast<uint32_t>(cap)) {
-      sm.keys[q] = static_cast<uint32_t>(c >> 32);
-      sm.idx[q] = static_cast<uint32_t>(c & 0xFFFFFFFFull);
+      const uint32_t kk = static_cast<uint32_t>(c[u] >> 32);
+      sm.keys[q] = kk;
+      sm.idx[q] = static_cast<uint32_t>(c[u] & 0xFFFFFFFFull);
+      kmax = max(kmax, kk);
+      kmin = min(kmin, kk);
     }
     p += __popc(m);
   }
-  __syncthreads();
+  block_minmax<NT>(sm, kmax, kmin);
   const int L = static_cast<int>(min(tot, static_cast<unsigned long long>(cap)));
   if (L <= k) {                          // fewer valid candidates than k (n > k makes this rare)
     for (int i = tid; i < k; i += NT) out[i] = i < L ? static_cast<int32_t>(sm.idx[i]) : -1;
     return;
   }
-  select_block<NT>(sm, L, k, [&](int i, int j) { out[j] = static_cast<int32_t>(sm.idx[i]); });
+  select_block<NT>(sm, L, k, kmax, kmin, [&](int i, int j) { out[j] = static_cast<int32_t>(sm.idx[i]); });
 }
 
 size_t slice_smem(int cap, bool with_idx) {
@@ -383,8 +426,8 @@ cudaError_t launch_slice(const TopkArgs& a, int S, int len, int cap, unsigned lo
   cudaError_t e = cudaFuncSetAttribute(k_topk_slice<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  k_topk_slice<NT><<<static_cast<unsigned>(a.q_count) * S, NT, smem, s>>>(a, S, len, cap, cand);
-  return cudaGetLastError();
+  return launch_k(k_topk_slice<NT>, dim3(static_cast<unsigned>(a.q_count) * S), dim3(NT), smem, s, a, S, len, cap,
+                  cand);
 }
 
 template <int NT>
@@ -393,8 +436,7 @@ cudaError_t launch_merge(const TopkArgs& a, int S, int cap, const unsigned long 
   cudaError_t e = cudaFuncSetAttribute(k_topk_merge<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  k_topk_merge<NT><<<static_cast<unsigned>(a.q_count), NT, smem, s>>>(a, S, cap, cand);
-  return cudaGetLastError();
+  return launch_k(k_topk_merge<NT>, dim3(static_cast<unsigned>(a.q_count)), dim3(NT), smem, s, a, S, cap, cand);
 }
 
 cudaError_t launch_topk(const TopkArgs& a, void* cand_ws, cudaStream_t s, int* launches) {
@@ -404,11 +446,15 @@ cudaError_t launch_topk(const TopkArgs& a, void* cand_ws, cudaStream_t s, int* l
   if (S > 1 && (cand_ws == nullptr || static_cast<long long>(S) * a.k > kMergeCap)) return cudaErrorInvalidValue;
   const int cap1 = S == 1 ? ((a.N + 3) & ~3) : len;
   unsigned long long* cand = static_cast<unsigned long long*>(cand_ws);
-  cudaError_t e = launch_slice<1024>(a, S, len, cap1, cand, s);
+  cudaError_t e = launch_slice<CSA_TOPK_SLICE_NT>(a, S, len, cap1, cand, s);
   ++*launches;
   if (e != cudaSuccess || S == 1) return e;
-  const int cap2 = (S * a.k + 3) & ~3;
-  e = launch_merge<1024>(a, S, cap2, cand, s);
+  const int total = S * a.k;
+  const int cap2 = (total + 3) & ~3;
+  // the fewest threads that still hold every candidate in registers (kMergeRounds per warp)
+  if (total <= 256 * kMergeRounds) e = launch_merge<256>(a, S, cap2, cand, s);
+  else if (total <= 512 * kMergeRounds) e = launch_merge<512>(a, S, cap2, cand, s);
+  else e = launch_merge<1024>(a, S, cap2, cand, s);
   ++*launches;
   return e;
 }

@@ -15,7 +15,8 @@ def _dev_check(*ts):
 
 
 def _ws(nbytes: int, device) -> torch.Tensor:
-    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    # zero-filled: the status word at its start must begin cleared (it is sticky)
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
 def compress(Ca, Za, m, Cb=None, Zb=None, bias_a=None, bias_b=None, gamma=None, norm=True, rope=True,

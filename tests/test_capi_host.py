@@ -112,6 +112,28 @@ def test_index_validation_and_workspace():
     assert call(_idesc(B=0)) == C.CSA_OK
 
 
+def test_split_index_calls_validation_and_workspace():
+    assert C.lib.csa_index_score_workspace(ctypes.byref(_idesc())) == 256
+    assert C.lib.csa_index_score_workspace(ctypes.byref(_idesc(head_dim=96))) == 0
+    # decode rows longer than one selection slice keep (key, index) candidates of every slice
+    ws = C.lib.csa_topk_workspace(ctypes.byref(_idesc(B=32, Tq=1, N=32768, k=512)))
+    assert ws >= 256 + 32 * 2 * 512 * 8
+    assert C.lib.csa_topk_workspace(ctypes.byref(_idesc(B=1, Tq=65536, N=16384))) == 256   # one stage
+    sc = lambda desc, ws_ptr=FAKE, ws_bytes=1 << 30: C.lib.csa_index_score(
+        ctypes.byref(desc), FAKE, FAKE, FAKE, None, FAKE, FAKE, ws_ptr, ws_bytes, None)
+    assert sc(_idesc(n_heads=65)) == C.CSA_ERR_INVALID_ARG
+    assert sc(_idesc(N=300000)) == C.CSA_ERR_UNSUPPORTED
+    assert sc(_idesc(), ws_bytes=100) == C.CSA_ERR_WORKSPACE
+    assert sc(_idesc(key_fmt=C.CSA_FMT_FP8_ROWSCALE)) == C.CSA_ERR_INVALID_ARG
+    assert sc(_idesc(B=0)) == C.CSA_OK
+    tk = lambda desc, ws_ptr=FAKE, ws_bytes=1 << 30: C.lib.csa_topk(
+        ctypes.byref(desc), FAKE, FAKE, FAKE, ws_ptr, ws_bytes, None)
+    assert tk(_idesc(k=0)) == C.CSA_ERR_INVALID_ARG
+    assert tk(_idesc(), ws_ptr=None) == C.CSA_ERR_WORKSPACE
+    assert tk(_idesc(B=32, Tq=1, N=32768, k=512), ws_bytes=256) == C.CSA_ERR_WORKSPACE
+    assert tk(_idesc(B=0)) == C.CSA_OK
+
+
 def _adesc(**kw):
     d = dict(B=2, Tq=1, N=1000, H=64, d=512, rope_dims=64, k=64, m=4, Wcap=128, window=128, scale=0.0,
              rope_theta=160000.0, inv_freq=None, eps=1e-6, kv_fmt=C.CSA_FMT_BF16, flags=3)

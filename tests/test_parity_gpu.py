@@ -167,6 +167,41 @@ def test_index_topk_decode_1m_fp8_full():
     _index_case(inp["qI"], inp["w"], inp["kI"], inp["q_pos"], 4, w.k, kI_scale=inp["kI_scale"])
 
 
+@pytest.mark.parametrize("B,Tq,N,nI,dI,k", [
+    (32, 1, 32768, 64, 128, 512),      # decode: rows split into slices, then merged
+    (1, 300, 2000, 64, 128, 512),      # prefill-like rows, one stage
+    (2, 5, 777, 16, 64, 40),           # ragged
+])
+def test_split_score_and_topk_calls_equal_fused_call(B, Tq, N, nI, dI, k):
+    qI = S.normal_bf16((B, Tq, nI, dI), 5, S.TID["qI"], DEV)
+    w = S.uniform_f64((B, Tq, nI), 5, S.TID["w"], DEV).float()
+    kI = S.normal_bf16((B, N, dI), 5, S.TID["kI"], DEV)
+    q_pos = (4 * N - 4 * Tq + 4 * torch.arange(Tq, dtype=torch.int32, device=DEV)).repeat(B, 1).contiguous()
+    q_pos[0, 0] = 6                              # a short row (k > visible entries)
+    desc = P.index_desc(B, Tq, N, nI, dI, k, 4)
+    sc_f = torch.empty((B, Tq, N), dtype=torch.float32, device=DEV)
+    idx_f = P.index_topk(qI, w, kI, q_pos, 4, k, score_out=sc_f)
+    sc = torch.full((B, Tq, N), float("nan"), dtype=torch.float32, device=DEV)
+    ws = torch.zeros(max(C.csa_index_score_workspace(desc), C.csa_topk_workspace(desc)), dtype=torch.uint8,
+                     device=DEV)
+    C.check(C.csa_index_score(desc, qI, w, kI, None, q_pos, sc, ws), "csa_index_score")
+    idx = torch.full((B, Tq, k), -7, dtype=torch.int32, device=DEV)
+    C.check(C.csa_topk(desc, sc, q_pos, idx, ws), "csa_topk")
+    torch.cuda.synchronize()
+    assert C.csa_read_device_status(ws)[0] == C.CSA_OK
+    nv = torch.clamp((q_pos.long() + 1) // 4, max=N)
+    mask = torch.arange(N, device=DEV)[None, None, :] >= nv[..., None]
+    assert torch.equal(sc[~mask], sc_f[~mask])            # visible scores, bit for bit
+    assert torch.all(torch.isnan(sc[mask]))               # the rest of each row is left untouched
+    assert torch.equal(idx, idx_f)
+    # the selector reads visible entries only: garbage past N_vis changes nothing
+    sc2 = torch.where(mask, torch.full_like(sc, 3.0e38), sc)
+    idx2 = torch.full_like(idx, -7)
+    C.check(C.csa_topk(desc, sc2, q_pos, idx2, ws), "csa_topk")
+    torch.cuda.synchronize()
+    assert torch.equal(idx2, idx_f)
+
+
 # ------------------------------------------------------------------------------------------------ attention
 
 def _oracle_attend_rows(inp, idx_np, m, window, pairs, fp8=False, dense=False, **kw):
@@ -281,8 +316,8 @@ def test_attend_hca_prefill_sampled():
 @pytest.mark.parametrize("flags,H", [((True, True), 32), ((False, False), 32), ((True, False), 32),
                                      ((True, True), 64), ((False, False), 128), ((True, False), 64)])
 def test_attend_flags_and_edges(flags, H):
-    """Small decode-like case: -1 pads, windows clipped at 0, ring wrap, sink, flags off, lse.
-    32 heads run the warp-MMA kernel, multiples of 64 heads the tensor-memory kernel."""
+    """Small decode-like case: -1 pads, windows clipped at 0, ring wrap, sink, flags off, lse,
+    with 32 heads (16 per CTA) and 64 / 128 heads (64 per CTA when the grid is large enough)."""
     qnr, unrot = flags
     B, d, N, k, Wcap = 3, 512, 300, 40, 160
     q = S.normal_bf16((B, 1, H, d), 11, 1, DEV)
@@ -325,12 +360,12 @@ def test_attend_bad_index_is_reported_and_skipped(H, d):
     assert torch.equal(out_b, out_g)
 
 
-def test_attend_tc_prefill_rows_and_large_logits():
-    """Prefill-shaped call (one split per query, 640 rows in 10 chunks) where late entries have much
-    larger logits, so a head's maximum grows by more than 2^8 between chunks (the kernel then
-    rescales its accumulator in tensor memory).  The query is the oracle's own normalised and
-    rotated q_hat rounded to bf16 and passed with the query preprocessing off, so both sides use
-    identical logits and the comparison isolates the attention arithmetic."""
+def test_attend_prefill_rows_and_large_logits():
+    """Prefill-shaped call (one split per query, 640 slots) where late entries have much larger
+    logits, so the running maximum of the online softmax jumps between chunks.  The query is the
+    oracle's own normalised and rotated q_hat rounded to bf16 and passed with the query
+    preprocessing off, so both sides use identical logits and the comparison isolates the
+    attention arithmetic."""
     B, T, H, d, N, k = 1, 96, 64, 512, 200, 512
     q_pos = (torch.arange(T, dtype=torch.int32) * 8 + 7)[None]
     q_raw = S.normal_f64((B, T, H, d), 13, 1).numpy()
@@ -353,7 +388,7 @@ def test_attend_tc_prefill_rows_and_large_logits():
     inp = dict(q=q, kv=kv, win=win, sink=sink, q_pos=q_pos)
     ts = list(range(0, T, 5)) + [T - 1]
     ref, lref = _oracle_attend_rows(inp, idx_np, 4, 128, [(0, t) for t in ts], q_norm_rope=False)
-    assert_close(out[0, ts], ref, "tc prefill rows")
+    assert_close(out[0, ts], ref, "prefill rows, large logits")
     assert_lse(lse[0, ts], lref, "lse")
 
 

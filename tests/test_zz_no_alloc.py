@@ -52,7 +52,7 @@ def test_noalloc_matches_workspace_call_twice_in_a_row():
         qI, w, kI, kI_scale, q_pos = _case(c["B"], c["N"], c["nI"], c["dI"], c["k"], c["seed"], c["fp8"])
         desc = P.index_desc(c["B"], 1, c["N"], c["nI"], c["dI"], c["k"], 4, fp8=c["fp8"])
         assert C.csa_index_topk_workspace(desc) <= C.CSA_NOALLOC_SCRATCH_BYTES
-        ws = torch.empty(C.csa_index_topk_workspace(desc), dtype=torch.uint8, device="cuda")
+        ws = torch.zeros(C.csa_index_topk_workspace(desc), dtype=torch.uint8, device="cuda")
         ref = torch.full((c["B"], 1, c["k"]), -7, dtype=torch.int32, device="cuda")
         got = torch.full_like(ref, -7)
         C.check(C.csa_index_topk(desc, qI, w, kI, kI_scale, q_pos, ref, None, ws), "csa_index_topk")
