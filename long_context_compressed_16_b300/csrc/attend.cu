@@ -45,18 +45,23 @@ struct AttnCfg {
   static constexpr size_t red_off = sc_off + (FP8 ? size_t(2) * CK * NB * 4 : 0);
   static constexpr size_t lsum_off = red_off + size_t(HG) * 4 * 4;
   static constexpr size_t ptr_off = lsum_off + size_t(HG) * 4 * 4;
-  static constexpr size_t rope_off = ptr_off + size_t(2) * CK * 8;   // float2 [kMaxRopePairs]
+  static constexpr size_t rope_off = ptr_off + size_t(3) * CK * 8;   // float2 [kMaxRopePairs]
   static constexpr size_t smem = rope_off + size_t(kMaxRopePairs) * 8;
   static_assert(!FP8 || (NG == 1 && D == 512), "the FP8 cache path runs 16 heads per CTA, d = 512");
 };
 
-__device__ __forceinline__ int slot_row(const AttendArgs& a, int b, long long qi, int t, int Kq, int s,
-                                        bool& win_row, int32_t* status) {
+// The idx value of slot s (its only global read), loaded ahead of slot_row.
+__device__ __forceinline__ int slot_raw(const AttendArgs& a, long long qi, int Kq, int s) {
+  return (s < Kq && a.idx != nullptr) ? a.idx[qi * a.k + s] : 0;
+}
+
+__device__ __forceinline__ int slot_row(const AttendArgs& a, int t, int Kq, int s, int raw, bool& win_row,
+                                        int32_t* status) {
   // returns the row index (entry index or ring slot) or -1 when the slot holds nothing
   if (s < Kq) {
     win_row = false;
     if (a.idx == nullptr) return s;
-    const int e = a.idx[qi * a.k + s];
+    const int e = raw;
     if (e == -1) return -1;
     if (e < -1 || e >= a.N) {
       report_error(status, CSA_ERR_DEVICE_CHECK, e);
@@ -107,13 +112,20 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
   const unsigned char* winb = static_cast<const unsigned char*>(a.win);
   const unsigned char* dummy = static_cast<const unsigned char*>(a.q);   // source of zero-size copies
 
-  auto compute_ptrs = [&](int c, int buf) {
+  // Row pointers of chunk c live in rowptr[(c % 3) * CK ...]: the idx values of chunk c + 2 are
+  // loaded at the top of chunk c's iteration and turned into pointers after its QK^T product,
+  // so their latency hides behind that product instead of stalling the next gather.
+  auto load_raw = [&](int c) -> int {
+    const int s = s_begin + c * CK + tid;
+    return (tid < CK && s < s_end) ? slot_raw(a, qi, Kq, s) : 0;
+  };
+  auto compute_ptrs = [&](int c, int buf, int raw) {
     if (tid < CK) {
       const int s = s_begin + c * CK + tid;
       const unsigned char* p = nullptr;
       if (s < s_end) {
         bool isw = false;
-        const int r = slot_row(a, b, qi, t, Kq, s, isw, a.status);
+        const int r = slot_row(a, t, Kq, s, raw, isw, a.status);
         if (r >= 0) {
           p = isw ? winb + (static_cast<size_t>(b) * a.Wcap + r) * (D * 2)
                   : kvb + (static_cast<size_t>(b) * a.N + r) * C::ROWB;
@@ -124,11 +136,11 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
     }
   };
   // cp.async of chunk rows into Ks (bf16) or the FP8 staging area (window rows go straight to Ks)
-  auto issue_loads = [&](int buf) {
+  auto issue_loads = [&](int buf, int pbuf) {
     constexpr int CPR = D * 2 / 16;
     for (int c = tid; c < CK * CPR; c += C::THREADS) {
       const int r = c / CPR, q = c % CPR;
-      const unsigned char* p = rowptr[buf * CK + r];
+      const unsigned char* p = rowptr[pbuf * CK + r];
       __nv_bfloat16* kd = Ks + (buf * CK + r) * KS + q * 8;
       if (!FP8) {
         cp_async16(kd, p ? p + q * 16 : dummy, p != nullptr);
@@ -156,9 +168,12 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
 
   // the first chunk's row gather is in flight while the query block is prepared
   if (nchunks > 0) {
-    compute_ptrs(0, 0);
+    const int raw0 = load_raw(0);
+    const int raw1 = nchunks > 1 ? load_raw(1) : 0;
+    compute_ptrs(0, 0, raw0);
+    if (nchunks > 1) compute_ptrs(1, 1, raw1);
     __syncthreads();
-    issue_loads(0);
+    issue_loads(0, 0);
     cp_async_commit();
   }
 
@@ -251,10 +266,11 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
 
   for (int c = 0; c < nchunks; ++c) {
     const int buf = c & 1;
-    if (c + 1 < nchunks) compute_ptrs(c + 1, buf ^ 1);
+    const int pb = c % 3;
+    const int raw_next = c + 2 < nchunks ? load_raw(c + 2) : 0;
     __syncthreads();                                   // (A)
     if (c + 1 < nchunks) {
-      issue_loads(buf ^ 1);
+      issue_loads(buf ^ 1, (c + 1) % 3);
       cp_async_commit();
       cp_async_wait<1>();
     } else {
@@ -267,7 +283,7 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
       // rows and the RoPE block use scale 1)
       for (int idx = tid; idx < CK * (D / 8); idx += C::THREADS) {
         const int r = idx / (D / 8), p8 = idx % (D / 8);
-        const unsigned char* p = rowptr[buf * CK + r];
+        const unsigned char* p = rowptr[pb * CK + r];
         const bool isw = (reinterpret_cast<uintptr_t>(p) & 1u) != 0;
         const unsigned char* row = St + (buf * CK + r) * C::ROWB;
         if ((p8 & 7) == 0) {
@@ -350,6 +366,8 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
         sacc[0][3] = fmaf(pacc[3], s1, sacc[0][3]);
       }
     }
+    // chunk c + 2's pointers: rowptr[(c + 2) % 3] last served chunk c - 1, finished before (A)
+    if (c + 2 < nchunks) compute_ptrs(c + 2, (c + 2) % 3, raw_next);
     // ---- mask, scale to log2 domain, row max over this warp's keys
     float cmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
@@ -357,7 +375,7 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int key = wq * 8 * NKT + n * 8 + 2 * (lane & 3) + (e & 1);
-        const bool ok = rowptr[buf * CK + key] != nullptr;
+        const bool ok = rowptr[pb * CK + key] != nullptr;
         const float v = ok ? sacc[n][e] * sl2 : -INFINITY;
         sacc[n][e] = v;
         cmax[e >> 1] = fmaxf(cmax[e >> 1], v);
