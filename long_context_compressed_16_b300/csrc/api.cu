@@ -12,7 +12,10 @@ std::atomic<uint64_t> g_launches{0};
 
 constexpr size_t kScoreChunkCap = size_t(256) << 20;   // bytes of fp32 scores per top-k pass
 #ifndef CSA_ATT_DECODE_SPLIT
-#define CSA_ATT_DECODE_SPLIT 192                        // decode attention slots per split (x 64)
+#define CSA_ATT_DECODE_SPLIT 192                        // decode attention slots per split, bf16 rows
+#endif
+#ifndef CSA_ATT_DECODE_SPLIT_FP8
+#define CSA_ATT_DECODE_SPLIT_FP8 128                    // the same for mixed FP8 rows
 #endif
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -113,10 +116,13 @@ AttendPlan plan_attend(const csa_attend_desc* d, bool csa_mode) {
   AttendPlan p;
   p.n_slots = (csa_mode ? d->k : d->N) + d->window;
   if (p.n_slots < 1) p.n_slots = 1;
-  // Decode (one query per sequence) splits the slot range in fixed 256-slot pieces, merged by a
-  // second kernel (192 slots: three 64-row chunks); the split size never depends on the batch.
-  // Prefill keeps one split per query.
-  p.split_slots = (d->Tq == 1) ? CSA_ATT_DECODE_SPLIT : ((p.n_slots + 63) / 64) * 64;
+  // Decode (one query per sequence) splits the slot range in fixed pieces merged by a second
+  // kernel: 192 slots (three 64-row chunks) for bf16 rows (64 heads per CTA), 128 slots (four
+  // 32-row chunks) for the FP8 rows (16 heads per CTA, so four CTAs share a split's rows).  The
+  // split size depends on the row format only, never on the batch.  Prefill keeps one split
+  // per query.
+  const int dec_split = d->kv_fmt == CSA_FMT_FP8_MIXED ? CSA_ATT_DECODE_SPLIT_FP8 : CSA_ATT_DECODE_SPLIT;
+  p.split_slots = (d->Tq == 1) ? dec_split : ((p.n_slots + 63) / 64) * 64;
   p.n_splits = (p.n_slots + p.split_slots - 1) / p.split_slots;
   if (p.n_splits < 1) p.n_splits = 1;
   p.partial_bytes = csa::attend_partial_bytes(d->B * d->Tq, d->H, d->d, p.n_splits);
