@@ -44,11 +44,14 @@ struct Cfg {
   static constexpr int Q_REGION = NCOL * 128;
   static constexpr int Q_BYTES = NREG * Q_REGION;
   static constexpr int QB = NCOL >= 256 ? 1 : 2;          // query-block buffers
-  static constexpr int EW = 8;                            // epilogue warps: two sets of four
+  // FP8 keys with N <= 128: the widening to bf16 is the busiest role, so 8 converter warps and
+  // one set of 4 epilogue warps; otherwise 8 epilogue warps (two sets of four) and 4 converters
+  static constexpr bool CONV_HEAVY = FP8 && NCOL <= 128;
+  static constexpr int EW = CONV_HEAVY ? 4 : 8;           // epilogue warps
   // NCOL <= 128: the two sets take alternate tiles; wider: they split the group's queries
-  static constexpr bool TSPLIT = NCOL <= 128;
+  static constexpr bool TSPLIT = EW == 8 && NCOL <= 128;
   static constexpr int ACC_ARRIVALS = 32 * (TSPLIT ? EW / 2 : EW);   // epilogue threads per tile
-  static constexpr int CW = FP8 ? 4 : 0;                  // converter warps
+  static constexpr int CW = FP8 ? (CONV_HEAVY ? 8 : 4) : 0;   // converter warps
   static constexpr int THREADS = 32 * (4 + EW + CW);
   static constexpr int W_FLOATS = EW * NCOL;              // per-epilogue-warp copy of the head weights
   static constexpr int GMAX = 16;                         // queries per group (NCOL / 16 heads at most)
@@ -387,7 +390,7 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
     const int quarter = warp & 3;                 // TMEM lanes [32*quarter, +32)
     const int set = ew >> 2;                      // warp set: its tile parity or its query half
     const int half = C::TSPLIT ? 0 : set;
-    constexpr int SPLIT = C::TSPLIT ? 1 : 2;
+    constexpr int SPLIT = C::TSPLIT ? 1 : C::EW / 4;
     const int NHP = p.NHP, G = p.G;
     const int qs_per = (G + SPLIT - 1) / SPLIT;
     const int j_lo = half * qs_per, j_hi = min(G, j_lo + qs_per);
