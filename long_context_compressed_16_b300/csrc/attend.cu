@@ -659,14 +659,9 @@ size_t attend_partial_bytes(int Q, int H, int d, int n_splits) {
   return static_cast<size_t>(Q) * n_splits * H * (d + 2) * sizeof(float);
 }
 
-#ifndef CSA_ATTEND_TC
-#define CSA_ATTEND_TC 1                 // 512-dim bf16 rows on the tcgen05 kernel (attend_tc.cu)
-#endif
-
 cudaError_t launch_attend(const AttendArgs& a, cudaStream_t s, int* launches) {
   const int Q = a.B * a.Tq;
   if (Q == 0) return cudaSuccess;
-  if (CSA_ATTEND_TC && attend_tc_supported(a)) return launch_attend_tc(a, s, launches);
   // 64 heads per CTA (each gathered row read once) when that still gives work to at least half
   // of the SMs, otherwise 16 heads per CTA; the numerics are identical
   int sms = 148;

@@ -243,9 +243,7 @@ cudaError_t launch_attend_combine(const AttendArgs& a, cudaStream_t s, int* laun
 
 
 cudaError_t launch_attend(const AttendArgs& a, cudaStream_t s, int* launches);
-// tcgen05 attention for 512-dim bf16 rows, 64 heads per CTA (attend_tc.cu).
-bool attend_tc_supported(const AttendArgs& a);
-cudaError_t launch_attend_tc(const AttendArgs& a, cudaStream_t s, int* launches);
+
 
 
 }  // namespace csa
