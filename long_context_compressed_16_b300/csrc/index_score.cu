@@ -31,6 +31,9 @@ constexpr int kMaxSmem = 232448;        // dynamic shared memory per block on sm
 #ifndef CSA_IDX_MAX_STAGES
 #define CSA_IDX_MAX_STAGES 6            // key-tile stages in flight per CTA (capped by shared memory)
 #endif
+#ifndef CSA_IDX_EVICT_FIRST
+#define CSA_IDX_EVICT_FIRST 0           // 1: key tiles loaded with an L2 evict-first hint
+#endif
 #ifndef CSA_IDX_WALK_CHUNK
 #define CSA_IDX_WALK_CHUNK 0            // > 0: CTAs take chunks of this many tiles round-robin
 #endif
@@ -310,8 +313,13 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
         } else {
           if (!tc::mbar_wait(&empty[s], ph ^ 1, abort_flag)) { fail(2); ok = false; break; }
           tc::mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-          for (int r = 0; r < C::NREG; ++r)
-            tc::tma_load_3d(kbuf + s * C::STAGE_BYTES + r * C::KEY_REGION, &kmap, r * 64, wk.t * KT, wk.gi.b, &full[s]);
+          for (int r = 0; r < C::NREG; ++r) {
+            if (CSA_IDX_EVICT_FIRST)
+              tc::tma_load_3d_hint(kbuf + s * C::STAGE_BYTES + r * C::KEY_REGION, &kmap, r * 64, wk.t * KT, wk.gi.b,
+                                   &full[s], tc::policy_evict_first());
+            else
+              tc::tma_load_3d(kbuf + s * C::STAGE_BYTES + r * C::KEY_REGION, &kmap, r * 64, wk.t * KT, wk.gi.b, &full[s]);
+          }
         }
         ++n;
       }

@@ -30,7 +30,7 @@ constexpr int kMergeCap = 16384;     // candidates one merge CTA holds (keys + i
 #define CSA_TOPK_TARGET_CTAS 128
 #endif
 #ifndef CSA_TOPK_SLICE_NT
-#define CSA_TOPK_SLICE_NT 1024
+#define CSA_TOPK_SLICE_NT 512        // two or more slice CTAs per SM (1024: one; prefill rows 2x slower)
 #endif
 constexpr int kTargetCtas = CSA_TOPK_TARGET_CTAS;   // split rows until the first stage has about this many CTAs
 constexpr int kMergeRounds = 16;     // 32-candidate rounds per merge warp (registers per thread)
