@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-prefill", action="store_true", help="skip the 65536-token prefill leg")
     ap.add_argument("--prefill-steps", type=int, default=3)
+    ap.add_argument("--lowp", action="store_true",
+                    help="FP8 workloads: the low-precision indexer (query quantised to e4m3, FP8 tensor cores)")
     ap.add_argument("--quick", action="store_true",
                     help="time exactly one block of K steps; no clock sampling, e2e or CPU leg (for profilers)")
     return ap.parse_args()
@@ -308,7 +310,9 @@ def run_ours(args):
     inp = S.make_inputs(w, dev)
     B, N, k = w.B, w.N, w.k
     fp8 = w.fp8
-    idesc = P.index_desc(B, 1, N, w.nI, w.dI, k, w.m, fp8=fp8)
+    if args.lowp and not fp8:
+        raise SystemExit("--lowp needs an FP8 workload (e4m3 indexer keys)")
+    idesc = P.index_desc(B, 1, N, w.nI, w.dI, k, w.m, fp8=fp8, lowp=args.lowp)
     adesc = P.attend_desc(B, 1, N, w.H, w.d, k=k, m=w.m, Wcap=w.window, window=w.window, fp8=fp8)
     ws_s = torch.zeros(max(256, C.csa_index_score_workspace(idesc)), dtype=torch.uint8, device=dev)
     ws_t = torch.zeros(max(256, C.csa_topk_workspace(idesc)), dtype=torch.uint8, device=dev)
@@ -496,6 +500,8 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "B": B, "N": N, "context_tokens": w.m * N, "k": k, "H": w.H, "d": w.d,
                    "indexer_heads": w.nI, "indexer_dim": w.dI, "window": w.window, "kv_format": "fp8_mixed" if fp8 else "bf16",
+                   "indexer": "fp8 tensor cores, e4m3 query (low precision)" if args.lowp else
+                              ("e4m3 keys widened to bf16" if fp8 else "bf16"),
                    "l2": f"inputs larger than L2: {step_bytes / 2**20:.0f} MiB read per step (126 MB L2), no flush", "timed_blocks": len(blocks),
                    "timing": "step: one CUDA graph of the three calls per step, CUDA events around each replay; "
                              "breakdown and roofline: each call's graph replayed K times back to back",

@@ -61,7 +61,14 @@ typedef enum {
    * value = code * scale. */
   CSA_FMT_FP8_MIXED = 1,
   /* Indexer keys: e4m3 codes [.., dI] plus one fp32 scale per row; value = code * scale. */
-  CSA_FMT_FP8_ROWSCALE = 2
+  CSA_FMT_FP8_ROWSCALE = 2,
+  /* Low-precision indexer (the pages' FP4/FP8 indexer, "DeepSeek-V4 技术报告深度解读" 5.4): keys
+   * as CSA_FMT_FP8_ROWSCALE, and the query is quantised too, per (query, head) row of head_dim
+   * 128: scale = amax/448 in fp32 (1 for an all-zero row), codes = e4m3 round-to-nearest-even,
+   * saturating, of q/scale computed in fp32.  The contraction runs on the FP8 tensor cores; the
+   * scores are those of the dequantised query against the dequantised keys (fp32 sums), so they
+   * differ from CSA_FMT_FP8_ROWSCALE's by the query quantisation only.  head_dim must be 128. */
+  CSA_FMT_FP8_ROWSCALE_LOWP = 3
 } csa_format;
 
 #define CSA_FP8_MIXED_ROW_BYTES 608
@@ -120,7 +127,7 @@ csa_status csa_compress(const csa_compress_desc* desc, const void* Ca, const voi
  *
  * qI: bf16 [B, Tq, n_heads, head_dim].  w: fp32 [B, Tq, n_heads].
  * kI: bf16 [B, N, head_dim] (key_fmt CSA_FMT_BF16) or e4m3 [B, N, head_dim] with
- *     kI_scale fp32 [B, N] (CSA_FMT_FP8_ROWSCALE).
+ *     kI_scale fp32 [B, N] (CSA_FMT_FP8_ROWSCALE, CSA_FMT_FP8_ROWSCALE_LOWP).
  * q_pos: int32 [B, Tq].  idx_out: int32 [B, Tq, k].
  * score_out: fp32 [B, Tq, N] or NULL; when given, visible scores are written there and
  *     invisible ones are -inf.
@@ -130,7 +137,7 @@ csa_status csa_compress(const csa_compress_desc* desc, const void* Ca, const voi
  * ------------------------------------------------------------------------------------------- */
 typedef struct {
   int B, Tq, N, n_heads, head_dim, k, m;
-  csa_format key_fmt;      /* CSA_FMT_BF16 or CSA_FMT_FP8_ROWSCALE */
+  csa_format key_fmt;      /* CSA_FMT_BF16, CSA_FMT_FP8_ROWSCALE or CSA_FMT_FP8_ROWSCALE_LOWP */
 } csa_index_desc;
 
 size_t csa_index_topk_workspace(const csa_index_desc* desc);

@@ -26,6 +26,7 @@ CSA_ERR_TIMEOUT = 6
 CSA_FMT_BF16 = 0
 CSA_FMT_FP8_MIXED = 1
 CSA_FMT_FP8_ROWSCALE = 2
+CSA_FMT_FP8_ROWSCALE_LOWP = 3
 CSA_FP8_MIXED_ROW_BYTES = 608
 CSA_NOALLOC_SCRATCH_BYTES = 8 << 20
 # flags

@@ -50,7 +50,14 @@ struct IndexPlan {
   long long chunk;   // groups per score + top-k pass
   size_t score_bytes;  // fp32 score rows of one chunk (rounded up to 256 bytes)
   size_t cand_bytes;   // two-stage top-k candidates of one chunk (0 for rows <= one slice)
+  size_t q8_bytes;     // low-precision indexer: e4m3 query rows of one chunk (0 otherwise)
+  size_t wp_bytes;     // low-precision indexer: scaled head weights of one chunk
 };
+
+inline bool is_lowp(const csa_index_desc* d) { return d->key_fmt == CSA_FMT_FP8_ROWSCALE_LOWP; }
+inline bool fp8_keys(const csa_index_desc* d) {
+  return d->key_fmt == CSA_FMT_FP8_ROWSCALE || d->key_fmt == CSA_FMT_FP8_ROWSCALE_LOWP;
+}
 
 bool index_desc_ok(const csa_index_desc* d) {
   if (!d) return false;
@@ -58,7 +65,9 @@ bool index_desc_ok(const csa_index_desc* d) {
   if (d->n_heads < 1 || d->n_heads > 64) return false;
   if (d->head_dim != 64 && d->head_dim != 128) return false;
   if (d->k < 1 || d->k > 2048) return false;
-  if (d->key_fmt != CSA_FMT_BF16 && d->key_fmt != CSA_FMT_FP8_ROWSCALE) return false;
+  if (d->key_fmt != CSA_FMT_BF16 && d->key_fmt != CSA_FMT_FP8_ROWSCALE && d->key_fmt != CSA_FMT_FP8_ROWSCALE_LOWP)
+    return false;
+  if (d->key_fmt == CSA_FMT_FP8_ROWSCALE_LOWP && d->head_dim != 128) return false;
   return true;
 }
 
@@ -87,6 +96,9 @@ IndexPlan plan_index(const csa_index_desc* d) {
     if (c > cand) cand = c;
   }
   p.cand_bytes = round256(cand);
+  const size_t lowp_rows = is_lowp(d) ? static_cast<size_t>(p.chunk) * p.G * d->n_heads : 0;
+  p.q8_bytes = round256(lowp_rows * 128);
+  p.wp_bytes = round256(lowp_rows * sizeof(float));
   return p;
 }
 
@@ -211,7 +223,7 @@ csa_status csa_compress(const csa_compress_desc* d, const void* Ca, const void* 
 size_t csa_index_topk_workspace(const csa_index_desc* d) {
   if (!index_desc_ok(d)) return 0;
   const IndexPlan p = plan_index(d);
-  return csa::kStatusBytes + p.score_bytes + p.cand_bytes;
+  return csa::kStatusBytes + p.score_bytes + p.cand_bytes + p.q8_bytes + p.wp_bytes;
 }
 
 csa_status csa_index_topk(const csa_index_desc* d, const void* qI, const float* w, const void* kI,
@@ -222,12 +234,15 @@ csa_status csa_index_topk(const csa_index_desc* d, const void* qI, const float* 
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const IndexPlan plan = plan_index(d);
   if (!ws) return CSA_ERR_WORKSPACE;
-  if (ws_bytes < csa::kStatusBytes + (score_out ? 0 : plan.score_bytes) + plan.cand_bytes) return CSA_ERR_WORKSPACE;
+  if (ws_bytes < csa::kStatusBytes + (score_out ? 0 : plan.score_bytes) + plan.cand_bytes + plan.q8_bytes +
+                     plan.wp_bytes)
+    return CSA_ERR_WORKSPACE;
   if (!aligned16(ws)) return CSA_ERR_INVALID_ARG;
   const long long Q = static_cast<long long>(d->B) * d->Tq;
   if (Q == 0) return CSA_OK;
   if (!qI || !w || !q_pos || !idx_out || (!kI && d->N > 0)) return CSA_ERR_INVALID_ARG;
-  const bool fp8 = d->key_fmt == CSA_FMT_FP8_ROWSCALE;
+  const bool fp8 = fp8_keys(d);
+  const bool lowp = is_lowp(d);
   if (fp8 && !kI_scale && d->N > 0) return CSA_ERR_INVALID_ARG;
   if (!aligned16(qI) || (kI && !aligned16(kI))) return CSA_ERR_INVALID_ARG;
 
@@ -243,7 +258,11 @@ csa_status csa_index_topk(const csa_index_desc* d, const void* qI, const float* 
 
   const long long gpb = (d->Tq + plan.G - 1) / plan.G;
   unsigned char* wsb = static_cast<unsigned char*>(ws);
-  void* cand = plan.cand_bytes ? wsb + csa::kStatusBytes + (score_out ? 0 : plan.score_bytes) : nullptr;
+  unsigned char* after_scores = wsb + csa::kStatusBytes + (score_out ? 0 : plan.score_bytes);
+  void* cand = plan.cand_bytes ? after_scores : nullptr;
+  unsigned char* q8 = after_scores + plan.cand_bytes;                    // low-precision query rows
+  float* wp = reinterpret_cast<float*>(q8 + plan.q8_bytes);
+  ia.lowp = lowp ? 1 : 0;
   int launches = 0;
   cudaError_t e = cudaSuccess;
   if (d->N == 0) {
@@ -265,6 +284,15 @@ csa_status csa_index_topk(const csa_index_desc* d, const void* qI, const float* 
     ia.q_begin = static_cast<int>(g0);
     ia.q_count = static_cast<int>(g1 - g0);
     ia.score_row_offset = score_out ? 0 : static_cast<int>(q_first);
+    if (lowp) {
+      // this chunk's query rows, quantised into the workspace; the score kernel addresses them by
+      // global query index, so its base pointers step back by the chunk's first row
+      const long long row0 = q_first * d->n_heads;
+      e = csa::launch_quant_q(qI, w, q8, wp, row0, (q_last - q_first) * d->n_heads, stream, &launches);
+      if (e != cudaSuccess) break;
+      ia.qI = q8 - row0 * 128;
+      ia.w = wp - row0;
+    }
     e = csa::launch_index_score_groups(ia, grouping, score_out ? 1 : 0, stream, &launches);
     if (e != cudaSuccess) break;
     ta.scores = scores;
@@ -278,9 +306,16 @@ csa_status csa_index_topk(const csa_index_desc* d, const void* qI, const float* 
   return from_cuda(e);
 }
 
+// low-precision indexer: e4m3 query rows and scaled weights of all B*Tq queries
+size_t lowp_all_bytes(const csa_index_desc* d) {
+  if (!is_lowp(d)) return 0;
+  const size_t rows = static_cast<size_t>(d->B) * d->Tq * d->n_heads;
+  return round256(rows * 128) + round256(rows * sizeof(float));
+}
+
 size_t csa_index_score_workspace(const csa_index_desc* d) {
   if (!index_desc_ok(d)) return 0;
-  return csa::kStatusBytes;
+  return csa::kStatusBytes + lowp_all_bytes(d);
 }
 
 csa_status csa_index_score(const csa_index_desc* d, const void* qI, const float* w, const void* kI,
@@ -290,12 +325,12 @@ csa_status csa_index_score(const csa_index_desc* d, const void* qI, const float*
   if (d->N > 262144) return CSA_ERR_UNSUPPORTED;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (!ws) return CSA_ERR_WORKSPACE;
-  if (ws_bytes < csa::kStatusBytes) return CSA_ERR_WORKSPACE;
+  if (ws_bytes < csa::kStatusBytes + lowp_all_bytes(d)) return CSA_ERR_WORKSPACE;
   if (!aligned16(ws)) return CSA_ERR_INVALID_ARG;
   const long long Q = static_cast<long long>(d->B) * d->Tq;
   if (Q == 0 || d->N == 0) return CSA_OK;
   if (!qI || !w || !q_pos || !kI || !score_out) return CSA_ERR_INVALID_ARG;
-  const bool fp8 = d->key_fmt == CSA_FMT_FP8_ROWSCALE;
+  const bool fp8 = fp8_keys(d);
   if (fp8 && !kI_scale) return CSA_ERR_INVALID_ARG;
   if (!aligned16(qI) || !aligned16(kI)) return CSA_ERR_INVALID_ARG;
   const IndexPlan plan = plan_index(d);
@@ -310,8 +345,18 @@ csa_status csa_index_score(const csa_index_desc* d, const void* qI, const float*
   ia.q_count = static_cast<int>(plan.groups);
   ia.score_row_offset = 0;
   int launches = 0;
-  const cudaError_t e =
-      csa::launch_index_score_groups(ia, csa::index_grouping(d->n_heads, d->Tq), 0, stream, &launches);
+  cudaError_t e = cudaSuccess;
+  if (is_lowp(d)) {
+    const long long rows = Q * d->n_heads;
+    unsigned char* q8 = static_cast<unsigned char*>(ws) + csa::kStatusBytes;
+    float* wp = reinterpret_cast<float*>(q8 + round256(static_cast<size_t>(rows) * 128));
+    e = csa::launch_quant_q(qI, w, q8, wp, 0, rows, stream, &launches);
+    ia.qI = q8;
+    ia.w = wp;
+    ia.lowp = 1;
+  }
+  if (e == cudaSuccess)
+    e = csa::launch_index_score_groups(ia, csa::index_grouping(d->n_heads, d->Tq), 0, stream, &launches);
   count(launches);
   if (e == cudaErrorInvalidValue) return CSA_ERR_UNSUPPORTED;
   return from_cuda(e);

@@ -176,6 +176,7 @@ struct IndexArgs {
   float* scores;            // score rows of N floats
   int32_t* status;          // workspace status word (bounded-wait timeouts)
   int B, Tq, N, nI, dI, m, fp8;
+  int lowp;                 // qI is the e4m3 query (q8) and w the scaled weights: FP8 tensor cores
   int q_begin, q_count;     // range of query GROUPS (G consecutive queries of one sequence)
   int score_row_offset;     // flattened query q (= b*Tq + i) owns score row q - score_row_offset
 };
@@ -199,6 +200,10 @@ inline IndexGrouping index_grouping(int nI, int Tq) {
 
 // Scores for the query groups [q_begin, q_begin + q_count).  fill_invisible: also write -inf
 // for every s in [N_vis, N) so that the rows are complete.
+// Low-precision indexer query: rows [row0, row0 + rows) of qI ([.., 128] bf16) and w -> q8
+// ([rows, 128] e4m3) and wp ([rows] fp32), both counted from row0.
+cudaError_t launch_quant_q(const void* qI, const float* w, void* q8, float* wp, long long row0, long long rows,
+                           cudaStream_t s, int* launches);
 cudaError_t launch_index_score_groups(const IndexArgs& a, const IndexGrouping& gr, int fill_invisible,
                                       cudaStream_t s, int* launches);
 

@@ -38,23 +38,30 @@ constexpr int kMaxSmem = 232448;        // dynamic shared memory per block on sm
 #define CSA_IDX_WALK_CHUNK 0            // > 0: CTAs take chunks of this many tiles round-robin
 #endif
 
-template <int DI, int NCOL, bool FP8>
+// FP8: e4m3 keys with per-row scales.  LP (low-precision indexer): the query is e4m3 too and the
+// contraction runs on the FP8 tensor cores (kind::f8f6f4, K = 32 per instruction); otherwise FP8
+// keys are widened to bf16 in shared memory by converter warps.
+template <int DI, int NCOL, bool FP8, bool LP = false>
 struct Cfg {
-  static constexpr int NREG = DI / 64;                    // 128-byte swizzle regions per row
+  static constexpr bool WIDEN = FP8 && !LP;               // converter warps widen e4m3 to bf16
+  static constexpr int ESIZE = LP ? 1 : 2;                // operand bytes per element
+  static constexpr int REG_ELEMS = 128 / ESIZE;           // elements per 128-byte swizzle row
+  static constexpr int NREG = DI * ESIZE / 128;           // 128-byte swizzle regions per row
+  static constexpr int KSTEPS = LP ? DI / 32 : DI / 16;   // MMAs per key tile
   static constexpr int KEY_REGION = KT * 128;
   static constexpr int STAGE_BYTES = NREG * KEY_REGION;   // bf16 key operand per stage
-  static constexpr int STAGED_BYTES = FP8 ? KT * DI : 0;  // e4m3 staging per stage
+  static constexpr int STAGED_BYTES = WIDEN ? KT * DI : 0;  // e4m3 staging per stage
   static constexpr int Q_REGION = NCOL * 128;
   static constexpr int Q_BYTES = NREG * Q_REGION;
   static constexpr int QB = NCOL >= 256 ? 1 : 2;          // query-block buffers
   // FP8 keys with N <= 128: the widening to bf16 is the busiest role, so 8 converter warps and
   // one set of 4 epilogue warps; otherwise 8 epilogue warps (two sets of four) and 4 converters
-  static constexpr bool CONV_HEAVY = FP8 && NCOL <= 128;
+  static constexpr bool CONV_HEAVY = WIDEN && NCOL <= 128;
   static constexpr int EW = CONV_HEAVY ? 4 : 8;           // epilogue warps
   // NCOL <= 128: the two sets take alternate tiles; wider: they split the group's queries
   static constexpr bool TSPLIT = EW == 8 && NCOL <= 128;
   static constexpr int ACC_ARRIVALS = 32 * (TSPLIT ? EW / 2 : EW);   // epilogue threads per tile
-  static constexpr int CW = FP8 ? (CONV_HEAVY ? 8 : 4) : 0;   // converter warps
+  static constexpr int CW = WIDEN ? (CONV_HEAVY ? 8 : 4) : 0;   // converter warps
   static constexpr int THREADS = 32 * (4 + EW + CW);
   static constexpr int W_FLOATS = EW * NCOL;              // per-epilogue-warp copy of the head weights
   static constexpr int GMAX = 16;                         // queries per group (NCOL / 16 heads at most)
@@ -202,11 +209,11 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf162(uint16_t v) {
   return pack_bf16x2(f.x, f.y);
 }
 
-template <int DI, int NCOL, bool FP8>
-__global__ void __launch_bounds__(Cfg<DI, NCOL, FP8>::THREADS, 1)
+template <int DI, int NCOL, bool FP8, bool LP>
+__global__ void __launch_bounds__(Cfg<DI, NCOL, FP8, LP>::THREADS, 1)
 k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
               const TcParams p) {
-  using C = Cfg<DI, NCOL, FP8>;
+  using C = Cfg<DI, NCOL, FP8, LP>;
   constexpr int S = C::STAGES;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // TMA destinations and the 128-byte swizzle atoms need 1024-byte alignment of the shared-window
@@ -248,7 +255,7 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      tc::mbar_init(&full[s], FP8 ? C::CW * 32 : 1);
+      tc::mbar_init(&full[s], C::WIDEN ? C::CW * 32 : 1);
       tc::mbar_init(&empty[s], 1);
       tc::mbar_init(&sfull[s], 1);
       tc::mbar_init(&sempty[s], C::CW * 32 > 0 ? C::CW * 32 : 1);
@@ -301,12 +308,12 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
           tc::mbar_arrive_expect_tx(&qfull[qb], C::Q_BYTES);
           const int z = wk.gi.b * a.Tq + wk.gi.i0;
           for (int r = 0; r < C::NREG; ++r)
-            tc::tma_load_3d(qbuf + qb * C::Q_BYTES + r * C::Q_REGION, &qmap, r * 64, 0, z, &qfull[qb]);
+            tc::tma_load_3d(qbuf + qb * C::Q_BYTES + r * C::Q_REGION, &qmap, r * C::REG_ELEMS, 0, z, &qfull[qb]);
           ++nq;
         }
         const int s = static_cast<int>(n % S);
         const uint32_t ph = static_cast<uint32_t>((n / S) & 1);
-        if (FP8) {
+        if (C::WIDEN) {
           if (!tc::mbar_wait(&sempty[s], ph ^ 1, abort_flag)) { fail(2); ok = false; break; }
           tc::mbar_arrive_expect_tx(&sfull[s], C::STAGED_BYTES);
           tc::tma_load_3d(sbuf + s * C::STAGED_BYTES, &kmap, 0, wk.t * KT, wk.gi.b, &sfull[s]);
@@ -315,10 +322,11 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
           tc::mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
           for (int r = 0; r < C::NREG; ++r) {
             if (CSA_IDX_EVICT_FIRST)
-              tc::tma_load_3d_hint(kbuf + s * C::STAGE_BYTES + r * C::KEY_REGION, &kmap, r * 64, wk.t * KT, wk.gi.b,
-                                   &full[s], tc::policy_evict_first());
+              tc::tma_load_3d_hint(kbuf + s * C::STAGE_BYTES + r * C::KEY_REGION, &kmap, r * C::REG_ELEMS, wk.t * KT,
+                                   wk.gi.b, &full[s], tc::policy_evict_first());
             else
-              tc::tma_load_3d(kbuf + s * C::STAGE_BYTES + r * C::KEY_REGION, &kmap, r * 64, wk.t * KT, wk.gi.b, &full[s]);
+              tc::tma_load_3d(kbuf + s * C::STAGE_BYTES + r * C::KEY_REGION, &kmap, r * C::REG_ELEMS, wk.t * KT,
+                              wk.gi.b, &full[s]);
           }
         }
         ++n;
@@ -327,7 +335,7 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
       // each barrier follows from the issue counts; no per-stage arrays in local memory)
       for (int s = 0; s < S; ++s) {
         const long long cnt = issued_into(n, s, S);
-        if (cnt > 0 && !tc::mbar_wait(FP8 ? &sfull[s] : &full[s], static_cast<uint32_t>((cnt - 1) & 1), nullptr))
+        if (cnt > 0 && !tc::mbar_wait(C::WIDEN ? &sfull[s] : &full[s], static_cast<uint32_t>((cnt - 1) & 1), nullptr))
           report_error(a.status, CSA_ERR_TIMEOUT, 9);
       }
       for (int i = 0; i < C::QB; ++i) {
@@ -340,7 +348,7 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (lane 0 only)
     if (lane == 0) {
-      constexpr uint32_t idesc = tc::umma_idesc_bf16(KT, NCOL);
+      constexpr uint32_t idesc = LP ? tc::umma_idesc_e4m3(KT, NCOL) : tc::umma_idesc_bf16(KT, NCOL);
       Walker wk;
       wk.init(p, ngroups);
       long long n = 0;
@@ -362,11 +370,12 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
         const uint32_t kaddr = tc::sptr(kbuf + s * C::STAGE_BYTES);
         const uint32_t qaddr = tc::sptr(qbuf + (gc % C::QB) * C::Q_BYTES);
 #pragma unroll
-        for (int k = 0; k < DI / 16; ++k) {
+        for (int k = 0; k < C::KSTEPS; ++k) {               // 32 bytes of K per instruction
           const int r = k >> 2, off = (k & 3) * 32;
           const uint64_t ad = tc::umma_desc_sw128(kaddr + r * C::KEY_REGION + off);
           const uint64_t bd = tc::umma_desc_sw128(qaddr + r * C::Q_REGION + off);
-          tc::umma_bf16(tmem + acc * NCOL, ad, bd, idesc, k > 0 ? 1u : 0u);
+          if (LP) tc::umma_e4m3(tmem + acc * NCOL, ad, bd, idesc, k > 0 ? 1u : 0u);
+          else tc::umma_bf16(tmem + acc * NCOL, ad, bd, idesc, k > 0 ? 1u : 0u);
         }
         tc::umma_commit(&empty[s]);
         tc::umma_commit(&accfull[acc]);
@@ -480,7 +489,7 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
       tc::mbar_arrive(&accempty[acc]);
       ++n;
     }
-  } else if (FP8 && warp >= 4 + C::EW) {
+  } else if (C::WIDEN && warp >= 4 + C::EW) {
     // ------------------------------------------------------------ e4m3 -> bf16 converters
     const int ctid = threadIdx.x - 32 * (4 + C::EW);
     Walker wk;
@@ -535,20 +544,27 @@ int sm_count() {
   return n;
 }
 
-template <int DI, int NCOL, bool FP8>
+template <int DI, int NCOL, bool FP8, bool LP>
 cudaError_t launch_t(const IndexArgs& a, const IndexGrouping& gr, int fill_invisible, cudaStream_t s,
                      int* launches) {
-  using C = Cfg<DI, NCOL, FP8>;
+  using C = Cfg<DI, NCOL, FP8, LP>;
   CUtensorMap kmap, qmap;
   bool ok;
-  if (FP8)
+  if (LP)
+    ok = make_map_3d(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.kI, DI, a.N, a.B, DI, KT, 1,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+  else if (FP8)
     ok = make_map_3d(&kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.kI, DI, a.N, a.B, DI, KT, 1,
                      CU_TENSOR_MAP_SWIZZLE_NONE);
   else
     ok = make_map_3d(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.kI, DI, a.N, a.B, 64, KT, 1,
                      CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_map_3d(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.qI, DI, a.nI,
-                         static_cast<uint64_t>(a.B) * a.Tq, 64, gr.NHP, gr.G, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (LP)
+    ok = ok && make_map_3d(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.qI, DI, a.nI,
+                           static_cast<uint64_t>(a.B) * a.Tq, C::REG_ELEMS, gr.NHP, gr.G, CU_TENSOR_MAP_SWIZZLE_128B);
+  else
+    ok = ok && make_map_3d(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.qI, DI, a.nI,
+                           static_cast<uint64_t>(a.B) * a.Tq, 64, gr.NHP, gr.G, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
   TcParams p;
   p.G = gr.G;
@@ -563,25 +579,49 @@ cudaError_t launch_t(const IndexArgs& a, const IndexGrouping& gr, int fill_invis
   long long grid = sms;
   if (p.mode != 1 && p.F < grid) grid = p.F;
   if (grid < 1) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(k_index_score<DI, NCOL, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(k_index_score<DI, NCOL, FP8, LP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM);
   if (e != cudaSuccess) return e;
-  e = launch_k(k_index_score<DI, NCOL, FP8>, dim3(static_cast<unsigned>(grid)), dim3(C::THREADS),
+  e = launch_k(k_index_score<DI, NCOL, FP8, LP>, dim3(static_cast<unsigned>(grid)), dim3(C::THREADS),
                static_cast<size_t>(C::SMEM), s, a, kmap, qmap, p);
   ++*launches;
   return e;
 }
 
-template <int DI, bool FP8>
+template <int DI, bool FP8, bool LP>
 cudaError_t launch_di(const IndexArgs& a, const IndexGrouping& gr, int fill, cudaStream_t s, int* launches) {
   switch (gr.NCOL) {
-    case 16: return launch_t<DI, 16, FP8>(a, gr, fill, s, launches);
-    case 32: return launch_t<DI, 32, FP8>(a, gr, fill, s, launches);
-    case 64: return launch_t<DI, 64, FP8>(a, gr, fill, s, launches);
-    case 128: return launch_t<DI, 128, FP8>(a, gr, fill, s, launches);
-    case 256: return launch_t<DI, 256, FP8>(a, gr, fill, s, launches);
+    case 16: return launch_t<DI, 16, FP8, LP>(a, gr, fill, s, launches);
+    case 32: return launch_t<DI, 32, FP8, LP>(a, gr, fill, s, launches);
+    case 64: return launch_t<DI, 64, FP8, LP>(a, gr, fill, s, launches);
+    case 128: return launch_t<DI, 128, FP8, LP>(a, gr, fill, s, launches);
+    case 256: return launch_t<DI, 256, FP8, LP>(a, gr, fill, s, launches);
   }
   return cudaErrorInvalidValue;
+}
+
+// Low-precision indexer query: one warp per (query, head) row of 128 dims.  scale = amax / 448
+// (1 for an all-zero row), codes = e4m3 RNE-saturated (q / scale) with the quotient in fp32, and
+// the head weight absorbs the scale (ReLU commutes with a positive factor): wp = w * scale.
+__global__ void __launch_bounds__(128) k_quant_q(const __nv_bfloat16* __restrict__ qI, const float* __restrict__ w,
+                                                 uint8_t* __restrict__ q8, float* __restrict__ wp, long long row0,
+                                                 long long rows) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const long long r = static_cast<long long>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const uint2 u = *reinterpret_cast<const uint2*>(qI + (row0 + r) * 128 + lane * 4);
+  const float v[4] = {bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y)};
+  float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float scale = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(__fdiv_rn(v[1], scale)), "f"(__fdiv_rn(v[0], scale)));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(__fdiv_rn(v[3], scale)), "f"(__fdiv_rn(v[2], scale)));
+  *reinterpret_cast<uint32_t*>(q8 + r * 128 + lane * 4) = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  if (lane == 0) wp[r] = w[row0 + r] * scale;
 }
 
 }  // namespace
@@ -590,11 +630,26 @@ cudaError_t launch_di(const IndexArgs& a, const IndexGrouping& gr, int fill, cud
 cudaError_t launch_index_score_groups(const IndexArgs& a, const IndexGrouping& gr, int fill_invisible,
                                       cudaStream_t s, int* launches) {
   if (a.q_count <= 0 || a.N <= 0) return cudaSuccess;
-  if (a.dI == 128) return a.fp8 ? launch_di<128, true>(a, gr, fill_invisible, s, launches)
-                                : launch_di<128, false>(a, gr, fill_invisible, s, launches);
-  if (a.dI == 64) return a.fp8 ? launch_di<64, true>(a, gr, fill_invisible, s, launches)
-                               : launch_di<64, false>(a, gr, fill_invisible, s, launches);
+  if (a.lowp) return a.dI == 128 ? launch_di<128, true, true>(a, gr, fill_invisible, s, launches)
+                                  : cudaErrorInvalidValue;
+  if (a.dI == 128) return a.fp8 ? launch_di<128, true, false>(a, gr, fill_invisible, s, launches)
+                                : launch_di<128, false, false>(a, gr, fill_invisible, s, launches);
+  if (a.dI == 64) return a.fp8 ? launch_di<64, true, false>(a, gr, fill_invisible, s, launches)
+                               : launch_di<64, false, false>(a, gr, fill_invisible, s, launches);
   return cudaErrorInvalidValue;
+}
+
+// rows [row0, row0 + rows) of qI [.., 128] bf16 / w -> q8 [rows, 128] e4m3 / wp [rows] (rows
+// counted from row0)
+cudaError_t launch_quant_q(const void* qI, const float* w, void* q8, float* wp, long long row0, long long rows,
+                           cudaStream_t s, int* launches) {
+  if (rows <= 0) return cudaSuccess;
+  const long long blocks = (rows + 3) / 4;
+  if (blocks > 2147483647LL) return cudaErrorInvalidValue;
+  const cudaError_t e = launch_k(k_quant_q, dim3(static_cast<unsigned>(blocks)), dim3(128), 0, s,
+                                 static_cast<const __nv_bfloat16*>(qI), w, static_cast<uint8_t*>(q8), wp, row0, rows);
+  ++*launches;
+  return e;
 }
 
 }  // namespace csa

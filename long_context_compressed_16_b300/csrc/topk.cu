@@ -29,9 +29,7 @@ constexpr int kMergeCap = 16384;     // candidates one merge CTA holds (keys + i
 #ifndef CSA_TOPK_TARGET_CTAS
 #define CSA_TOPK_TARGET_CTAS 128
 #endif
-#ifndef CSA_TOPK_SLICE_NT
-#define CSA_TOPK_SLICE_NT 512        // two or more slice CTAs per SM (1024: one; prefill rows 2x slower)
-#endif
+
 constexpr int kTargetCtas = CSA_TOPK_TARGET_CTAS;   // split rows until the first stage has about this many CTAs
 constexpr int kMergeRounds = 16;     // 32-candidate rounds per merge warp (registers per thread)
 constexpr int kDigit = 8;
@@ -446,7 +444,11 @@ cudaError_t launch_topk(const TopkArgs& a, void* cand_ws, cudaStream_t s, int* l
   if (S > 1 && (cand_ws == nullptr || static_cast<long long>(S) * a.k > kMergeCap)) return cudaErrorInvalidValue;
   const int cap1 = S == 1 ? ((a.N + 3) & ~3) : len;
   unsigned long long* cand = static_cast<unsigned long long*>(cand_ws);
-  cudaError_t e = launch_slice<CSA_TOPK_SLICE_NT>(a, S, len, cap1, cand, s);
+  // threads per selecting CTA: whole rows (many queries, one slice each) on 256 threads, several
+  // CTAs per SM; the slices of a small batch's long rows on 1024 (measured: 1024 threads were 2.5x
+  // slower than 256 on prefill rows; 256 and 512 threads 20% and 8% slower than 1024 on the 8192-key
+  // decode slices).  The result does not depend on the choice.
+  cudaError_t e = S == 1 ? launch_slice<256>(a, S, len, cap1, cand, s) : launch_slice<1024>(a, S, len, cap1, cand, s);
   ++*launches;
   if (e != cudaSuccess || S == 1) return e;
   const int total = S * a.k;

@@ -192,6 +192,51 @@ def index_scores(qI, w, kI, q_pos, m):
     return out
 
 
+def e4m3_encode_rne(x32) -> np.ndarray:
+    """fp32 values -> OCP FP8 E4M3 codes (uint8): round to nearest, ties to even, saturating to
+    +-448 (the largest finite code); finite input never becomes NaN.  Written from the format
+    definition: normals (1 + f/8) 2^(e-7) for e = 1..15 (S.1111.111 excluded), subnormals
+    (f/8) 2^-6."""
+    x = np.asarray(x32, dtype=np.float32).astype(np.float64)
+    sign = np.signbit(x)
+    v = np.abs(x)
+    out = np.zeros(v.shape, dtype=np.int64)
+    sub = v < 2.0 ** -6
+    # subnormal range: units of 2^-9; rounding up to 8 units gives the smallest normal (code 8)
+    out = np.where(sub, np.rint(v / 2.0 ** -9).astype(np.int64), out)
+    vn = np.where(sub, 1.0, v)
+    mant, ex = np.frexp(vn)                        # vn = mant * 2^ex, mant in [0.5, 1)
+    e = ex - 1                                     # vn = (2 mant) 2^e, 2 mant in [1, 2)
+    f = np.rint((2.0 * mant - 1.0) * 8.0).astype(np.int64)
+    e = np.where(f == 8, e + 1, e)
+    f = np.where(f == 8, 0, f)
+    code = (e + 7) * 8 + f
+    code = np.where(code > 0x7E, 0x7E, code)       # above 448 (or onto the NaN pattern): 448
+    out = np.where(sub, out, code)
+    return (out | np.where(sign, 0x80, 0)).astype(np.uint8)
+
+
+def quantize_query_e4m3(qI):
+    """Low-precision indexer query (the pages' FP4/FP8 indexer, 5.4 of the technical-report
+    digest): each (query, head) row of q^I gets scale = amax / 448 in fp32 (1 when the row is all
+    zero) and codes = e4m3_RNE(q / scale) with the quotient rounded to fp32, the precision the
+    GPU divides in.  Returns (codes uint8 [..., dI], scale fp32 [...])."""
+    q = np.asarray(qI, dtype=np.float64)
+    amax = np.max(np.abs(q), axis=-1).astype(np.float32)
+    scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    y = (q.astype(np.float32) / scale[..., None]).astype(np.float32)
+    return e4m3_encode_rne(y), scale
+
+
+def index_scores_lowp(qI, w, kI, q_pos, m):
+    """Indexer scores with the query quantised by quantize_query_e4m3 (the keys are already the
+    dequantised FP8 keys): I_{t,s} = sum_h w_{t,h} ReLU(q8_{t,h} . K_s) in fp64 over the exact
+    dequantised operands."""
+    codes, scale = quantize_query_e4m3(qI)
+    q8 = e4m3_to_f64(codes) * scale.astype(np.float64)[..., None]
+    return index_scores(q8, w, kI, q_pos, m)
+
+
 def topk_select(scores, q_pos, m, k):
     """TopK_k over the visible scores of each query.  R14: ties go to the smaller s; with fewer
     than k visible entries all are taken and the row is padded with -1.

@@ -467,3 +467,46 @@ def test_whole_path_is_causal():
     out = run(st2, ist2, win2)
     assert np.array_equal(out[0, :t + 1], ref[0, :t + 1])
     assert not np.allclose(out[0, t + 1:], ref[0, t + 1:])
+
+
+# ------------------------------------------------------------------ low-precision indexer query
+
+def test_e4m3_encoder_round_trips_every_code_and_rounds_half_to_even():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)   # no NaNs
+    vals = O.e4m3_to_f64(codes)
+    assert np.array_equal(O.e4m3_encode_rne(vals.astype(np.float32)), codes)
+    # midpoints between neighbouring positive codes round to the even mantissa
+    pos = np.arange(0, 0x7E)
+    lo, hi = O.e4m3_to_f64(pos), O.e4m3_to_f64(pos + 1)
+    mid = ((lo + hi) / 2).astype(np.float32)
+    got = O.e4m3_encode_rne(mid).astype(np.int64)
+    want = np.where(pos % 2 == 0, pos, pos + 1)
+    exact = mid.astype(np.float64) == (lo + hi) / 2          # midpoints exactly representable in fp32
+    assert np.array_equal(got[exact], want[exact])
+    # saturation and underflow
+    assert O.e4m3_encode_rne(np.float32([448.0, 460.0, 1e6, -1e6])).tolist() == [0x7E, 0x7E, 0x7E, 0xFE]
+    assert O.e4m3_encode_rne(np.float32([2.0 ** -10, -2.0 ** -10, 0.0])).tolist() == [0, 0x80, 0]
+
+
+def test_e4m3_encoder_matches_torch_in_range():
+    x = (rng.standard_normal(50000) * 10.0 ** rng.integers(-3, 3, 50000)).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.e4m3_encode_rne(x), ref)
+
+
+def test_query_quantisation_scale_and_amax_code():
+    q = rnd(3, 5, 128)
+    codes, scale = O.quantize_query_e4m3(q)
+    amax = np.max(np.abs(q), axis=-1)
+    assert np.allclose(scale, amax / 448.0, rtol=1e-6)
+    # the largest element of every row maps to the largest code
+    i = np.argmax(np.abs(q), axis=-1)
+    top = np.take_along_axis(codes, i[..., None], axis=-1)[..., 0] & 0x7F
+    assert np.all(top == 0x7E)
+    # dequantised values are within half an e4m3 step (relative 2^-4) of the inputs
+    deq = O.e4m3_to_f64(codes) * scale[..., None]
+    big = np.abs(q) > amax[..., None] * 2.0 ** -6
+    assert np.all(np.abs(deq - q)[big] <= np.abs(q)[big] * 2.0 ** -4 + 1e-12)
+    zc, zs = O.quantize_query_e4m3(np.zeros((2, 128)))
+    assert np.all(zc == 0) and np.all(zs == 1.0)
