@@ -6,7 +6,7 @@
 // accumulator lives in tensor memory, one TMEM lane per key, so the ReLU / w-weighted head sum is
 // a per-thread loop over TMEM columns with no cross-lane reduction.
 //
-// One persistent CTA per SM, warp-specialised:
+// Persistent CTAs, one or two per SM, warp-specialised:
 //   warp 0        TMA producer: key tiles (3-D tensor map, 128-byte swizzle, zero fill past N)
 //                 into a ring of shared-memory stages, and each group's query block
 //   warp 1        owns the TMEM allocation; one lane issues tcgen05.mma (M=128, N=G*heads,
@@ -28,6 +28,9 @@ namespace {
 
 constexpr int KT = 128;                 // keys per tile = MMA M
 constexpr int kMaxSmem = 232448;        // dynamic shared memory per block on sm_100-class parts
+#ifndef CSA_IDX_CTAS
+#define CSA_IDX_CTAS 2                  // two CTAs per SM where they fit (N <= 64, no widening warps)
+#endif
 #ifndef CSA_IDX_MAX_STAGES
 #define CSA_IDX_MAX_STAGES 6            // key-tile stages in flight per CTA (capped by shared memory)
 #endif
@@ -53,11 +56,16 @@ struct Cfg {
   static constexpr int STAGED_BYTES = WIDEN ? KT * DI : 0;  // e4m3 staging per stage
   static constexpr int Q_REGION = NCOL * 128;
   static constexpr int Q_BYTES = NREG * Q_REGION;
-  static constexpr int QB = NCOL >= 256 ? 1 : 2;          // query-block buffers
+  // CTAs per SM: two independent pipelines per SM keep twice the key tiles in flight (measured on
+  // the 128K decode: 56 -> 47 us, 0.75 -> 0.90 of the copy bandwidth); only when both fit in tensor
+  // memory (4 x NCOL columns each) and in the registers (no widening warps)
+  static constexpr int CTAS = (CSA_IDX_CTAS == 2 && NCOL <= 64 && !(FP8 && !LP)) ? 2 : 1;
+  static constexpr int SMEM_CAP = CTAS == 2 ? 114688 : kMaxSmem;
+  static constexpr int QB = (NCOL >= 256 || CTAS == 2) ? 1 : 2;   // query-block buffers
   // FP8 keys with N <= 128: the widening to bf16 is the busiest role, so 8 converter warps and
   // one set of 4 epilogue warps; otherwise 8 epilogue warps (two sets of four) and 4 converters
   static constexpr bool CONV_HEAVY = WIDEN && NCOL <= 128;
-  static constexpr int EW = CONV_HEAVY ? 4 : 8;           // epilogue warps
+  static constexpr int EW = (CONV_HEAVY || CTAS == 2) ? 4 : 8;   // epilogue warps
   // NCOL <= 128: the two sets take alternate tiles; wider: they split the group's queries
   static constexpr bool TSPLIT = EW == 8 && NCOL <= 128;
   static constexpr int ACC_ARRIVALS = 32 * (TSPLIT ? EW / 2 : EW);   // epilogue threads per tile
@@ -68,14 +76,15 @@ struct Cfg {
   static constexpr int NV_INTS = EW * GMAX;               // per-epilogue-warp visible counts of the group
   static constexpr int MISC = 1024;                       // barriers, TMEM address, flags
   static constexpr int FIXED = 1024 /*alignment slack*/ + QB * Q_BYTES + W_FLOATS * 4 + NV_INTS * 4 + MISC;
-  static constexpr int S_RAW = (kMaxSmem - FIXED) / (STAGE_BYTES + STAGED_BYTES);
+  static constexpr int S_RAW = (SMEM_CAP - FIXED) / (STAGE_BYTES + STAGED_BYTES);
   static constexpr int STAGES = S_RAW > CSA_IDX_MAX_STAGES ? CSA_IDX_MAX_STAGES : S_RAW;
   static constexpr int SMEM = FIXED + STAGES * (STAGE_BYTES + STAGED_BYTES);
   static constexpr int ACC = NCOL <= 128 ? 4 : 2;            // accumulator buffers in tensor memory
   static constexpr int TMEM_COLS = (ACC * NCOL) <= 32 ? 32 : (ACC * NCOL) <= 64 ? 64 : (ACC * NCOL) <= 128 ? 128
                                    : (ACC * NCOL) <= 256 ? 256 : 512;
   static_assert(STAGES >= 2, "shared memory too small for two stages");
-  static_assert(SMEM <= kMaxSmem, "shared memory budget");
+  static_assert(SMEM <= SMEM_CAP, "shared memory budget");
+  static_assert(CTAS == 1 || TMEM_COLS <= 256, "two CTAs per SM must share the 512 TMEM columns");
   static_assert(NCOL % 16 == 0 && NCOL >= 16 && NCOL <= 256, "UMMA N for M = 128");
 };
 
@@ -210,7 +219,7 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf162(uint16_t v) {
 }
 
 template <int DI, int NCOL, bool FP8, bool LP>
-__global__ void __launch_bounds__(Cfg<DI, NCOL, FP8, LP>::THREADS, 1)
+__global__ void __launch_bounds__(Cfg<DI, NCOL, FP8, LP>::THREADS, Cfg<DI, NCOL, FP8, LP>::CTAS)
 k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
               const TcParams p) {
   using C = Cfg<DI, NCOL, FP8, LP>;
@@ -576,7 +585,7 @@ cudaError_t launch_t(const IndexArgs& a, const IndexGrouping& gr, int fill_invis
   p.mode = groups >= 4LL * sms ? 1 : (CSA_IDX_WALK_CHUNK > 0 ? 2 : 0);
   p.chunk = CSA_IDX_WALK_CHUNK > 0 ? CSA_IDX_WALK_CHUNK : 1;
   p.F = groups * p.tiles_max;
-  long long grid = sms;
+  long long grid = static_cast<long long>(sms) * C::CTAS;
   if (p.mode != 1 && p.F < grid) grid = p.F;
   if (grid < 1) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(k_index_score<DI, NCOL, FP8, LP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
