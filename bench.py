@@ -220,6 +220,87 @@ def prefill_flops(w):
     return idx_flops, att_flops
 
 
+def run_other(args, dev, stream):
+    """The remaining workloads of the method, reported beside the headline (no target): HCA decode at
+    1M context (batch 8, dense attention over 8192 entries), the HCA prefill chunk (T = 32768: the
+    m' = 128 compressor and dense attention over <= 256 entries), and the tiny CSA prefill (T = 2048,
+    all four calls).  Each call is replayed from a CUDA graph, CUDA events around K replays."""
+    import torch
+    from long_context_compressed_16_b300 import capi as C
+    from long_context_compressed_16_b300 import pipeline as P
+    from long_context_compressed_16_b300 import synth as S
+
+    def graph_ms(fns, reps):
+        g = torch.cuda.CUDAGraph()
+        for fn in fns:                      # warm (and first-call setup) outside the capture
+            fn(stream.cuda_stream)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            for fn in fns:
+                fn(torch.cuda.current_stream().cuda_stream)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    res = {}
+    # HCA decode, 1M-token contexts
+    w = S.WORKLOADS["hca_decode_1m_b8"]
+    inp = S.make_inputs(w, dev)
+    ad = P.attend_desc(w.B, 1, w.N, w.H, w.d, k=0, m=w.m, Wcap=w.window, window=w.window)
+    ws = torch.zeros(max(256, C.hca_attend_workspace(ad)), dtype=torch.uint8, device=dev)
+    out = torch.empty((w.B, 1, w.H, w.d), dtype=torch.bfloat16, device=dev)
+    ms = graph_ms([lambda sp: C.check(C.hca_attend(ad, inp["q"], inp["kv"], inp["win"], inp["sink"], inp["q_pos"], out,
+                                                   None, ws, stream=sp), "hca_attend")], max(5, args.steps))
+    byts = w.B * ((w.N + w.window) * w.d * 2 + 2 * w.H * w.d * 2)
+    res["hca_decode_1m_b8"] = {"query_tok_per_s": w.B / (ms * 1e-3), "ms_per_step": ms,
+                               "hbm_GBps": byts / (ms * 1e-3) / 1e9, "algorithmic_bytes": byts}
+    del inp, ws, out
+    # HCA prefill chunk: compress (m' = 128) + dense attention
+    w = S.WORKLOADS["hca_prefill_t32768"]
+    inp = S.make_inputs(w, dev)
+    kv = torch.empty((1, w.N, w.d), dtype=torch.bfloat16, device=dev)
+    ad = P.attend_desc(1, w.T, w.N, w.H, w.d, k=0, m=w.m, Wcap=w.T, window=w.window)
+    ws = torch.zeros(max(256, C.hca_attend_workspace(ad)), dtype=torch.uint8, device=dev)
+    out = torch.empty((1, w.T, w.H, w.d), dtype=torch.bfloat16, device=dev)
+    ms_c = graph_ms([lambda sp: P.compress(inp["C"], inp["Z"], w.m, out=kv, stream=sp)], 5)
+    ms_a = graph_ms([lambda sp: C.check(C.hca_attend(ad, inp["q"], kv, inp["win"], inp["sink"], inp["q_pos"], out, None,
+                                                     ws, stream=sp), "hca_attend")], 3)
+    rows = sum(min(w.N, (t + 1) // w.m) + min(w.window, t + 1) for t in range(w.T))
+    res["hca_prefill_t32768"] = {"tok_per_s": w.T / ((ms_c + ms_a) * 1e-3), "ms_per_chunk": ms_c + ms_a,
+                                 "breakdown_ms": {"csa_compress": ms_c, "hca_attend": ms_a},
+                                 "attend_TFLOPs": rows * 4 * w.H * w.d / (ms_a * 1e-3) / 1e12}
+    del inp, kv, ws, out
+    # tiny CSA prefill: all four calls
+    w = S.WORKLOADS["tiny_csa_prefill_t2048"]
+    inp = S.make_inputs(w, dev)
+    kv = torch.empty((1, w.N, w.d), dtype=torch.bfloat16, device=dev)
+    kI = torch.empty((1, w.N, w.dI), dtype=torch.bfloat16, device=dev)
+    idx = torch.empty((1, w.T, w.k), dtype=torch.int32, device=dev)
+    out = torch.empty((1, w.T, w.H, w.d), dtype=torch.bfloat16, device=dev)
+    idesc = P.index_desc(1, w.T, w.N, w.nI, w.dI, w.k, w.m)
+    ad = P.attend_desc(1, w.T, w.N, w.H, w.d, k=w.k, m=w.m, Wcap=w.T, window=w.window)
+    wsi = torch.zeros(max(256, C.csa_index_topk_workspace(idesc)), dtype=torch.uint8, device=dev)
+    wsa = torch.zeros(max(256, C.csa_attend_workspace(ad)), dtype=torch.uint8, device=dev)
+    ms = graph_ms([
+        lambda sp: P.compress(inp["Ca"], inp["Za"], w.m, Cb=inp["Cb"], Zb=inp["Zb"], out=kv, stream=sp),
+        lambda sp: P.compress(inp["Ca_I"], inp["Za_I"], w.m, Cb=inp["Cb_I"], Zb=inp["Zb_I"], rope=False, rope_dims=0,
+                              out=kI, stream=sp),
+        lambda sp: C.check(C.csa_index_topk(idesc, inp["qI"], inp["w"], kI, None, inp["q_pos"], idx, None, wsi,
+                                            stream=sp), "csa_index_topk"),
+        lambda sp: C.check(C.csa_attend(ad, inp["q"], kv, idx, inp["win"], inp["sink"], inp["q_pos"], out, None, wsa,
+                                        stream=sp), "csa_attend")], 10)
+    res["tiny_csa_prefill_t2048"] = {"tok_per_s": w.T / (ms * 1e-3), "ms_per_chunk": ms}
+    del inp, kv, kI, idx, out, wsi, wsa
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_prefill(args, dev, stream):
     """One CSA prefill chunk (T = 65536) through the four calls, timed per call with CUDA events."""
     import torch
@@ -481,6 +562,9 @@ def run_ours(args):
     prefill = None
     if not args.quick and not args.no_prefill:
         prefill = run_prefill(args, dev, stream)
+    other = None
+    if not args.quick and not args.no_prefill and rank == 0:
+        other = run_other(args, dev, stream)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.quick:
@@ -517,6 +601,7 @@ def run_ours(args):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "prefill": prefill,
+        "other_workloads": other,
         "device_status": dev_status,
         "clocks": clocks,
     }
