@@ -257,6 +257,79 @@ csa_status hca_attend(const csa_attend_desc* desc, const void* q, const void* kv
                       float* lse, void* workspace, size_t ws_bytes, csa_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * csa_cache_append -- hybrid KV cache maintenance for one attention layer of B sequences.
+ *
+ * Source: "DeepSeek V4 模型技术大全", the hybrid KV cache passage (C_state = the SWA window's last
+ * n_win rows and the compressors' unclosed tails; C_classical = the closed CSA entries, indexer
+ * keys and HCA entries; prefix reuse at lcm(4, 128) = 128-token boundaries, the tail recomputed)
+ * and the CSA / HCA compressor equations quoted for csa_compress.
+ *
+ * Appends tokens t0 .. t0+n-1 (n = 1 is one decode step; t0 = 0 with the whole prompt fills the
+ * cache after prefill).  Tokens 0 .. t0-1 must have been appended before with the same buffers.
+ *   - Every entry i whose block closes inside the chunk, i.e. m*(i+1)-1 in [t0, t0+n), is
+ *     compressed exactly as csa_compress would compute entry i of the whole sequence (same
+ *     arithmetic, RoPE position m*i) and written to kv[b, i] (and the indexer key to kI[b, i]).
+ *     Rows of blocks that began before t0 come from the tail rings in `state`.
+ *   - Window row of token u goes to win[b, u mod Wcap] for u in [max(t0, t0+n-Wcap), t0+n).
+ *   - The tail rings keep the last R stream rows (R = 2m with overlap, else m).
+ * Entries compress in a first kernel; the rings and the window are written in a second one
+ * ordered after it on `stream`, so a chunk may overwrite the slots it reads.
+ *
+ * CSA layer: overlap = 1, m = 4, rows Ca, Cb, Za, Zb (and the indexer streams when dI > 0).
+ * HCA layer: overlap = 0, m = 128, rows Ca (the C stream) and Za (its gate logits Z).
+ * rows->*: bf16 [B, n, d] (the *_I streams [B, n, dI]); rows->win: bf16 [B, n, d], the tokens'
+ *     window rows as csa_attend reads them.
+ * params->*: as csa_compress's bias_a, bias_b ([m, width] fp32) and gamma ([width] fp32); NULL
+ *     = zero biases / unit gamma.
+ * bufs->kv: bf16 [B, N_cap, d]; bufs->kI: bf16 [B, N_cap, dI] (dI > 0); bufs->win: bf16
+ *     [B, Wcap, d]; bufs->state: csa_cache_state_bytes(desc) bytes, zero or as left by the
+ *     previous append (opaque; a copy of it and of win taken at token t restores the cache to t).
+ * Requires (t0+n)/m <= N_cap, t0 + n < 2^31.  Widths as csa_compress (d, dI multiples of 64 in
+ * [64, 1024]).  Invalid arguments return CSA_ERR_INVALID_ARG / CSA_ERR_UNSUPPORTED before any
+ * launch; n = 0 or B = 0 is a no-op.
+ * ------------------------------------------------------------------------------------------- */
+typedef struct {
+  int B;                   /* sequences that advance together */
+  int d;                   /* entry and window row width */
+  int dI;                  /* indexer key width; 0 = no indexer stream (HCA layers) */
+  int m;                   /* compression ratio */
+  int overlap;             /* 1: CSA (two streams, block i-1 overlaps); 0: HCA */
+  int Wcap;                /* window ring slots */
+  int N_cap;               /* entries the kv / kI buffers hold per sequence */
+  int rope_dims;           /* RoPE on the main entries, as csa_compress */
+  float rope_theta;
+  const float* inv_freq;   /* HOST pointer or NULL */
+  float eps;
+  unsigned flags;          /* CSA_COMPRESS_* for the main entries */
+  unsigned index_flags;    /* CSA_COMPRESS_* for the indexer keys (rotation not supported) */
+} csa_cache_desc;
+
+typedef struct {
+  const void *Ca, *Cb, *Za, *Zb;
+  const void *Ca_I, *Cb_I, *Za_I, *Zb_I;
+  const void* win;
+} csa_cache_rows;
+
+typedef struct {
+  const float *bias_a, *bias_b, *gamma;
+  const float *bias_a_I, *bias_b_I, *gamma_I;
+} csa_cache_params;
+
+typedef struct {
+  void* kv;
+  void* kI;
+  void* win;
+  void* state;
+} csa_cache_buffers;
+
+/* Bytes of the opaque tail state for this descriptor (0 if it is invalid). */
+size_t csa_cache_state_bytes(const csa_cache_desc* desc);
+
+csa_status csa_cache_append(const csa_cache_desc* desc, int64_t t0, int n, const csa_cache_rows* rows,
+                            const csa_cache_params* params, const csa_cache_buffers* bufs,
+                            csa_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
  * Status helpers.
  * csa_read_device_status: waits for `stream`, reads the status word at the start of a
  * workspace that a previous call used, returns CSA_OK, CSA_ERR_DEVICE_CHECK (a range check

@@ -39,7 +39,8 @@ CSA_ATTEND_WRITE_LSE = 4
 EXPORTS = ("csa_compress", "csa_index_topk_workspace", "csa_index_topk", "csa_attend_workspace",
            "hca_attend_workspace", "csa_attend", "hca_attend", "csa_read_device_status", "csa_clear_device_status",
            "csa_status_string", "csa_launch_count", "csa_index_topk_noalloc", "csa_index_score_workspace",
-           "csa_index_score", "csa_topk_workspace", "csa_topk", "csa_selftest_bounded_wait")
+           "csa_index_score", "csa_topk_workspace", "csa_topk", "csa_selftest_bounded_wait",
+           "csa_cache_state_bytes", "csa_cache_append")
 
 
 class csa_compress_desc(ctypes.Structure):
@@ -58,6 +59,24 @@ class csa_attend_desc(ctypes.Structure):
                 ("rope_dims", c_int), ("k", c_int), ("m", c_int), ("Wcap", c_int), ("window", c_int),
                 ("scale", c_float), ("rope_theta", c_float), ("inv_freq", POINTER(c_float)),
                 ("eps", c_float), ("kv_fmt", c_int), ("flags", c_uint)]
+
+
+class csa_cache_desc(ctypes.Structure):
+    _fields_ = [("B", c_int), ("d", c_int), ("dI", c_int), ("m", c_int), ("overlap", c_int), ("Wcap", c_int),
+                ("N_cap", c_int), ("rope_dims", c_int), ("rope_theta", c_float), ("inv_freq", POINTER(c_float)),
+                ("eps", c_float), ("flags", c_uint), ("index_flags", c_uint)]
+
+
+class csa_cache_rows(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in ("Ca", "Cb", "Za", "Zb", "Ca_I", "Cb_I", "Za_I", "Zb_I", "win")]
+
+
+class csa_cache_params(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in ("bias_a", "bias_b", "gamma", "bias_a_I", "bias_b_I", "gamma_I")]
+
+
+class csa_cache_buffers(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in ("kv", "kI", "win", "state")]
 
 
 class CsaError(RuntimeError):
@@ -103,6 +122,11 @@ def _load() -> ctypes.CDLL:
     lib.csa_status_string.restype = ctypes.c_char_p
     lib.csa_selftest_bounded_wait.argtypes = [vp, c_size_t, ctypes.c_int64, vp]
     lib.csa_selftest_bounded_wait.restype = c_int
+    lib.csa_cache_state_bytes.argtypes = [POINTER(csa_cache_desc)]
+    lib.csa_cache_state_bytes.restype = c_size_t
+    lib.csa_cache_append.argtypes = [POINTER(csa_cache_desc), ctypes.c_int64, c_int, POINTER(csa_cache_rows),
+                                     POINTER(csa_cache_params), POINTER(csa_cache_buffers), vp]
+    lib.csa_cache_append.restype = c_int
     lib.csa_launch_count.argtypes = []
     lib.csa_launch_count.restype = c_uint64
     return lib
@@ -233,3 +257,17 @@ def csa_selftest_bounded_wait(workspace, limit_ns, ws_bytes=None, stream=None) -
 
 def csa_launch_count() -> int:
     return int(lib.csa_launch_count())
+
+
+def csa_cache_state_bytes(desc) -> int:
+    return lib.csa_cache_state_bytes(ctypes.byref(desc))
+
+
+def csa_cache_append(desc, t0, n, rows, params, bufs, stream=None) -> int:
+    """rows / params / bufs: dicts of tensors (or addresses) keyed by the C struct's field names;
+    missing keys are NULL."""
+    r = csa_cache_rows(**{k: _p(v) for k, v in rows.items()})
+    p = csa_cache_params(**{k: _p(v) for k, v in (params or {}).items()})
+    b = csa_cache_buffers(**{k: _p(v) for k, v in bufs.items()})
+    return lib.csa_cache_append(ctypes.byref(desc), int(t0), int(n), ctypes.byref(r),
+                                ctypes.byref(p) if params is not None else None, ctypes.byref(b), _stream(stream))

@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/csa.h: argument validation, workspace layout,
 // RoPE tables and kernel orchestration.  Nothing here allocates device memory.
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstring>
 
@@ -34,6 +35,43 @@ bool make_rope(int r, float theta, const float* inv_freq, csa::RopeParams* rp) {
 }
 
 void count(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
+
+csa_status cache_desc_check(const csa_cache_desc* d) {
+  if (!d) return CSA_ERR_INVALID_ARG;
+  if (d->B < 0 || d->m < 1 || d->m > 256 || d->Wcap < 1 || d->N_cap < 0 || !(d->eps >= 0.f))
+    return CSA_ERR_INVALID_ARG;
+  if (d->d < 64 || d->d > 1024 || (d->d % 64) != 0) return CSA_ERR_UNSUPPORTED;
+  if (d->dI < 0) return CSA_ERR_INVALID_ARG;
+  if (d->dI != 0 && (d->dI < 64 || d->dI > 1024 || (d->dI % 64) != 0 || !d->overlap)) return CSA_ERR_UNSUPPORTED;
+  if (d->rope_dims < 0 || d->rope_dims > d->d || (d->rope_dims % 8) != 0 || d->rope_dims > 2 * csa::kMaxRopePairs)
+    return CSA_ERR_UNSUPPORTED;
+  if (d->index_flags & CSA_COMPRESS_ROPE) return CSA_ERR_UNSUPPORTED;
+  return CSA_OK;
+}
+
+// Tail rings in the state buffer, each bf16 [B, R, width] on a 256-byte boundary:
+// CSA: Ca, Cb, Za, Zb (width d) then Ca_I, Cb_I, Za_I, Zb_I (width dI); HCA: Ca, Za.
+struct CacheLayout {
+  size_t off[8];
+  int width[8];
+  int n, R;
+  size_t total;
+};
+
+CacheLayout cache_layout(const csa_cache_desc* d) {
+  CacheLayout L{};
+  L.R = d->overlap ? 2 * d->m : d->m;
+  L.n = d->overlap ? (d->dI > 0 ? 8 : 4) : 2;
+  size_t at = 0;
+  for (int s = 0; s < L.n; ++s) {
+    L.width[s] = s < 4 ? d->d : d->dI;
+    L.off[s] = at;
+    const size_t bytes = static_cast<size_t>(d->B) * L.R * L.width[s] * 2;
+    at += (bytes + 255) & ~static_cast<size_t>(255);
+  }
+  L.total = at;
+  return L;
+}
 
 }  // namespace
 
@@ -213,9 +251,99 @@ csa_status csa_compress(const csa_compress_desc* d, const void* Ca, const void* 
   a.rope = (d->flags & CSA_COMPRESS_ROPE) != 0 && d->rope_dims > 0;
   a.pos_shift = d->pos_shift;
   a.eps = d->eps;
+  a.out_N = N;
   if (!make_rope(d->rope_dims, d->rope_theta, d->inv_freq, &a.rp)) return CSA_ERR_INVALID_ARG;
   int launches = 0;
   const cudaError_t e = csa::launch_compress(a, reinterpret_cast<cudaStream_t>(stream), &launches);
+  count(launches);
+  return from_cuda(e);
+}
+
+size_t csa_cache_state_bytes(const csa_cache_desc* d) {
+  if (cache_desc_check(d) != CSA_OK) return 0;
+  return cache_layout(d).total;
+}
+
+csa_status csa_cache_append(const csa_cache_desc* d, int64_t t0, int n, const csa_cache_rows* rows,
+                            const csa_cache_params* params, const csa_cache_buffers* bufs, csa_stream_t stream_) {
+  const csa_status st = cache_desc_check(d);
+  if (st != CSA_OK) return st;
+  if (t0 < 0 || n < 0 || t0 + n > INT32_MAX) return CSA_ERR_INVALID_ARG;
+  const int T0 = static_cast<int>(t0);
+  const int i_begin = T0 / d->m;
+  const int i_end = (T0 + n) / d->m;
+  if (i_end > d->N_cap) return CSA_ERR_INVALID_ARG;
+  if (n == 0 || d->B == 0) return CSA_OK;
+  if (!rows || !bufs) return CSA_ERR_INVALID_ARG;
+  const bool idx = d->dI > 0;
+  const void* in_main[4] = {rows->Ca, rows->Cb, rows->Za, rows->Zb};
+  const void* in_idx[4] = {rows->Ca_I, rows->Cb_I, rows->Za_I, rows->Zb_I};
+  for (int s = 0; s < 4; ++s) {
+    const bool used = d->overlap || s == 0 || s == 2;
+    if (used && (!in_main[s] || !aligned16(in_main[s]))) return CSA_ERR_INVALID_ARG;
+    if (idx && (!in_idx[s] || !aligned16(in_idx[s]))) return CSA_ERR_INVALID_ARG;
+  }
+  if (!rows->win || !aligned16(rows->win) || !bufs->win || !aligned16(bufs->win) || !bufs->state ||
+      !aligned16(bufs->state))
+    return CSA_ERR_INVALID_ARG;
+  if (i_end > i_begin && (!bufs->kv || !aligned16(bufs->kv) || (idx && (!bufs->kI || !aligned16(bufs->kI)))))
+    return CSA_ERR_INVALID_ARG;
+  const csa_cache_params none{};
+  const csa_cache_params& p = params ? *params : none;
+  const float* fptr[6] = {p.bias_a, p.bias_b, p.gamma, p.bias_a_I, p.bias_b_I, p.gamma_I};
+  for (const float* f : fptr)
+    if (f && !aligned16(f)) return CSA_ERR_INVALID_ARG;
+
+  const CacheLayout L = cache_layout(d);
+  char* state = static_cast<char*>(bufs->state);
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int launches = 0;
+  cudaError_t e = cudaSuccess;
+  if (i_end > i_begin) {
+    for (int part = 0; part < (idx ? 2 : 1) && e == cudaSuccess; ++part) {
+      const void* const* in = part ? in_idx : in_main;
+      const int s0 = part ? 4 : 0;     // first ring of this part in the layout
+      csa::CompressArgs a{};
+      a.Ca = in[0]; a.Za = in[2];
+      a.Cb = d->overlap ? in[1] : nullptr; a.Zb = d->overlap ? in[3] : nullptr;
+      a.bias_a = part ? p.bias_a_I : p.bias_a;
+      a.bias_b = d->overlap ? (part ? p.bias_b_I : p.bias_b) : nullptr;
+      a.gamma = part ? p.gamma_I : p.gamma;
+      a.out = part ? bufs->kI : bufs->kv;
+      a.B = d->B; a.T = n; a.d = part ? d->dI : d->d; a.m = d->m; a.N = i_end - i_begin;
+      a.overlap = d->overlap ? 1 : 0;
+      const unsigned fl = part ? d->index_flags : d->flags;
+      a.norm = (fl & CSA_COMPRESS_NORM) != 0;
+      a.rope = !part && (fl & CSA_COMPRESS_ROPE) != 0 && d->rope_dims > 0;
+      a.eps = d->eps;
+      a.t0 = T0; a.i_begin = i_begin; a.out_N = d->N_cap;
+      a.ring.R = L.R;
+      a.ring.Ca = state + L.off[s0 + 0];
+      a.ring.Za = state + L.off[s0 + (d->overlap ? 2 : 1)];
+      a.ring.Cb = d->overlap ? state + L.off[s0 + 1] : nullptr;
+      a.ring.Zb = d->overlap ? state + L.off[s0 + 3] : nullptr;
+      if (!make_rope(part ? 0 : d->rope_dims, d->rope_theta, d->inv_freq, &a.rp)) return CSA_ERR_INVALID_ARG;
+      e = csa::launch_compress(a, stream, &launches);
+    }
+  }
+  if (e == cudaSuccess) {
+    csa::RingArgs r{};
+    r.B = d->B; r.t0 = T0; r.n = n;
+    const void* srcs[8];
+    int ns = 0;
+    if (d->overlap) {
+      for (int s = 0; s < 4; ++s) srcs[ns++] = in_main[s];
+      if (idx)
+        for (int s = 0; s < 4; ++s) srcs[ns++] = in_idx[s];
+    } else {
+      srcs[ns++] = in_main[0];
+      srcs[ns++] = in_main[2];
+    }
+    for (int s = 0; s < ns; ++s) r.job[s] = csa::RingJob{srcs[s], state + L.off[s], L.width[s], L.R};
+    r.job[ns] = csa::RingJob{rows->win, bufs->win, d->d, d->Wcap};
+    r.n_jobs = ns + 1;
+    e = csa::launch_ring_rows(r, stream, &launches);
+  }
   count(launches);
   return from_cuda(e);
 }

@@ -156,16 +156,41 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // ------------------------------------------------------------------ launchers (internal)
 namespace csa {
 
-struct CompressArgs {
+// Rows of tokens before the chunk (cache append): stream rows of token u at slot u mod R of
+// [B, R, d] rings.  Unused (R = 0) when the chunk starts at token 0.
+struct CompressRing {
   const void *Ca, *Cb, *Za, *Zb;
+  int R;
+};
+
+struct CompressArgs {
+  const void *Ca, *Cb, *Za, *Zb;   // the chunk's rows: tokens t0 .. t0+T-1, [B, T, d]
   const float *bias_a, *bias_b, *gamma;
-  void* out;
+  void* out;                       // [B, out_N, d]: entry i at row i
   int B, T, d, m, N, overlap, norm, rope;
   int pos_shift;
   float eps;
   RopeParams rp;
+  int t0;                          // first token of the chunk (0 for a whole-sequence call)
+  int i_begin;                     // entries i_begin .. i_begin+N-1 are computed
+  int out_N;
+  CompressRing ring;
 };
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s, int* launches);
+
+// Row scatter into rings (cache append): job j copies rows of tokens [lo, t0+n) of src
+// [B, n, w] to dst [B, R, w] slot u mod R, lo = max(t0, t0+n-R).
+struct RingJob {
+  const void* src;
+  void* dst;
+  int w, R;
+};
+constexpr int kMaxRingJobs = 9;
+struct RingArgs {
+  RingJob job[kMaxRingJobs];
+  int n_jobs, B, t0, n;
+};
+cudaError_t launch_ring_rows(const RingArgs& a, cudaStream_t s, int* launches);
 
 struct IndexArgs {
   const void* qI;

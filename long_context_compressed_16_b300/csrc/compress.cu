@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(256) k_compress(CompressArgs a, int RS, int EP
   const long long gidx = static_cast<long long>(blockIdx.x) * EPC + e;
   const bool active = gidx < total;
   const int b = active ? static_cast<int>(gidx / a.N) : 0;
-  const int i = active ? static_cast<int>(gidx % a.N) : 0;
+  const int i = active ? a.i_begin + static_cast<int>(gidx % a.N) : 0;
   const int c0 = cg * 8;
   const int d = a.d;
 
@@ -53,6 +53,10 @@ __global__ void __launch_bounds__(256) k_compress(CompressArgs a, int RS, int EP
     const __nv_bfloat16* Ca = static_cast<const __nv_bfloat16*>(a.Ca);
     const __nv_bfloat16* Zb = static_cast<const __nv_bfloat16*>(a.Zb);
     const __nv_bfloat16* Cb = static_cast<const __nv_bfloat16*>(a.Cb);
+    const __nv_bfloat16* rZa = static_cast<const __nv_bfloat16*>(a.ring.Za);
+    const __nv_bfloat16* rCa = static_cast<const __nv_bfloat16*>(a.ring.Ca);
+    const __nv_bfloat16* rZb = static_cast<const __nv_bfloat16*>(a.ring.Zb);
+    const __nv_bfloat16* rCb = static_cast<const __nv_bfloat16*>(a.ring.Cb);
     for (int r0 = r_lo; r0 < r_hi; r0 += 4) {
       const int nr = min(4, r_hi - r0);
       uint4 zv[4], cv[4];
@@ -66,9 +70,15 @@ __global__ void __launch_bounds__(256) k_compress(CompressArgs a, int RS, int EP
           const int j = isb ? r - a.m : r;
           const long long tok = isb ? static_cast<long long>(a.m) * (i - 1) + j
                                     : static_cast<long long>(a.m) * i + j;
-          const size_t off = (static_cast<size_t>(b) * a.T + tok) * d + c0;
-          zv[u] = ldg_nc((isb ? Zb : Za) + off);
-          cv[u] = ldg_nc((isb ? Cb : Ca) + off);
+          if (tok >= a.t0) {              // a row of this call's chunk
+            const size_t off = (static_cast<size_t>(b) * a.T + (tok - a.t0)) * d + c0;
+            zv[u] = ldg_nc((isb ? Zb : Za) + off);
+            cv[u] = ldg_nc((isb ? Cb : Ca) + off);
+          } else {                        // an earlier token: the tail ring, slot tok mod R
+            const size_t off = (static_cast<size_t>(b) * a.ring.R + tok % a.ring.R) * d + c0;
+            zv[u] = ldg_nc((isb ? rZb : rZa) + off);
+            cv[u] = ldg_nc((isb ? rCb : rCa) + off);
+          }
           const float* bp = isb ? a.bias_b : a.bias_a;
           if (bp != nullptr) bptr[u] = bp + static_cast<size_t>(j) * d + c0;
         }
@@ -186,10 +196,47 @@ __global__ void __launch_bounds__(256) k_compress(CompressArgs a, int RS, int EP
   o.z = pack_bf16x2(outv[4], outv[5]);
   o.w = pack_bf16x2(outv[6], outv[7]);
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-  *reinterpret_cast<uint4*>(out + (static_cast<size_t>(b) * a.N + i) * d + c0) = o;
+  *reinterpret_cast<uint4*>(out + (static_cast<size_t>(b) * a.out_N + i) * d + c0) = o;
+}
+
+// One 16-byte vector per thread; blockIdx.y is the job.  Every job's row width is a multiple
+// of 8 channels, so a vector never straddles rows.
+__global__ void __launch_bounds__(256) k_ring_rows(RingArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const RingJob jb = a.job[blockIdx.y];
+  const int lo = max(a.t0, a.t0 + a.n - jb.R);
+  const int keep = a.t0 + a.n - lo;
+  const int vpr = jb.w >> 3;
+  const long long total = static_cast<long long>(a.B) * keep * vpr;
+  for (long long v = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; v < total;
+       v += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(v % vpr);
+    const long long rb = v / vpr;
+    const int u = lo + static_cast<int>(rb % keep);
+    const int b = static_cast<int>(rb / keep);
+    const uint4 x = ldg_nc(static_cast<const __nv_bfloat16*>(jb.src) +
+                           (static_cast<size_t>(b) * a.n + (u - a.t0)) * jb.w + c * 8);
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(jb.dst) +
+                              (static_cast<size_t>(b) * jb.R + u % jb.R) * jb.w + c * 8) = x;
+  }
 }
 
 }  // namespace
+
+cudaError_t launch_ring_rows(const RingArgs& a, cudaStream_t s, int* launches) {
+  if (a.n_jobs == 0 || a.n == 0 || a.B == 0) return cudaSuccess;
+  long long most = 0;
+  for (int j = 0; j < a.n_jobs; ++j) {
+    const int keep = a.t0 + a.n - max(a.t0, a.t0 + a.n - a.job[j].R);
+    most = max(most, static_cast<long long>(a.B) * keep * (a.job[j].w >> 3));
+  }
+  long long bx = (most + 255) / 256;
+  if (bx > 1184) bx = 1184;       // 148 SMs x 8 blocks; the loop covers the rest
+  const cudaError_t e = launch_k(k_ring_rows, dim3(static_cast<unsigned>(bx), a.n_jobs), dim3(256), 0, s, a);
+  ++*launches;
+  return e;
+}
 
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s, int* launches) {
   const int TPE = a.d / 8;
