@@ -298,6 +298,45 @@ def run_other(args, dev, stream):
     res["tiny_csa_prefill_t2048"] = {"tok_per_s": w.T / (ms * 1e-3), "ms_per_chunk": ms}
     del inp, kv, kI, idx, out, wsi, wsa
     torch.cuda.empty_cache()
+    # grouped output projection (Flash widths: 64 heads x 512, g = 8, r_o = 1024, hidden 4096)
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        pk = json.load(f)
+    n_h, d_h, g, r_o, d_out = 64, 512, 8, 1024, 4096
+    K = n_h // g * d_h
+    Wd = S.weight_bf16((g, r_o, K), 5, S.TID["W_down"], K, dev)
+    Wp = S.weight_bf16((d_out, g * r_o), 5, S.TID["W_proj"], g * r_o, dev)
+    wso = torch.zeros(256, dtype=torch.uint8, device=dev)
+    for name, T, reps in (("out_proj_t65536", 65536, 5), ("out_proj_decode_b32", 32, 50)):
+        Oa = S.normal_bf16((T, n_h, d_h), 5, S.TID["O"], dev)
+        z = torch.empty((T, g * r_o), dtype=torch.bfloat16, device=dev)
+        y = torch.empty((T, d_out), dtype=torch.bfloat16, device=dev)
+        ms = graph_ms([lambda sp: P.out_proj(Oa, Wd, g, W_proj=Wp, z=z, y=y, workspace=wso, stream=sp)], reps)
+        flops = 2.0 * T * (n_h * d_h * r_o + g * r_o * d_out)
+        byts = (Wd.numel() + Wp.numel() + Oa.numel() + 2 * z.numel() + y.numel()) * 2
+        tf = flops / (ms * 1e-3) / 1e12
+        res[name] = {"tok_per_s": T / (ms * 1e-3), "ms": ms, "TFLOPs": tf, "flops": flops,
+                     "tensor_frac_of_sustained": tf / pk.get("bf16_tflops_sustained", 1386.7),
+                     "hbm_GBps": byts / (ms * 1e-3) / 1e9, "algorithmic_bytes": byts,
+                     "hbm_frac": byts / (ms * 1e-3) / 1e9 / pk.get("hbm_gbs", 6504.1)}
+        del Oa, z, y
+    del Wd, Wp
+    # decode cache maintenance: one token appended to 32 sequences (CSA layer, d = 512, dI = 128)
+    from long_context_compressed_16_b300.cache import LayerCache
+    B, d, dI = 32, 512, 128
+    cache = LayerCache("csa", B, 4096, d=d, dI=dI, device=dev)
+    rows = {n: S.normal_bf16((B, 1, dI if n.endswith("_I") else d), 9, S.TID[n], dev)
+            for n in ("Ca", "Cb", "Za", "Zb", "Ca_I", "Cb_I", "Za_I", "Zb_I")}
+    rows["win"] = S.normal_bf16((B, 1, d), 9, S.TID["win"], dev)
+    bufs = {"kv": cache.kv, "kI": cache.kI, "win": cache.win, "state": cache.state}
+    for t0 in range(3):                          # t = 3 closes entry 0 below
+        C.check(C.csa_cache_append(cache.desc, t0, 1, rows, {}, bufs, stream.cuda_stream), "csa_cache_append")
+    ms_open = graph_ms([lambda sp: C.check(C.csa_cache_append(cache.desc, 5, 1, rows, {}, bufs, sp), "append")], 50)
+    ms_close = graph_ms([lambda sp: C.check(C.csa_cache_append(cache.desc, 7, 1, rows, {}, bufs, sp), "append")], 50)
+    res["cache_append_decode_b32"] = {"us_per_token_no_entry_closes": ms_open * 1e3,
+                                      "us_per_token_entry_closes": ms_close * 1e3,
+                                      "note": "one token for 32 sequences; every 4th token closes a CSA entry"}
+    del cache, rows, bufs
+    torch.cuda.empty_cache()
     return res
 
 

@@ -330,6 +330,38 @@ csa_status csa_cache_append(const csa_cache_desc* desc, int64_t t0, int n, const
                             csa_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * csa_out_proj -- grouped output projection of the attention output.
+ *
+ * Source: "DeepSeek V4 模型技术大全", the grouped output projection equations of the CSA path and
+ * its component-table row (Flash: n_h = 64, d_h = 512, g = 8, r_o = 1024, hidden size 4096):
+ *   O = Concat(o^(1) .. o^(n_h)) split into g groups O^[u] of n_h/g consecutive heads,
+ *   z^[u] = O^[u] W_down^[u]   (W_down^[u] of (n_h/g) d_h x r_o),
+ *   y = Proj(Concat_u z^[u])   (Proj: a linear map g r_o -> d_out).
+ * Products accumulate in fp32 on the tensor cores; z is stored in bf16 and y is computed from
+ * that bf16 z.
+ *
+ * O: bf16 [T, n_heads, head_dim] (the attention output, T = B x Tq).
+ * W_down: bf16 [groups, rank, K], K = (n_heads/groups) x head_dim: row n of group u holds
+ *     column n of W_down^[u] (the matrix stored transposed, K contiguous).
+ * W_proj: bf16 [d_out, groups x rank] (Proj's matrix stored the same way); unused if d_out = 0.
+ * z: bf16 [T, groups x rank] output.  y: bf16 [T, d_out] output (d_out > 0).
+ * workspace: at least csa_out_proj_workspace(desc) bytes (the status word), first 8 bytes zero.
+ * Supported: groups divides n_heads; K, rank and d_out multiples of 64; T < 2^31.
+ * ------------------------------------------------------------------------------------------- */
+typedef struct {
+  int T;                   /* tokens */
+  int n_heads, head_dim;
+  int groups;              /* g */
+  int rank;                /* r_o */
+  int d_out;               /* width of y; 0 = compute z only */
+} csa_out_proj_desc;
+
+size_t csa_out_proj_workspace(const csa_out_proj_desc* desc);
+
+csa_status csa_out_proj(const csa_out_proj_desc* desc, const void* O, const void* W_down, const void* W_proj,
+                        void* z, void* y, void* workspace, size_t ws_bytes, csa_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
  * Status helpers.
  * csa_read_device_status: waits for `stream`, reads the status word at the start of a
  * workspace that a previous call used, returns CSA_OK, CSA_ERR_DEVICE_CHECK (a range check

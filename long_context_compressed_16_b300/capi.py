@@ -40,7 +40,7 @@ EXPORTS = ("csa_compress", "csa_index_topk_workspace", "csa_index_topk", "csa_at
            "hca_attend_workspace", "csa_attend", "hca_attend", "csa_read_device_status", "csa_clear_device_status",
            "csa_status_string", "csa_launch_count", "csa_index_topk_noalloc", "csa_index_score_workspace",
            "csa_index_score", "csa_topk_workspace", "csa_topk", "csa_selftest_bounded_wait",
-           "csa_cache_state_bytes", "csa_cache_append")
+           "csa_cache_state_bytes", "csa_cache_append", "csa_out_proj_workspace", "csa_out_proj")
 
 
 class csa_compress_desc(ctypes.Structure):
@@ -59,6 +59,11 @@ class csa_attend_desc(ctypes.Structure):
                 ("rope_dims", c_int), ("k", c_int), ("m", c_int), ("Wcap", c_int), ("window", c_int),
                 ("scale", c_float), ("rope_theta", c_float), ("inv_freq", POINTER(c_float)),
                 ("eps", c_float), ("kv_fmt", c_int), ("flags", c_uint)]
+
+
+class csa_out_proj_desc(ctypes.Structure):
+    _fields_ = [("T", c_int), ("n_heads", c_int), ("head_dim", c_int), ("groups", c_int), ("rank", c_int),
+                ("d_out", c_int)]
 
 
 class csa_cache_desc(ctypes.Structure):
@@ -127,6 +132,10 @@ def _load() -> ctypes.CDLL:
     lib.csa_cache_append.argtypes = [POINTER(csa_cache_desc), ctypes.c_int64, c_int, POINTER(csa_cache_rows),
                                      POINTER(csa_cache_params), POINTER(csa_cache_buffers), vp]
     lib.csa_cache_append.restype = c_int
+    lib.csa_out_proj_workspace.argtypes = [POINTER(csa_out_proj_desc)]
+    lib.csa_out_proj_workspace.restype = c_size_t
+    lib.csa_out_proj.argtypes = [POINTER(csa_out_proj_desc), vp, vp, vp, vp, vp, vp, c_size_t, vp]
+    lib.csa_out_proj.restype = c_int
     lib.csa_launch_count.argtypes = []
     lib.csa_launch_count.restype = c_uint64
     return lib
@@ -271,3 +280,13 @@ def csa_cache_append(desc, t0, n, rows, params, bufs, stream=None) -> int:
     b = csa_cache_buffers(**{k: _p(v) for k, v in bufs.items()})
     return lib.csa_cache_append(ctypes.byref(desc), int(t0), int(n), ctypes.byref(r),
                                 ctypes.byref(p) if params is not None else None, ctypes.byref(b), _stream(stream))
+
+
+def csa_out_proj_workspace(desc) -> int:
+    return lib.csa_out_proj_workspace(ctypes.byref(desc))
+
+
+def csa_out_proj(desc, O, W_down, W_proj, z, y, workspace, ws_bytes=None, stream=None) -> int:
+    n = _nbytes(workspace) if ws_bytes is None else ws_bytes
+    return lib.csa_out_proj(ctypes.byref(desc), _p(O), _p(W_down), _p(W_proj), _p(z), _p(y), _p(workspace), n,
+                            _stream(stream))

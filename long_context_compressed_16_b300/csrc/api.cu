@@ -49,6 +49,18 @@ csa_status cache_desc_check(const csa_cache_desc* d) {
   return CSA_OK;
 }
 
+csa_status out_proj_check(const csa_out_proj_desc* d) {
+  if (!d) return CSA_ERR_INVALID_ARG;
+  if (d->T < 0 || d->n_heads < 1 || d->head_dim < 1 || d->groups < 1 || d->rank < 1 || d->d_out < 0)
+    return CSA_ERR_INVALID_ARG;
+  if (d->n_heads % d->groups != 0) return CSA_ERR_INVALID_ARG;
+  const long long K = static_cast<long long>(d->n_heads / d->groups) * d->head_dim;
+  if (K % 64 != 0 || d->rank % 64 != 0 || d->d_out % 64 != 0) return CSA_ERR_UNSUPPORTED;
+  if (K > (1 << 20) || static_cast<long long>(d->groups) * d->rank > (1 << 20) || d->d_out > (1 << 20))
+    return CSA_ERR_UNSUPPORTED;
+  return CSA_OK;
+}
+
 // Tail rings in the state buffer, each bf16 [B, R, width] on a 256-byte boundary:
 // CSA: Ca, Cb, Za, Zb (width d) then Ca_I, Cb_I, Za_I, Zb_I (width dI); HCA: Ca, Za.
 struct CacheLayout {
@@ -255,6 +267,30 @@ csa_status csa_compress(const csa_compress_desc* d, const void* Ca, const void* 
   if (!make_rope(d->rope_dims, d->rope_theta, d->inv_freq, &a.rp)) return CSA_ERR_INVALID_ARG;
   int launches = 0;
   const cudaError_t e = csa::launch_compress(a, reinterpret_cast<cudaStream_t>(stream), &launches);
+  count(launches);
+  return from_cuda(e);
+}
+
+size_t csa_out_proj_workspace(const csa_out_proj_desc* d) {
+  return out_proj_check(d) == CSA_OK ? csa::kStatusBytes : 0;
+}
+
+csa_status csa_out_proj(const csa_out_proj_desc* d, const void* O, const void* W_down, const void* W_proj, void* z,
+                        void* y, void* ws, size_t ws_bytes, csa_stream_t stream_) {
+  const csa_status st = out_proj_check(d);
+  if (st != CSA_OK) return st;
+  if (!ws || ws_bytes < csa::kStatusBytes) return CSA_ERR_WORKSPACE;
+  if (!aligned16(ws)) return CSA_ERR_INVALID_ARG;
+  if (d->T == 0) return CSA_OK;
+  if (!O || !W_down || !z || !aligned16(O) || !aligned16(W_down) || !aligned16(z)) return CSA_ERR_INVALID_ARG;
+  if (d->d_out > 0 && (!W_proj || !y || !aligned16(W_proj) || !aligned16(y))) return CSA_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  int32_t* status = static_cast<int32_t*>(ws);
+  const int K = d->n_heads / d->groups * d->head_dim;
+  int launches = 0;
+  cudaError_t e = csa::launch_gemm_tn(O, W_down, z, d->T, d->rank, K, d->groups, status, stream, &launches);
+  if (e == cudaSuccess && d->d_out > 0)
+    e = csa::launch_gemm_tn(z, W_proj, y, d->T, d->d_out, d->groups * d->rank, 1, status, stream, &launches);
   count(launches);
   return from_cuda(e);
 }

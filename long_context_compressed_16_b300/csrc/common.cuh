@@ -192,6 +192,12 @@ struct RingArgs {
 };
 cudaError_t launch_ring_rows(const RingArgs& a, cudaStream_t s, int* launches);
 
+// C[m][u][n] = sum_k A[m][u][k] B[u][n][k] (bf16 in, fp32 accumulate, bf16 out); A [M][G][K],
+// B [G][N][K], C [M][G][N]; K and N multiples of 64.
+cudaError_t launch_gemm_tn(const void* A, const void* B, void* C, int M, int N, int K, int G, int32_t* status,
+                           cudaStream_t s, int* launches);
+int gemm_tn_tile_n(int M, int N, int G);
+
 struct IndexArgs {
   const void* qI;
   const float* w;

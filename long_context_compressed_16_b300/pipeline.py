@@ -107,3 +107,26 @@ def hca_attend(q, kv, win, sink, q_pos, m=128, window=128, rope_dims=64, theta=1
     """Dense shared-KV attention over all closed entries + window + sink."""
     return _attend(False, q, kv, None, win, sink, q_pos, m, window, rope_dims, theta, scale, fp8, q_norm_rope,
                    out_unrotate, want_lse, inv_freq, out, lse, workspace, stream)
+
+
+def out_proj(O, W_down, groups, W_proj=None, z=None, y=None, workspace=None, stream=None):
+    """Grouped output projection.  O: bf16 [T, n_heads, head_dim] (or [B, Tq, H, d]);
+    W_down: bf16 [groups, rank, (n_heads/groups) head_dim]; W_proj: bf16 [d_out, groups rank] or
+    None.  Returns (z [T, groups rank], y [T, d_out] or None)."""
+    _dev_check(O, W_down, W_proj)
+    H, d = O.shape[-2], O.shape[-1]
+    T = O.numel() // (H * d)
+    G, rank, _ = W_down.shape
+    d_out = 0 if W_proj is None else W_proj.shape[0]
+    desc = C.csa_out_proj_desc(T=T, n_heads=H, head_dim=d, groups=G, rank=rank, d_out=d_out)
+    if z is None:
+        z = torch.empty((T, G * rank), dtype=torch.bfloat16, device=O.device)
+    if y is None and d_out:
+        y = torch.empty((T, d_out), dtype=torch.bfloat16, device=O.device)
+    if workspace is None:
+        n = C.csa_out_proj_workspace(desc)
+        if n == 0:
+            raise C.CsaError(C.CSA_ERR_UNSUPPORTED, "csa_out_proj")
+        workspace = _ws(n, O.device)
+    C.check(C.csa_out_proj(desc, O, W_down, W_proj, z, y, workspace, stream=stream), "csa_out_proj")
+    return z, y

@@ -32,6 +32,7 @@ TID = {
     "C": 9, "Z": 10,
     "q": 11, "qI": 12, "w": 13, "kv": 14, "kI": 15, "win": 16, "sink": 17,
     "outlier_kv": 18, "outlier_kI": 19,
+    "O": 20, "W_down": 21, "W_proj": 22,
 }
 
 
@@ -134,6 +135,11 @@ def normal_bf16(shape, seed, tensor_id, device="cpu", scale_channels=None) -> to
     idx, factor = scale_channels
     x[..., idx.to(device)] *= factor
     return f64_to_bf16(x)
+
+
+def weight_bf16(shape, seed, tensor_id, fan_in: int, device="cpu") -> torch.Tensor:
+    """Random-init projection weights: N(0, 1/fan_in) values rounded to bf16."""
+    return f64_to_bf16(normal_f64(shape, seed, tensor_id, device) / math.sqrt(fan_in))
 
 
 def e4m3_encode(v: torch.Tensor) -> torch.Tensor:

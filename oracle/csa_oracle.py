@@ -320,3 +320,34 @@ def attend(q, kv, win, sink, q_pos, m, window, idx=None, query_subset=None, **kw
         ents = range(n_visible(pos, m, N)) if idx is None else idx[b][t]
         o[b, t], lse[b, t] = attend_query(q[b, t], pos, kv[b], ents, win[b], window, sink, **kw)
     return o, lse
+
+
+# ------------------------------------------------------------------------------------------------
+# grouped output projection
+# ------------------------------------------------------------------------------------------------
+
+
+def out_proj(O, W_down, W_proj=None):
+    """Grouped output projection ("DeepSeek V4 模型技术大全", the grouped output projection
+    equations: O = Concat of the n_h head outputs split into g groups O^[u] of n_h/g consecutive
+    heads; z^[u] = O^[u] W_down^[u]; y = Proj(Concat_u z^[u])).
+
+    O: [T, n_h, d_h]; W_down: [g, r_o, (n_h/g) d_h], group u's matrix stored transposed (row n
+    holds column n of W_down^[u]); W_proj: [d_out, g r_o] or None (Proj stored the same way).
+    R26: z is kept in bf16 between the two products (rounded here with the oracle's own
+    bf16 rounding), so y is the product of that rounded z.
+    Returns (z fp64 [T, g r_o] before rounding, y fp64 [T, d_out] or None)."""
+    O = np.asarray(O, dtype=np.float64)
+    W_down = np.asarray(W_down, dtype=np.float64)
+    T, n_h, d_h = O.shape
+    g, r_o, K = W_down.shape
+    assert n_h % g == 0 and K == (n_h // g) * d_h
+    heads = n_h // g
+    z = np.empty((T, g * r_o))
+    for u in range(g):
+        Ou = O[:, u * heads:(u + 1) * heads, :].reshape(T, K)     # O^[u]: the group's heads side by side
+        z[:, u * r_o:(u + 1) * r_o] = Ou @ W_down[u].T              # O^[u] W_down^[u]
+    if W_proj is None:
+        return z, None
+    y = bf16_to_f64(bf16_round(z)) @ np.asarray(W_proj, dtype=np.float64).T
+    return z, y

@@ -37,7 +37,9 @@ def test_library_exports_every_declared_symbol():
 
 def test_descriptor_layout_matches_c(tmp_path):
     structs = {"csa_compress_desc": C.csa_compress_desc, "csa_index_desc": C.csa_index_desc,
-               "csa_attend_desc": C.csa_attend_desc}
+               "csa_attend_desc": C.csa_attend_desc, "csa_out_proj_desc": C.csa_out_proj_desc,
+               "csa_cache_desc": C.csa_cache_desc, "csa_cache_rows": C.csa_cache_rows,
+               "csa_cache_params": C.csa_cache_params, "csa_cache_buffers": C.csa_cache_buffers}
     lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "csa.h"', "int main(void){"]
     for sname, cls in structs.items():
         lines.append(f'printf("{sname} size %zu\\n", sizeof({sname}));')
@@ -166,3 +168,24 @@ def test_binding_refuses_to_run_without_the_library(tmp_path, monkeypatch):
     monkeypatch.setattr(C, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         C._load()
+
+
+def test_out_proj_validation_and_workspace():
+    desc = lambda **kw: C.csa_out_proj_desc(**{**dict(T=300, n_heads=64, head_dim=512, groups=8, rank=1024,
+                                                      d_out=4096), **kw})
+    assert C.csa_out_proj_workspace(desc()) == 256
+    for bad in (dict(groups=3), dict(rank=100), dict(d_out=100), dict(head_dim=12), dict(T=-1), dict(groups=0)):
+        assert C.csa_out_proj_workspace(desc(**bad)) == 0, bad
+    ws = FAKE
+    call = lambda d, **p: C.csa_out_proj(d, p.get("O", FAKE), p.get("Wd", FAKE), p.get("Wp", FAKE),
+                                         p.get("z", FAKE), p.get("y", FAKE), p.get("ws", ws), p.get("n", 256), stream=0)
+    assert call(desc(T=0)) == C.CSA_OK                                  # no rows: no launch
+    assert call(desc(groups=3)) == C.CSA_ERR_INVALID_ARG
+    assert call(desc(rank=96)) == C.CSA_ERR_UNSUPPORTED
+    assert call(desc(), n=128) == C.CSA_ERR_WORKSPACE
+    assert call(desc(), ws=None) == C.CSA_ERR_WORKSPACE
+    assert call(desc(), O=None) == C.CSA_ERR_INVALID_ARG
+    assert call(desc(), O=FAKE + 8) == C.CSA_ERR_INVALID_ARG
+    assert call(desc(), Wp=None) == C.CSA_ERR_INVALID_ARG              # d_out > 0 needs Proj
+    assert call(desc(), y=None) == C.CSA_ERR_INVALID_ARG
+    assert C.lib.csa_out_proj(None, None, None, None, None, None, None, 0, None) == C.CSA_ERR_INVALID_ARG

@@ -510,3 +510,40 @@ def test_query_quantisation_scale_and_amax_code():
     assert np.all(np.abs(deq - q)[big] <= np.abs(q)[big] * 2.0 ** -4 + 1e-12)
     zc, zs = O.quantize_query_e4m3(np.zeros((2, 128)))
     assert np.all(zc == 0) and np.all(zs == 1.0)
+
+
+# ------------------------------------------------------------------------------------------------ grouped output projection
+
+def test_out_proj_equals_one_block_diagonal_product():
+    """Grouping heads u*n_h/g .. (u+1)*n_h/g - 1 with their own W_down^[u] is one product of the
+    flattened O with the block-diagonal matrix diag(W_down^[1], .., W_down^[g])."""
+    from scipy.linalg import block_diag
+    rng = np.random.default_rng(5)
+    T, n_h, d_h, g, r_o = 7, 6, 4, 3, 5
+    Oa = rng.standard_normal((T, n_h, d_h))
+    Wd = rng.standard_normal((g, r_o, (n_h // g) * d_h))
+    z, y = O.out_proj(Oa, Wd)
+    assert y is None
+    dense = block_diag(*[Wd[u].T for u in range(g)])            # [n_h d_h, g r_o]
+    np.testing.assert_allclose(z, Oa.reshape(T, n_h * d_h) @ dense, rtol=1e-12, atol=1e-12)
+
+
+def test_out_proj_tiny_by_hand_and_bf16_intermediate():
+    """n_h = 4 heads of d_h = 1, g = 2, r_o = 1: z = (1*1 + 2*10, 3*100 + 4*1000) = (21, 4300);
+    z is held in bf16 (4300 -> 4288, the bf16 spacing at 4096 is 32) before Proj."""
+    Oa = np.array([[[1.0], [2.0], [3.0], [4.0]]])
+    Wd = np.array([[[1.0, 10.0]], [[100.0, 1000.0]]])
+    Wp = np.array([[1.0, 1.0], [2.0, -1.0]])
+    z, y = O.out_proj(Oa, Wd, Wp)
+    np.testing.assert_array_equal(z, [[21.0, 4300.0]])
+    np.testing.assert_array_equal(y, [[21.0 + 4288.0, 42.0 - 4288.0]])
+
+
+def test_out_proj_page_configuration():
+    """Flash: n_h = 64 heads of d_h = 512, g = 8, r_o = 1024, hidden 4096: each W_down^[u] is
+    (n_h/g) d_h x r_o = 4096 x 1024, and the two products have equal work per token."""
+    with open(os.path.join(HERE, "golden", "page_numbers.json")) as f:
+        c = next(x for x in json.load(f)["cases"] if x["id"] == "out_proj_flash")
+    K = c["n_h"] // c["g"] * c["d_h"]
+    assert K == c["w_down_rows"] and c["r_o"] == c["w_down_cols"]
+    assert c["n_h"] * c["d_h"] * c["r_o"] == c["g"] * c["r_o"] * c["hidden"]
