@@ -92,7 +92,7 @@ typedef enum {
  * Ca, Za: bf16 [B, T, d].  Cb, Zb: bf16 [B, T, d] when overlap = 1, else ignored (may be NULL).
  * bias_a, bias_b: fp32 [m, d] or NULL (zero).  gamma: fp32 [d] or NULL (one).
  * out: bf16 [B, N, d].
- * Supported: d % 64 == 0 and 64 <= d <= 1024; 1 <= m <= 256; rope_dims even and <= d;
+ * Supported: d a power of two in [64, 1024]; 1 <= m <= 256; rope_dims even and <= d;
  * out_fmt CSA_FMT_BF16.
  * ------------------------------------------------------------------------------------------- */
 enum { CSA_COMPRESS_NORM = 1u, CSA_COMPRESS_ROPE = 2u };
@@ -284,7 +284,7 @@ csa_status hca_attend(const csa_attend_desc* desc, const void* q, const void* kv
  * bufs->kv: bf16 [B, N_cap, d]; bufs->kI: bf16 [B, N_cap, dI] (dI > 0); bufs->win: bf16
  *     [B, Wcap, d]; bufs->state: csa_cache_state_bytes(desc) bytes, zero or as left by the
  *     previous append (opaque; a copy of it and of win taken at token t restores the cache to t).
- * Requires (t0+n)/m <= N_cap, t0 + n < 2^31.  Widths as csa_compress (d, dI multiples of 64 in
+ * Requires (t0+n)/m <= N_cap, t0 + n < 2^31.  Widths as csa_compress (d, dI powers of two in
  * [64, 1024]).  Invalid arguments return CSA_ERR_INVALID_ARG / CSA_ERR_UNSUPPORTED before any
  * launch; n = 0 or B = 0 is a no-op.
  * ------------------------------------------------------------------------------------------- */

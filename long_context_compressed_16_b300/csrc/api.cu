@@ -36,13 +36,17 @@ bool make_rope(int r, float theta, const float* inv_freq, csa::RopeParams* rp) {
 
 void count(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
 
+// Compressor row widths: a power of two in [64, 1024], so an entry's d/8 threads form a
+// power-of-two group for the RMSNorm reduction.
+inline bool compress_width_ok(int w) { return w >= 64 && w <= 1024 && (w & (w - 1)) == 0; }
+
 csa_status cache_desc_check(const csa_cache_desc* d) {
   if (!d) return CSA_ERR_INVALID_ARG;
   if (d->B < 0 || d->m < 1 || d->m > 256 || d->Wcap < 1 || d->N_cap < 0 || !(d->eps >= 0.f))
     return CSA_ERR_INVALID_ARG;
-  if (d->d < 64 || d->d > 1024 || (d->d % 64) != 0) return CSA_ERR_UNSUPPORTED;
+  if (!compress_width_ok(d->d)) return CSA_ERR_UNSUPPORTED;
   if (d->dI < 0) return CSA_ERR_INVALID_ARG;
-  if (d->dI != 0 && (d->dI < 64 || d->dI > 1024 || (d->dI % 64) != 0 || !d->overlap)) return CSA_ERR_UNSUPPORTED;
+  if (d->dI != 0 && (!compress_width_ok(d->dI) || !d->overlap)) return CSA_ERR_UNSUPPORTED;
   if (d->rope_dims < 0 || d->rope_dims > d->d || (d->rope_dims % 8) != 0 || d->rope_dims > 2 * csa::kMaxRopePairs)
     return CSA_ERR_UNSUPPORTED;
   if (d->index_flags & CSA_COMPRESS_ROPE) return CSA_ERR_UNSUPPORTED;
@@ -242,7 +246,7 @@ csa_status csa_compress(const csa_compress_desc* d, const void* Ca, const void* 
                         void* out, csa_stream_t stream) {
   if (!d) return CSA_ERR_INVALID_ARG;
   if (d->B < 0 || d->T < 0 || d->m < 1 || d->m > 256) return CSA_ERR_INVALID_ARG;
-  if (d->d < 64 || d->d > 1024 || (d->d % 64) != 0) return CSA_ERR_UNSUPPORTED;
+  if (!compress_width_ok(d->d)) return CSA_ERR_UNSUPPORTED;
   if (d->rope_dims < 0 || d->rope_dims > d->d || (d->rope_dims % 8) != 0 ||
       d->rope_dims > 2 * csa::kMaxRopePairs)
     return CSA_ERR_UNSUPPORTED;

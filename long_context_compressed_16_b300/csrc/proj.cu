@@ -9,8 +9,8 @@
 // group u holds column n of the group's matrix), C written in bf16 with fp32 accumulation.  The
 // grouped product is A = O viewed as [T][g][(n_h/g) d_h]; Proj is the same GEMM with one group.
 //
-// Persistent kernel, one CTA per SM, 128 x BN output tiles (n fastest, then the group, then m, so
-// CTAs working at the same time share their activation panel in L2):
+// Persistent kernel, one CTA per SM, 128 x BN output tiles (n fastest, then m, then the group, so
+// CTAs working at the same time share their activation panel and their group's weights in L2):
 //   warp 0      TMA producer: one 128 x 64 activation tile and one BN x 64 weight tile per stage
 //               (128-byte swizzle) into a 4..8-stage ring
 //   warp 1      one thread issues tcgen05.mma (M = 128, N = BN, K = 16) into one of two TMEM
@@ -62,15 +62,17 @@ struct GemmArgs {
   int32_t* status;
 };
 
-// Tile t -> (m tile, group, n tile).  Default order: n fastest, then the group, then m, so CTAs
-// working at the same time share an activation panel.  SWAP: m (the few activation rows) fastest.
+// Tile t -> (m tile, group, n tile).  Default order: n fastest, then m, then the group: CTAs
+// working at the same time share an activation panel (its n tiles run side by side), and one
+// group's weights stay in L2 while all its activation panels stream past once.  SWAP: m (the
+// few activation rows) fastest.
 template <bool SWAP>
 __device__ __forceinline__ void tile_coords(const GemmArgs& a, long long t, int& mt, int& g, int& nt) {
   if (!SWAP) {
     nt = static_cast<int>(t % a.tiles_n);
     const long long r = t / a.tiles_n;
-    g = static_cast<int>(r % a.G);
-    mt = static_cast<int>(r / a.G);
+    mt = static_cast<int>(r % a.tiles_m);
+    g = static_cast<int>(r / a.tiles_m);
   } else {
     mt = static_cast<int>(t % a.tiles_m);
     const long long r = t / a.tiles_m;

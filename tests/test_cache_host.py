@@ -68,7 +68,7 @@ def test_cache_state_bytes():
     assert C.csa_cache_state_bytes(_desc(dI=0, m=128, overlap=0)) == 2 * 2 * 128 * 512 * 2
     # ring sizes round up to 256 bytes each
     assert C.csa_cache_state_bytes(_desc(B=1, d=64, dI=0, m=1, rope_dims=0)) == 4 * 256
-    for bad in (dict(d=100), dict(dI=96), dict(m=0), dict(Wcap=0), dict(overlap=0),   # indexer needs overlap
+    for bad in (dict(d=100), dict(d=384), dict(dI=96), dict(dI=192), dict(m=0), dict(Wcap=0), dict(overlap=0),   # indexer needs overlap
                 dict(index_flags=C.CSA_COMPRESS_ROPE), dict(rope_dims=6), dict(eps=-1.0)):
         assert C.csa_cache_state_bytes(_desc(**bad)) == 0, bad
 

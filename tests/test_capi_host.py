@@ -79,6 +79,7 @@ def test_compress_validation():
                                                 p.get("out", FAKE), None)
     assert call(_cdesc(d=100)) == C.CSA_ERR_UNSUPPORTED
     assert call(_cdesc(d=2048)) == C.CSA_ERR_UNSUPPORTED
+    assert call(_cdesc(d=192)) == C.CSA_ERR_UNSUPPORTED     # widths are powers of two (norm reduction)
     assert call(_cdesc(m=0)) == C.CSA_ERR_INVALID_ARG
     assert call(_cdesc(rope_dims=60)) == C.CSA_ERR_UNSUPPORTED
     assert call(_cdesc(out_fmt=C.CSA_FMT_FP8_MIXED)) == C.CSA_ERR_UNSUPPORTED
