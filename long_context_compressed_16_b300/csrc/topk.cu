@@ -30,6 +30,13 @@ constexpr int kMergeCap = 16384;     // candidates one merge CTA holds (keys + i
 #define CSA_TOPK_TARGET_CTAS 128
 #endif
 
+#ifndef CSA_TOPK_CLUSTER
+#define CSA_TOPK_CLUSTER 1           // rows of 2..8 slices: one cluster per row instead of slices + merge
+#endif
+#ifndef CSA_TOPK_CLUSTER_LONG
+#define CSA_TOPK_CLUSTER_LONG 1      // rows of more than 8 two-stage slices: 8 longer slices in a cluster
+#endif
+constexpr int kClusterMax = 8;       // portable cluster size
 constexpr int kTargetCtas = CSA_TOPK_TARGET_CTAS;   // split rows until the first stage has about this many CTAs
 constexpr int kMergeRounds = 16;     // 32-candidate rounds per merge warp (registers per thread)
 constexpr int kDigit = 8;
@@ -317,6 +324,270 @@ __global__ void __launch_bounds__(NT) k_topk_slice(TopkArgs a, int S, int slice_
   });
 }
 
+// ------------------------------------------------------------------ one-stage cluster selection
+// A row of S <= 8 slices is selected by one thread-block cluster of S CTAs (CTA r = slice r)
+// instead of slices plus a merge: every radix pass adds the slices' local histograms through
+// distributed shared memory, so all CTAs see the row's histogram and take the same decisions.
+// Each CTA then counts its keys above the threshold and its ties, the CTAs exchange these counts,
+// and each writes its selected entries at its own offset of the output row (lower slices first,
+// so the row stays in increasing index order; ties go to the lower slices first, then to the
+// smaller index inside a slice).  Same result as the two-stage path.
+//
+// The cluster barriers are hardware barriers that every thread of every CTA reaches the same
+// number of times: the pass decisions come from the same summed histogram in every CTA, and no
+// CTA leaves before the last barrier (not even on a failed range check, which only empties its
+// slice), so no wait depends on a peer taking another path.
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Words at the same shared-memory offset as `p` in CTA `rank` of this cluster.  The loads carry
+// no memory clobber, so a lane's independent remote loads are all in flight together; they stay
+// between the cluster barriers around them because those are volatile asm with a memory clobber.
+__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
+  const uint32_t la = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(rank));
+  return ra;
+}
+__device__ __forceinline__ uint32_t ld_peer(const uint32_t* p, uint32_t rank) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(peer_addr(p, rank)));
+  return v;
+}
+__device__ __forceinline__ uint4 ld_peer4(const uint32_t* p, uint32_t rank) {   // p 16-byte aligned
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(peer_addr(p, rank)));
+  return v;
+}
+
+size_t cluster_smem(int cap) {
+  return static_cast<size_t>(cap) * 4 + 2 * kBins * 4 + 64 * 4 + 34 * 8 + 8 * 4 + 4 * 4;
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NT) k_topk_cluster(TopkArgs a, int S, int slice_len, int cap) {
+  extern __shared__ __align__(16) uint32_t tsm[];
+  grid_dep_wait();
+  grid_dep_launch();
+  TkSmem sm;
+  sm.keys = tsm;
+  sm.idx = nullptr;
+  uint32_t* hist2 = tsm + cap;                                  // [2][kBins], one per pass parity
+  sm.hist = hist2;
+  sm.red = hist2 + 2 * kBins;
+  sm.ws = reinterpret_cast<unsigned long long*>(sm.red + 64);
+  sm.xchg = reinterpret_cast<uint32_t*>(sm.ws + 34);
+  uint32_t* pub = sm.xchg + 8;                                  // [0..1] key max / min, [2..3] counts
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t rank = cluster_rank();
+  const long long qrel = blockIdx.x / S;                        // a cluster = S consecutive blocks
+  const long long qi = a.q_begin + qrel;
+  const int n = n_visible(a.q_pos[qi], a.m, a.N);
+  const int k = a.k;
+  int32_t* out = a.idx_out + qi * k;
+  if (n <= k) {                      // the same in every CTA of the cluster: no selection, no barrier
+    if (rank == 0)
+      for (int i = tid; i < k; i += NT) out[i] = i < n ? i : -1;
+    return;
+  }
+  const int lo = static_cast<int>(rank) * slice_len;
+  int L = max(0, min(n, lo + slice_len) - lo);
+  if (L > cap) {                     // cannot happen with a valid launch; the CTA still takes part
+    if (tid == 0) report_error(a.status, CSA_ERR_DEVICE_CHECK, L);
+    L = 0;
+  }
+  for (int i = tid; i < 2 * kBins; i += NT) hist2[i] = 0u;
+  const float* row = a.scores + (qi - a.score_row_offset) * static_cast<long long>(a.N);
+  uint32_t kmax = 0u, kmin = 0xFFFFFFFFu;
+  load_keys<NT>(sm.keys, row + lo, L, kmax, kmin);
+  block_minmax<NT>(sm, kmax, kmin);
+  if (tid == 0) {
+    pub[0] = kmax;
+    pub[1] = kmin;
+  }
+  cluster_barrier();                                            // keys, zeroed histograms, max / min
+  if (warp == 0) {                       // lane r reads CTA r's pair; one warp reduction
+    uint32_t mx = 0u, mn = 0xFFFFFFFFu;
+    if (lane < S) {
+      mx = ld_peer(&pub[0], lane);
+      mn = ld_peer(&pub[1], lane);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    }
+    if (lane == 0) {
+      sm.xchg[0] = mx;
+      sm.xchg[1] = mn;
+    }
+  }
+  __syncthreads();
+  const uint32_t gmax = sm.xchg[0], gmin = sm.xchg[1];
+
+  int pos = (gmax == gmin) ? 0 : 32 - __clz(gmax ^ gmin);
+  uint32_t prefix = pos >= 32 ? 0u : (gmax >> pos) << pos;
+  int remaining = k;
+  int cmp_shift = pos;
+  int buf = 0;
+  while (pos > 0) {
+    const int nbits = pos < kDigit ? pos : kDigit;
+    const int shift = pos - nbits;
+    const uint32_t dmask = (1u << nbits) - 1u;
+    const uint32_t hmask = pos >= 32 ? 0u : ~((1u << pos) - 1u);
+    uint32_t* hist = hist2 + buf * kBins;
+    for (int i = tid; i < L; i += NT) {
+      const uint32_t kk = sm.keys[i];
+      if ((kk & hmask) == prefix) atomicAdd(&hist[(kk >> shift) & dmask], 1u);
+    }
+    cluster_barrier();                                          // every slice's histogram of this pass
+    if (warp == 0) {
+      const int nb = 1 << nbits;
+      uint32_t c[kBinsPerLane];
+      uint32_t csum = 0;
+      // lane's bins nb-1-8*lane-u (u = 0..7) are the 8 consecutive words from lo8 = nb-8-8*lane;
+      // sums run over the CTAs in fixed order, so every CTA gets the same counts
+#pragma unroll
+      for (int u = 0; u < kBinsPerLane; ++u) c[u] = 0u;
+      const int lo8 = nb - kBinsPerLane * (lane + 1);
+      if (lo8 >= 0) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {                  // 4 bins at a time: all CTAs' loads in flight
+          uint4 v[kClusterMax];
+#pragma unroll
+          for (int r = 0; r < kClusterMax; ++r)
+            if (r < S) v[r] = ld_peer4(&hist[lo8 + 4 * h], r);
+#pragma unroll
+          for (int r = 0; r < kClusterMax; ++r) {
+            if (r < S) {
+              c[7 - 4 * h] += v[r].x; c[6 - 4 * h] += v[r].y;
+              c[5 - 4 * h] += v[r].z; c[4 - 4 * h] += v[r].w;
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < kBinsPerLane; ++u) {
+          const int bin = nb - 1 - (kBinsPerLane * lane + u);
+          if (bin >= 0)
+            for (int r = 0; r < S; ++r) c[u] += ld_peer(&hist[bin], r);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kBinsPerLane; ++u) csum += c[u];
+      // the other parity's histogram was last read by the peers before they reached this
+      // pass's barrier: clear it for the next pass
+      uint32_t* other = hist2 + (buf ^ 1) * kBins;
+      for (int i = lane; i < kBins; i += 32) other[i] = 0u;
+      uint32_t incl = csum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      uint32_t above = incl - csum;
+      const uint32_t rem = static_cast<uint32_t>(remaining);
+#pragma unroll
+      for (int u = 0; u < kBinsPerLane; ++u) {
+        if (above < rem && rem <= above + c[u]) {
+          sm.xchg[2] = static_cast<uint32_t>(nb - 1 - (kBinsPerLane * lane + u));
+          sm.xchg[3] = rem - above;
+          sm.xchg[4] = c[u];
+        }
+        above += c[u];
+      }
+    }
+    __syncthreads();
+    prefix |= (sm.xchg[2] & dmask) << shift;
+    remaining = static_cast<int>(min(sm.xchg[3], static_cast<uint32_t>(remaining)));
+    const uint32_t bin_count = sm.xchg[4];
+    pos = shift;
+    cmp_shift = shift;
+    buf ^= 1;
+    if (bin_count == static_cast<uint32_t>(remaining)) break;
+  }
+
+  // this slice's keys above the threshold (gt) and in it (eq), per warp and in total
+  const uint32_t thr = cmp_shift >= 32 ? 0u : prefix >> cmp_shift;
+  constexpr int NW = NT / 32;
+  const int per_w = ((L + NW - 1) / NW + 31) & ~31;
+  const int w_lo = min(L, warp * per_w), w_hi = min(L, w_lo + per_w);
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  uint32_t gt = 0, eq = 0;
+  for (int base = w_lo; base < w_hi; base += 32) {
+    const int i = base + lane;
+    uint32_t kt = 0;
+    const bool in = i < w_hi;
+    if (in) kt = cmp_shift >= 32 ? 0u : sm.keys[i] >> cmp_shift;
+    gt += __popc(__ballot_sync(0xffffffffu, in && kt > thr));
+    eq += __popc(__ballot_sync(0xffffffffu, in && kt == thr));
+  }
+  unsigned long long tot;
+  const unsigned long long ex = block_excl_scan(lane == 0 ? (static_cast<unsigned long long>(gt) << 32) | eq : 0ull,
+                                                sm.ws, &tot);
+  if (tid == 0) {
+    pub[2] = static_cast<uint32_t>(tot >> 32);
+    pub[3] = static_cast<uint32_t>(tot & 0xFFFFFFFFu);
+  }
+  cluster_barrier();                                            // every slice's counts
+  const uint32_t rem = static_cast<uint32_t>(remaining);
+  if (warp == 0) {
+    // lane r < rank reads CTA r's counts.  Ties are taken greedily from the lowest slice, so the
+    // lower slices together take min(their ties, rem) of them: this slice's output offset is
+    // (their entries above the threshold) + min(their ties, rem)
+    uint32_t g = 0u, e = 0u;
+    if (static_cast<uint32_t>(lane) < rank) {
+      g = ld_peer(&pub[2], lane);
+      e = ld_peer(&pub[3], lane);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      g += __shfl_xor_sync(0xffffffffu, g, o);
+      e += __shfl_xor_sync(0xffffffffu, e, o);
+    }
+    if (lane == 0) {
+      sm.xchg[5] = g + min(e, rem);
+      sm.xchg[6] = e;
+    }
+  }
+  __syncthreads();
+  const uint32_t out_base = sm.xchg[5], eq_lower = sm.xchg[6];
+  const uint32_t my_eq = static_cast<uint32_t>(tot & 0xFFFFFFFFu);
+  const uint32_t my_rem = rem > eq_lower ? min(rem - eq_lower, my_eq) : 0u;   // ties this slice takes
+  const unsigned long long exw = __shfl_sync(0xffffffffu, ex, 0);
+  uint32_t g_before = static_cast<uint32_t>(exw >> 32);
+  uint32_t e_before = static_cast<uint32_t>(exw & 0xFFFFFFFFu);
+  for (int base = w_lo; base < w_hi; base += 32) {
+    const int i = base + lane;
+    uint32_t kt = 0;
+    const bool in = i < w_hi;
+    if (in) kt = cmp_shift >= 32 ? 0u : sm.keys[i] >> cmp_shift;
+    const uint32_t mg = __ballot_sync(0xffffffffu, in && kt > thr);
+    const uint32_t me = __ballot_sync(0xffffffffu, in && kt == thr);
+    const uint32_t g_rank = g_before + __popc(mg & lt_mask);
+    const uint32_t e_rank = e_before + __popc(me & lt_mask);
+    bool take = false;
+    if (in && kt > thr) take = true;
+    if (in && kt == thr) take = e_rank < my_rem;
+    if (take) {
+      const uint32_t j = out_base + g_rank + min(e_rank, my_rem);
+      if (j < static_cast<uint32_t>(k)) out[j] = lo + i;
+    }
+    g_before += __popc(mg);
+    e_before += __popc(me);
+  }
+  cluster_barrier();                         // no CTA leaves while a peer may still read its counts
+}
+
 // Stage 2: one CTA per query merges the S * k candidates of its slices.
 template <int NT>
 __global__ void __launch_bounds__(NT) k_topk_merge(TopkArgs a, int S, int cap, const unsigned long long* cand) {
@@ -437,10 +708,56 @@ cudaError_t launch_merge(const TopkArgs& a, int S, int cap, const unsigned long 
   return launch_k(k_topk_merge<NT>, dim3(static_cast<unsigned>(a.q_count)), dim3(NT), smem, s, a, S, cap, cand);
 }
 
+// One cluster of S CTAs per query (S <= 8).  Returns cudaErrorNotSupported, before launching,
+// when the device cannot hold such a cluster.
+template <int NT>
+cudaError_t launch_cluster(const TopkArgs& a, int S, int len, cudaStream_t s) {
+  const size_t smem = cluster_smem(len);
+  cudaError_t e = cudaFuncSetAttribute(k_topk_cluster<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.q_count) * S);
+  cfg.blockDim = dim3(NT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(S);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, k_topk_cluster<NT>, &cfg);
+  if (e != cudaSuccess) return e;
+  if (clusters < 1) return cudaErrorNotSupported;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k_topk_cluster<NT>, a, S, len, len);
+}
+
 cudaError_t launch_topk(const TopkArgs& a, void* cand_ws, cudaStream_t s, int* launches) {
   if (a.q_count == 0) return cudaSuccess;
   const int len = topk_slice_len(a.q_count, a.N, a.k);
   const int S = topk_slices(a.q_count, a.N, a.k);
+  if (S > 1 && CSA_TOPK_CLUSTER && a.N <= kClusterMax * kSlice) {
+    // one-stage selection by a cluster per query (at most 8 slices: rows cut for the two-stage
+    // path into more are re-cut into 8 of at most 32768); falls through to the two stages only
+    // when the device cannot hold the cluster (the result is the same either way)
+    int cl_len = len, cl_S = S;
+    if (S > kClusterMax && CSA_TOPK_CLUSTER_LONG) {
+      cl_len = ((a.N + kClusterMax - 1) / kClusterMax + kMinSlice - 1) / kMinSlice * kMinSlice;
+      cl_S = (a.N + cl_len - 1) / cl_len;
+    }
+    const cudaError_t e = cl_S <= kClusterMax ? launch_cluster<1024>(a, cl_S, cl_len, s) : cudaErrorNotSupported;
+    if (e != cudaErrorNotSupported) {
+      ++*launches;
+      return e;
+    }
+    (void)cudaGetLastError();
+  }
   if (S > 1 && (cand_ws == nullptr || static_cast<long long>(S) * a.k > kMergeCap)) return cudaErrorInvalidValue;
   const int cap1 = S == 1 ? ((a.N + 3) & ~3) : len;
   unsigned long long* cand = static_cast<unsigned long long*>(cand_ws);
