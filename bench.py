@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--prefill-steps", type=int, default=3)
     ap.add_argument("--lowp", action="store_true",
                     help="FP8 workloads: the low-precision indexer (query quantised to e4m3, FP8 tensor cores)")
+    ap.add_argument("--case", choices=["compress", "out_proj"], default=None,
+                    help="time one library call on a profiler-sized input and exit (no contract line)")
+    ap.add_argument("--case-tokens", type=int, default=65536, help="tokens of the --case input")
     ap.add_argument("--quick", action="store_true",
                     help="time exactly one block of K steps; no clock sampling, e2e or CPU leg (for profilers)")
     return ap.parse_args()
@@ -647,8 +650,51 @@ def run_ours(args):
     print(json.dumps(line))
 
 
+def run_case(args):
+    """One library call on a small input, repeated: the command the ncu summaries under profiles/
+    capture.  compress: the CSA main-stream compressor (T tokens of four [T, 512] bf16 streams);
+    out_proj: the grouped output projection at Flash widths (O [T, 64, 512])."""
+    import torch
+    from long_context_compressed_16_b300 import pipeline as P
+    from long_context_compressed_16_b300 import synth as S
+    dev = torch.device("cuda", 0)
+    T = args.case_tokens
+    if args.case == "compress":
+        x = {n: S.normal_bf16((1, T, 512), 3, S.TID[n], dev) for n in ("Ca", "Cb", "Za", "Zb")}
+        out = torch.empty((1, T // 4, 512), dtype=torch.bfloat16, device=dev)
+        fn = lambda: P.compress(x["Ca"], x["Za"], 4, Cb=x["Cb"], Zb=x["Zb"], out=out)
+        byts = 4 * T * 512 * 2 + (T // 4) * 512 * 2
+        unit = ("GB/s", lambda ms: byts / (ms * 1e-3) / 1e9)
+    else:
+        n_h, d_h, g, r_o, d_out = 64, 512, 8, 1024, 4096
+        K = n_h // g * d_h
+        Oa = S.normal_bf16((T, n_h, d_h), 5, S.TID["O"], dev)
+        Wd = S.weight_bf16((g, r_o, K), 5, S.TID["W_down"], K, dev)
+        Wp = S.weight_bf16((d_out, g * r_o), 5, S.TID["W_proj"], g * r_o, dev)
+        z = torch.empty((T, g * r_o), dtype=torch.bfloat16, device=dev)
+        y = torch.empty((T, d_out), dtype=torch.bfloat16, device=dev)
+        ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+        fn = lambda: P.out_proj(Oa, Wd, g, W_proj=Wp, z=z, y=y, workspace=ws)
+        flops = 2.0 * T * (n_h * d_h * r_o + g * r_o * d_out)
+        unit = ("TFLOP/s", lambda ms: flops / (ms * 1e-3) / 1e12)
+    for _ in range(max(1, args.warmup)):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(max(1, args.steps)):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / max(1, args.steps)
+    print(json.dumps({"case": args.case, "tokens": T, "ms_per_call": ms, unit[0]: unit[1](ms)}), flush=True)
+
+
 def main():
     args = parse()
+    if args.case is not None:
+        run_case(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

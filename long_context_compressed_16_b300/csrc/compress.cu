@@ -211,13 +211,16 @@ __global__ void __launch_bounds__(256) k_compress(CompressArgs a, int RS, int EP
     const __nv_bfloat16* rCb = static_cast<const __nv_bfloat16*>(a.ring.Cb);
     auto fetch = [&](int r, uint4& zv, uint4& cv) {
       const bool isb = r >= 4;
-      const long long tok = isb ? 4LL * (i - 1) + (r - 4) : 4LL * i + r;
+      // token indices stay below 2^31 (checked by the host), so 32-bit arithmetic: a 64-bit
+      // remainder is a long software sequence on the GPU
+      const int tok = isb ? 4 * (i - 1) + (r - 4) : 4 * i + r;
       if (tok >= a.t0) {
         const size_t off = (static_cast<size_t>(b) * a.T + (tok - a.t0)) * d + c0;
         zv = ldg_nc((isb ? Zb : Za) + off);
         cv = ldg_nc((isb ? Cb : Ca) + off);
       } else {
-        const size_t off = (static_cast<size_t>(b) * a.ring.R + tok % a.ring.R) * d + c0;
+        const uint32_t slot = static_cast<uint32_t>(tok) % static_cast<uint32_t>(a.ring.R);
+        const size_t off = (static_cast<size_t>(b) * a.ring.R + slot) * d + c0;
         zv = ldg_nc((isb ? rZb : rZa) + off);
         cv = ldg_nc((isb ? rCb : rCa) + off);
       }
@@ -251,14 +254,14 @@ __global__ void __launch_bounds__(256) k_compress(CompressArgs a, int RS, int EP
           const int r = r0 + u;
           const bool isb = r >= a.m;
           const int j = isb ? r - a.m : r;
-          const long long tok = isb ? static_cast<long long>(a.m) * (i - 1) + j
-                                    : static_cast<long long>(a.m) * i + j;
+          const int tok = isb ? a.m * (i - 1) + j : a.m * i + j;     // < 2^31 (checked by the host)
           if (tok >= a.t0) {              // a row of this call's chunk
             const size_t off = (static_cast<size_t>(b) * a.T + (tok - a.t0)) * d + c0;
             zv[u] = ldg_nc((isb ? Zb : Za) + off);
             cv[u] = ldg_nc((isb ? Cb : Ca) + off);
           } else {                        // an earlier token: the tail ring, slot tok mod R
-            const size_t off = (static_cast<size_t>(b) * a.ring.R + tok % a.ring.R) * d + c0;
+            const uint32_t slot = static_cast<uint32_t>(tok) % static_cast<uint32_t>(a.ring.R);
+            const size_t off = (static_cast<size_t>(b) * a.ring.R + slot) * d + c0;
             zv[u] = ldg_nc((isb ? rZb : rZa) + off);
             cv[u] = ldg_nc((isb ? rCb : rCa) + off);
           }
