@@ -11,7 +11,10 @@ namespace {
 
 std::atomic<uint64_t> g_launches{0};
 
-constexpr size_t kScoreChunkCap = size_t(256) << 20;   // bytes of fp32 scores per top-k pass
+#ifndef CSA_SCORE_CHUNK_MIB
+#define CSA_SCORE_CHUNK_MIB 256
+#endif
+constexpr size_t kScoreChunkCap = size_t(CSA_SCORE_CHUNK_MIB) << 20;   // bytes of fp32 scores per top-k pass
 #ifndef CSA_ATT_DECODE_SPLIT
 #define CSA_ATT_DECODE_SPLIT 192                        // decode attention slots per split, bf16 rows
 #endif

@@ -28,9 +28,27 @@ __device__ __forceinline__ uint4 ldg_nc(const void* p) {
 // One online-softmax step over the nr (<= RC) rows in zv / cv (8 channels each, bf16 pairs),
 // with their bias rows (or null).  Both compressor kernels run exactly this code, so their
 // results agree bit for bit.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <int RC>
 __device__ __forceinline__ void softmax_step(const uint4* zv, const uint4* cv, const float* const* bptr, int nr,
                                              float* mx, float* sm, float* acc) {
+  // the rows' biases, 8 channels each, loaded once per row (zero without a bias)
+  float bias[RC][8];
+#pragma unroll
+  for (int u = 0; u < RC; ++u) {
+    float4 b0 = make_float4(0.f, 0.f, 0.f, 0.f), b1 = b0;
+    if (u < nr && bptr[u] != nullptr) {
+      b0 = __ldg(reinterpret_cast<const float4*>(bptr[u]));
+      b1 = __ldg(reinterpret_cast<const float4*>(bptr[u] + 4));
+    }
+    bias[u][0] = b0.x; bias[u][1] = b0.y; bias[u][2] = b0.z; bias[u][3] = b0.w;
+    bias[u][4] = b1.x; bias[u][5] = b1.y; bias[u][6] = b1.z; bias[u][7] = b1.w;
+  }
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     float z[RC], cvals[RC];
@@ -42,28 +60,22 @@ __device__ __forceinline__ void softmax_step(const uint4* zv, const uint4* cv, c
         const uint32_t cw = (&cv[u].x)[c >> 1];
         const float zb = (c & 1) ? bf16hi(zw) : bf16lo(zw);
         cvals[u] = (c & 1) ? bf16hi(cw) : bf16lo(cw);
-        z[u] = (zb + (bptr[u] ? __ldg(bptr[u] + c) : 0.f)) * kLog2e;
+        z[u] = (zb + bias[u][c]) * kLog2e;
         cm = fmaxf(cm, z[u]);
       }
     }
-    const float alpha = (mx[c] == -INFINITY) ? 0.f : exp2f(mx[c] - cm);
+    const float alpha = (mx[c] == -INFINITY) ? 0.f : ex2_approx(mx[c] - cm);
     float s = sm[c] * alpha, ac = acc[c] * alpha;
 #pragma unroll
     for (int u = 0; u < RC; ++u) {
       if (u < nr) {
-        const float p = exp2f(z[u] - cm);
+        const float p = ex2_approx(z[u] - cm);
         s += p;
         ac = fmaf(p, cvals[u], ac);
       }
     }
     mx[c] = cm; sm[c] = s; acc[c] = ac;
   }
-}
-
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
 }
 
 // CSA entry with m = 4 (R = 4 rows for entry 0, 8 otherwise), exact two-pass softmax per channel:
