@@ -36,6 +36,9 @@ constexpr int kMergeCap = 16384;     // candidates one merge CTA holds (keys + i
 #ifndef CSA_TOPK_CLUSTER_LONG
 #define CSA_TOPK_CLUSTER_LONG 1      // rows of more than 8 two-stage slices: 8 longer slices in a cluster
 #endif
+#ifndef CSA_TOPK_CLUSTER_NT
+#define CSA_TOPK_CLUSTER_NT 1024     // threads per CTA of the cluster selection
+#endif
 constexpr int kClusterMax = 8;       // portable cluster size
 constexpr int kTargetCtas = CSA_TOPK_TARGET_CTAS;   // split rows until the first stage has about this many CTAs
 constexpr int kMergeRounds = 16;     // 32-candidate rounds per merge warp (registers per thread)
@@ -751,7 +754,8 @@ cudaError_t launch_topk(const TopkArgs& a, void* cand_ws, cudaStream_t s, int* l
       cl_len = ((a.N + kClusterMax - 1) / kClusterMax + kMinSlice - 1) / kMinSlice * kMinSlice;
       cl_S = (a.N + cl_len - 1) / cl_len;
     }
-    const cudaError_t e = cl_S <= kClusterMax ? launch_cluster<1024>(a, cl_S, cl_len, s) : cudaErrorNotSupported;
+    const cudaError_t e = cl_S <= kClusterMax ? launch_cluster<CSA_TOPK_CLUSTER_NT>(a, cl_S, cl_len, s)
+                                              : cudaErrorNotSupported;
     if (e != cudaErrorNotSupported) {
       ++*launches;
       return e;
