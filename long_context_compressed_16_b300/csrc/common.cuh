@@ -198,7 +198,7 @@ cudaError_t launch_ring_rows(const RingArgs& a, cudaStream_t s, int* launches);
 // B [G][N][K], C [M][G][N]; K and N multiples of 64.
 cudaError_t launch_gemm_tn(const void* A, const void* B, void* C, int M, int N, int K, int G, int32_t* status,
                            cudaStream_t s, int* launches);
-int gemm_tn_tile_n(int M, int N, int G);
+int gemm_tn_tile_n(int M, int N, int K, int G);
 
 struct IndexArgs {
   const void* qI;

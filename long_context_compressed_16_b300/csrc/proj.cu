@@ -35,10 +35,20 @@ constexpr int GBK = 64;    // K elements per stage: one 128-byte swizzled row
 // activation rows (16..64), so the weights, which dominate the traffic, fill whole 128-row tiles
 // and every SM streams its own slice of them.  Either way each output element is one MMA chain
 // over K in the same order (no split of K), so a row's result does not depend on the variant.
+#ifndef CSA_GEMM_SWAP_ATOMS
+#define CSA_GEMM_SWAP_ATOMS 2
+#endif
+
 template <int BN, bool SWAP>
 struct GCfg {
-  static constexpr int A_BYTES = GBM * GBK * 2;
-  static constexpr int B_BYTES = BN * GBK * 2;
+  // K atoms (64 elements, one 128-byte swizzled row each) per stage.  The weight-major variant
+  // loads two, so each weight row is read 256 contiguous bytes at a time; the MMA chain over K
+  // runs in the same order either way.
+  static constexpr int ATOMS = SWAP ? CSA_GEMM_SWAP_ATOMS : 1;
+  static constexpr int ATOM_A = GBM * GBK * 2;
+  static constexpr int ATOM_B = BN * GBK * 2;
+  static constexpr int A_BYTES = ATOMS * ATOM_A;
+  static constexpr int B_BYTES = ATOMS * ATOM_B;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int MAX_STAGES = SWAP ? 12 : 8;
   static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > MAX_STAGES ? MAX_STAGES : (200 * 1024) / STAGE_BYTES;
@@ -140,7 +150,7 @@ k_gemm_tn(const GemmArgs a, const __grid_constant__ CUtensorMap amap, const __gr
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int KB = a.K / GBK;
+  const int KB = a.K / (GBK * C::ATOMS);
 
   auto fail = [&](int where) {
     *abort_flag = 1;
@@ -161,12 +171,18 @@ k_gemm_tn(const GemmArgs a, const __grid_constant__ CUtensorMap amap, const __gr
           if (!tc::mbar_wait(&empty[s], ph ^ 1, abort_flag)) { fail(1); ok = false; break; }
           tc::mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
           unsigned char* st = smem + static_cast<size_t>(s) * C::STAGE_BYTES;
-          if (!SWAP) {     // MMA A side: 128 activation rows; B side: BN weight rows
-            tc::tma_load_3d(st, &amap, kb * GBK, g, mt * GBM, &full[s]);
-            tc::tma_load_3d(st + C::A_BYTES, &bmap, kb * GBK, nt * BN, g, &full[s]);
-          } else {         // MMA A side: 128 weight rows; B side: BN activation rows
-            tc::tma_load_3d(st, &bmap, kb * GBK, nt * GBM, g, &full[s]);
-            tc::tma_load_3d(st + C::A_BYTES, &amap, kb * GBK, g, mt * BN, &full[s]);
+#pragma unroll
+          for (int at = 0; at < C::ATOMS; ++at) {
+            const int kx = (kb * C::ATOMS + at) * GBK;
+            unsigned char* sa = st + at * C::ATOM_A;
+            unsigned char* sb = st + C::A_BYTES + at * C::ATOM_B;
+            if (!SWAP) {   // MMA A side: 128 activation rows; B side: BN weight rows
+              tc::tma_load_3d(sa, &amap, kx, g, mt * GBM, &full[s]);
+              tc::tma_load_3d(sb, &bmap, kx, nt * BN, g, &full[s]);
+            } else {       // MMA A side: 128 weight rows; B side: BN activation rows
+              tc::tma_load_3d(sa, &bmap, kx, nt * GBM, g, &full[s]);
+              tc::tma_load_3d(sb, &amap, kx, g, mt * BN, &full[s]);
+            }
           }
           ++n;
         }
@@ -200,9 +216,11 @@ k_gemm_tn(const GemmArgs a, const __grid_constant__ CUtensorMap amap, const __gr
           const uint32_t aaddr = tc::sptr(smem + static_cast<size_t>(s) * C::STAGE_BYTES);
           const uint32_t baddr = aaddr + C::A_BYTES;
 #pragma unroll
-          for (int k = 0; k < GBK / 16; ++k)          // 32 bytes of K per instruction
-            tc::umma_bf16(dt, tc::umma_desc_sw128(aaddr + k * 32), tc::umma_desc_sw128(baddr + k * 32), idesc,
-                          (kb | k) ? 1u : 0u);
+          for (int at = 0; at < C::ATOMS; ++at)
+#pragma unroll
+            for (int k = 0; k < GBK / 16; ++k)        // 32 bytes of K per instruction
+              tc::umma_bf16(dt, tc::umma_desc_sw128(aaddr + at * C::ATOM_A + k * 32),
+                            tc::umma_desc_sw128(baddr + at * C::ATOM_B + k * 32), idesc, (kb | at | k) ? 1u : 0u);
           tc::umma_commit(&empty[s]);
           issued = true;
           ++n;
@@ -319,8 +337,8 @@ cudaError_t launch_bn(const void* A, const void* B, void* Cout, int M, int N, in
 
 // Tile shape for an M x N x K product over G groups: a negative value -BT selects the swapped
 // variant with BT activation rows per tile (M <= 64 and N a multiple of 128).
-int gemm_tn_tile_n(int M, int N, int G) {
-  if (M <= 64 && N % GBM == 0) return -((M + 15) / 16 * 16);
+int gemm_tn_tile_n(int M, int N, int K, int G) {
+  if (M <= 64 && N % GBM == 0 && K % (GBK * CSA_GEMM_SWAP_ATOMS) == 0) return -((M + 15) / 16 * 16);
   const long long mt = (M + GBM - 1) / GBM;
   const int sms = sms_here();
   if (N % 256 == 0 && mt * G * (N / 256) >= sms) return 256;
@@ -331,7 +349,7 @@ int gemm_tn_tile_n(int M, int N, int G) {
 cudaError_t launch_gemm_tn(const void* A, const void* B, void* Cout, int M, int N, int K, int G, int32_t* status,
                            cudaStream_t s, int* launches) {
   if (M == 0 || N == 0 || G == 0) return cudaSuccess;
-  switch (gemm_tn_tile_n(M, N, G)) {
+  switch (gemm_tn_tile_n(M, N, K, G)) {
     case 256: return launch_bn<256, false>(A, B, Cout, M, N, K, G, status, s, launches);
     case 128: return launch_bn<128, false>(A, B, Cout, M, N, K, G, status, s, launches);
     case 64: return launch_bn<64, false>(A, B, Cout, M, N, K, G, status, s, launches);
