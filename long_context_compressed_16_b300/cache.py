@@ -85,7 +85,17 @@ class LayerCache:
         (CSA: Ca, Cb, Za, Zb, Ca_I, Cb_I, Za_I, Zb_I, win; HCA: Ca, Za, win).  With `snapshots`,
         the chunk is cut at every 128-token boundary it crosses and a checkpoint is stored there
         under its token count.  Returns the entries that closed."""
+        names = (("Ca", "Cb", "Za", "Zb", "Ca_I", "Cb_I", "Za_I", "Zb_I") if self.kind == "csa" else ("Ca", "Za")) + ("win",)
+        missing = [k for k in names if k not in rows]
+        if missing:
+            raise ValueError(f"rows missing: {missing}")
         n = rows["win"].shape[1]
+        for k in names:
+            r = rows[k]
+            width = self.dI if k.endswith("_I") else self.d
+            if (r.dtype != torch.bfloat16 or not r.is_cuda or not r.is_contiguous()
+                    or tuple(r.shape) != (self.B, n, width)):
+                raise ValueError(f"rows[{k!r}] must be a contiguous CUDA bf16 tensor of shape {(self.B, n, width)}")
         if self.t + n > self.cap:
             raise ValueError("cache is full")
         t_first = self.t

@@ -113,11 +113,22 @@ def out_proj(O, W_down, groups, W_proj=None, z=None, y=None, workspace=None, str
     """Grouped output projection.  O: bf16 [T, n_heads, head_dim] (or [B, Tq, H, d]);
     W_down: bf16 [groups, rank, (n_heads/groups) head_dim]; W_proj: bf16 [d_out, groups rank] or
     None.  Returns (z [T, groups rank], y [T, d_out] or None)."""
-    _dev_check(O, W_down, W_proj)
+    _dev_check(O, W_down, W_proj, z, y)
     H, d = O.shape[-2], O.shape[-1]
     T = O.numel() // (H * d)
-    G, rank, _ = W_down.shape
+    G, rank, K = W_down.shape
     d_out = 0 if W_proj is None else W_proj.shape[0]
+    # the library takes plain pointers: every extent it reads or writes is checked here
+    if any(t is not None and t.dtype != torch.bfloat16 for t in (O, W_down, W_proj, z, y)):
+        raise ValueError("out_proj takes bf16 tensors")
+    if G != groups or H % G != 0 or K != (H // G) * d:
+        raise ValueError(f"W_down must be [groups, rank, (n_heads/groups) head_dim] = [{groups}, r, {H // max(groups, 1) * d}]")
+    if W_proj is not None and tuple(W_proj.shape) != (d_out, G * rank):
+        raise ValueError(f"W_proj must be [d_out, groups rank] = [d_out, {G * rank}]")
+    if z is not None and tuple(z.shape) != (T, G * rank):
+        raise ValueError(f"z must be [{T}, {G * rank}]")
+    if y is not None and d_out and tuple(y.shape) != (T, d_out):
+        raise ValueError(f"y must be [{T}, {d_out}]")
     desc = C.csa_out_proj_desc(T=T, n_heads=H, head_dim=d, groups=G, rank=rank, d_out=d_out)
     if z is None:
         z = torch.empty((T, G * rank), dtype=torch.bfloat16, device=O.device)
