@@ -16,7 +16,9 @@
  *     FP8 E4M3.  Host pointers appear only where a comment says HOST.
  *   - The library allocates no memory and keeps no global mutable state: it is re-entrant and
  *     thread-safe.  Scratch memory is a caller-supplied workspace whose size the matching
- *     *_workspace() query returns.
+ *     *_workspace() query returns.  Two documented exceptions: the launch counter read by
+ *     csa_launch_count (instrumentation), and the fixed scratch array of
+ *     csa_index_topk_noalloc.
  *   - Every call only enqueues kernels on `stream` and returns; nothing synchronises.
  *   - Invalid or unsupported descriptors are rejected before any launch.  A failed launch
  *     returns CSA_ERR_CUDA.  Device-detected problems (an index out of range, a bounded wait
