@@ -3,11 +3,15 @@
 // C^Comp equations; HCA path, S and C^Comp equations.)
 //
 // Pure HBM stream: every input row is read exactly once (entry i owns a-block i and b-block i-1),
-// with 16-byte vector loads of 8 channels.  A thread owns 8 channels of one entry and a
-// contiguous run of that entry's rows; the per-channel softmax runs online over chunks of 2 rows
-// (one exp per logit plus one rescale per chunk).  Long blocks (HCA, m' = 128) are split over
-// several row groups whose partial (max, sum, acc) are merged in shared memory in fixed order,
-// so results are deterministic.
+// in 16-byte vectors of 8 channels; a thread owns 8 channels of one entry.
+//   - CSA with m = 4 (the method's ratio): an exact two-pass softmax per channel over the entry's
+//     8 rows (4 for entry 0): the maximum first, then one hardware exp2 per logit (csa4_entry).
+//     Whole sequences run in k_compress_staged, which bulk-copies a block of entries' rows into
+//     shared memory first; cache appends run the same routine in k_compress, so both agree bit
+//     for bit.
+//   - Other cases (HCA, m' = 128; other m): the softmax runs online over chunks of 2 (CSA) or 4
+//     (HCA) rows in k_compress; long blocks are split over row groups whose partial (max, sum,
+//     acc) are merged in shared memory in fixed order, so results are deterministic.
 #include "common.cuh"
 #include "tc.cuh"
 
