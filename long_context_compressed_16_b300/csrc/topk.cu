@@ -2,7 +2,7 @@
 // equation), ties to the smaller entry index.
 //
 // Radix select on order-preserving 32-bit keys of the fp32 scores, one CTA per slice of at most
-// 32768 candidates, everything in that CTA's shared memory (no clusters, no inter-CTA waits).
+// 32768 candidates, the slice's keys in that CTA's shared memory.
 // The first 8-bit digit starts at the highest bit where the slice's largest and smallest keys
 // differ (the bits above are common to all of them), so the histogram spreads over the scores'
 // actual range; each pass narrows the threshold bin, and the search stops once the threshold bin
@@ -12,7 +12,9 @@
 // increasing entry index: entries above the threshold bin and, inside it, the smallest indices
 // first.
 //
-// Rows longer than one slice run in two stages: every slice writes its own top-k (key, index)
+// Rows longer than one slice: up to 8 x 32768 entries, one thread-block cluster per row selects
+// in one stage (k_topk_cluster, below: the slices' histograms are summed over distributed shared
+// memory).  Longer rows run in two stages: every slice writes its own top-k (key, index)
 // candidates in index order, and a merge CTA selects the top-k of the concatenation.  This is
 // exact: an entry of the row's top-k is also in its slice's top-k (with the same smaller-index
 // rule for ties), and the concatenated candidates stay in increasing index order.
