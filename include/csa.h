@@ -188,11 +188,17 @@ csa_status csa_topk(const csa_index_desc* desc, const float* scores, const int32
  *   - Requests whose csa_index_topk_workspace() exceeds CSA_NOALLOC_SCRATCH_BYTES return
  *     CSA_ERR_UNSUPPORTED before any CUDA call (decode at N = 262144 fits up to B = 7; a
  *     prefill chunk fits while Tq * N * 4 bytes, rounded up to 4-query groups, stays under it).
- *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
- *     with that device current and caches it; make that first call before any stream capture.
+ *   - The first call in a CUDA context looks up the array's device address
+ *     (cudaGetSymbolAddress, with the calling thread's current device and context) and caches
+ *     it under the context's unique ID (cuCtxGetId); make that first call before any stream
+ *     capture.  A caller's own context, or the primary context created again after
+ *     cudaDeviceReset, gets a lookup of its own.
  *   - Every call on a device shares the one array and it keeps the last call's contents: calls
  *     that may overlap on the GPU (other streams, other threads) race and must be serialised by
- *     the caller.  The status word in the array is not readable by the caller.
+ *     the caller.  Each call zeroes the array's status word on `stream` (an 8-byte
+ *     cudaMemsetAsync) before its kernels.  The caller cannot read that word, so this call
+ *     cannot report device-detected problems (an index out of range, a bounded wait that gave
+ *     up); a caller that needs them uses csa_index_topk with its own workspace.
  * Errors are otherwise those of csa_index_topk.
  * ------------------------------------------------------------------------------------------- */
 #define CSA_NOALLOC_SCRATCH_BYTES (8u << 20)

@@ -1,6 +1,6 @@
 """Builds libcsa.so (the C-ABI library) in-tree with nvcc for sm_103a.
 
-    python -m long_context_compressed_16_b300.build [--verbose]
+    python -m long_context_compressed_16_b300.build [--verbose] [--force]
 """
 from __future__ import annotations
 
@@ -23,25 +23,42 @@ def nvcc() -> str:
     return "nvcc"
 
 
+def _run(cmd):
+    return subprocess.run(cmd, capture_output=True, text=True)
+
+
 def build(verbose: bool = False, force: bool = False) -> str:
+    """Compiles every source to an object file (in parallel, one nvcc per file) and links the
+    shared library.  Skips the work when the library is newer than every source and header."""
     srcs = [os.path.join(CSRC, s) for s in SOURCES]
     deps = srcs + [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "tc.cuh"), os.path.join(ROOT, "include", "csa.h")]
     if not force and os.path.exists(LIB):
         t = os.path.getmtime(LIB)
         if all(os.path.getmtime(p) <= t for p in deps):
             return LIB
-    cmd = [nvcc(), "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC", *ARCH,
-           "-I", os.path.join(ROOT, "include"), "-o", LIB + ".tmp", *srcs, "-lcudart"]
+    objdir = os.path.join(PKG, "_build")
+    os.makedirs(objdir, exist_ok=True)
+    common = [nvcc(), "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", *ARCH, "-I", os.path.join(ROOT, "include")]
     if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    r = subprocess.run(cmd, capture_output=True, text=True)
+        common.insert(1, "-Xptxas=-v")
+    objs = [os.path.join(objdir, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    headers = deps[len(srcs):]
+    stale = [(s, o) for s, o in zip(srcs, objs)
+             if force or not os.path.exists(o) or any(os.path.getmtime(p) > os.path.getmtime(o) for p in [s, *headers])]
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=max(1, min(len(stale), os.cpu_count() or 4))) as ex:
+        results = list(ex.map(_run, [common + ["-c", s, "-o", o] for s, o in stale]))
+    for (s, _), r in zip(stale, results):
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {os.path.basename(s)}:\n" + r.stdout + r.stderr)
+        if verbose:
+            sys.stderr.write(f"== {os.path.basename(s)}\n" + r.stdout + r.stderr)
+    r = _run([nvcc(), "-shared", *ARCH, "-o", LIB + ".tmp", *objs, "-lcudart"])
     if r.returncode != 0:
-        raise RuntimeError("nvcc failed:\n" + r.stdout + r.stderr)
-    if verbose:
-        sys.stderr.write(r.stdout + r.stderr)
+        raise RuntimeError("nvcc link failed:\n" + r.stdout + r.stderr)
     os.replace(LIB + ".tmp", LIB)
     return LIB
 
 
 if __name__ == "__main__":
-    print(build(verbose="--verbose" in sys.argv, force=True))
+    print(build(verbose="--verbose" in sys.argv, force="--force" in sys.argv))

@@ -196,8 +196,30 @@ def csa_index_topk_workspace(desc) -> int:
     return lib.csa_index_topk_workspace(ctypes.byref(desc))
 
 
+def _check_index_tensors(desc, qI, w, kI, kI_scale, q_pos, idx_out, score_out):
+    """The indexer calls take plain pointers: when torch tensors are passed, every extent the
+    library reads or writes is checked against the descriptor first (raw addresses are the
+    caller's responsibility)."""
+    import torch
+    B, Tq, N, nI, dI, k = desc.B, desc.Tq, desc.N, desc.n_heads, desc.head_dim, desc.k
+    fp8 = desc.key_fmt in (CSA_FMT_FP8_ROWSCALE, CSA_FMT_FP8_ROWSCALE_LOWP)
+    want = [("qI", qI, (B, Tq, nI, dI), torch.bfloat16), ("w", w, (B, Tq, nI), torch.float32),
+            ("kI", kI, (B, N, dI), torch.uint8 if fp8 else torch.bfloat16),
+            ("q_pos", q_pos, (B, Tq), torch.int32), ("idx_out", idx_out, (B, Tq, k), torch.int32),
+            ("score_out", score_out, (B, Tq, N), torch.float32)]
+    if fp8:
+        want.append(("kI_scale", kI_scale, (B, N), torch.float32))
+    for name, t, shape, dtype in want:
+        if t is None or isinstance(t, int):
+            continue
+        if tuple(t.shape) != shape or t.dtype != dtype or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name}: expected a contiguous CUDA {dtype} tensor of shape {shape}, "
+                             f"got {t.dtype} {tuple(t.shape)} on {t.device}")
+
+
 def csa_index_topk(desc, qI, w, kI, kI_scale, q_pos, idx_out, score_out, workspace, ws_bytes=None,
                    stream=None) -> int:
+    _check_index_tensors(desc, qI, w, kI, kI_scale, q_pos, idx_out, score_out)
     n = _nbytes(workspace) if ws_bytes is None else ws_bytes
     return lib.csa_index_topk(ctypes.byref(desc), _p(qI), _p(w), _p(kI), _p(kI_scale), _p(q_pos), _p(idx_out),
                               _p(score_out), _p(workspace), n, _stream(stream))
@@ -206,6 +228,7 @@ def csa_index_topk(desc, qI, w, kI, kI_scale, q_pos, idx_out, score_out, workspa
 def csa_index_topk_noalloc(desc, qI, w, kI, kI_scale, q_pos, idx_out, score_out, stream=None) -> int:
     """csa_index_topk without a workspace argument: the library's fixed device scratch array is
     used instead (for callers that cannot allocate device memory; see include/csa.h)."""
+    _check_index_tensors(desc, qI, w, kI, kI_scale, q_pos, idx_out, score_out)
     return lib.csa_index_topk_noalloc(ctypes.byref(desc), _p(qI), _p(w), _p(kI), _p(kI_scale), _p(q_pos),
                                       _p(idx_out), _p(score_out), _stream(stream))
 

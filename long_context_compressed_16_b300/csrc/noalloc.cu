@@ -9,8 +9,12 @@
 // until the process exits; its size is CSA_NOALLOC_SCRATCH_BYTES.
 //
 // The host side never dereferences the array's name: in host code it is only a stand-in, and
-// the real device address comes from cudaGetSymbolAddress, once per device, with that device
-// current.  The address is cached, so later calls make no CUDA call beyond the launches.
+// the real device address comes from cudaGetSymbolAddress with the device current.  That address
+// belongs to one CUDA context (the module is loaded once per context), so the cache is keyed by
+// the context's process-unique ID (cuCtxGetId): a caller's own context, or the new primary
+// context after cudaDeviceReset, gets its own lookup instead of another context's address.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -19,22 +23,57 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_index_scratch[CSA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
 
-// Device address of this device's copy of g_index_scratch (looked up on first use).
+template <typename Fn>
+Fn driver_fn(const char* name, int version) {
+  void* f = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &f, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<Fn>(f);
+}
+
+constexpr int kCacheSlots = 64;
+struct ScratchSlot {
+  unsigned long long ctx_id;
+  void* addr;
+};
+std::mutex g_scratch_mu;
+ScratchSlot g_slots[kCacheSlots] = {};
+int g_next_slot = 0;
+
+// Device address of g_index_scratch in the calling thread's current context.  The first call in
+// a context looks the address up; later calls in that context find it in the cache.
 csa_status scratch_address(void** out) {
+  static const CtxGetCurrentFn get_ctx = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent", 12000);
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId", 12000);
+  if (!get_ctx || !get_id) return CSA_ERR_CUDA;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return CSA_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return CSA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_index_scratch) != cudaSuccess || p == nullptr) return CSA_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) {
+    // no context bound to this thread yet: cudaSetDevice binds (and initialises) the device's
+    // primary context, the one the runtime would use for the launches
+    if (cudaSetDevice(dev) != cudaSuccess) return CSA_ERR_CUDA;
+    if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return CSA_ERR_CUDA;
   }
-  *out = g_scratch_addr[dev];
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return CSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  for (const ScratchSlot& s : g_slots) {
+    if (s.addr != nullptr && s.ctx_id == id) {
+      *out = s.addr;
+      return CSA_OK;
+    }
+  }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_index_scratch) != cudaSuccess || p == nullptr) return CSA_ERR_CUDA;
+  g_slots[g_next_slot] = ScratchSlot{id, p};
+  g_next_slot = (g_next_slot + 1) % kCacheSlots;
+  *out = p;
   return CSA_OK;
 }
 
@@ -49,8 +88,10 @@ extern "C" csa_status csa_index_topk_noalloc(const csa_index_desc* desc, const v
   void* scratch = nullptr;
   const csa_status st = scratch_address(&scratch);
   if (st != CSA_OK) return st;
-  // csa_index_topk clears the status word itself and writes every score it later reads, so the
-  // previous call's contents of the array need no clearing here.
+  // The kernels write every score they later read, so the previous call's scores need no
+  // clearing.  The status word does: csa_index_topk only ever sets it, so it is zeroed on the
+  // stream before each call (the caller cannot read it; see the header).
+  if (cudaMemsetAsync(scratch, 0, 8, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return CSA_ERR_CUDA;
   return csa_index_topk(desc, qI, w, kI, kI_scale, q_pos, idx_out, score_out, scratch,
                         CSA_NOALLOC_SCRATCH_BYTES, stream);
 }

@@ -512,6 +512,37 @@ def test_query_quantisation_scale_and_amax_code():
     assert np.all(zc == 0) and np.all(zs == 1.0)
 
 
+def test_index_scores_lowp_by_hand():
+    """Low-precision indexer scores, computed by hand from the e4m3 format (1 sign, 4 exponent
+    bits with bias 7, 3 mantissa bits; subnormals in units of 2^-9) and the per-(query, head)
+    scale amax/448 ("DeepSeek-V4 技术报告深度解读" 5.4, FP4/FP8 indexer; the I_{t,s} equation).
+
+    head 0: q = (896, 3, 0.3, -10): amax 896 -> scale 2 exactly; q/2 = (448, 1.5, 0.15, -5).
+            0.15 lies in [2^-3, 2^-2), step 2^-6: 0.15 = 9.6 steps -> 10 steps = 0.15625, so the
+            dequantised row is (896, 3, 0.3125, -10).
+    head 1: q = (1, -2, 0.01, 14): amax 14 -> scale 1/32 exactly; q*32 = (32, -64, 0.32, 448).
+            0.32 lies in [2^-2, 2^-1), step 2^-5: 10.24 steps -> 10 = 0.3125, dequantised
+            0.3125/32 = 0.009765625.  (With head 0's scale instead, 0.005 would be subnormal and
+            come back as 3 * 2^-9 * 2 = 0.01171875: the per-row scale is visible.)
+    keys: K_0 = (1, 1, 1, 1), K_1 = (0, 1, -4, 1); weights w = (0.5, 2).
+      s = 0: head 0 889.3125, head 1 13.009765625 -> 0.5*889.3125 + 2*13.009765625 = 470.67578125
+      s = 1: head 0 -8.25 -> ReLU 0, head 1 11.9609375 -> 2*11.9609375 = 23.921875"""
+    qI = np.array([[[[896.0, 3.0, 0.3, -10.0], [1.0, -2.0, 0.01, 14.0]]]])
+    w = np.array([[[0.5, 2.0]]])
+    kI = np.array([[[1.0, 1.0, 1.0, 1.0], [0.0, 1.0, -4.0, 1.0]]])
+    q_pos = [[8]]
+    codes, scale = O.quantize_query_e4m3(qI)
+    np.testing.assert_array_equal(scale[0, 0], np.array([2.0, 1.0 / 32.0], dtype=np.float32))
+    np.testing.assert_array_equal(O.e4m3_to_f64(codes[0, 0, 0]), [448.0, 1.5, 0.15625, -5.0])
+    np.testing.assert_array_equal(O.e4m3_to_f64(codes[0, 0, 1]), [32.0, -64.0, 0.3125, 448.0])
+    got = O.index_scores_lowp(qI, w, kI, q_pos, 4)
+    np.testing.assert_array_equal(got[0, 0], [470.67578125, 23.921875])
+    # the unquantised query gives different scores (0.5*889.3 + 2*13.01 = 470.67 and 23.92):
+    # the quantisation is really applied
+    plain = O.index_scores(qI, w, kI, q_pos, 4)
+    assert plain[0, 0, 0] != got[0, 0, 0] and plain[0, 0, 1] != got[0, 0, 1]
+
+
 # ------------------------------------------------------------------------------------------------ grouped output projection
 
 def test_out_proj_equals_one_block_diagonal_product():
