@@ -12,7 +12,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libcsa.so")
-SOURCES = ["api.cu", "compress.cu", "index_score.cu", "topk.cu", "attend.cu", "noalloc.cu", "selftest.cu", "proj.cu"]
+SOURCES = ["api.cu", "compress.cu", "index_score.cu", "topk.cu", "attend.cu", "attend_tc.cu", "noalloc.cu", "selftest.cu", "proj.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

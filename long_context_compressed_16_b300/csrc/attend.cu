@@ -9,6 +9,10 @@
 // gathered CK at a time with cp.async into a double-buffered shared-memory tile; the heads x keys
 // logits and the heads x d output run on the tensor
 // cores; the softmax is online in the log2 domain and the sink joins the normaliser at the end.
+// bf16 rows: the query enters the logits exactly.  q_hat = inv * RoPE_t(q) (inv the RMSNorm
+// factor), so the unrotated dims are the query's own bf16 bits, the rotated dims a bf16 hi + lo
+// pair (the lo block spans the last r rounded up to 16 dims, zero where nothing is rotated), and
+// inv multiplies the fp32 logit.  The FP8 rows use an fp16 hi + lo split of q_hat instead.
 // Split boundaries sit at fixed multiples of the split size in slot space, never depending on
 // the batch, and splits are merged by a second kernel in fixed order (batch-invariant decode).
 #include "common.cuh"
@@ -29,6 +33,7 @@ struct AttnCfg {
   static constexpr int HG = 16 * NG;                          // heads per CTA
   static constexpr int THREADS = 128 * NG;
   static constexpr int QS = D + 8;                            // padded smem row strides (bf16)
+  static constexpr int LS = 128 + 8;                          // lo block of the rotated dims (r <= 128)
   static constexpr int KS = D + 8;
   static constexpr int PS = CK + 8;
   static constexpr int ROWB = FP8 ? CSA_FP8_MIXED_ROW_BYTES : D * 2;   // global row bytes
@@ -38,7 +43,9 @@ struct AttnCfg {
   static constexpr int NB = FP8 ? D / 64 : 1;
   static constexpr int QPARTS = FP8 ? 2 : 1;
   static constexpr size_t q_off = 0;
-  static constexpr size_t k_off = q_off + size_t(QPARTS) * HG * QS * 2;
+  static constexpr size_t lo_off = q_off + size_t(QPARTS) * HG * QS * 2;
+  static constexpr size_t inv_off = lo_off + (FP8 ? 0 : size_t(HG) * LS * 2);
+  static constexpr size_t k_off = inv_off + (FP8 ? 0 : size_t(HG) * 4);
   static constexpr size_t st_off = k_off + size_t(2) * CK * KS * 2;
   static constexpr size_t p_off = st_off + (FP8 ? size_t(2) * CK * ROWB : 0);
   static constexpr size_t sc_off = p_off + size_t(NB) * HG * PS * 2;
@@ -91,6 +98,8 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
   float* lsum = reinterpret_cast<float*>(smem + C::lsum_off);
   const unsigned char** rowptr = reinterpret_cast<const unsigned char**>(smem + C::ptr_off);
   float2* rope_tab = reinterpret_cast<float2*>(smem + C::rope_off);   // (cos, sin) of t * inv_freq_j
+  __nv_bfloat16* Qlo = reinterpret_cast<__nv_bfloat16*>(smem + C::lo_off);   // bf16 rows: [HG][LS]
+  float* qinv = reinterpret_cast<float*>(smem + C::inv_off);                 // bf16 rows: [HG]
   grid_dep_wait();
   grid_dep_launch();
 
@@ -177,8 +186,10 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
     cp_async_commit();
   }
 
-  // ---------------- prologue: q_hat = RoPE_t(RMSNorm(q)) -> bf16 in shared memory.  The query's
-  // rotation angles are shared by all heads: one (cos, sin) table per CTA.
+  // ---------------- prologue: the query block in shared memory (bf16 rows: raw q, the rotated
+  // dims as hi + lo, inv per head; FP8 rows: q_hat = RoPE_t(RMSNorm(q)) as fp16 hi + lo).  The
+  // query's rotation angles are shared by all heads: one (cos, sin) table per CTA.
+  const int r16 = (a.q_norm_rope && !FP8) ? ((a.rp.r + 15) & ~15) : 0;   // dims of the lo block
   if (tid < a.rp.r / 2) {
     float cs, sn;
     rope_cos_sin(static_cast<double>(t), a.rp.inv_freq[tid], cs, sn);
@@ -213,8 +224,12 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
         const float inv = 1.0f / sqrtf(ss / static_cast<float>(D) + a.eps);
+        if constexpr (FP8) {
 #pragma unroll
-        for (int c = 0; c < E; ++c) v[c] *= inv;
+          for (int c = 0; c < E; ++c) v[c] *= inv;
+        } else if (lane == 0) {
+          qinv[hl] = inv;
+        }
         const int cbase = lane * E;
         if (cbase + E > D - a.rp.r) {
 #pragma unroll
@@ -226,6 +241,21 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
               const float x0 = v[c], x1 = v[c + 1];
               v[c] = x0 * cs - x1 * sn;
               v[c + 1] = x0 * sn + x1 * cs;
+            }
+          }
+        }
+      }
+      if constexpr (!FP8) {
+        if (!a.q_norm_rope && lane == 0) qinv[hl] = 1.f;
+        // lo half of the last r16 dims (zero where the dim is not rotated: raw q is exact in bf16)
+        const int cbase = lane * E;
+        if (r16 > 0 && cbase + E > D - r16) {
+#pragma unroll
+          for (int c = 0; c < E; ++c) {
+            const int ch = cbase + c;
+            if (ch >= D - r16) {
+              const float hi = __bfloat162float(__float2bfloat16_rn(v[c]));
+              Qlo[hl * C::LS + (ch - (D - r16))] = __float2bfloat16_rn(v[c] - hi);
             }
           }
         }
@@ -337,6 +367,27 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
           mma_bf16_16816(sacc[0], af, bb0);
         }
       }
+      // lo half of the rotated dims against the keys' last r16 dims
+      for (int kl = 0; kl < r16 / 16; ++kl) {
+        const int kd = D - r16 + kl * 16;
+        uint32_t af[4];
+        ldmatrix_x4(af[0], af[1], af[2], af[3],
+                    smem_u32(Qlo + (16 * g + (lane & 15)) * C::LS + kl * 16 + (lane >> 4) * 8));
+        if (NKT == 2) {
+          uint32_t b0, b1, b2, b3;
+          const int key = wq * 16 + (lane >> 4) * 8 + (lane & 7);
+          ldmatrix_x4(b0, b1, b2, b3, smem_u32(Kb + key * KS + kd + ((lane >> 3) & 1) * 8));
+          const uint32_t bb0[2] = {b0, b1}, bb1[2] = {b2, b3};
+          mma_bf16_16816(sacc[0], af, bb0);
+          mma_bf16_16816(sacc[NKT - 1], af, bb1);
+        } else {
+          uint32_t b0, b1;
+          const int key = wq * 8 + (lane & 7);
+          ldmatrix_x2(b0, b1, smem_u32(Kb + key * KS + kd + ((lane >> 3) & 1) * 8));
+          const uint32_t bb0[2] = {b0, b1};
+          mma_bf16_16816(sacc[0], af, bb0);
+        }
+      }
     } else {
       // z = sum_b scale_{j,b} * (q_hat_b . code_{j,b}), q_hat = hi + lo (fp16), each block in fp32
       const float* scb = bscale + buf * CK * C::NB;
@@ -368,7 +419,13 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
     }
     // chunk c + 2's pointers: rowptr[(c + 2) % 3] last served chunk c - 1, finished before (A)
     if (c + 2 < nchunks) compute_ptrs(c + 2, (c + 2) % 3, raw_next);
-    // ---- mask, scale to log2 domain, row max over this warp's keys
+    // ---- mask, scale to log2 domain (bf16 rows: times the head's RMSNorm factor), row max over
+    // this warp's keys
+    float rsc[2] = {sl2, sl2};
+    if constexpr (!FP8) {
+      rsc[0] = sl2 * qinv[16 * g + (lane >> 2)];
+      rsc[1] = sl2 * qinv[16 * g + (lane >> 2) + 8];
+    }
     float cmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
     for (int n = 0; n < NKT; ++n) {
@@ -376,7 +433,7 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
       for (int e = 0; e < 4; ++e) {
         const int key = wq * 8 * NKT + n * 8 + 2 * (lane & 3) + (e & 1);
         const bool ok = rowptr[pb * CK + key] != nullptr;
-        const float v = ok ? sacc[n][e] * sl2 : -INFINITY;
+        const float v = ok ? sacc[n][e] * rsc[e >> 1] : -INFINITY;
         sacc[n][e] = v;
         cmax[e >> 1] = fmaxf(cmax[e >> 1], v);
       }
@@ -662,6 +719,9 @@ size_t attend_partial_bytes(int Q, int H, int d, int n_splits) {
 cudaError_t launch_attend(const AttendArgs& a, cudaStream_t s, int* launches) {
   const int Q = a.B * a.Tq;
   if (Q == 0) return cudaSuccess;
+#ifndef CSA_ATT_WARP_MMA_ONLY
+  if (attend_tc_supported(a)) return launch_attend_tc(a, s, launches);
+#endif
   // 64 heads per CTA (each gathered row read once) when that still gives work to at least half
   // of the SMs, otherwise 16 heads per CTA; the numerics are identical
   int sms = 148;

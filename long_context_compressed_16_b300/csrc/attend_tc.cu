@@ -1,0 +1,659 @@
+// Shared K=V multi-query attention on the 5th-generation tensor cores for 512-dim bf16 rows, 64
+// query heads per CTA ("DeepSeek V4 模型技术大全", component table rows Shared K=V MQA, query/KV
+// RMSNorm, partial RoPE, attention sink, SWA; the HCA visibility set; the reverse-rotation note).
+// Same slots, splits and partial format as the warp-MMA kernel in attend.cu, which keeps the other
+// shapes (d = 128, the FP8 cache, head counts that are not a multiple of 64, other RoPE widths).
+//
+// Exact query path.  q_hat = RoPE_t(RMSNorm(q)) = inv * RoPE_t(q) with inv = 1/sqrt(mean(q^2)+eps),
+// so q_hat . K = inv * (q[0, d-r) . K[0, d-r) + RoPE_t(q)[d-r, d) . K[d-r, d)).  The unrotated dims
+// enter the product as the query's own bf16 bits (exact), the r rotated dims as a bf16 hi + lo pair
+// (about 16 significant bits), and inv multiplies the fp32 logit.  No rounding of the normalised
+// query stands between the inputs and the logits beyond the fp32 sums of the tensor cores.
+//
+// A CTA is persistent over work items (query, group of 64 heads, split of the slot range) and is
+// warp-specialised; 64 rows per chunk, two chunk buffers:
+//   loader warps (2)              the idx row -> row pointers, cp.async of the chunk's rows straight
+//                                 into the 128-byte swizzled operand layout; loader b owns buffer b
+//   MMA warp (1 thread)           S^T(c) = K q'^T   M = 128 (the chunk's 64 rows are TMEM lanes
+//                                 0..63), N = 64 heads, K = 512 (+ 64 for the lo half of the
+//                                 rotated dims), fp32 in TMEM, two buffers; S^T of the next chunk
+//                                 (also across items) is issued before the PV of the current one
+//                                 O^T += V^T P^T(c)  M = 128 dims (4 tiles), N = 64 heads, K = 64
+//                                 rows; V^T is the chunk's rows through an MN-major descriptor
+//   softmax warps (4)             one thread per (row, 32 heads): the chunk maximum per head by a
+//                                 butterfly over the warp and a pair exchange; a per-head reference
+//                                 maximum that moves only when a chunk exceeds it by more than 2^8;
+//                                 p = exp2(z - ref) rounded to bf16 into P^T (K-major, swizzled);
+//                                 running sums of the unrounded p per thread
+//   correction warps (4)          the query block of the next item (a TMA load of the raw q rows,
+//                                 inv per head, the rotated dims' hi / lo), the rescale of O^T in
+//                                 TMEM when a reference moved, and the epilogue (sink, normaliser,
+//                                 reverse rotation, bf16 output or split partials)
+// Every wait is bounded (CSA_ERR_TIMEOUT in the status word, never a hang).
+#include "common.cuh"
+#include "tc.cuh"
+
+namespace csa {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int D = 512;
+constexpr int HG = 64;                        // heads per CTA (MMA N)
+constexpr int CK = 64;                        // rows per chunk
+constexpr int NREG = D / 64;                  // 128-byte column regions of a row
+constexpr float kRescaleLog2 = 8.f;           // a head's reference maximum moves only past 2^8
+constexpr uint64_t kWaitNs = 1000000000ull;   // 1 s: every wait here normally ends in microseconds
+
+constexpr int QREG = HG * 128;                // one 64-dim region of the query block
+constexpr int KVREG = 2 * CK * 128;           // one 64-dim region of both chunk buffers
+constexpr int PTB = HG * 128;                 // P^T of one chunk: 64 heads x 64 rows, bf16
+constexpr int OFF_Q = 0;                      // regions 0..7: the raw query (rotated dims: hi)
+constexpr int OFF_QLO = OFF_Q + NREG * QREG;  // region 8: lo half of the rotated dims
+constexpr int OFF_KV = OFF_QLO + QREG;
+constexpr int OFF_PT = OFF_KV + NREG * KVREG; // also absorbs the M = 128 read of buffer 1 past region 7
+constexpr int OFF_MISC = OFF_PT + 2 * PTB;
+constexpr int M_ROWPTR = 0;                   // [2][CK] row pointers
+constexpr int M_ROPE = 1024;                  // [2][32] (cos, sin) of t * inv_freq, by item parity
+constexpr int M_CSCALE = M_ROPE + 512;        // [2][HG] log2-domain logit factor per head (scale * inv)
+constexpr int M_REF = M_CSCALE + 512;         // [HG] reference maximum (log2 domain)
+constexpr int M_FAC = M_REF + 256;            // [2][HG] factor of chunk buffer b
+constexpr int M_RED = M_FAC + 512;            // [2][HG] pair exchange of the softmax halves
+constexpr int M_FREF = M_RED + 512;           // [2][HG] final reference per item parity
+constexpr int M_FL = M_FREF + 512;            // [2][HG] final sums per item parity
+constexpr int M_EFAC = M_FL + 512;            // [HG] epilogue factor
+constexpr int M_FLAG = M_EFAC + 256;          // [2][2] rescale needed (buffer, head half)
+constexpr int M_BARS = M_FLAG + 16;
+// Barriers used once per item come in pairs by item parity where a waiter could otherwise see
+// two completions before it looks (items of one chunk let the producer run an item ahead).
+enum {
+  B_QTMA = 0, B_QREADY, B_QFREE = B_QREADY + 2, B_KVFULL, B_KVEMPTY = B_KVFULL + 2, B_SFULL = B_KVEMPTY + 2,
+  B_PFULL = B_SFULL + 2, B_CDONE = B_PFULL + 2, B_OREADY = B_CDONE + 2, B_OFREE, B_SMDONE = B_OFREE + 4,
+  B_DRAIN = B_SMDONE + 2, NBARS
+};
+constexpr int M_TMEM = M_BARS + NBARS * 8;
+constexpr int M_ABORT = M_TMEM + 4;
+constexpr int MISC_BYTES = 4864;
+constexpr int SMEM = 1024 + OFF_MISC + MISC_BYTES;
+static_assert(M_BARS % 8 == 0 && M_ABORT + 4 <= MISC_BYTES, "misc layout");
+static_assert(SMEM <= 232448, "shared memory budget");
+constexpr int TMEM_COLS = 512;                // S^T at columns 0 / 64, O^T tiles at 128 + 64 mt
+constexpr int NT = 12 * 32;                   // 12 warps: up to 168 registers per thread
+constexpr int kMmaWarp = 3;
+
+// warp roles: softmax 0, 1, 8, 9 (TMEM lane quarters 0 and 1 = rows 0..63); loaders 2 (buffer 0)
+// and 10 (buffer 1); MMA 3; correction 4..7 (lane quarters 0..3 = the dims of an O^T tile); warp 11
+// has no role
+__device__ __forceinline__ bool is_softmax_warp(int w) { return w == 0 || w == 1 || w == 8 || w == 9; }
+__device__ __forceinline__ bool is_loader_warp(int w) { return w == 2 || w == 10; }
+
+// Butterfly over 32 values per lane: afterwards v[0] of lane L holds the reduction over the 32
+// lanes of value L (max when MAX, else sum).
+template <bool MAX>
+__device__ __forceinline__ void butterfly32(float* v, int lane) {
+#pragma unroll
+  for (int o = 16, nc = 32; o >= 1; o >>= 1, nc >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i < nc / 2) {
+        const float send = up ? v[i] : v[i + nc / 2];
+        const float keep = up ? v[i + nc / 2] : v[i];
+        const float recv = __shfl_xor_sync(0xffffffffu, send, o);
+        v[i] = MAX ? fmaxf(keep, recv) : keep + recv;
+      }
+    }
+  }
+}
+
+struct Item {
+  long long qi;
+  int h0, split, t, b, Kq, s_begin, s_end, nch;
+};
+
+__device__ __forceinline__ Item item_at(const AttendArgs& a, long long it) {
+  const long long per_q = static_cast<long long>(a.H / HG) * a.n_splits;
+  Item r;
+  r.qi = it / per_q;
+  const int rem = static_cast<int>(it - r.qi * per_q);
+  r.h0 = (rem / a.n_splits) * HG;
+  r.split = rem % a.n_splits;
+  r.b = static_cast<int>(r.qi / a.Tq);
+  r.t = a.q_pos[r.qi];
+  const int nvis = n_visible(r.t, a.m, a.N);
+  r.Kq = (a.idx == nullptr) ? nvis : a.k;
+  const int nslots = r.Kq + a.window;
+  r.s_begin = r.split * a.split_slots;
+  r.s_end = min(nslots, r.s_begin + a.split_slots);
+  r.nch = r.s_end > r.s_begin ? (r.s_end - r.s_begin + CK - 1) / CK : 0;
+  return r;
+}
+
+// The next item of this CTA after `it` that has rows (-1 if none).
+__device__ __forceinline__ long long next_with_rows(const AttendArgs& a, long long it, long long items, Item& out) {
+  for (long long j = it + gridDim.x; j < items; j += gridDim.x) {
+    const Item r = item_at(a, j);
+    if (r.nch > 0) {
+      out = r;
+      return j;
+    }
+  }
+  return -1;
+}
+
+__global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const __grid_constant__ CUtensorMap qmap) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024u - (tc::sptr(smem_raw) & 1023u)) & 1023u);
+  unsigned char* qs = sm + OFF_Q;
+  unsigned char* kvs = sm + OFF_KV;
+  unsigned char* pts = sm + OFF_PT;
+  unsigned char* misc = sm + OFF_MISC;
+  const unsigned char** rowptr = reinterpret_cast<const unsigned char**>(misc + M_ROWPTR);
+  float2* rope = reinterpret_cast<float2*>(misc + M_ROPE);
+  float* cscale = reinterpret_cast<float*>(misc + M_CSCALE);
+  float* ref = reinterpret_cast<float*>(misc + M_REF);
+  float* facb = reinterpret_cast<float*>(misc + M_FAC);
+  float* red = reinterpret_cast<float*>(misc + M_RED);
+  float* fref = reinterpret_cast<float*>(misc + M_FREF);
+  float* fl = reinterpret_cast<float*>(misc + M_FL);
+  float* efac = reinterpret_cast<float*>(misc + M_EFAC);
+  volatile int* flag = reinterpret_cast<volatile int*>(misc + M_FLAG);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(misc + M_BARS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + M_TMEM);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + M_ABORT);
+  grid_dep_wait();
+  grid_dep_launch();
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long items = static_cast<long long>(a.B) * a.Tq * (a.H / HG) * a.n_splits;
+  const float sl2 = a.scale * kLog2e;
+  const int n_lo = (a.q_norm_rope && a.rp.r > 0) ? 1 : 0;   // the rotated dims are region 7 (r = 64)
+
+  if ((tc::sptr(sm) & 1023u) != 0u) {               // the swizzled operands need 1024-byte alignment
+    if (tid == 0) report_error(a.status, CSA_ERR_DEVICE_CHECK, -2000);
+    return;
+  }
+  if (tid == 0) {
+    // a wait of this call already gave up: this CTA does no work instead of waiting in turn
+    *abort_flag = (*reinterpret_cast<volatile int32_t*>(a.status) == CSA_ERR_TIMEOUT) ? 1 : 0;
+    for (int i = 0; i < NBARS; ++i) tc::mbar_init(&bars[i], (i >= B_OFREE && i < B_OFREE + 4) ? 4u : 1u);
+    tc::fence_barrier_init();
+    tc::prefetch_tensormap(&qmap);
+  }
+  if (warp == kMmaWarp) {
+    tc::tmem_alloc(tmem_slot, TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  if (tid < HG) ref[tid] = -INFINITY;
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto fail = [&](int where) {
+    *abort_flag = 1;
+    report_error(a.status, CSA_ERR_TIMEOUT, where);
+  };
+  auto wait = [&](int bi, long long use, int where) {   // the phase of the use-th completion
+    const bool ok = tc::mbar_wait(&bars[bi], static_cast<uint32_t>(use & 1), abort_flag, kWaitNs);
+    if (!ok) fail(where);
+    return ok;
+  };
+
+  if (is_softmax_warp(warp)) {
+    // ------------------------------------------------------------ softmax warps
+    const int quarter = warp & 1;                        // rows 32 * quarter + lane
+    const int hh = warp >> 3;                            // heads 32 * hh + i
+    const int st = quarter + 2 * hh;
+    const int j = quarter * 32 + lane;
+    float ps[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) ps[i] = 0.f;
+    long long n = 0, g = 0;
+    for (long long it = blockIdx.x; it < items; it += gridDim.x) {
+      const Item I = item_at(a, it);
+      if (I.nch == 0) continue;
+      const int par = static_cast<int>(n & 1);
+      wait(B_QREADY + par, n >> 1, 60);                  // this item's logit factors
+      const float* cs = cscale + par * HG + hh * 32;
+      for (int c = 0; c < I.nch; ++c, ++g) {
+        const int buf = static_cast<int>(g & 1);
+        wait(B_SFULL + buf, g >> 1, 61);
+        wait(B_KVFULL + buf, g >> 1, 62);                // the loaders' row pointers of this chunk
+        tc::tc_fence_after();
+        float z[32], v[32];
+        tc::tmem_ld32_wait(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + buf * HG + hh * 32, z);
+        const bool valid = rowptr[buf * CK + j] != nullptr;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          z[i] = valid ? z[i] * cs[i] : -INFINITY;
+          v[i] = z[i];
+        }
+        butterfly32<true>(v, lane);
+        red[quarter * HG + hh * 32 + lane] = v[0];
+        tc::named_bar_sync(1, 128);
+        if (quarter == 0) {                              // one thread per head moves its reference
+          const int h = hh * 32 + lane;
+          const float cm = fmaxf(red[h], red[HG + h]);
+          const float rold = ref[h];
+          float f = 1.f;
+          bool need = false;
+          if (cm > rold + kRescaleLog2 || (rold == -INFINITY && cm > -INFINITY)) {
+            f = (rold == -INFINITY) ? 0.f : exp2f(rold - cm);
+            need = c > 0 && rold > -INFINITY;            // O^T holds terms scaled by rold
+            ref[h] = cm;
+          }
+          facb[buf * HG + h] = f;
+          const bool any = __any_sync(0xffffffffu, need);
+          if (lane == 0) flag[buf * 2 + hh] = any ? 1 : 0;
+        }
+        tc::named_bar_sync(1, 128);
+        // p = exp2(z - ref) rounded to bf16 into P^T[h][j]; running sums of the unrounded p
+        unsigned char* pt = pts + buf * PTB;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int h = hh * 32 + i;
+          const float r = ref[h];
+          const float p = exp2f(z[i] - (r == -INFINITY ? 0.f : r));
+          ps[i] = fmaf(ps[i], facb[buf * HG + h], p);
+          *reinterpret_cast<__nv_bfloat16*>(pt + h * 128 + (((j >> 3) ^ (h & 7)) << 4) + (j & 7) * 2) =
+              __float2bfloat16_rn(p);
+        }
+        tc::fence_proxy_async_smem();
+        tc::tc_fence_before();
+        tc::named_bar_sync(1, 128);
+        if (st == 0 && lane == 0) tc::mbar_arrive(&bars[B_PFULL + buf]);
+      }
+      // the item's sums over its rows, per head
+      butterfly32<false>(ps, lane);
+      red[quarter * HG + hh * 32 + lane] = ps[0];
+      tc::named_bar_sync(1, 128);
+      if (quarter == 0) {
+        const int h = hh * 32 + lane;
+        fref[par * HG + h] = ref[h];
+        fl[par * HG + h] = red[h] + red[HG + h];
+        ref[h] = -INFINITY;
+      }
+      tc::named_bar_sync(1, 128);
+      if (st == 0 && lane == 0) tc::mbar_arrive(&bars[B_SMDONE + par]);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) ps[i] = 0.f;
+      ++n;
+    }
+  } else if (is_loader_warp(warp)) {
+    // ------------------------------------------------------------ loader warps
+    const int buf = warp >= 8 ? 1 : 0;                   // the chunk buffer this warp fills
+    const unsigned char* kvb = static_cast<const unsigned char*>(a.kv);
+    const unsigned char* winb = static_cast<const unsigned char*>(a.win);
+    const unsigned char* dummy = static_cast<const unsigned char*>(a.q);   // source of zero-size copies
+    long long g = 0;
+    for (long long it = blockIdx.x; it < items; it += gridDim.x) {
+      const Item I = item_at(a, it);
+      for (int c = 0; c < I.nch; ++c, ++g) {
+        if (static_cast<int>(g & 1) != buf) continue;
+        // lane L: row pointers of rows L and L + 32; 16-byte columns L and L + 32 of every row
+        int raw[2];
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int s = I.s_begin + c * CK + lane + 32 * hf;
+          raw[hf] = (s < I.s_end && s < I.Kq && a.idx != nullptr) ? a.idx[I.qi * a.k + s] : 0;
+        }
+        if (g >= 2) wait(B_KVEMPTY + buf, (g - 2) >> 1, 63);   // the PV of chunk g-2 has read this buffer
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int s = I.s_begin + c * CK + lane + 32 * hf;
+          const unsigned char* p = nullptr;
+          if (s < I.s_end) {
+            if (s < I.Kq) {
+              const int e = (a.idx == nullptr) ? s : raw[hf];
+              if (e >= 0 && e < a.N) {
+                p = kvb + (static_cast<size_t>(I.b) * a.N + e) * (D * 2);
+              } else if (e != -1) {
+                report_error(a.status, CSA_ERR_DEVICE_CHECK, e);
+              }
+            } else {
+              const int jw = s - I.Kq;
+              const int u = I.t - a.window + 1 + jw;
+              if (jw < a.window && u >= 0) p = winb + (static_cast<size_t>(I.b) * a.Wcap + u % a.Wcap) * (D * 2);
+            }
+          }
+          rowptr[buf * CK + lane + 32 * hf] = p;
+        }
+        __syncwarp();
+        if (!*abort_flag) {
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int col = lane + 32 * hf;
+            const int region = col >> 3, cc = col & 7;
+            unsigned char* dst0 = kvs + region * KVREG + buf * CK * 128;
+#pragma unroll 8
+            for (int r = 0; r < CK; ++r) {
+              const unsigned char* rp = rowptr[buf * CK + r];
+              cp_async16(dst0 + r * 128 + ((cc ^ (r & 7)) << 4), rp ? rp + col * 16 : dummy, rp != nullptr);
+            }
+          }
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bars[B_KVFULL + buf]);
+      }
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ correction warps
+    const int quarter = warp & 3;                        // TMEM lanes 32 * quarter + lane
+    const int ct = tid - 4 * 32;                         // 0..127
+    long long n = 0, g = 0, qtma_uses = 0;
+    // query block of item J into the operand regions; logit factors and rotation table of parity par
+    auto prep = [&](const Item& J, int par) {
+      if (ct == 0) {
+        tc::mbar_arrive_expect_tx(&bars[B_QTMA], HG * D * 2);
+#pragma unroll
+        for (int r = 0; r < NREG; ++r)
+          tc::tma_load_2d(qs + r * QREG, &qmap, r * 64, static_cast<int>(J.qi * a.H + J.h0), &bars[B_QTMA]);
+      }
+      if (ct < a.rp.r / 2) {
+        float cs, sn;
+        rope_cos_sin(static_cast<double>(J.t), a.rp.inv_freq[ct], cs, sn);
+        rope[par * 32 + ct] = make_float2(cs, sn);
+      }
+      // the copies land whatever happened elsewhere: wait for them without the abort flag
+      if (!tc::mbar_wait(&bars[B_QTMA], static_cast<uint32_t>(qtma_uses & 1), nullptr, kWaitNs)) fail(64);
+      ++qtma_uses;
+      tc::named_bar_sync(2, 128);
+      const int region = lane >> 2, c0 = (lane & 3) * 2;
+      const bool rot = n_lo && lane * 16 >= D - a.rp.r;
+      for (int hl = 0; hl < HG / 4; ++hl) {
+        const int h = quarter * (HG / 4) + hl;
+        unsigned char* row = qs + region * QREG + h * 128;
+        uint4* p0 = reinterpret_cast<uint4*>(row + ((c0 ^ (h & 7)) << 4));
+        uint4* p1 = reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (h & 7)) << 4));
+        const uint4 u0 = *p0, u1 = *p1;
+        float v[16] = {bf16lo(u0.x), bf16hi(u0.x), bf16lo(u0.y), bf16hi(u0.y), bf16lo(u0.z), bf16hi(u0.z),
+                       bf16lo(u0.w), bf16hi(u0.w), bf16lo(u1.x), bf16hi(u1.x), bf16lo(u1.y), bf16hi(u1.y),
+                       bf16lo(u1.z), bf16hi(u1.z), bf16lo(u1.w), bf16hi(u1.w)};
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) ss = fmaf(v[k], v[k], ss);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane == 0) {
+          const float inv = 1.0f / sqrtf(ss / static_cast<float>(D) + a.eps);
+          cscale[par * HG + h] = a.q_norm_rope ? sl2 * inv : sl2;
+        }
+        if (rot) {
+          uint32_t hw[8], lw[8];
+#pragma unroll
+          for (int k = 0; k < 16; k += 2) {
+            const float2 cssn = rope[par * 32 + ((lane * 16 + k - (D - a.rp.r)) >> 1)];
+            const float x0 = v[k] * cssn.x - v[k + 1] * cssn.y;
+            const float x1 = v[k] * cssn.y + v[k + 1] * cssn.x;
+            hw[k / 2] = pack_bf16x2(x0, x1);
+            lw[k / 2] = pack_bf16x2(x0 - bf16lo(hw[k / 2]), x1 - bf16hi(hw[k / 2]));
+          }
+          *p0 = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *p1 = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+          unsigned char* lrow = qs + OFF_QLO - OFF_Q + h * 128;
+          *reinterpret_cast<uint4*>(lrow + ((c0 ^ (h & 7)) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          *reinterpret_cast<uint4*>(lrow + (((c0 + 1) ^ (h & 7)) << 4)) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+        }
+      }
+      tc::fence_proxy_async_smem();
+      tc::named_bar_sync(2, 128);
+      if (ct == 0) tc::mbar_arrive(&bars[B_QREADY + par]);
+    };
+
+    {
+      Item J0;
+      if (next_with_rows(a, static_cast<long long>(blockIdx.x) - gridDim.x, items, J0) >= 0) prep(J0, 0);
+    }
+    __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(a.out);
+    const int Q = a.B * a.Tq;
+    for (long long it = blockIdx.x; it < items; it += gridDim.x) {
+      const Item I = item_at(a, it);
+      if (I.nch == 0) {
+        // no rows in this item: the output is the sink alone (zeros) or an empty partial
+        if (a.n_splits == 1) {
+          for (int e = ct; e < HG * D / 8; e += 128) {
+            const int h = e / (D / 8), d8 = e % (D / 8);
+            *reinterpret_cast<uint4*>(outp + (I.qi * a.H + I.h0 + h) * static_cast<long long>(D) + d8 * 8) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          if (a.lse != nullptr && ct < HG) a.lse[I.qi * a.H + I.h0 + ct] = a.sink[I.h0 + ct];
+        } else {
+          float* po = a.partial;
+          float* pml = a.partial + static_cast<size_t>(Q) * a.n_splits * a.H * D;
+          for (int e = ct; e < HG * D / 4; e += 128) {
+            const int h = e / (D / 4), d4 = e % (D / 4);
+            const size_t rowi = (static_cast<size_t>(I.qi) * a.n_splits + I.split) * a.H + I.h0 + h;
+            *reinterpret_cast<float4*>(po + rowi * D + d4 * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          if (ct < HG) {
+            const size_t rowi = (static_cast<size_t>(I.qi) * a.n_splits + I.split) * a.H + I.h0 + ct;
+            pml[rowi * 2 + 0] = -INFINITY;
+            pml[rowi * 2 + 1] = 0.f;
+          }
+        }
+        continue;
+      }
+      const int par = static_cast<int>(n & 1);
+      for (int c = 0; c < I.nch; ++c, ++g) {
+        if (c == I.nch - 1) {
+          Item J;
+          if (next_with_rows(a, it, items, J) >= 0) {
+            wait(B_QFREE, n, 65);                        // the last S^T of this item has read the query block
+            prep(J, par ^ 1);
+          }
+        }
+        if (c == 0) continue;                            // the first chunk starts the accumulator: no rescale
+        const int buf = static_cast<int>(g & 1);
+        wait(B_PFULL + buf, g >> 1, 66);
+        if (flag[buf * 2] | flag[buf * 2 + 1]) {
+          // a reference moved: O^T (this quarter's lanes, all heads) times the chunk's factors, once
+          // the PV of chunk g-1 has landed
+          wait(B_KVEMPTY + ((g - 1) & 1), (g - 1) >> 1, 67);
+          tc::tc_fence_after();
+#pragma unroll 1
+          for (int mt = 0; mt < 4; ++mt) {
+            const uint32_t ta = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + 2 * HG + mt * HG;
+            float o[64];
+            tc::tmem_ld64_wait(ta, o);
+#pragma unroll
+            for (int h = 0; h < 64; ++h) o[h] *= facb[buf * HG + h];
+            tc::tmem_st64_wait(ta, o);
+          }
+        }
+        tc::tc_fence_before();
+        tc::named_bar_sync(2, 128);
+        if (ct == 0) tc::mbar_arrive(&bars[B_CDONE + buf]);
+      }
+      // ---------------- epilogue: O^T out of TMEM, normalised (one split) or as a partial
+      wait(B_OREADY, n, 68);
+      wait(B_SMDONE + par, n >> 1, 69);
+      tc::tc_fence_after();
+      if (ct < HG) {
+        const int h = ct, hgl = I.h0 + h;
+        const float r = fref[par * HG + h], l = fl[par * HG + h];
+        if (a.n_splits == 1) {
+          const float a2 = a.sink[hgl] * kLog2e;
+          const float M = fmaxf(r, a2);
+          const float f = (r == -INFINITY) ? 0.f : exp2f(r - M);
+          const float L = l * f + exp2f(a2 - M);
+          efac[h] = f / L;
+          if (a.lse != nullptr) a.lse[I.qi * a.H + hgl] = (M + log2f(L)) * kLn2;
+        } else {
+          float* pml = a.partial + static_cast<size_t>(Q) * a.n_splits * a.H * D;
+          const size_t rowi = (static_cast<size_t>(I.qi) * a.n_splits + I.split) * a.H + hgl;
+          pml[rowi * 2 + 0] = r;
+          pml[rowi * 2 + 1] = l;
+        }
+      }
+      tc::named_bar_sync(2, 128);
+#pragma unroll 1
+      for (int mt = 0; mt < 4; ++mt) {
+        float o[64];
+        tc::tmem_ld64_wait(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + 2 * HG + mt * HG, o);
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bars[B_OFREE + mt]);   // the next item's PV may overwrite the tile
+        const int dim = mt * 128 + quarter * 32 + lane;
+        if (a.n_splits == 1) {
+          // lanes 2i and 2i+1 swap one value per head pair, so that each lane holds two adjacent dims
+          // of one head: the even lane head 2hp, the odd lane head 2hp+1 (a 4-byte store each)
+          const int dd = dim & ~1;
+          const bool unrot = a.out_unrotate && dd >= D - a.rp.r;
+          float cs = 1.f, sn = 0.f;
+          if (unrot) {                                  // rotation by -t
+            const float2 cssn = rope[par * 32 + ((dd - (D - a.rp.r)) >> 1)];
+            cs = cssn.x;
+            sn = -cssn.y;
+          }
+          const bool odd = (lane & 1) != 0;
+#pragma unroll
+          for (int hp = 0; hp < 32; ++hp) {
+            const float xe = o[2 * hp] * efac[2 * hp];
+            const float xo = o[2 * hp + 1] * efac[2 * hp + 1];
+            const float recv = __shfl_xor_sync(0xffffffffu, odd ? xe : xo, 1);
+            float x0 = odd ? recv : xe, x1 = odd ? xo : recv;
+            if (unrot) {
+              const float y0 = x0 * cs - x1 * sn, y1 = x0 * sn + x1 * cs;
+              x0 = y0;
+              x1 = y1;
+            }
+            const int h = I.h0 + 2 * hp + (odd ? 1 : 0);
+            *reinterpret_cast<uint32_t*>(outp + (I.qi * a.H + h) * static_cast<long long>(D) + dd) =
+                pack_bf16x2(x0, x1);
+          }
+        } else {
+          float* po = a.partial;
+#pragma unroll 8
+          for (int h = 0; h < 64; ++h) {
+            const size_t rowi = (static_cast<size_t>(I.qi) * a.n_splits + I.split) * a.H + I.h0 + h;
+            po[rowi * D + dim] = o[h];
+          }
+        }
+      }
+      tc::named_bar_sync(2, 128);                        // efac and this parity's tables are free again
+      ++n;
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer (lane 0 only)
+    if (lane == 0) {
+      constexpr uint32_t idS = tc::umma_idesc_bf16(128, HG, 0, 0);
+      constexpr uint32_t idPV = tc::umma_idesc_bf16(128, HG, 1, 0);
+      const uint32_t kva = tc::sptr(kvs), qa = tc::sptr(qs), pa = tc::sptr(pts);
+      bool issued = false;
+      auto issue_s = [&](long long g) {
+        const int buf = static_cast<int>(g & 1);
+#pragma unroll 4
+        for (int k = 0; k < D / 16; ++k) {
+          const int r = k >> 2, off = (k & 3) * 32;
+          const uint64_t ad = tc::umma_desc_sw128(kva + r * KVREG + buf * CK * 128 + off);
+          const uint64_t bd = tc::umma_desc_sw128(qa + r * QREG + off);
+          tc::umma_bf16(tmem + buf * HG, ad, bd, idS, k > 0 ? 1u : 0u);
+        }
+        for (int k = 0; k < 4 * n_lo; ++k) {           // lo half of the rotated dims against region 7
+          const uint64_t ad = tc::umma_desc_sw128(kva + (NREG - 1) * KVREG + buf * CK * 128 + k * 32);
+          const uint64_t bd = tc::umma_desc_sw128(qa + (OFF_QLO - OFF_Q) + k * 32);
+          tc::umma_bf16(tmem + buf * HG, ad, bd, idS, 1u);
+        }
+        tc::umma_commit(&bars[B_SFULL + buf]);
+        issued = true;
+      };
+      int cd_cnt[2] = {0, 0};
+      long long n = 0, g = 0;
+      bool ok = true;
+      Item cur;
+      long long it = next_with_rows(a, static_cast<long long>(blockIdx.x) - gridDim.x, items, cur);
+      if (it >= 0) {
+        ok = wait(B_QREADY, 0, 70) && wait(B_KVFULL, 0, 71);   // item 0: parity slot 0, first use
+        if (ok) {
+          tc::tc_fence_after();
+          issue_s(0);
+          if (cur.nch == 1) tc::umma_commit(&bars[B_QFREE]);
+        }
+      }
+      while (ok && it >= 0) {
+        Item nxt;
+        const long long it_next = next_with_rows(a, it, items, nxt);
+        for (int c = 0; ok && c < cur.nch; ++c, ++g) {
+          // S^T of the next chunk (of this item, or the first of the next one) before this PV
+          if (c + 1 < cur.nch || it_next >= 0) {
+            const bool new_item = c + 1 >= cur.nch;
+            if (new_item) ok = wait(B_QREADY + static_cast<int>((n + 1) & 1), (n + 1) >> 1, 72);
+            ok = ok && wait(B_KVFULL + static_cast<int>((g + 1) & 1), (g + 1) >> 1, 73);
+            if (!ok) break;
+            tc::tc_fence_after();
+            issue_s(g + 1);
+            if ((!new_item && c + 2 == cur.nch) || (new_item && nxt.nch == 1)) tc::umma_commit(&bars[B_QFREE]);
+          }
+          const int buf = static_cast<int>(g & 1);
+          ok = wait(B_PFULL + buf, g >> 1, 74);
+          if (ok && c > 0) ok = wait(B_CDONE + buf, cd_cnt[buf]++, 75);
+          if (!ok) break;
+          tc::tc_fence_after();
+#pragma unroll 1
+          for (int mt = 0; mt < 4; ++mt) {
+            if (c == 0 && n > 0) {
+              if (!(ok = wait(B_OFREE + mt, n - 1, 76))) break;
+              tc::tc_fence_after();
+            }
+#pragma unroll
+            for (int k = 0; k < CK / 16; ++k) {
+              const uint64_t ad = tc::umma_desc_sw128_mn(kva + (2 * mt) * KVREG + (buf * CK + 16 * k) * 128, KVREG, 1024);
+              const uint64_t bd = tc::umma_desc_sw128(pa + buf * PTB + k * 32);
+              tc::umma_bf16(tmem + 2 * HG + mt * HG, ad, bd, idPV, (c > 0 || k > 0) ? 1u : 0u);
+            }
+          }
+          if (!ok) break;
+          tc::umma_commit(&bars[B_KVEMPTY + buf]);
+          if (c + 1 == cur.nch) tc::umma_commit(&bars[B_OREADY]);
+        }
+        ++n;
+        it = it_next;
+        cur = nxt;
+      }
+      if (issued) {                                      // all MMAs done before TMEM is released
+        tc::umma_commit(&bars[B_DRAIN]);
+        if (!tc::mbar_wait(&bars[B_DRAIN], 0, nullptr, kWaitNs)) report_error(a.status, CSA_ERR_TIMEOUT, 77);
+      }
+    }
+    __syncwarp();
+  }
+
+  // ---------------- teardown: every MMA complete (the MMA thread drained) before TMEM is released
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == kMmaWarp) tc::tmem_dealloc(tmem, TMEM_COLS);
+}
+
+}  // namespace
+
+bool attend_tc_supported(const AttendArgs& a) {
+  return a.d == D && !a.fp8 && a.H % HG == 0 && (a.rp.r == 64 || a.rp.r == 0);
+}
+
+cudaError_t launch_attend_tc(const AttendArgs& a, cudaStream_t s, int* launches) {
+  const long long Q = static_cast<long long>(a.B) * a.Tq;
+  const long long items = Q * (a.H / HG) * a.n_splits;
+  if (items == 0) return cudaSuccess;
+  CUtensorMap qmap;
+  const uint64_t dims[2] = {static_cast<uint64_t>(D), static_cast<uint64_t>(Q) * a.H};
+  const uint32_t box[2] = {64, HG};
+  if (!tc::make_tensor_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.q, 2, dims, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(k_attend_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  if (e != cudaSuccess) return e;
+  int sms = 148, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long grid = items < sms ? items : sms;
+  e = launch_k(k_attend_tc, dim3(static_cast<unsigned>(grid)), dim3(NT), static_cast<size_t>(SMEM), s, a, qmap);
+  ++*launches;
+  if (e != cudaSuccess || a.n_splits == 1) return e;
+  return launch_attend_combine(a, s, launches);
+}
+
+}  // namespace csa

@@ -281,6 +281,9 @@ cudaError_t launch_attend_combine(const AttendArgs& a, cudaStream_t s, int* laun
 
 
 cudaError_t launch_attend(const AttendArgs& a, cudaStream_t s, int* launches);
+// The tensor-core kernel for 512-dim bf16 rows and 64-head groups (attend_tc.cu).
+bool attend_tc_supported(const AttendArgs& a);
+cudaError_t launch_attend_tc(const AttendArgs& a, cudaStream_t s, int* launches);
 
 
 

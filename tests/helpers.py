@@ -8,8 +8,10 @@ The max-abs bar is read on unit-scale outputs: |gpu - ref| <= 2e-2 * max(1, |ref
 For |ref| <= 1 this is the plain bar; above 1 it cannot hold for any bf16 output (the bf16
 spacing at 8..16 is 0.0625), which the FP8 workload's x20 outlier channels reach (|out| ~ 55).
 
-LSE bar: 1e-2 absolute.  The kernels round the normalised query to bf16 before the QK product,
-which moves each logit by ~1e-3 (rms) and the log-sum-exp by up to a few 1e-3."""
+LSE bar: |gpu - ref| <= 2e-3 + 1e-4 |ref|.  The log-sum-exp is computed from the logits alone: the
+query enters them exactly (its bf16 bits, the rotated dims as a bf16 hi + lo pair, the RMSNorm
+factor in fp32), the keys are the inputs' own bf16 / e4m3 values, and the sums run in fp32, so
+fp32 accumulation over 512 dims bounds the error far below this bar."""
 import numpy as np
 import torch
 
@@ -18,7 +20,8 @@ from oracle import csa_oracle as O
 MAX_ABS = 2e-2
 REL_L2 = 5e-3
 TIE_REL = 1e-3
-LSE_ATOL = 1e-2
+LSE_ATOL = 2e-3
+LSE_RTOL = 1e-4
 
 
 def bits16(t: torch.Tensor) -> np.ndarray:
@@ -44,10 +47,12 @@ def assert_close(gpu_bf16: torch.Tensor, ref: np.ndarray, what: str, max_abs=MAX
     return ma, rl
 
 
-def assert_lse(gpu: torch.Tensor, ref: np.ndarray, what: str, atol=LSE_ATOL):
+def assert_lse(gpu: torch.Tensor, ref: np.ndarray, what: str, atol=LSE_ATOL, rtol=LSE_RTOL):
     g = gpu.detach().cpu().double().numpy()
-    err = float(np.max(np.abs(g - ref)))
-    assert err <= atol, f"{what}: lse max error {err:.3e} (bar {atol})"
+    excess = np.abs(g - ref) - (atol + rtol * np.abs(ref))
+    worst = float(np.max(excess)) if excess.size else -1.0
+    err = float(np.max(np.abs(g - ref))) if excess.size else 0.0
+    assert worst <= 0.0, f"{what}: lse max error {err:.3e} (bar {atol} + {rtol} |lse|)"
 
 
 def check_topk_row(g: np.ndarray, scores: np.ndarray, nvis: int, k: int, what: str):

@@ -447,6 +447,50 @@ def test_attend_prefill_rows_and_large_logits():
     assert_lse(lse[0, ts], lref, "lse")
 
 
+def test_attend_persistent_items_and_empty_rows():
+    """Many more work items than CTAs (one CTA runs several queries and head groups in turn), two
+    head groups, and queries that see no rows at all (t < 127 with no window: the output is zero
+    and the LSE is the sink logit) interleaved with queries of up to 64 entries."""
+    B, T, H, d, N, m = 1, 400, 128, 512, 64, 128
+    rng = np.random.default_rng(17)
+    ts = np.concatenate([np.arange(0, 40), rng.integers(0, N * m, T - 40)])
+    rng.shuffle(ts)
+    q_pos = torch.from_numpy(ts.astype(np.int32))[None].to(DEV)
+    q = S.normal_bf16((B, T, H, d), 14, 1, DEV)
+    kv = S.normal_bf16((B, N, d), 14, 2, DEV)
+    win = S.normal_bf16((B, 128, d), 14, 3, DEV)
+    sink = (S.normal_f64((H,), 14, 4) * 2).float().to(DEV)
+    out, lse, ws = P.hca_attend(q, kv, win, sink, q_pos, m=m, window=0, want_lse=True)
+    torch.cuda.synchronize()
+    assert C.csa_read_device_status(ws)[0] == C.CSA_OK
+    inp = dict(q=q, kv=kv, win=win, sink=sink, q_pos=q_pos)
+    pick = sorted(set(rng.integers(0, T, 60).tolist()) | {int(np.argmin(ts)), int(np.argmax(ts))})
+    ref, lref = _oracle_attend_rows(inp, None, m, 0, [(0, t) for t in pick], dense=True)
+    assert_close(out[0, pick], ref, "persistent items")
+    assert_lse(lse[0, pick], lref, "lse")
+    empty = [i for i in range(T) if ts[i] < m - 1]
+    assert torch.count_nonzero(out[0, empty]) == 0
+    assert torch.equal(lse[0, empty], sink[None].expand(len(empty), H))
+
+
+def test_attend_decode_splits_with_empty_splits():
+    """Decode with fixed 512-slot splits where short contexts leave later splits without rows
+    (their partials are empty and the merge skips them)."""
+    B, H, d, N, m = 6, 64, 512, 2048, 128
+    q_pos = torch.tensor([[200], [70000], [N * m - 1], [5000], [130], [N * m - 300]], dtype=torch.int32, device=DEV)
+    q = S.normal_bf16((B, 1, H, d), 15, 1, DEV)
+    kv = S.normal_bf16((B, N, d), 15, 2, DEV)
+    win = S.normal_bf16((B, 128, d), 15, 3, DEV)
+    sink = S.normal_f64((H,), 15, 4).float().to(DEV)
+    out, lse, ws = P.hca_attend(q, kv, win, sink, q_pos, m=m, want_lse=True)
+    torch.cuda.synchronize()
+    assert C.csa_read_device_status(ws)[0] == C.CSA_OK
+    inp = dict(q=q, kv=kv, win=win, sink=sink, q_pos=q_pos)
+    ref, lref = _oracle_attend_rows(inp, None, m, 128, [(b, 0) for b in range(B)], dense=True)
+    assert_close(out[:, 0], ref, "decode with empty splits")
+    assert_lse(lse[:, 0], lref, "lse")
+
+
 # ------------------------------------------------------------------------------------------------ whole path
 
 def test_prefill_chain_small_end_to_end():
