@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--prefill-steps", type=int, default=3)
     ap.add_argument("--lowp", action="store_true",
                     help="FP8 workloads: the low-precision indexer (query quantised to e4m3, FP8 tensor cores)")
-    ap.add_argument("--case", choices=["compress", "out_proj"], default=None,
+    ap.add_argument("--case", choices=["compress", "out_proj", "attend", "index_prefill"], default=None,
                     help="time one library call on a profiler-sized input and exit (no contract line)")
     ap.add_argument("--case-tokens", type=int, default=65536, help="tokens of the --case input")
     ap.add_argument("--quick", action="store_true",
@@ -252,6 +252,39 @@ def run_other(args, dev, stream):
         return e0.elapsed_time(e1) / reps
 
     res = {}
+    # CSA decode at 1M context with the mixed FP8 cache (B = 4, N = 262144, k = 1024): the indexer
+    # on e4m3 keys widened to bf16, and the low-precision indexer (e4m3 query, FP8 tensor cores)
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        hbm = json.load(f).get("hbm_gbs", 6400.0)
+    w = S.WORKLOADS["csa_decode_1m_b4_fp8"]
+    inp = S.make_inputs(w, dev)
+    scores = torch.empty((w.B, 1, w.N), dtype=torch.float32, device=dev)
+    idx = torch.empty((w.B, 1, w.k), dtype=torch.int32, device=dev)
+    out = torch.empty((w.B, 1, w.H, w.d), dtype=torch.bfloat16, device=dev)
+    adesc = P.attend_desc(w.B, 1, w.N, w.H, w.d, k=w.k, m=w.m, Wcap=w.window, window=w.window, fp8=True)
+    ws_a = torch.zeros(max(256, C.csa_attend_workspace(adesc)), dtype=torch.uint8, device=dev)
+    byts = w.B * (w.N * (w.dI + 4) + w.nI * w.dI * 2 + w.nI * 4 + w.k * 4) + \
+        w.B * (w.k * 608 + w.window * w.d * 2 + 2 * w.H * w.d * 2 + w.k * 4)
+    for lowp in (False, True):
+        idesc = P.index_desc(w.B, 1, w.N, w.nI, w.dI, w.k, w.m, fp8=True, lowp=lowp)
+        ws_s = torch.zeros(max(256, C.csa_index_score_workspace(idesc)), dtype=torch.uint8, device=dev)
+        ws_t = torch.zeros(max(256, C.csa_topk_workspace(idesc)), dtype=torch.uint8, device=dev)
+        fns = [lambda sp: C.check(C.csa_index_score(idesc, inp["qI"], inp["w"], inp["kI"], inp["kI_scale"], inp["q_pos"],
+                                                    scores, ws_s, stream=sp), "csa_index_score"),
+               lambda sp: C.check(C.csa_topk(idesc, scores, inp["q_pos"], idx, ws_t, stream=sp), "csa_topk"),
+               lambda sp: C.check(C.csa_attend(adesc, inp["q"], inp["kv"], idx, inp["win"], inp["sink"], inp["q_pos"],
+                                               out, None, ws_a, stream=sp), "csa_attend")]
+        reps = max(5, args.steps)
+        ms = graph_ms(fns, reps)
+        parts = [graph_ms([f], reps) for f in fns]
+        res["csa_decode_1m_b4_fp8" + ("_lowp" if lowp else "")] = {
+            "query_tok_per_s": w.B / (ms * 1e-3), "ms_per_step": ms,
+            "breakdown_ms": {"csa_index_score": parts[0], "csa_topk": parts[1], "csa_attend": parts[2]},
+            "algorithmic_bytes": byts, "hbm_GBps": byts / (ms * 1e-3) / 1e9, "hbm_frac": byts / (ms * 1e-3) / 1e9 / hbm,
+            "indexer": "e4m3 query, FP8 tensor cores" if lowp else "e4m3 keys widened to bf16"}
+        del ws_s, ws_t
+    del inp, scores, idx, out, ws_a
+    torch.cuda.empty_cache()
     # HCA decode, 1M-token contexts
     w = S.WORKLOADS["hca_decode_1m_b8"]
     inp = S.make_inputs(w, dev)
@@ -568,11 +601,18 @@ def run_ours(args):
     for _ in range(3):
         e2e_step()
     torch.cuda.synchronize()
+    # the whole step (copies in, the three public calls, copies out) captured once and replayed
+    g_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_e2e):
+        e2e_step()
+    for _ in range(3):
+        g_e2e.replay()
+    torch.cuda.synchronize()
     e_t = []
     for i in range(0 if args.quick else K):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        e2e_step()
+        g_e2e.replay()
         e1.record(stream)
         e_t.append((e0, e1))
     torch.cuda.synchronize()
@@ -630,7 +670,9 @@ def run_ours(args):
                               ("e4m3 keys widened to bf16" if fp8 else "bf16"),
                    "l2": f"inputs larger than L2: {step_bytes / 2**20:.0f} MiB read per step (126 MB L2), no flush", "timed_blocks": len(blocks),
                    "timing": "step: one CUDA graph of the three calls per step, CUDA events around each replay; "
-                             "breakdown and roofline: each call's graph replayed K times back to back",
+                             "breakdown and roofline: each call's graph replayed K times back to back; "
+                             "e2e: one CUDA graph per step of the host-to-device copies, the three calls and the "
+                             "device-to-host copies",
                    "parallelism": f"dp{world}"},
         "breakdown_ms": {"csa_index_score": t_score, "csa_topk": t_topk, "csa_attend": t_att},
         "roofline": {"bound": "hbm", "kernel": "k_index_score", "achieved": achieved,
@@ -653,13 +695,41 @@ def run_ours(args):
 def run_case(args):
     """One library call on a small input, repeated: the command the ncu summaries under profiles/
     capture.  compress: the CSA main-stream compressor (T tokens of four [T, 512] bf16 streams);
-    out_proj: the grouped output projection at Flash widths (O [T, 64, 512])."""
+    out_proj: the grouped output projection at Flash widths (O [T, 64, 512]); attend /
+    index_prefill: the sparse attention / the indexer scores of a CSA prefill chunk of T tokens."""
     import torch
     from long_context_compressed_16_b300 import pipeline as P
     from long_context_compressed_16_b300 import synth as S
     dev = torch.device("cuda", 0)
     T = args.case_tokens
-    if args.case == "compress":
+    if args.case in ("attend", "index_prefill"):
+        # the CSA prefill shapes at T tokens (N = T / 4 entries, 64 heads x 512, k = 512): the
+        # attention over seeded random selections, or the indexer scores of every causal pair
+        from long_context_compressed_16_b300 import capi as C
+        w = S.scaled(S.WORKLOADS["csa_prefill_t65536"], T=T, N=T // 4)
+        inp = S.make_inputs(w, dev)
+        if args.case == "attend":
+            kv = S.normal_bf16((1, w.N, w.d), 3, S.TID["kv"], dev)
+            g = torch.Generator(device=dev).manual_seed(7)
+            nvis = torch.clamp((inp["q_pos"][0].long() + 1) // w.m, max=w.N)
+            idx = (torch.rand((w.T, w.k), generator=g, device=dev) * nvis[:, None]).long()
+            idx = torch.where(torch.arange(w.k, device=dev)[None] < nvis[:, None], idx, -1).int()[None].contiguous()
+            adesc = P.attend_desc(1, w.T, w.N, w.H, w.d, k=w.k, m=w.m, Wcap=w.T, window=w.window)
+            ws = torch.zeros(max(256, C.csa_attend_workspace(adesc)), dtype=torch.uint8, device=dev)
+            out = torch.empty((1, w.T, w.H, w.d), dtype=torch.bfloat16, device=dev)
+            fn = lambda: C.check(C.csa_attend(adesc, inp["q"], kv, idx, inp["win"], inp["sink"], inp["q_pos"], out,
+                                              None, ws), "csa_attend")
+            _, flops = prefill_flops(w)
+        else:
+            kI = S.normal_bf16((1, w.N, w.dI), 3, S.TID["kI"], dev)
+            idesc = P.index_desc(1, w.T, w.N, w.nI, w.dI, w.k, w.m)
+            ws = torch.zeros(max(256, C.csa_index_score_workspace(idesc)), dtype=torch.uint8, device=dev)
+            scores = torch.empty((1, w.T, w.N), dtype=torch.float32, device=dev)
+            fn = lambda: C.check(C.csa_index_score(idesc, inp["qI"], inp["w"], kI, None, inp["q_pos"], scores, ws),
+                                 "csa_index_score")
+            flops, _ = prefill_flops(w)
+        unit = ("TFLOP/s", lambda ms: flops / (ms * 1e-3) / 1e12)
+    elif args.case == "compress":
         x = {n: S.normal_bf16((1, T, 512), 3, S.TID[n], dev) for n in ("Ca", "Cb", "Za", "Zb")}
         out = torch.empty((1, T // 4, 512), dtype=torch.bfloat16, device=dev)
         fn = lambda: P.compress(x["Ca"], x["Za"], 4, Cb=x["Cb"], Zb=x["Zb"], out=out)

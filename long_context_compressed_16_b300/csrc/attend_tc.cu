@@ -11,24 +11,27 @@
 // query stands between the inputs and the logits beyond the fp32 sums of the tensor cores.
 //
 // A CTA is persistent over work items (query, group of 64 heads, split of the slot range) and is
-// warp-specialised; 64 rows per chunk, two chunk buffers:
-//   loader warps (2)              the idx row -> row pointers, cp.async of the chunk's rows straight
-//                                 into the 128-byte swizzled operand layout; loader b owns buffer b
-//   MMA warp (1 thread)           S^T(c) = K q'^T   M = 128 (the chunk's 64 rows are TMEM lanes
-//                                 0..63), N = 64 heads, K = 512 (+ 64 for the lo half of the
-//                                 rotated dims), fp32 in TMEM, two buffers; S^T of the next chunk
-//                                 (also across items) is issued before the PV of the current one
-//                                 O^T += V^T P^T(c)  M = 128 dims (4 tiles), N = 64 heads, K = 64
-//                                 rows; V^T is the chunk's rows through an MN-major descriptor
-//   softmax warps (4)             one thread per (row, 32 heads): the chunk maximum per head by a
-//                                 butterfly over the warp and a pair exchange; a per-head reference
-//                                 maximum that moves only when a chunk exceeds it by more than 2^8;
-//                                 p = exp2(z - ref) rounded to bf16 into P^T (K-major, swizzled);
-//                                 running sums of the unrounded p per thread
-//   correction warps (4)          the query block of the next item (a TMA load of the raw q rows,
-//                                 inv per head, the rotated dims' hi / lo), the rescale of O^T in
-//                                 TMEM when a reference moved, and the epilogue (sink, normaliser,
-//                                 reverse rotation, bf16 output or split partials)
+// warp-specialised around two 64-row chunk buffers:
+//   loader warps (7)       row pointers from the idx row, then cp.async of the chunk's 4096 16-byte
+//                          pieces straight into the 128-byte swizzled operand layout.  Gathering
+//                          scattered rows is bound by how many warps issue copies (one warp needs
+//                          ~9K cycles per 64 KB, sixteen ~2.3K), hence seven warps
+//   MMA warp (1 thread)    S^T(c) = K q'^T   M = 128 (the chunk's 64 rows are TMEM lanes 0..63),
+//                          N = 64 heads, K = 512 (+ 64 for the lo half of the rotated dims), fp32 in
+//                          TMEM, two buffers
+//                          O^T += V^T P^T(c) M = 128 dims (4 tiles), N = 64 heads, K = 64 rows;
+//                          V^T is the chunk's rows through an MN-major descriptor
+//                          S^T and PV are issued greedily in chunk order, each as soon as its inputs
+//                          are ready, so one buffer's gather never holds back the other's products
+//   softmax warps (8)      one thread per (row, 16 heads): per-head chunk maxima by a butterfly
+//                          over the warp and a pair exchange; a per-head reference maximum that
+//                          moves only when a chunk exceeds it by more than 2^8; p = exp2(z - ref)
+//                          rounded to bf16 into P^T (K-major, swizzled); running sums of the
+//                          unrounded p per thread
+//   correction warps (4)   the query block of the next item (a TMA load of the raw q rows, inv per
+//                          head, the rotated dims' hi / lo), the rescale of O^T in TMEM when a
+//                          reference moved, and the epilogue (sink, normaliser, reverse rotation,
+//                          bf16 output or split partials)
 // Every wait is bounded (CSA_ERR_TIMEOUT in the status word, never a hang).
 #include "common.cuh"
 #include "tc.cuh"
@@ -59,17 +62,17 @@ constexpr int M_ROPE = 1024;                  // [2][32] (cos, sin) of t * inv_f
 constexpr int M_CSCALE = M_ROPE + 512;        // [2][HG] log2-domain logit factor per head (scale * inv)
 constexpr int M_REF = M_CSCALE + 512;         // [HG] reference maximum (log2 domain)
 constexpr int M_FAC = M_REF + 256;            // [2][HG] factor of chunk buffer b
-constexpr int M_RED = M_FAC + 512;            // [2][HG] pair exchange of the softmax halves
+constexpr int M_RED = M_FAC + 512;            // [2][HG] pair exchange of the two row quarters
 constexpr int M_FREF = M_RED + 512;           // [2][HG] final reference per item parity
 constexpr int M_FL = M_FREF + 512;            // [2][HG] final sums per item parity
 constexpr int M_EFAC = M_FL + 512;            // [HG] epilogue factor
-constexpr int M_FLAG = M_EFAC + 256;          // [2][2] rescale needed (buffer, head half)
-constexpr int M_BARS = M_FLAG + 16;
+constexpr int M_FLAG = M_EFAC + 256;          // [2][4] rescale needed (buffer, head quarter)
+constexpr int M_BARS = M_FLAG + 32;
 // Barriers used once per item come in pairs by item parity where a waiter could otherwise see
 // two completions before it looks (items of one chunk let the producer run an item ahead).
 enum {
   B_QTMA = 0, B_QREADY, B_QFREE = B_QREADY + 2, B_KVFULL, B_KVEMPTY = B_KVFULL + 2, B_SFULL = B_KVEMPTY + 2,
-  B_PFULL = B_SFULL + 2, B_CDONE = B_PFULL + 2, B_OREADY = B_CDONE + 2, B_OFREE, B_SMDONE = B_OFREE + 4,
+  B_PFULL = B_SFULL + 2, B_CDONE = B_PFULL + 2, B_OREADY = B_CDONE + 2, B_OFREE, B_SMDONE = B_OFREE + 1,
   B_DRAIN = B_SMDONE + 2, NBARS
 };
 constexpr int M_TMEM = M_BARS + NBARS * 8;
@@ -79,24 +82,28 @@ constexpr int SMEM = 1024 + OFF_MISC + MISC_BYTES;
 static_assert(M_BARS % 8 == 0 && M_ABORT + 4 <= MISC_BYTES, "misc layout");
 static_assert(SMEM <= 232448, "shared memory budget");
 constexpr int TMEM_COLS = 512;                // S^T at columns 0 / 64, O^T tiles at 128 + 64 mt
-constexpr int NT = 12 * 32;                   // 12 warps: up to 168 registers per thread
-constexpr int kMmaWarp = 3;
 
-// warp roles: softmax 0, 1, 8, 9 (TMEM lane quarters 0 and 1 = rows 0..63); loaders 2 (buffer 0)
-// and 10 (buffer 1); MMA 3; correction 4..7 (lane quarters 0..3 = the dims of an O^T tile); warp 11
-// has no role
-__device__ __forceinline__ bool is_softmax_warp(int w) { return w == 0 || w == 1 || w == 8 || w == 9; }
-__device__ __forceinline__ bool is_loader_warp(int w) { return w == 2 || w == 10; }
+// warp roles (20 warps).  TMEM lane quarter = warp % 4.  softmax: warps 0,1,4,5,8,9,12,13 (lane
+// quarters 0 and 1 = the chunk's 64 rows; head quarter = warp / 4); loaders: 2,3,6,7,10,11,14;
+// MMA: 15; correction: 16..19 (lane quarters 0..3 = the dims of an O^T tile)
+constexpr int NWARPS = 20;
+constexpr int NT = NWARPS * 32;
+constexpr int kMmaWarp = 15;
+constexpr int kNLoad = 7 * 32;
+constexpr int BAR_SOFTMAX = 1, BAR_CORR = 2, BAR_LOAD = 3;
+__device__ __forceinline__ bool is_softmax_warp(int w) { return w < 16 && (w & 3) < 2; }
+__device__ __forceinline__ bool is_loader_warp(int w) { return w < 15 && (w & 3) >= 2; }
+__device__ __forceinline__ int loader_index(int w) { return (w >> 2) * 2 + (w & 1); }   // 0..6
 
-// Butterfly over 32 values per lane: afterwards v[0] of lane L holds the reduction over the 32
-// lanes of value L (max when MAX, else sum).
+// Butterfly over 16 values per lane and the 32 lanes: afterwards v[0] of lane L (and of lane L^1)
+// holds the reduction over all 32 lanes of value (L >> 1) & 15 (max when MAX, else sum).
 template <bool MAX>
-__device__ __forceinline__ void butterfly32(float* v, int lane) {
+__device__ __forceinline__ void butterfly16(float* v, int lane) {
 #pragma unroll
-  for (int o = 16, nc = 32; o >= 1; o >>= 1, nc >>= 1) {
+  for (int o = 16, nc = 16; o >= 2; o >>= 1, nc >>= 1) {
     const bool up = (lane & o) != 0;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 8; ++i) {
       if (i < nc / 2) {
         const float send = up ? v[i] : v[i + nc / 2];
         const float keep = up ? v[i + nc / 2] : v[i];
@@ -105,6 +112,8 @@ __device__ __forceinline__ void butterfly32(float* v, int lane) {
       }
     }
   }
+  const float r = __shfl_xor_sync(0xffffffffu, v[0], 1);
+  v[0] = MAX ? fmaxf(v[0], r) : v[0] + r;
 }
 
 struct Item {
@@ -142,6 +151,28 @@ __device__ __forceinline__ long long next_with_rows(const AttendArgs& a, long lo
   return -1;
 }
 
+// Walks the chunks of this CTA's items with rows, in order: the item, its count n among items with
+// rows, the chunk c within the item and the global chunk index g.
+struct Cursor {
+  long long it, n, g;
+  Item I;
+  int c;
+  __device__ __forceinline__ void start(const AttendArgs& a, long long items) {
+    it = next_with_rows(a, static_cast<long long>(blockIdx.x) - gridDim.x, items, I);
+    n = 0;
+    g = 0;
+    c = 0;
+  }
+  __device__ __forceinline__ bool valid() const { return it >= 0; }
+  __device__ __forceinline__ void advance(const AttendArgs& a, long long items) {
+    ++g;
+    if (++c < I.nch) return;
+    c = 0;
+    ++n;
+    it = next_with_rows(a, it, items, I);
+  }
+};
+
 __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (tc::sptr(smem_raw) & 1023u)) & 1023u);
@@ -177,7 +208,7 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
   if (tid == 0) {
     // a wait of this call already gave up: this CTA does no work instead of waiting in turn
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(a.status) == CSA_ERR_TIMEOUT) ? 1 : 0;
-    for (int i = 0; i < NBARS; ++i) tc::mbar_init(&bars[i], (i >= B_OFREE && i < B_OFREE + 4) ? 4u : 1u);
+    for (int i = 0; i < NBARS; ++i) tc::mbar_init(&bars[i], i == B_OFREE ? 4u : 1u);
     tc::fence_barrier_init();
     tc::prefetch_tensormap(&qmap);
   }
@@ -203,147 +234,141 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
   if (is_softmax_warp(warp)) {
     // ------------------------------------------------------------ softmax warps
     const int quarter = warp & 1;                        // rows 32 * quarter + lane
-    const int hh = warp >> 3;                            // heads 32 * hh + i
-    const int st = quarter + 2 * hh;
+    const int hq = warp >> 2;                            // heads 16 * hq + i
     const int j = quarter * 32 + lane;
-    float ps[32];
+    const int sid = quarter * 32 + hq * 64 + lane;       // 0..255 within the softmax group
+    float ps[16];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) ps[i] = 0.f;
-    long long n = 0, g = 0;
-    for (long long it = blockIdx.x; it < items; it += gridDim.x) {
-      const Item I = item_at(a, it);
-      if (I.nch == 0) continue;
-      const int par = static_cast<int>(n & 1);
-      wait(B_QREADY + par, n >> 1, 60);                  // this item's logit factors
-      const float* cs = cscale + par * HG + hh * 32;
-      for (int c = 0; c < I.nch; ++c, ++g) {
-        const int buf = static_cast<int>(g & 1);
-        wait(B_SFULL + buf, g >> 1, 61);
-        wait(B_KVFULL + buf, g >> 1, 62);                // the loaders' row pointers of this chunk
-        tc::tc_fence_after();
-        float z[32], v[32];
-        tc::tmem_ld32_wait(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + buf * HG + hh * 32, z);
-        const bool valid = rowptr[buf * CK + j] != nullptr;
+    for (int i = 0; i < 16; ++i) ps[i] = 0.f;
+    Cursor cur;
+    cur.start(a, items);
+    while (cur.valid()) {
+      const int par = static_cast<int>(cur.n & 1);
+      const int c = cur.c;
+      const long long g = cur.g;
+      if (c == 0) wait(B_QREADY + par, cur.n >> 1, 60);   // this item's logit factors
+      const float* cs = cscale + par * HG + hq * 16;
+      const int buf = static_cast<int>(g & 1);
+      wait(B_SFULL + buf, g >> 1, 61);
+      wait(B_KVFULL + buf, g >> 1, 62);                  // the loaders' row pointers of this chunk
+      tc::tc_fence_after();
+      float z[16], v[16];
+      tc::tmem_ld16_wait(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + buf * HG + hq * 16, z);
+      const bool valid = rowptr[buf * CK + j] != nullptr;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          z[i] = valid ? z[i] * cs[i] : -INFINITY;
-          v[i] = z[i];
-        }
-        butterfly32<true>(v, lane);
-        red[quarter * HG + hh * 32 + lane] = v[0];
-        tc::named_bar_sync(1, 128);
-        if (quarter == 0) {                              // one thread per head moves its reference
-          const int h = hh * 32 + lane;
+      for (int i = 0; i < 16; ++i) {
+        z[i] = valid ? z[i] * cs[i] : -INFINITY;
+        v[i] = z[i];
+      }
+      butterfly16<true>(v, lane);
+      if ((lane & 1) == 0) red[quarter * HG + hq * 16 + (lane >> 1)] = v[0];
+      tc::named_bar_sync(BAR_SOFTMAX, 256);
+      if (quarter == 0) {                                // even lanes own a head each
+        const int h = hq * 16 + (lane >> 1);
+        bool need = false;
+        if ((lane & 1) == 0) {
           const float cm = fmaxf(red[h], red[HG + h]);
-          const float rold = ref[h];
+          const float rold = c == 0 ? -INFINITY : ref[h];   // a new item starts from -inf
           float f = 1.f;
-          bool need = false;
           if (cm > rold + kRescaleLog2 || (rold == -INFINITY && cm > -INFINITY)) {
             f = (rold == -INFINITY) ? 0.f : exp2f(rold - cm);
             need = c > 0 && rold > -INFINITY;            // O^T holds terms scaled by rold
             ref[h] = cm;
+          } else if (c == 0) {
+            ref[h] = rold;
           }
           facb[buf * HG + h] = f;
-          const bool any = __any_sync(0xffffffffu, need);
-          if (lane == 0) flag[buf * 2 + hh] = any ? 1 : 0;
         }
-        tc::named_bar_sync(1, 128);
-        // p = exp2(z - ref) rounded to bf16 into P^T[h][j]; running sums of the unrounded p
-        unsigned char* pt = pts + buf * PTB;
+        const bool any = __any_sync(0xffffffffu, need);
+        if (lane == 0) flag[buf * 4 + hq] = any ? 1 : 0;
+      }
+      tc::named_bar_sync(BAR_SOFTMAX, 256);
+      // p = exp2(z - ref) rounded to bf16 into P^T[h][j]; running sums of the unrounded p
+      unsigned char* pt = pts + buf * PTB;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int h = hh * 32 + i;
-          const float r = ref[h];
-          const float p = exp2f(z[i] - (r == -INFINITY ? 0.f : r));
-          ps[i] = fmaf(ps[i], facb[buf * HG + h], p);
-          *reinterpret_cast<__nv_bfloat16*>(pt + h * 128 + (((j >> 3) ^ (h & 7)) << 4) + (j & 7) * 2) =
-              __float2bfloat16_rn(p);
+      for (int i = 0; i < 16; ++i) {
+        const int h = hq * 16 + i;
+        const float r = ref[h];
+        const float p = exp2f(z[i] - (r == -INFINITY ? 0.f : r));
+        ps[i] = fmaf(ps[i], facb[buf * HG + h], p);
+        *reinterpret_cast<__nv_bfloat16*>(pt + h * 128 + (((j >> 3) ^ (h & 7)) << 4) + (j & 7) * 2) =
+            __float2bfloat16_rn(p);
+      }
+      tc::fence_proxy_async_smem();
+      tc::tc_fence_before();
+      tc::named_bar_sync(BAR_SOFTMAX, 256);
+      if (sid == 0) tc::mbar_arrive(&bars[B_PFULL + buf]);
+      if (c + 1 == cur.I.nch) {
+        // the item's sums over its rows, per head
+        butterfly16<false>(ps, lane);
+        if ((lane & 1) == 0) red[quarter * HG + hq * 16 + (lane >> 1)] = ps[0];
+        tc::named_bar_sync(BAR_SOFTMAX, 256);
+        if (quarter == 0 && (lane & 1) == 0) {
+          const int h = hq * 16 + (lane >> 1);
+          fref[par * HG + h] = ref[h];
+          fl[par * HG + h] = red[h] + red[HG + h];
         }
-        tc::fence_proxy_async_smem();
-        tc::tc_fence_before();
-        tc::named_bar_sync(1, 128);
-        if (st == 0 && lane == 0) tc::mbar_arrive(&bars[B_PFULL + buf]);
-      }
-      // the item's sums over its rows, per head
-      butterfly32<false>(ps, lane);
-      red[quarter * HG + hh * 32 + lane] = ps[0];
-      tc::named_bar_sync(1, 128);
-      if (quarter == 0) {
-        const int h = hh * 32 + lane;
-        fref[par * HG + h] = ref[h];
-        fl[par * HG + h] = red[h] + red[HG + h];
-        ref[h] = -INFINITY;
-      }
-      tc::named_bar_sync(1, 128);
-      if (st == 0 && lane == 0) tc::mbar_arrive(&bars[B_SMDONE + par]);
+        tc::named_bar_sync(BAR_SOFTMAX, 256);
+        if (sid == 0) tc::mbar_arrive(&bars[B_SMDONE + par]);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) ps[i] = 0.f;
-      ++n;
+        for (int i = 0; i < 16; ++i) ps[i] = 0.f;
+      }
+      cur.advance(a, items);
     }
   } else if (is_loader_warp(warp)) {
     // ------------------------------------------------------------ loader warps
-    const int buf = warp >= 8 ? 1 : 0;                   // the chunk buffer this warp fills
+    const int lt = loader_index(warp) * 32 + lane;       // 0..223
     const unsigned char* kvb = static_cast<const unsigned char*>(a.kv);
     const unsigned char* winb = static_cast<const unsigned char*>(a.win);
     const unsigned char* dummy = static_cast<const unsigned char*>(a.q);   // source of zero-size copies
-    long long g = 0;
-    for (long long it = blockIdx.x; it < items; it += gridDim.x) {
-      const Item I = item_at(a, it);
-      for (int c = 0; c < I.nch; ++c, ++g) {
-        if (static_cast<int>(g & 1) != buf) continue;
-        // lane L: row pointers of rows L and L + 32; 16-byte columns L and L + 32 of every row
-        int raw[2];
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const int s = I.s_begin + c * CK + lane + 32 * hf;
-          raw[hf] = (s < I.s_end && s < I.Kq && a.idx != nullptr) ? a.idx[I.qi * a.k + s] : 0;
-        }
-        if (g >= 2) wait(B_KVEMPTY + buf, (g - 2) >> 1, 63);   // the PV of chunk g-2 has read this buffer
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const int s = I.s_begin + c * CK + lane + 32 * hf;
-          const unsigned char* p = nullptr;
-          if (s < I.s_end) {
-            if (s < I.Kq) {
-              const int e = (a.idx == nullptr) ? s : raw[hf];
-              if (e >= 0 && e < a.N) {
-                p = kvb + (static_cast<size_t>(I.b) * a.N + e) * (D * 2);
-              } else if (e != -1) {
-                report_error(a.status, CSA_ERR_DEVICE_CHECK, e);
-              }
-            } else {
-              const int jw = s - I.Kq;
-              const int u = I.t - a.window + 1 + jw;
-              if (jw < a.window && u >= 0) p = winb + (static_cast<size_t>(I.b) * a.Wcap + u % a.Wcap) * (D * 2);
+    Cursor cur;
+    cur.start(a, items);
+    while (cur.valid()) {
+      const Item& I = cur.I;
+      const long long g = cur.g;
+      const int buf = static_cast<int>(g & 1);
+      const int s = I.s_begin + cur.c * CK + lt;
+      const int raw = (lt < CK && s < I.s_end && s < I.Kq && a.idx != nullptr) ? a.idx[I.qi * a.k + s] : 0;
+      if (g >= 2) wait(B_KVEMPTY + buf, (g - 2) >> 1, 63);   // the PV of chunk g-2 has read this buffer
+      if (lt < CK) {
+        const unsigned char* p = nullptr;
+        if (s < I.s_end) {
+          if (s < I.Kq) {
+            const int e = (a.idx == nullptr) ? s : raw;
+            if (e >= 0 && e < a.N) {
+              p = kvb + (static_cast<size_t>(I.b) * a.N + e) * (D * 2);
+            } else if (e != -1) {
+              report_error(a.status, CSA_ERR_DEVICE_CHECK, e);
             }
-          }
-          rowptr[buf * CK + lane + 32 * hf] = p;
-        }
-        __syncwarp();
-        if (!*abort_flag) {
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            const int col = lane + 32 * hf;
-            const int region = col >> 3, cc = col & 7;
-            unsigned char* dst0 = kvs + region * KVREG + buf * CK * 128;
-#pragma unroll 8
-            for (int r = 0; r < CK; ++r) {
-              const unsigned char* rp = rowptr[buf * CK + r];
-              cp_async16(dst0 + r * 128 + ((cc ^ (r & 7)) << 4), rp ? rp + col * 16 : dummy, rp != nullptr);
-            }
+          } else {
+            const int jw = s - I.Kq;
+            const int u = I.t - a.window + 1 + jw;
+            if (jw < a.window && u >= 0) p = winb + (static_cast<size_t>(I.b) * a.Wcap + u % a.Wcap) * (D * 2);
           }
         }
-        cp_async_commit();
-        cp_async_wait<0>();
-        tc::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&bars[B_KVFULL + buf]);
+        rowptr[buf * CK + lt] = p;
       }
+      tc::named_bar_sync(BAR_LOAD, kNLoad);
+      if (!*abort_flag) {
+        unsigned char* dst0 = kvs + buf * CK * 128;
+        for (int i = lt; i < CK * 64; i += kNLoad) {
+          const int row = i >> 6, col = i & 63;
+          const unsigned char* rp = rowptr[buf * CK + row];
+          cp_async16(dst0 + (col >> 3) * KVREG + row * 128 + (((col & 7) ^ (row & 7)) << 4), rp ? rp + col * 16 : dummy,
+                     rp != nullptr);
+        }
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+      tc::fence_proxy_async_smem();
+      tc::named_bar_sync(BAR_LOAD, kNLoad);
+      if (lt == 0) tc::mbar_arrive(&bars[B_KVFULL + buf]);
+      cur.advance(a, items);
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 16) {
     // ------------------------------------------------------------ correction warps
     const int quarter = warp & 3;                        // TMEM lanes 32 * quarter + lane
-    const int ct = tid - 4 * 32;                         // 0..127
+    const int ct = tid - 16 * 32;                        // 0..127
     long long n = 0, g = 0, qtma_uses = 0;
     // query block of item J into the operand regions; logit factors and rotation table of parity par
     auto prep = [&](const Item& J, int par) {
@@ -361,46 +386,48 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
       // the copies land whatever happened elsewhere: wait for them without the abort flag
       if (!tc::mbar_wait(&bars[B_QTMA], static_cast<uint32_t>(qtma_uses & 1), nullptr, kWaitNs)) fail(64);
       ++qtma_uses;
-      tc::named_bar_sync(2, 128);
-      const int region = lane >> 2, c0 = (lane & 3) * 2;
-      const bool rot = n_lo && lane * 16 >= D - a.rp.r;
-      for (int hl = 0; hl < HG / 4; ++hl) {
-        const int h = quarter * (HG / 4) + hl;
-        unsigned char* row = qs + region * QREG + h * 128;
-        uint4* p0 = reinterpret_cast<uint4*>(row + ((c0 ^ (h & 7)) << 4));
-        uint4* p1 = reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (h & 7)) << 4));
-        const uint4 u0 = *p0, u1 = *p1;
-        float v[16] = {bf16lo(u0.x), bf16hi(u0.x), bf16lo(u0.y), bf16hi(u0.y), bf16lo(u0.z), bf16hi(u0.z),
-                       bf16lo(u0.w), bf16hi(u0.w), bf16lo(u1.x), bf16hi(u1.x), bf16lo(u1.y), bf16hi(u1.y),
-                       bf16lo(u1.z), bf16hi(u1.z), bf16lo(u1.w), bf16hi(u1.w)};
-        float ss = 0.f;
+      tc::named_bar_sync(BAR_CORR, 128);
+      // two threads per head: thread ct owns head ct / 2, dims [256 (ct & 1), + 256) = regions
+      // 4 (ct & 1) .. + 3; the odd thread also holds the rotated dims (region 7)
+      const int h = ct >> 1, half = ct & 1;
+      float ss = 0.f;
+#pragma unroll 4
+      for (int k = 0; k < 32; ++k) {
+        const int region = half * 4 + (k >> 3), ch = k & 7;
+        const uint4 u = *reinterpret_cast<const uint4*>(qs + region * QREG + h * 128 + ((ch ^ (h & 7)) << 4));
+        const float x[8] = {bf16lo(u.x), bf16hi(u.x), bf16lo(u.y), bf16hi(u.y),
+                            bf16lo(u.z), bf16hi(u.z), bf16lo(u.w), bf16hi(u.w)};
 #pragma unroll
-        for (int k = 0; k < 16; ++k) ss = fmaf(v[k], v[k], ss);
+        for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+      }
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      if (half == 0) {
+        const float inv = 1.0f / sqrtf(ss / static_cast<float>(D) + a.eps);
+        cscale[par * HG + h] = a.q_norm_rope ? sl2 * inv : sl2;
+      }
+      if (n_lo && half == 1) {
+        // rotated dims 448..511: hi back into region 7, lo into region 8
+#pragma unroll 2
+        for (int ch = 0; ch < 8; ++ch) {
+          unsigned char* at = qs + (NREG - 1) * QREG + h * 128 + ((ch ^ (h & 7)) << 4);
+          const uint4 u = *reinterpret_cast<const uint4*>(at);
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+          uint32_t hw[4], lw[4];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        if (lane == 0) {
-          const float inv = 1.0f / sqrtf(ss / static_cast<float>(D) + a.eps);
-          cscale[par * HG + h] = a.q_norm_rope ? sl2 * inv : sl2;
-        }
-        if (rot) {
-          uint32_t hw[8], lw[8];
-#pragma unroll
-          for (int k = 0; k < 16; k += 2) {
-            const float2 cssn = rope[par * 32 + ((lane * 16 + k - (D - a.rp.r)) >> 1)];
-            const float x0 = v[k] * cssn.x - v[k + 1] * cssn.y;
-            const float x1 = v[k] * cssn.y + v[k + 1] * cssn.x;
-            hw[k / 2] = pack_bf16x2(x0, x1);
-            lw[k / 2] = pack_bf16x2(x0 - bf16lo(hw[k / 2]), x1 - bf16hi(hw[k / 2]));
+          for (int p = 0; p < 4; ++p) {
+            const float2 cssn = rope[par * 32 + ch * 4 + p];
+            const float x0 = bf16lo(w[p]), x1 = bf16hi(w[p]);
+            const float y0 = x0 * cssn.x - x1 * cssn.y, y1 = x0 * cssn.y + x1 * cssn.x;
+            hw[p] = pack_bf16x2(y0, y1);
+            lw[p] = pack_bf16x2(y0 - bf16lo(hw[p]), y1 - bf16hi(hw[p]));
           }
-          *p0 = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *p1 = make_uint4(hw[4], hw[5], hw[6], hw[7]);
-          unsigned char* lrow = qs + OFF_QLO - OFF_Q + h * 128;
-          *reinterpret_cast<uint4*>(lrow + ((c0 ^ (h & 7)) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-          *reinterpret_cast<uint4*>(lrow + (((c0 + 1) ^ (h & 7)) << 4)) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+          *reinterpret_cast<uint4*>(at) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(qs + (OFF_QLO - OFF_Q) + h * 128 + ((ch ^ (h & 7)) << 4)) =
+              make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
       }
       tc::fence_proxy_async_smem();
-      tc::named_bar_sync(2, 128);
+      tc::named_bar_sync(BAR_CORR, 128);
       if (ct == 0) tc::mbar_arrive(&bars[B_QREADY + par]);
     };
 
@@ -449,23 +476,24 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
         if (c == 0) continue;                            // the first chunk starts the accumulator: no rescale
         const int buf = static_cast<int>(g & 1);
         wait(B_PFULL + buf, g >> 1, 66);
-        if (flag[buf * 2] | flag[buf * 2 + 1]) {
+        if (flag[buf * 4] | flag[buf * 4 + 1] | flag[buf * 4 + 2] | flag[buf * 4 + 3]) {
           // a reference moved: O^T (this quarter's lanes, all heads) times the chunk's factors, once
           // the PV of chunk g-1 has landed
           wait(B_KVEMPTY + ((g - 1) & 1), (g - 1) >> 1, 67);
           tc::tc_fence_after();
 #pragma unroll 1
-          for (int mt = 0; mt < 4; ++mt) {
-            const uint32_t ta = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + 2 * HG + mt * HG;
-            float o[64];
-            tc::tmem_ld64_wait(ta, o);
+          for (int part = 0; part < 8; ++part) {
+            const uint32_t ta = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + 2 * HG + part * 32;
+            const int hb = (part & 1) * 32;
+            float o[32];
+            tc::tmem_ld32_wait(ta, o);
 #pragma unroll
-            for (int h = 0; h < 64; ++h) o[h] *= facb[buf * HG + h];
-            tc::tmem_st64_wait(ta, o);
+            for (int h = 0; h < 32; ++h) o[h] *= facb[buf * HG + hb + h];
+            tc::tmem_st32_wait(ta, o);
           }
         }
         tc::tc_fence_before();
-        tc::named_bar_sync(2, 128);
+        tc::named_bar_sync(BAR_CORR, 128);
         if (ct == 0) tc::mbar_arrive(&bars[B_CDONE + buf]);
       }
       // ---------------- epilogue: O^T out of TMEM, normalised (one split) or as a partial
@@ -489,18 +517,23 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
           pml[rowi * 2 + 1] = l;
         }
       }
-      tc::named_bar_sync(2, 128);
+      tc::named_bar_sync(BAR_CORR, 128);
+      float* po = a.partial;
+      const bool odd = (lane & 1) != 0;
 #pragma unroll 1
-      for (int mt = 0; mt < 4; ++mt) {
-        float o[64];
-        tc::tmem_ld64_wait(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + 2 * HG + mt * HG, o);
-        tc::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&bars[B_OFREE + mt]);   // the next item's PV may overwrite the tile
+      for (int part = 0; part < 8; ++part) {
+        const int mt = part >> 1, hb = (part & 1) * 32;  // O^T tile mt, heads hb .. hb + 31
+        float o[32];
+        tc::tmem_ld32_wait(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + 2 * HG + mt * HG + hb, o);
+        if (part == 7) {
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&bars[B_OFREE]);   // the next item's PV may overwrite O^T
+        }
         const int dim = mt * 128 + quarter * 32 + lane;
         if (a.n_splits == 1) {
-          // lanes 2i and 2i+1 swap one value per head pair, so that each lane holds two adjacent dims
-          // of one head: the even lane head 2hp, the odd lane head 2hp+1 (a 4-byte store each)
+          // lanes 2i and 2i+1 swap one value per head pair, so that each lane holds two adjacent
+          // dims of one head: the even lane head hb + 2hp, the odd lane head hb + 2hp + 1
           const int dd = dim & ~1;
           const bool unrot = a.out_unrotate && dd >= D - a.rp.r;
           float cs = 1.f, sn = 0.f;
@@ -509,11 +542,10 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
             cs = cssn.x;
             sn = -cssn.y;
           }
-          const bool odd = (lane & 1) != 0;
 #pragma unroll
-          for (int hp = 0; hp < 32; ++hp) {
-            const float xe = o[2 * hp] * efac[2 * hp];
-            const float xo = o[2 * hp + 1] * efac[2 * hp + 1];
+          for (int hp = 0; hp < 16; ++hp) {
+            const float xe = o[2 * hp] * efac[hb + 2 * hp];
+            const float xo = o[2 * hp + 1] * efac[hb + 2 * hp + 1];
             const float recv = __shfl_xor_sync(0xffffffffu, odd ? xe : xo, 1);
             float x0 = odd ? recv : xe, x1 = odd ? xo : recv;
             if (unrot) {
@@ -521,20 +553,17 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
               x0 = y0;
               x1 = y1;
             }
-            const int h = I.h0 + 2 * hp + (odd ? 1 : 0);
+            const int h = I.h0 + hb + 2 * hp + (odd ? 1 : 0);
             *reinterpret_cast<uint32_t*>(outp + (I.qi * a.H + h) * static_cast<long long>(D) + dd) =
                 pack_bf16x2(x0, x1);
           }
         } else {
-          float* po = a.partial;
-#pragma unroll 8
-          for (int h = 0; h < 64; ++h) {
-            const size_t rowi = (static_cast<size_t>(I.qi) * a.n_splits + I.split) * a.H + I.h0 + h;
-            po[rowi * D + dim] = o[h];
-          }
+          const size_t row0 = (static_cast<size_t>(I.qi) * a.n_splits + I.split) * a.H + I.h0 + hb;
+#pragma unroll
+          for (int h = 0; h < 32; ++h) po[(row0 + h) * D + dim] = o[h];
         }
       }
-      tc::named_bar_sync(2, 128);                        // efac and this parity's tables are free again
+      tc::named_bar_sync(BAR_CORR, 128);                 // efac and this parity's tables are free again
       ++n;
     }
   } else if (warp == kMmaWarp) {
@@ -546,73 +575,88 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
       bool issued = false;
       auto issue_s = [&](long long g) {
         const int buf = static_cast<int>(g & 1);
-#pragma unroll 4
+        const uint32_t abase = kva + buf * CK * 128;
+#pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const int r = k >> 2, off = (k & 3) * 32;
-          const uint64_t ad = tc::umma_desc_sw128(kva + r * KVREG + buf * CK * 128 + off);
-          const uint64_t bd = tc::umma_desc_sw128(qa + r * QREG + off);
+          const uint64_t ad = tc::umma_desc_sw128(abase + (k >> 2) * KVREG + (k & 3) * 32);
+          const uint64_t bd = tc::umma_desc_sw128(qa + (k >> 2) * QREG + (k & 3) * 32);
           tc::umma_bf16(tmem + buf * HG, ad, bd, idS, k > 0 ? 1u : 0u);
         }
-        for (int k = 0; k < 4 * n_lo; ++k) {           // lo half of the rotated dims against region 7
-          const uint64_t ad = tc::umma_desc_sw128(kva + (NREG - 1) * KVREG + buf * CK * 128 + k * 32);
-          const uint64_t bd = tc::umma_desc_sw128(qa + (OFF_QLO - OFF_Q) + k * 32);
-          tc::umma_bf16(tmem + buf * HG, ad, bd, idS, 1u);
+        if (n_lo) {                                      // lo half of the rotated dims against region 7
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t ad = tc::umma_desc_sw128(abase + (NREG - 1) * KVREG + k * 32);
+            const uint64_t bd = tc::umma_desc_sw128(qa + (OFF_QLO - OFF_Q) + k * 32);
+            tc::umma_bf16(tmem + buf * HG, ad, bd, idS, 1u);
+          }
         }
         tc::umma_commit(&bars[B_SFULL + buf]);
         issued = true;
       };
-      int cd_cnt[2] = {0, 0};
-      long long n = 0, g = 0;
-      bool ok = true;
-      Item cur;
-      long long it = next_with_rows(a, static_cast<long long>(blockIdx.x) - gridDim.x, items, cur);
-      if (it >= 0) {
-        ok = wait(B_QREADY, 0, 70) && wait(B_KVFULL, 0, 71);   // item 0: parity slot 0, first use
-        if (ok) {
-          tc::tc_fence_after();
-          issue_s(0);
-          if (cur.nch == 1) tc::umma_commit(&bars[B_QFREE]);
-        }
-      }
-      while (ok && it >= 0) {
-        Item nxt;
-        const long long it_next = next_with_rows(a, it, items, nxt);
-        for (int c = 0; ok && c < cur.nch; ++c, ++g) {
-          // S^T of the next chunk (of this item, or the first of the next one) before this PV
-          if (c + 1 < cur.nch || it_next >= 0) {
-            const bool new_item = c + 1 >= cur.nch;
-            if (new_item) ok = wait(B_QREADY + static_cast<int>((n + 1) & 1), (n + 1) >> 1, 72);
-            ok = ok && wait(B_KVFULL + static_cast<int>((g + 1) & 1), (g + 1) >> 1, 73);
-            if (!ok) break;
-            tc::tc_fence_after();
-            issue_s(g + 1);
-            if ((!new_item && c + 2 == cur.nch) || (new_item && nxt.nch == 1)) tc::umma_commit(&bars[B_QFREE]);
-          }
-          const int buf = static_cast<int>(g & 1);
-          ok = wait(B_PFULL + buf, g >> 1, 74);
-          if (ok && c > 0) ok = wait(B_CDONE + buf, cd_cnt[buf]++, 75);
-          if (!ok) break;
-          tc::tc_fence_after();
-#pragma unroll 1
-          for (int mt = 0; mt < 4; ++mt) {
-            if (c == 0 && n > 0) {
-              if (!(ok = wait(B_OFREE + mt, n - 1, 76))) break;
-              tc::tc_fence_after();
-            }
+      auto issue_pv = [&](long long g, int c) {
+        const int buf = static_cast<int>(g & 1);
 #pragma unroll
-            for (int k = 0; k < CK / 16; ++k) {
-              const uint64_t ad = tc::umma_desc_sw128_mn(kva + (2 * mt) * KVREG + (buf * CK + 16 * k) * 128, KVREG, 1024);
-              const uint64_t bd = tc::umma_desc_sw128(pa + buf * PTB + k * 32);
-              tc::umma_bf16(tmem + 2 * HG + mt * HG, ad, bd, idPV, (c > 0 || k > 0) ? 1u : 0u);
-            }
+        for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+          for (int k = 0; k < CK / 16; ++k) {
+            const uint64_t ad = tc::umma_desc_sw128_mn(kva + (2 * mt) * KVREG + (buf * CK + 16 * k) * 128, KVREG, 1024);
+            const uint64_t bd = tc::umma_desc_sw128(pa + buf * PTB + k * 32);
+            tc::umma_bf16(tmem + 2 * HG + mt * HG, ad, bd, idPV, (c > 0 || k > 0) ? 1u : 0u);
           }
-          if (!ok) break;
-          tc::umma_commit(&bars[B_KVEMPTY + buf]);
-          if (c + 1 == cur.nch) tc::umma_commit(&bars[B_OREADY]);
         }
-        ++n;
-        it = it_next;
-        cur = nxt;
+        tc::umma_commit(&bars[B_KVEMPTY + buf]);
+      };
+      // two cursors over the same chunk sequence: S^T runs at most one chunk ahead of PV (its
+      // TMEM buffer is free once the softmax of the chunk two back is done, i.e. once that
+      // chunk's PV could be issued)
+      Cursor cs, cp;
+      cs.start(a, items);
+      cp.start(a, items);
+      int cd_cnt[2] = {0, 0};
+      bool ok = true;
+      uint64_t t_last = tc::globaltimer_ns();
+      uint32_t spins = 0;
+      while (ok && cp.valid()) {
+        bool progress = false;
+        if (cs.valid() && cs.g <= cp.g + 1) {
+          const int buf = static_cast<int>(cs.g & 1);
+          const bool qok = cs.c != 0 || tc::mbar_try_wait(&bars[B_QREADY + static_cast<int>(cs.n & 1)],
+                                                           static_cast<uint32_t>((cs.n >> 1) & 1));
+          if (qok && tc::mbar_try_wait(&bars[B_KVFULL + buf], static_cast<uint32_t>((cs.g >> 1) & 1))) {
+            tc::tc_fence_after();
+            issue_s(cs.g);
+            if (cs.c + 1 == cs.I.nch) tc::umma_commit(&bars[B_QFREE]);
+            cs.advance(a, items);
+            progress = true;
+          }
+        }
+        if (cp.g < cs.g) {
+          const int buf = static_cast<int>(cp.g & 1);
+          bool ready = tc::mbar_try_wait(&bars[B_PFULL + buf], static_cast<uint32_t>((cp.g >> 1) & 1));
+          if (ready && cp.c > 0)
+            ready = tc::mbar_try_wait(&bars[B_CDONE + buf], static_cast<uint32_t>(cd_cnt[buf] & 1));
+          if (ready && cp.c == 0 && cp.n > 0)
+            ready = tc::mbar_try_wait(&bars[B_OFREE], static_cast<uint32_t>((cp.n - 1) & 1));
+          if (ready) {
+            if (cp.c > 0) ++cd_cnt[buf];
+            tc::tc_fence_after();
+            issue_pv(cp.g, cp.c);
+            if (cp.c + 1 == cp.I.nch) tc::umma_commit(&bars[B_OREADY]);
+            cp.advance(a, items);
+            progress = true;
+          }
+        }
+        if (progress) {
+          spins = 0;
+          t_last = tc::globaltimer_ns();
+        } else if ((++spins & 63u) == 0) {
+          if (*abort_flag) {
+            ok = false;
+          } else if (tc::globaltimer_ns() - t_last > kWaitNs) {
+            fail(70);
+            ok = false;
+          }
+        }
       }
       if (issued) {                                      // all MMAs done before TMEM is released
         tc::umma_commit(&bars[B_DRAIN]);
