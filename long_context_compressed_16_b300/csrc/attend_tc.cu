@@ -247,50 +247,85 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
       const int c = cur.c;
       const long long g = cur.g;
       if (c == 0) wait(B_QREADY + par, cur.n >> 1, 60);   // this item's logit factors
-      const float* cs = cscale + par * HG + hq * 16;
       const int buf = static_cast<int>(g & 1);
       wait(B_SFULL + buf, g >> 1, 61);
       wait(B_KVFULL + buf, g >> 1, 62);                  // the loaders' row pointers of this chunk
       tc::tc_fence_after();
-      float z[16], v[16];
+      float z[16], rr[16];
       tc::tmem_ld16_wait(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + buf * HG + hq * 16, z);
       const bool valid = rowptr[buf * CK + j] != nullptr;
+      {
+        const float4* cs4 = reinterpret_cast<const float4*>(cscale + par * HG + hq * 16);
+        const float4* rf4 = reinterpret_cast<const float4*>(ref + hq * 16);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        z[i] = valid ? z[i] * cs[i] : -INFINITY;
-        v[i] = z[i];
-      }
-      butterfly16<true>(v, lane);
-      if ((lane & 1) == 0) red[quarter * HG + hq * 16 + (lane >> 1)] = v[0];
-      tc::named_bar_sync(BAR_SOFTMAX, 256);
-      if (quarter == 0) {                                // even lanes own a head each
-        const int h = hq * 16 + (lane >> 1);
-        bool need = false;
-        if ((lane & 1) == 0) {
-          const float cm = fmaxf(red[h], red[HG + h]);
-          const float rold = c == 0 ? -INFINITY : ref[h];   // a new item starts from -inf
-          float f = 1.f;
-          if (cm > rold + kRescaleLog2 || (rold == -INFINITY && cm > -INFINITY)) {
-            f = (rold == -INFINITY) ? 0.f : exp2f(rold - cm);
-            need = c > 0 && rold > -INFINITY;            // O^T holds terms scaled by rold
-            ref[h] = cm;
-          } else if (c == 0) {
-            ref[h] = rold;
-          }
-          facb[buf * HG + h] = f;
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float4 cv = cs4[q4], rv = rf4[q4];
+          z[4 * q4 + 0] = valid ? z[4 * q4 + 0] * cv.x : -INFINITY;
+          z[4 * q4 + 1] = valid ? z[4 * q4 + 1] * cv.y : -INFINITY;
+          z[4 * q4 + 2] = valid ? z[4 * q4 + 2] * cv.z : -INFINITY;
+          z[4 * q4 + 3] = valid ? z[4 * q4 + 3] * cv.w : -INFINITY;
+          rr[4 * q4 + 0] = rv.x;
+          rr[4 * q4 + 1] = rv.y;
+          rr[4 * q4 + 2] = rv.z;
+          rr[4 * q4 + 3] = rv.w;
         }
-        const bool any = __any_sync(0xffffffffu, need);
-        if (lane == 0) flag[buf * 4 + hq] = any ? 1 : 0;
       }
-      tc::named_bar_sync(BAR_SOFTMAX, 256);
+      // Fast path: every logit of the chunk stays within 2^8 of its head's reference, so the
+      // reference does not move (factor 1) and no per-head maximum is needed.  The first chunk of
+      // an item, or any logit above the band, takes the exact path for the whole chunk.
+      bool over = c == 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) over |= z[i] > rr[i] + kRescaleLog2;
+      const bool slow = tc::named_bar_or(BAR_SOFTMAX, 256, over);
+      float ff[16];
+      if (slow) {
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = z[i];
+        butterfly16<true>(v, lane);
+        if ((lane & 1) == 0) red[quarter * HG + hq * 16 + (lane >> 1)] = v[0];
+        tc::named_bar_sync(BAR_SOFTMAX, 256);
+        if (quarter == 0) {                              // even lanes own a head each
+          const int h = hq * 16 + (lane >> 1);
+          bool need = false;
+          if ((lane & 1) == 0) {
+            const float cm = fmaxf(red[h], red[HG + h]);
+            const float rold = c == 0 ? -INFINITY : ref[h];   // a new item starts from -inf
+            float f = 1.f;
+            if (cm > rold + kRescaleLog2 || (rold == -INFINITY && cm > -INFINITY)) {
+              f = (rold == -INFINITY) ? 0.f : exp2f(rold - cm);
+              need = c > 0 && rold > -INFINITY;          // O^T holds terms scaled by rold
+              ref[h] = cm;
+            } else if (c == 0) {
+              ref[h] = rold;
+            }
+            facb[buf * HG + h] = f;
+          }
+          const bool any = __any_sync(0xffffffffu, need);
+          if (lane == 0) flag[buf * 4 + hq] = any ? 1 : 0;
+        }
+        tc::named_bar_sync(BAR_SOFTMAX, 256);
+        const float4* rf4 = reinterpret_cast<const float4*>(ref + hq * 16);
+        const float4* fc4 = reinterpret_cast<const float4*>(facb + buf * HG + hq * 16);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float4 rv = rf4[q4], fv = fc4[q4];
+          rr[4 * q4 + 0] = rv.x; rr[4 * q4 + 1] = rv.y; rr[4 * q4 + 2] = rv.z; rr[4 * q4 + 3] = rv.w;
+          ff[4 * q4 + 0] = fv.x; ff[4 * q4 + 1] = fv.y; ff[4 * q4 + 2] = fv.z; ff[4 * q4 + 3] = fv.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ff[i] = 1.f;
+        if (quarter == 0 && (lane & 1) == 0) facb[buf * HG + hq * 16 + (lane >> 1)] = 1.f;
+        if (quarter == 0 && lane == 0) flag[buf * 4 + hq] = 0;
+      }
       // p = exp2(z - ref) rounded to bf16 into P^T[h][j]; running sums of the unrounded p
       unsigned char* pt = pts + buf * PTB;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int h = hq * 16 + i;
-        const float r = ref[h];
-        const float p = exp2f(z[i] - (r == -INFINITY ? 0.f : r));
-        ps[i] = fmaf(ps[i], facb[buf * HG + h], p);
+        const float p = exp2f(z[i] - (rr[i] == -INFINITY ? 0.f : rr[i]));
+        ps[i] = fmaf(ps[i], ff[i], p);
         *reinterpret_cast<__nv_bfloat16*>(pt + h * 128 + (((j >> 3) ^ (h & 7)) << 4) + (j & 7) * 2) =
             __float2bfloat16_rn(p);
       }
@@ -573,6 +608,7 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
       constexpr uint32_t idPV = tc::umma_idesc_bf16(128, HG, 1, 0);
       const uint32_t kva = tc::sptr(kvs), qa = tc::sptr(qs), pa = tc::sptr(pts);
       bool issued = false;
+      // S^T(g): K = 512 over the query block, then the lo half of the rotated dims against region 7
       auto issue_s = [&](long long g) {
         const int buf = static_cast<int>(g & 1);
         const uint32_t abase = kva + buf * CK * 128;
@@ -582,7 +618,7 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
           const uint64_t bd = tc::umma_desc_sw128(qa + (k >> 2) * QREG + (k & 3) * 32);
           tc::umma_bf16(tmem + buf * HG, ad, bd, idS, k > 0 ? 1u : 0u);
         }
-        if (n_lo) {                                      // lo half of the rotated dims against region 7
+        if (n_lo) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint64_t ad = tc::umma_desc_sw128(abase + (NREG - 1) * KVREG + k * 32);
@@ -590,7 +626,6 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
             tc::umma_bf16(tmem + buf * HG, ad, bd, idS, 1u);
           }
         }
-        tc::umma_commit(&bars[B_SFULL + buf]);
         issued = true;
       };
       auto issue_pv = [&](long long g, int c) {
@@ -606,37 +641,46 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
         }
         tc::umma_commit(&bars[B_KVEMPTY + buf]);
       };
-      // two cursors over the same chunk sequence: S^T runs at most one chunk ahead of PV (its
+      // Two cursors over the same chunk sequence: S^T runs at most one chunk ahead of PV (its
       // TMEM buffer is free once the softmax of the chunk two back is done, i.e. once that
-      // chunk's PV could be issued)
+      // chunk's PV could be issued).  Measured alternatives that were slower: a ready PV before a
+      // ready S^T, and S^T issued in slices with PVs between them.
       Cursor cs, cp;
       cs.start(a, items);
       cp.start(a, items);
       int cd_cnt[2] = {0, 0};
+      int s_k = -1;                                      // 0: S^T(cs.g) ready to issue
       bool ok = true;
-      uint64_t t_last = tc::globaltimer_ns();
+      long long t_last = clock64();
       uint32_t spins = 0;
       while (ok && cp.valid()) {
         bool progress = false;
         if (cs.valid() && cs.g <= cp.g + 1) {
-          const int buf = static_cast<int>(cs.g & 1);
-          const bool qok = cs.c != 0 || tc::mbar_try_wait(&bars[B_QREADY + static_cast<int>(cs.n & 1)],
-                                                           static_cast<uint32_t>((cs.n >> 1) & 1));
-          if (qok && tc::mbar_try_wait(&bars[B_KVFULL + buf], static_cast<uint32_t>((cs.g >> 1) & 1))) {
-            tc::tc_fence_after();
+          if (s_k < 0) {
+            const int buf = static_cast<int>(cs.g & 1);
+            const bool qok = cs.c != 0 || tc::mbar_test_wait(&bars[B_QREADY + static_cast<int>(cs.n & 1)],
+                                                             static_cast<uint32_t>((cs.n >> 1) & 1));
+            if (qok && tc::mbar_test_wait(&bars[B_KVFULL + buf], static_cast<uint32_t>((cs.g >> 1) & 1))) {
+              tc::tc_fence_after();
+              s_k = 0;
+            }
+          }
+          if (s_k >= 0) {
             issue_s(cs.g);
+            tc::umma_commit(&bars[B_SFULL + static_cast<int>(cs.g & 1)]);
             if (cs.c + 1 == cs.I.nch) tc::umma_commit(&bars[B_QFREE]);
             cs.advance(a, items);
+            s_k = -1;
             progress = true;
           }
         }
         if (cp.g < cs.g) {
           const int buf = static_cast<int>(cp.g & 1);
-          bool ready = tc::mbar_try_wait(&bars[B_PFULL + buf], static_cast<uint32_t>((cp.g >> 1) & 1));
+          bool ready = tc::mbar_test_wait(&bars[B_PFULL + buf], static_cast<uint32_t>((cp.g >> 1) & 1));
           if (ready && cp.c > 0)
-            ready = tc::mbar_try_wait(&bars[B_CDONE + buf], static_cast<uint32_t>(cd_cnt[buf] & 1));
+            ready = tc::mbar_test_wait(&bars[B_CDONE + buf], static_cast<uint32_t>(cd_cnt[buf] & 1));
           if (ready && cp.c == 0 && cp.n > 0)
-            ready = tc::mbar_try_wait(&bars[B_OFREE], static_cast<uint32_t>((cp.n - 1) & 1));
+            ready = tc::mbar_test_wait(&bars[B_OFREE], static_cast<uint32_t>((cp.n - 1) & 1));
           if (ready) {
             if (cp.c > 0) ++cd_cnt[buf];
             tc::tc_fence_after();
@@ -648,11 +692,11 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
         }
         if (progress) {
           spins = 0;
-          t_last = tc::globaltimer_ns();
+          t_last = clock64();
         } else if ((++spins & 63u) == 0) {
           if (*abort_flag) {
             ok = false;
-          } else if (tc::globaltimer_ns() - t_last > kWaitNs) {
+          } else if (clock64() - t_last > 4000000000ll) {   // about 2 s of SM clock
             fail(70);
             ok = false;
           }
