@@ -77,7 +77,8 @@ enum {
 };
 constexpr int M_TMEM = M_BARS + NBARS * 8;
 constexpr int M_ABORT = M_TMEM + 4;
-constexpr int MISC_BYTES = 4864;
+constexpr int M_PML = (M_ABORT + 4 + 15) & ~15;   // [HG] (m, l) of this split (cluster merge)
+constexpr int MISC_BYTES = M_PML + HG * 8;
 constexpr int SMEM = 1024 + OFF_MISC + MISC_BYTES;
 static_assert(M_BARS % 8 == 0 && M_ABORT + 4 <= MISC_BYTES, "misc layout");
 static_assert(SMEM <= 232448, "shared memory budget");
@@ -94,6 +95,24 @@ constexpr int BAR_SOFTMAX = 1, BAR_CORR = 2, BAR_LOAD = 3;
 __device__ __forceinline__ bool is_softmax_warp(int w) { return w < 16 && (w & 3) < 2; }
 __device__ __forceinline__ bool is_loader_warp(int w) { return w < 15 && (w & 3) >= 2; }
 __device__ __forceinline__ int loader_index(int w) { return (w >> 2) * 2 + (w & 1); }   // 0..6
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Two floats at the same shared-memory offset as p (8-byte aligned) in CTA `rank` of the cluster.
+__device__ __forceinline__ float2 ld_peer2(const float* p, uint32_t rank) {
+  const uint32_t la = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(rank));
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(ra));
+  return v;
+}
 
 // Butterfly over 16 values per lane and the 32 lanes: afterwards v[0] of lane L (and of lane L^1)
 // holds the reduction over all 32 lanes of value (L >> 1) & 15 (max when MAX, else sum).
@@ -197,14 +216,14 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
   grid_dep_launch();
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const long long items = static_cast<long long>(a.B) * a.Tq * (a.H / HG) * a.n_splits;
+  // the swizzled operands need 1024-byte alignment; a CTA without it does no work (it still
+  // reaches every block and cluster barrier, so no peer waits on it)
+  const bool aligned = (tc::sptr(sm) & 1023u) == 0u;
+  const long long items = aligned ? static_cast<long long>(a.B) * a.Tq * (a.H / HG) * a.n_splits : 0;
   const float sl2 = a.scale * kLog2e;
   const int n_lo = (a.q_norm_rope && a.rp.r > 0) ? 1 : 0;   // the rotated dims are region 7 (r = 64)
 
-  if ((tc::sptr(sm) & 1023u) != 0u) {               // the swizzled operands need 1024-byte alignment
-    if (tid == 0) report_error(a.status, CSA_ERR_DEVICE_CHECK, -2000);
-    return;
-  }
+  if (!aligned && tid == 0) report_error(a.status, CSA_ERR_DEVICE_CHECK, -2000);
   if (tid == 0) {
     // a wait of this call already gave up: this CTA does no work instead of waiting in turn
     *abort_flag = (*reinterpret_cast<volatile int32_t*>(a.status) == CSA_ERR_TIMEOUT) ? 1 : 0;
@@ -476,7 +495,9 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
       const Item I = item_at(a, it);
       if (I.nch == 0) {
         // no rows in this item: the output is the sink alone (zeros) or an empty partial
-        if (a.n_splits == 1) {
+        if (a.cluster_merge) {
+          if (ct < HG) reinterpret_cast<float2*>(misc + M_PML)[ct] = make_float2(-INFINITY, 0.f);
+        } else if (a.n_splits == 1) {
           for (int e = ct; e < HG * D / 8; e += 128) {
             const int h = e / (D / 8), d8 = e % (D / 8);
             *reinterpret_cast<uint4*>(outp + (I.qi * a.H + I.h0 + h) * static_cast<long long>(D) + d8 * 8) =
@@ -545,6 +566,8 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
           const float L = l * f + exp2f(a2 - M);
           efac[h] = f / L;
           if (a.lse != nullptr) a.lse[I.qi * a.H + hgl] = (M + log2f(L)) * kLn2;
+        } else if (a.cluster_merge) {
+          reinterpret_cast<float2*>(misc + M_PML)[h] = make_float2(r, l);
         } else {
           float* pml = a.partial + static_cast<size_t>(Q) * a.n_splits * a.H * D;
           const size_t rowi = (static_cast<size_t>(I.qi) * a.n_splits + I.split) * a.H + hgl;
@@ -592,6 +615,11 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
             *reinterpret_cast<uint32_t*>(outp + (I.qi * a.H + h) * static_cast<long long>(D) + dd) =
                 pack_bf16x2(x0, x1);
           }
+        } else if (a.cluster_merge) {
+          // stage the split's accumulator as fp32 [head][dim] over the (now idle) chunk buffers
+          float* stage = reinterpret_cast<float*>(kvs);
+#pragma unroll
+          for (int h = 0; h < 32; ++h) stage[(hb + h) * D + dim] = o[h];
         } else {
           const size_t row0 = (static_cast<size_t>(I.qi) * a.n_splits + I.split) * a.H + I.h0 + hb;
 #pragma unroll
@@ -715,6 +743,74 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
   __syncthreads();
   tc::tc_fence_after();
   if (warp == kMmaWarp) tc::tmem_dealloc(tmem, TMEM_COLS);
+
+  if (a.cluster_merge) {
+    // ---------------- the splits of one query are the CTAs of this cluster (one item each, split =
+    // cluster rank).  Each staged its (m, l) and fp32 accumulator; CTA r merges output units
+    // [r U / S, (r + 1) U / S) of the U = 64 heads x 256 dim pairs, reading every split's staged
+    // accumulator over distributed shared memory in fixed split order:
+    //   out = sum_s O_s 2^(m_s - M) / (sum_s l_s 2^(m_s - M) + 2^(a_h - M)),  M = max(a_h, max_s m_s)
+    cluster_barrier();
+    const int S = a.n_splits;
+    const uint32_t rank = cluster_rank();
+    const Item I = item_at(a, blockIdx.x);
+    float* facm = reinterpret_cast<float*>(pts);                 // [S][HG] merge factors
+    const float* pml = reinterpret_cast<const float*>(misc + M_PML);
+    if (tid < HG) {
+      const int h = tid, hgl = I.h0 + h;
+      const float a2 = a.sink[hgl] * kLog2e;
+      float ms[8], ls[8];
+      float M = a2;
+#pragma unroll
+      for (int sp = 0; sp < 8; ++sp) {
+        if (sp < S) {
+          const float2 v = ld_peer2(pml + 2 * h, static_cast<uint32_t>(sp));
+          ms[sp] = v.x;
+          ls[sp] = v.y;
+          M = fmaxf(M, v.x);
+        }
+      }
+      float L = exp2f(a2 - M);
+#pragma unroll
+      for (int sp = 0; sp < 8; ++sp)
+        if (sp < S && ms[sp] != -INFINITY) L = fmaf(ls[sp], exp2f(ms[sp] - M), L);
+      const float linv = 1.0f / L;
+#pragma unroll
+      for (int sp = 0; sp < 8; ++sp)
+        if (sp < S) facm[sp * HG + h] = (ms[sp] == -INFINITY) ? 0.f : exp2f(ms[sp] - M) * linv;
+      if (rank == 0 && a.lse != nullptr) a.lse[I.qi * a.H + hgl] = (M + log2f(L)) * kLn2;
+    } else if (tid >= 128 && tid - 128 < a.rp.r / 2) {
+      float cs, sn;
+      rope_cos_sin(static_cast<double>(I.t), a.rp.inv_freq[tid - 128], cs, sn);
+      rope[32 + tid - 128] = make_float2(cs, -sn);                // rotation by -t
+    }
+    __syncthreads();
+    const float* stage = reinterpret_cast<const float*>(kvs);
+    __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(a.out);
+    constexpr int U = HG * (D / 2);
+    const int u1 = static_cast<int>((rank + 1) * static_cast<long long>(U) / S);
+    for (int u = static_cast<int>(rank * static_cast<long long>(U) / S) + tid; u < u1; u += NT) {
+      const int h = u / (D / 2), d = 2 * (u % (D / 2));
+      float x0 = 0.f, x1 = 0.f;
+      for (int sp = 0; sp < S; ++sp) {
+        const float f = facm[sp * HG + h];       // 0 for a split without rows (nothing staged)
+        if (f != 0.f) {
+          const float2 v = ld_peer2(stage + h * D + d, static_cast<uint32_t>(sp));
+          x0 = fmaf(v.x, f, x0);
+          x1 = fmaf(v.y, f, x1);
+        }
+      }
+      if (a.out_unrotate && d >= D - a.rp.r) {
+        const float2 cssn = rope[32 + ((d - (D - a.rp.r)) >> 1)];
+        const float y0 = x0 * cssn.x - x1 * cssn.y, y1 = x0 * cssn.y + x1 * cssn.x;
+        x0 = y0;
+        x1 = y1;
+      }
+      *reinterpret_cast<uint32_t*>(outp + (I.qi * a.H + I.h0 + h) * static_cast<long long>(D) + d) =
+          pack_bf16x2(x0, x1);
+    }
+    cluster_barrier();                                           // no CTA leaves while a peer reads it
+  }
 }
 
 }  // namespace
@@ -737,11 +833,41 @@ cudaError_t launch_attend_tc(const AttendArgs& a, cudaStream_t s, int* launches)
   if (e != cudaSuccess) return e;
   int sms = 148, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // Decode splits (2..8 per query): one CTA per split, the splits of a query in one cluster that
+  // merges them in shared memory; no partials in global memory and no second kernel.
+  if (a.n_splits > 1 && a.n_splits <= 8 && items <= 0x7fffffffLL) {
+    AttendArgs b = a;
+    b.cluster_merge = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(items));
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = static_cast<size_t>(SMEM);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(a.n_splits);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, k_attend_tc, &cfg) == cudaSuccess && clusters >= 1) {
+      cfg.numAttrs = 2;
+      e = cudaLaunchKernelEx(&cfg, k_attend_tc, b, qmap);
+      ++*launches;
+      return e;
+    }
+    (void)cudaGetLastError();                                      // fall back to partials + merge kernel
+  }
+  AttendArgs b = a;
+  b.cluster_merge = 0;
   const long long grid = items < sms ? items : sms;
-  e = launch_k(k_attend_tc, dim3(static_cast<unsigned>(grid)), dim3(NT), static_cast<size_t>(SMEM), s, a, qmap);
+  e = launch_k(k_attend_tc, dim3(static_cast<unsigned>(grid)), dim3(NT), static_cast<size_t>(SMEM), s, b, qmap);
   ++*launches;
   if (e != cudaSuccess || a.n_splits == 1) return e;
-  return launch_attend_combine(a, s, launches);
+  return launch_attend_combine(b, s, launches);
 }
 
 }  // namespace csa

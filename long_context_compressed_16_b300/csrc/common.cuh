@@ -273,6 +273,7 @@ struct AttendArgs {
   int n_slots;              // slots per query (k + window, or N + window)
   int split_slots;          // slots per split (multiple of the chunk size)
   int n_splits;
+  int cluster_merge;        // splits of a query merged inside a thread-block cluster (tensor-core kernel)
   RopeParams rp;
 };
 size_t attend_partial_bytes(int Q, int H, int d, int n_splits);
