@@ -252,6 +252,30 @@ def run_other(args, dev, stream):
         return e0.elapsed_time(e1) / reps
 
     res = {}
+    # CSA decode at 128K with BF16 index scores: the selector's time against fp32 scores, and the
+    # recall of its selection against the fp32 one
+    w = S.WORKLOADS["csa_decode_128k_b32"]
+    inp = S.make_inputs(w, dev)
+    sel, t_score, t_topk = {}, {}, {}
+    for bf in (False, True):
+        idesc = P.index_desc(w.B, 1, w.N, w.nI, w.dI, w.k, w.m, bf16_scores=bf)
+        ws_s = torch.zeros(max(256, C.csa_index_score_workspace(idesc)), dtype=torch.uint8, device=dev)
+        ws_t = torch.zeros(max(256, C.csa_topk_workspace(idesc)), dtype=torch.uint8, device=dev)
+        scores = torch.empty((w.B, 1, w.N), dtype=torch.float32, device=dev)
+        idx = torch.empty((w.B, 1, w.k), dtype=torch.int32, device=dev)
+        f_s = lambda sp: C.check(C.csa_index_score(idesc, inp["qI"], inp["w"], inp["kI"], None, inp["q_pos"], scores,
+                                                   ws_s, stream=sp), "csa_index_score")
+        f_t = lambda sp: C.check(C.csa_topk(idesc, scores, inp["q_pos"], idx, ws_t, stream=sp), "csa_topk")
+        t_score[bf] = graph_ms([f_s], max(5, args.steps))
+        t_topk[bf] = graph_ms([f_t], max(5, args.steps))
+        sel[bf] = torch.sort(idx[:, 0], dim=1).values
+        del ws_s, ws_t, scores
+    hits = int(sum(torch.isin(sel[True][i], sel[False][i]).sum() for i in range(w.B)))
+    res["csa_decode_128k_b32_bf16_scores"] = {
+        "topk_ms": t_topk[True], "topk_ms_fp32_scores": t_topk[False], "selector_speedup": t_topk[False] / t_topk[True],
+        "score_ms": t_score[True], "score_ms_fp32_scores": t_score[False], "recall_vs_fp32": hits / (w.B * w.k)}
+    del inp, sel
+    torch.cuda.empty_cache()
     # CSA decode at 1M context with the mixed FP8 cache (B = 4, N = 262144, k = 1024): the indexer
     # on e4m3 keys widened to bf16, and the low-precision indexer (e4m3 query, FP8 tensor cores)
     with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:

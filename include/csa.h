@@ -136,10 +136,20 @@ csa_status csa_compress(const csa_compress_desc* desc, const void* Ca, const voi
  * workspace: device buffer of at least csa_index_topk_workspace(desc) bytes.
  * Supported: head_dim 64 or 128; 1 <= n_heads <= 64; 1 <= k <= 2048; N <= 262144
  * (larger N returns CSA_ERR_UNSUPPORTED).
+ *
+ * score_fmt CSA_SCORE_BF16 ("DeepSeek-V4 技术报告深度解读" 5.4 and the indexer QK-path table row
+ * of "DeepSeek V4 模型技术大全": index scores in BF16 instead of FP32, for a faster top-k
+ * selector): every score is rounded to bf16 (round to nearest even) after the head sum and the
+ * FP8 row scale; the stored values (score_out, workspace rows) are those rounded values in fp32,
+ * and the top-k selects on them with the same rule (ties, which rounding makes frequent, go to
+ * the smaller s).  CSA_SCORE_FP32 (0, the default of a zeroed descriptor) keeps fp32 scores.
  * ------------------------------------------------------------------------------------------- */
+enum { CSA_SCORE_FP32 = 0, CSA_SCORE_BF16 = 1 };
+
 typedef struct {
   int B, Tq, N, n_heads, head_dim, k, m;
   csa_format key_fmt;      /* CSA_FMT_BF16, CSA_FMT_FP8_ROWSCALE or CSA_FMT_FP8_ROWSCALE_LOWP */
+  int score_fmt;           /* CSA_SCORE_FP32 (0) or CSA_SCORE_BF16 */
 } csa_index_desc;
 
 size_t csa_index_topk_workspace(const csa_index_desc* desc);

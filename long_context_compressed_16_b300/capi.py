@@ -28,6 +28,9 @@ CSA_FMT_FP8_MIXED = 1
 CSA_FMT_FP8_ROWSCALE = 2
 CSA_FMT_FP8_ROWSCALE_LOWP = 3
 CSA_FP8_MIXED_ROW_BYTES = 608
+# csa_index_desc.score_fmt
+CSA_SCORE_FP32 = 0
+CSA_SCORE_BF16 = 1
 CSA_NOALLOC_SCRATCH_BYTES = 8 << 20
 # flags
 CSA_COMPRESS_NORM = 1
@@ -51,7 +54,7 @@ class csa_compress_desc(ctypes.Structure):
 
 class csa_index_desc(ctypes.Structure):
     _fields_ = [("B", c_int), ("Tq", c_int), ("N", c_int), ("n_heads", c_int), ("head_dim", c_int),
-                ("k", c_int), ("m", c_int), ("key_fmt", c_int)]
+                ("k", c_int), ("m", c_int), ("key_fmt", c_int), ("score_fmt", c_int)]
 
 
 class csa_attend_desc(ctypes.Structure):

@@ -128,6 +128,7 @@ bool index_desc_ok(const csa_index_desc* d) {
   if (d->key_fmt != CSA_FMT_BF16 && d->key_fmt != CSA_FMT_FP8_ROWSCALE && d->key_fmt != CSA_FMT_FP8_ROWSCALE_LOWP)
     return false;
   if (d->key_fmt == CSA_FMT_FP8_ROWSCALE_LOWP && d->head_dim != 128) return false;
+  if (d->score_fmt != CSA_SCORE_FP32 && d->score_fmt != CSA_SCORE_BF16) return false;
   return true;
 }
 
@@ -427,11 +428,13 @@ csa_status csa_index_topk(const csa_index_desc* d, const void* qI, const float* 
   ia.qI = qI; ia.w = w; ia.kI = kI; ia.kI_scale = kI_scale; ia.q_pos = q_pos;
   ia.B = d->B; ia.Tq = d->Tq; ia.N = d->N; ia.nI = d->n_heads; ia.dI = d->head_dim; ia.m = d->m;
   ia.fp8 = fp8 ? 1 : 0;
+  ia.bf16_scores = d->score_fmt == CSA_SCORE_BF16 ? 1 : 0;
   ia.status = static_cast<int32_t*>(ws);
   const csa::IndexGrouping grouping = csa::index_grouping(d->n_heads, d->Tq);
   csa::TopkArgs ta{};
   ta.q_pos = q_pos; ta.idx_out = idx_out; ta.status = static_cast<int32_t*>(ws);
   ta.Tq = d->Tq; ta.N = d->N; ta.k = d->k; ta.m = d->m;
+  ta.key_shift = d->score_fmt == CSA_SCORE_BF16 ? 16 : 0;
 
   const long long gpb = (d->Tq + plan.G - 1) / plan.G;
   unsigned char* wsb = static_cast<unsigned char*>(ws);
@@ -516,6 +519,7 @@ csa_status csa_index_score(const csa_index_desc* d, const void* qI, const float*
   ia.qI = qI; ia.w = w; ia.kI = kI; ia.kI_scale = kI_scale; ia.q_pos = q_pos;
   ia.B = d->B; ia.Tq = d->Tq; ia.N = d->N; ia.nI = d->n_heads; ia.dI = d->head_dim; ia.m = d->m;
   ia.fp8 = fp8 ? 1 : 0;
+  ia.bf16_scores = d->score_fmt == CSA_SCORE_BF16 ? 1 : 0;
   ia.status = static_cast<int32_t*>(ws);
   ia.scores = score_out;
   ia.q_begin = 0;
@@ -562,6 +566,7 @@ csa_status csa_topk(const csa_index_desc* d, const float* scores, const int32_t*
   csa::TopkArgs ta{};
   ta.scores = scores; ta.q_pos = q_pos; ta.idx_out = idx_out; ta.status = static_cast<int32_t*>(ws);
   ta.Tq = d->Tq; ta.N = d->N; ta.k = d->k; ta.m = d->m;
+  ta.key_shift = d->score_fmt == CSA_SCORE_BF16 ? 16 : 0;
   ta.q_begin = 0; ta.q_count = static_cast<int>(Q); ta.score_row_offset = 0;
   int launches = 0;
   const cudaError_t e =

@@ -210,6 +210,7 @@ struct IndexArgs {
   int32_t* status;          // workspace status word (bounded-wait timeouts)
   int B, Tq, N, nI, dI, m, fp8;
   int lowp;                 // qI is the e4m3 query (q8) and w the scaled weights: FP8 tensor cores
+  int bf16_scores;          // round each score to bf16 (RNE) before it is stored
   int q_begin, q_count;     // range of query GROUPS (G consecutive queries of one sequence)
   int score_row_offset;     // flattened query q (= b*Tq + i) owns score row q - score_row_offset
 };
@@ -248,6 +249,7 @@ struct TopkArgs {
   int Tq, N, k, m;
   int q_begin, q_count;
   int score_row_offset;
+  int key_shift;            // 16 for scores rounded to bf16 (16-bit order keys), else 0
 };
 // Rows longer than one selection slice are selected in two stages; the first writes
 // topk_candidate_bytes(Q, N, k) bytes of (key, index) candidates for a launch over Q queries to

@@ -490,7 +490,10 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
           const size_t qi = static_cast<size_t>(wk.gi.b) * a.Tq + wk.gi.i0 + j;
           const int nv = nvb[j];
           float* dst = a.scores + (static_cast<long long>(qi) - a.score_row_offset) * a.N;
-          if (key < nv) dst[key] = sum * kscale;
+          if (key < nv) {
+            const float v = sum * kscale;
+            dst[key] = a.bf16_scores ? __bfloat162float(__float2bfloat16_rn(v)) : v;
+          }
           else if (p.fill_invisible) dst[key] = -INFINITY;
         }
       }

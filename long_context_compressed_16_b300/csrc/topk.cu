@@ -231,10 +231,12 @@ __device__ __forceinline__ void block_minmax(const TkSmem& sm, uint32_t& kmax, u
   kmin = mn;
 }
 
-// keys[i] = order_key(src[i]) for i < L, eight independent loads in flight per thread; returns
-// this thread's largest and smallest key through kmax / kmin.
+// keys[i] = order_key(src[i]) >> shift for i < L, eight independent loads in flight per thread;
+// returns this thread's largest and smallest key through kmax / kmin.  shift 16: scores rounded
+// to bf16, whose keys differ only in their top 16 bits (two radix passes instead of four).
 template <int NT>
-__device__ __forceinline__ void load_keys(uint32_t* keys, const float* src, int L, uint32_t& kmax, uint32_t& kmin) {
+__device__ __forceinline__ void load_keys(uint32_t* keys, const float* src, int L, uint32_t& kmax, uint32_t& kmin,
+                                          int shift) {
   constexpr int U = NT >= 1024 ? 8 : (NT >= 512 ? 16 : 32);   // loads in flight per thread
   for (int base = 0; base < L; base += NT * U) {
     float v[U];
@@ -247,7 +249,7 @@ __device__ __forceinline__ void load_keys(uint32_t* keys, const float* src, int 
     for (int u = 0; u < U; ++u) {
       const int i = base + u * NT + threadIdx.x;
       if (i < L) {
-        const uint32_t kk = order_key(v[u]);
+        const uint32_t kk = order_key(v[u]) >> shift;
         keys[i] = kk;
         kmax = max(kmax, kk);
         kmin = min(kmin, kk);
@@ -302,7 +304,7 @@ __global__ void __launch_bounds__(NT) k_topk_slice(TopkArgs a, int S, int slice_
     const float* row = a.scores + (qi - a.score_row_offset) * static_cast<long long>(a.N);
     uint32_t kmax = 0u, kmin = 0xFFFFFFFFu;
     clear_hist(sm);
-    load_keys<NT>(sm.keys, row + lo, L, kmax, kmin);
+    load_keys<NT>(sm.keys, row + lo, L, kmax, kmin, a.key_shift);
     block_minmax<NT>(sm, kmax, kmin);
     select_block<NT>(sm, L, k, kmax, kmin, [&](int i, int j) { out[j] = lo + i; });
     return;
@@ -311,7 +313,8 @@ __global__ void __launch_bounds__(NT) k_topk_slice(TopkArgs a, int S, int slice_
   if (L <= k) {
     const float* row = a.scores + (qi - a.score_row_offset) * static_cast<long long>(a.N);
     for (int i = tid; i < k; i += NT)
-      crow[i] = i < L ? (static_cast<unsigned long long>(order_key(row[lo + i])) << 32) | static_cast<uint32_t>(lo + i)
+      crow[i] = i < L ? (static_cast<unsigned long long>(order_key(row[lo + i]) >> a.key_shift) << 32) |
+                            static_cast<uint32_t>(lo + i)
                       : static_cast<unsigned long long>(kNoIndex);
     return;
   }
@@ -322,7 +325,7 @@ __global__ void __launch_bounds__(NT) k_topk_slice(TopkArgs a, int S, int slice_
   const float* row = a.scores + (qi - a.score_row_offset) * static_cast<long long>(a.N);
   uint32_t kmax = 0u, kmin = 0xFFFFFFFFu;
   clear_hist(sm);
-  load_keys<NT>(sm.keys, row + lo, L, kmax, kmin);
+  load_keys<NT>(sm.keys, row + lo, L, kmax, kmin, a.key_shift);
   block_minmax<NT>(sm, kmax, kmin);
   select_block<NT>(sm, L, k, kmax, kmin, [&](int i, int j) {
     crow[j] = (static_cast<unsigned long long>(sm.keys[i]) << 32) | static_cast<uint32_t>(lo + i);
@@ -413,7 +416,7 @@ __global__ void __launch_bounds__(NT) k_topk_cluster(TopkArgs a, int S, int slic
   for (int i = tid; i < 2 * kBins; i += NT) hist2[i] = 0u;
   const float* row = a.scores + (qi - a.score_row_offset) * static_cast<long long>(a.N);
   uint32_t kmax = 0u, kmin = 0xFFFFFFFFu;
-  load_keys<NT>(sm.keys, row + lo, L, kmax, kmin);
+  load_keys<NT>(sm.keys, row + lo, L, kmax, kmin, a.key_shift);
   block_minmax<NT>(sm, kmax, kmin);
   if (tid == 0) {
     pub[0] = kmax;

@@ -237,6 +237,15 @@ def index_scores_lowp(qI, w, kI, q_pos, m):
     return index_scores(q8, w, kI, q_pos, m)
 
 
+def round_scores_bf16(scores):
+    """Index scores held in BF16 instead of FP32 ("DeepSeek-V4 技术报告深度解读" 5.4 and the
+    indexer QK-path row of "DeepSeek V4 模型技术大全": the top-k selector works on BF16 scores):
+    every score rounded to the nearest bf16 value, ties to even, by this module's own rounding;
+    -inf stays -inf.  The selection then runs topk_select on the rounded scores, where ties (which
+    the rounding makes common) go to the smaller s (R14)."""
+    return bf16_to_f64(bf16_round(np.asarray(scores, dtype=np.float64)))
+
+
 def topk_select(scores, q_pos, m, k):
     """TopK_k over the visible scores of each query.  R14: ties go to the smaller s; with fewer
     than k visible entries all are taken and the row is padded with -1.

@@ -112,6 +112,8 @@ def test_index_validation_and_workspace():
     assert call(_idesc(), ws_ptr=None) == C.CSA_ERR_WORKSPACE
     assert call(_idesc(), ws_bytes=100) == C.CSA_ERR_WORKSPACE
     assert call(_idesc(key_fmt=C.CSA_FMT_FP8_ROWSCALE)) == C.CSA_ERR_INVALID_ARG   # scales missing
+    assert call(_idesc(score_fmt=2)) == C.CSA_ERR_INVALID_ARG                       # unknown score format
+    assert C.lib.csa_index_topk_workspace(ctypes.byref(_idesc(score_fmt=C.CSA_SCORE_BF16))) == ws
     assert call(_idesc(B=0)) == C.CSA_OK
 
 

@@ -543,6 +543,23 @@ def test_index_scores_lowp_by_hand():
     assert plain[0, 0, 0] != got[0, 0, 0] and plain[0, 0, 1] != got[0, 0, 1]
 
 
+def test_bf16_scores_round_to_nearest_even_and_ties_go_to_the_smaller_entry():
+    """bf16 keeps 8 significant bits: in [1, 2) the spacing is 2^-7.
+      s0 = 1            -> 1
+      s1 = 1 + 2^-8     -> halfway between 1 and 1 + 2^-7: ties to even -> 1
+      s2 = 1 + 3 2^-8   -> halfway between 1 + 2^-7 (odd) and 1 + 2^-6 (even) -> 1 + 2^-6
+      s3 = 1 + 2^-7 + 2^-10 -> nearest 1 + 2^-7
+    In fp64 the order is s2 > s3 > s1 > s0 (top-3 = {2, 3, 1}); after rounding s0 and s1 tie at
+    1 and the smaller index wins (top-3 = {2, 3, 0}); -inf stays -inf."""
+    sc = np.array([[[1.0, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, 1.0 + 2.0 ** -7 + 2.0 ** -10, -np.inf]]])
+    r = O.round_scores_bf16(sc)
+    np.testing.assert_array_equal(r[0, 0], [1.0, 1.0, 1.0 + 2.0 ** -6, 1.0 + 2.0 ** -7, -np.inf])
+    q_pos = [[4 * 4 - 1]]                         # m = 4: entries 0..3 visible
+    assert sorted(O.topk_select(sc, q_pos, 4, 3)[0, 0].tolist()) == [1, 2, 3]
+    assert sorted(O.topk_select(r, q_pos, 4, 3)[0, 0].tolist()) == [0, 2, 3]
+    assert O.topk_select(r, q_pos, 4, 1)[0, 0].tolist() == [2]
+
+
 # ------------------------------------------------------------------------------------------------ grouped output projection
 
 def test_out_proj_equals_one_block_diagonal_product():
