@@ -50,7 +50,8 @@ def parse():
     ap.add_argument("--prefill-steps", type=int, default=3)
     ap.add_argument("--lowp", action="store_true",
                     help="FP8 workloads: the low-precision indexer (query quantised to e4m3, FP8 tensor cores)")
-    ap.add_argument("--case", choices=["compress", "out_proj", "attend", "index_prefill"], default=None,
+    ap.add_argument("--case", choices=["compress", "out_proj", "attend", "index_prefill", "index_topk_prefill"],
+                    default=None,
                     help="time one library call on a profiler-sized input and exit (no contract line)")
     ap.add_argument("--case-tokens", type=int, default=65536, help="tokens of the --case input")
     ap.add_argument("--quick", action="store_true",
@@ -416,53 +417,80 @@ def run_prefill(args, dev, stream):
     out = torch.empty((1, w.T, w.H, w.d), dtype=torch.bfloat16, device=dev)
     idesc = P.index_desc(1, w.T, w.N, w.nI, w.dI, w.k, w.m)
     adesc = P.attend_desc(1, w.T, w.N, w.H, w.d, k=w.k, m=w.m, Wcap=w.T, window=w.window)
+    wsi = torch.zeros(max(256, C.csa_index_topk_workspace(idesc)), dtype=torch.uint8, device=dev)
     ws_s = torch.zeros(max(256, C.csa_index_score_workspace(idesc)), dtype=torch.uint8, device=dev)
     ws_t = torch.zeros(max(256, C.csa_topk_workspace(idesc)), dtype=torch.uint8, device=dev)
     ws_a = torch.zeros(max(256, C.csa_attend_workspace(adesc)), dtype=torch.uint8, device=dev)
-    scores = torch.empty((1, w.T, w.N), dtype=torch.float32, device=dev)       # 4 GiB, visible part written
 
     def step(evs=None):
+        # the prefill path: the indexer scores and the top-k selection in one fused call (the
+        # score rows are never stored)
         rec = (lambda i: evs[i].record(stream)) if evs else (lambda i: None)
         rec(0)
         P.compress(inp["Ca"], inp["Za"], w.m, Cb=inp["Cb"], Zb=inp["Zb"], out=kv, stream=sptr)
         P.compress(inp["Ca_I"], inp["Za_I"], w.m, Cb=inp["Cb_I"], Zb=inp["Zb_I"], rope=False, rope_dims=0, out=kI,
                    stream=sptr)
         rec(1)
-        C.check(C.csa_index_score(idesc, inp["qI"], inp["w"], kI, None, inp["q_pos"], scores, ws_s, stream=sptr),
-                "csa_index_score")
+        C.check(C.csa_index_topk(idesc, inp["qI"], inp["w"], kI, None, inp["q_pos"], idx, None, wsi, stream=sptr),
+                "csa_index_topk")
         rec(2)
-        C.check(C.csa_topk(idesc, scores, inp["q_pos"], idx, ws_t, stream=sptr), "csa_topk")
-        rec(3)
         C.check(C.csa_attend(adesc, inp["q"], kv, idx, inp["win"], inp["sink"], inp["q_pos"], out, None, ws_a,
                              stream=sptr), "csa_attend")
-        rec(4)
+        rec(3)
 
     step()
     torch.cuda.synchronize()
+    n0 = C.csa_launch_count()
+    C.check(C.csa_index_topk(idesc, inp["qI"], inp["w"], kI, None, inp["q_pos"], idx, None, wsi, stream=sptr),
+            "csa_index_topk")
+    fused_launches = C.csa_launch_count() - n0
     times = []
     for _ in range(max(1, args.prefill_steps)):
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         step(evs)
         torch.cuda.synchronize()
-        times.append([evs[i].elapsed_time(evs[i + 1]) for i in range(4)])
-    comp, ind, topk, att = (statistics.median(x[i] for x in times) for i in range(4))
-    total = comp + ind + topk + att
+        times.append([evs[i].elapsed_time(evs[i + 1]) for i in range(3)])
+    comp, ind, att = (statistics.median(x[i] for x in times) for i in range(3))
+    total = comp + ind + att
+    idx_ref = idx.clone()
+    # the unfused calls on the same inputs, for the breakdown: scores stored (4 GiB), then the
+    # selector kernels; the selection must be the same bit for bit
+    scores = torch.empty((1, w.T, w.N), dtype=torch.float32, device=dev)
+    split = []
+    for _ in range(max(1, args.prefill_steps)):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        evs[0].record(stream)
+        C.check(C.csa_index_score(idesc, inp["qI"], inp["w"], kI, None, inp["q_pos"], scores, ws_s, stream=sptr),
+                "csa_index_score")
+        evs[1].record(stream)
+        C.check(C.csa_topk(idesc, scores, inp["q_pos"], idx, ws_t, stream=sptr), "csa_topk")
+        evs[2].record(stream)
+        torch.cuda.synchronize()
+        split.append([evs[0].elapsed_time(evs[1]), evs[1].elapsed_time(evs[2])])
+    sc_ms, tk_ms = (statistics.median(x[i] for x in split) for i in range(2))
+    same = bool(torch.equal(idx, idx_ref))
     idx_flops, att_flops = prefill_flops(w)
     with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
         pk = json.load(f)
     peak = pk.get("bf16_tflops_sustained", 1386.7)
     ind_tf = idx_flops / (ind * 1e-3) / 1e12
+    sc_tf = idx_flops / (sc_ms * 1e-3) / 1e12
     att_tf = att_flops / (att * 1e-3) / 1e12
     comp_bytes = w.T * (4 * w.d + 4 * w.dI) * 2 + w.N * (w.d + w.dI) * 2
-    del inp, kv, kI, idx, out, ws_s, ws_t, ws_a, scores
+    del inp, kv, kI, idx, idx_ref, out, wsi, ws_s, ws_t, ws_a, scores
     torch.cuda.empty_cache()
     return {
         "workload": "csa_prefill_t65536", "tok_per_s": w.T / (total * 1e-3), "ms_per_chunk": total,
         "steps": len(times),
-        "breakdown_ms": {"csa_compress_x2": comp, "csa_index_score": ind, "csa_topk": topk, "csa_attend": att},
+        "breakdown_ms": {"csa_compress_x2": comp, "csa_index_topk": ind, "csa_attend": att},
+        "index_topk_launches": fused_launches,
+        "unfused_index_topk_ms": {"csa_index_score": sc_ms, "csa_topk": tk_ms, "total": sc_ms + tk_ms,
+                                  "same_selection": same},
         "indexer_tensor": {"achieved": ind_tf, "peak": peak, "unit": "TFLOP/s", "frac": ind_tf / peak,
                            "flops_per_launch": idx_flops, "peak_kind": "measured sustained",
-                           "note": "k_index_score alone (tcgen05), flops of the causal score contraction"},
+                           "score_only_achieved": sc_tf,
+                           "note": "k_index_score with the fused selection (tcgen05), flops of the causal score "
+                                   "contraction; score_only_achieved: the same kernel storing the scores"},
         "attend_tensor": {"achieved": att_tf, "peak": peak, "unit": "TFLOP/s", "frac": att_tf / peak,
                           "flops_per_launch": att_flops},
         "compress_hbm": {"achieved": comp_bytes / (comp * 1e-3) / 1e9, "unit": "GB/s", "bytes": comp_bytes},
@@ -749,13 +777,14 @@ def run_case(args):
     """One library call on a small input, repeated: the command the ncu summaries under profiles/
     capture.  compress: the CSA main-stream compressor (T tokens of four [T, 512] bf16 streams);
     out_proj: the grouped output projection at Flash widths (O [T, 64, 512]); attend /
-    index_prefill: the sparse attention / the indexer scores of a CSA prefill chunk of T tokens."""
+    index_prefill / index_topk_prefill: the sparse attention / the indexer scores / the fused
+    indexer scores + top-k selection of a CSA prefill chunk of T tokens."""
     import torch
     from long_context_compressed_16_b300 import pipeline as P
     from long_context_compressed_16_b300 import synth as S
     dev = torch.device("cuda", 0)
     T = args.case_tokens
-    if args.case in ("attend", "index_prefill"):
+    if args.case in ("attend", "index_prefill", "index_topk_prefill"):
         # the CSA prefill shapes at T tokens (N = T / 4 entries, 64 heads x 512, k = 512): the
         # attention over seeded random selections, or the indexer scores of every causal pair
         from long_context_compressed_16_b300 import capi as C
@@ -773,6 +802,14 @@ def run_case(args):
             fn = lambda: C.check(C.csa_attend(adesc, inp["q"], kv, idx, inp["win"], inp["sink"], inp["q_pos"], out,
                                               None, ws), "csa_attend")
             _, flops = prefill_flops(w)
+        elif args.case == "index_topk_prefill":
+            kI = S.normal_bf16((1, w.N, w.dI), 3, S.TID["kI"], dev)
+            idesc = P.index_desc(1, w.T, w.N, w.nI, w.dI, w.k, w.m)
+            ws = torch.zeros(max(256, C.csa_index_topk_workspace(idesc)), dtype=torch.uint8, device=dev)
+            idx = torch.empty((1, w.T, w.k), dtype=torch.int32, device=dev)
+            fn = lambda: C.check(C.csa_index_topk(idesc, inp["qI"], inp["w"], kI, None, inp["q_pos"], idx, None, ws),
+                                 "csa_index_topk")
+            flops, _ = prefill_flops(w)
         else:
             kI = S.normal_bf16((1, w.N, w.dI), 3, S.TID["kI"], dev)
             idesc = P.index_desc(1, w.T, w.N, w.nI, w.dI, w.k, w.m)

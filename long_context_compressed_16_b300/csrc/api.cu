@@ -11,6 +11,9 @@ namespace {
 
 std::atomic<uint64_t> g_launches{0};
 
+#ifndef CSA_INDEX_FUSED_SELECT
+#define CSA_INDEX_FUSED_SELECT 1   // 0: csa_index_topk always stores score rows and runs the selector kernels
+#endif
 #ifndef CSA_SCORE_CHUNK_MIB
 #define CSA_SCORE_CHUNK_MIB 256
 #endif
@@ -112,6 +115,10 @@ struct IndexPlan {
   size_t cand_bytes;   // two-stage top-k candidates of one chunk (0 for rows <= one slice)
   size_t q8_bytes;     // low-precision indexer: e4m3 query rows of one chunk (0 otherwise)
   size_t wp_bytes;     // low-precision indexer: scaled head weights of one chunk
+  // fused selection (scores never stored): the score kernel selects each query's top k from
+  // per-CTA candidate lists that take the place of the score rows in the workspace
+  bool sel;
+  size_t sel_bytes;
 };
 
 inline bool is_lowp(const csa_index_desc* d) { return d->key_fmt == CSA_FMT_FP8_ROWSCALE_LOWP; }
@@ -160,7 +167,24 @@ IndexPlan plan_index(const csa_index_desc* d) {
   const size_t lowp_rows = is_lowp(d) ? static_cast<size_t>(p.chunk) * p.G * d->n_heads : 0;
   p.q8_bytes = round256(lowp_rows * 128);
   p.wp_bytes = round256(lowp_rows * sizeof(float));
+  // the fused selection walks whole groups per CTA, so it needs enough groups to balance the
+  // persistent grid; its lists take the place of the score rows (below about 28K entries per row
+  // they are the smaller of the two)
+  const csa::IndexGrouping gr = csa::index_grouping(d->n_heads, d->Tq);
+  p.sel = CSA_INDEX_FUSED_SELECT && d->N > 0 &&
+          csa::index_select_supported(gr, d->head_dim, fp8_keys(d), is_lowp(d), d->N) &&
+          p.groups >= 4LL * csa::index_select_ctas();
+  p.sel_bytes = p.sel ? round256(csa::index_select_bytes(gr, d->N)) : 0;
   return p;
+}
+
+// Workspace after the status word: the score rows (unless the caller stores them) and the two-
+// stage selector's candidates, or the fused selection's lists, whichever is larger; then the
+// low-precision indexer's query rows and weights.
+size_t index_region_a(const IndexPlan& p, bool score_out) {
+  const size_t unfused = (score_out ? 0 : p.score_bytes) + p.cand_bytes;
+  const size_t fused = (p.sel && !score_out) ? p.sel_bytes : 0;
+  return unfused > fused ? unfused : fused;
 }
 
 // ---------------------------------------------------------------- attention planning
@@ -401,7 +425,7 @@ csa_status csa_cache_append(const csa_cache_desc* d, int64_t t0, int n, const cs
 size_t csa_index_topk_workspace(const csa_index_desc* d) {
   if (!index_desc_ok(d)) return 0;
   const IndexPlan p = plan_index(d);
-  return csa::kStatusBytes + p.score_bytes + p.cand_bytes + p.q8_bytes + p.wp_bytes;
+  return csa::kStatusBytes + index_region_a(p, false) + p.q8_bytes + p.wp_bytes;
 }
 
 csa_status csa_index_topk(const csa_index_desc* d, const void* qI, const float* w, const void* kI,
@@ -412,8 +436,7 @@ csa_status csa_index_topk(const csa_index_desc* d, const void* qI, const float* 
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const IndexPlan plan = plan_index(d);
   if (!ws) return CSA_ERR_WORKSPACE;
-  if (ws_bytes < csa::kStatusBytes + (score_out ? 0 : plan.score_bytes) + plan.cand_bytes + plan.q8_bytes +
-                     plan.wp_bytes)
+  if (ws_bytes < csa::kStatusBytes + index_region_a(plan, score_out != nullptr) + plan.q8_bytes + plan.wp_bytes)
     return CSA_ERR_WORKSPACE;
   if (!aligned16(ws)) return CSA_ERR_INVALID_ARG;
   const long long Q = static_cast<long long>(d->B) * d->Tq;
@@ -440,7 +463,7 @@ csa_status csa_index_topk(const csa_index_desc* d, const void* qI, const float* 
   unsigned char* wsb = static_cast<unsigned char*>(ws);
   unsigned char* after_scores = wsb + csa::kStatusBytes + (score_out ? 0 : plan.score_bytes);
   void* cand = plan.cand_bytes ? after_scores : nullptr;
-  unsigned char* q8 = after_scores + plan.cand_bytes;                    // low-precision query rows
+  unsigned char* q8 = wsb + csa::kStatusBytes + index_region_a(plan, score_out != nullptr);   // low-precision query rows
   float* wp = reinterpret_cast<float*>(q8 + plan.q8_bytes);
   ia.lowp = lowp ? 1 : 0;
   int launches = 0;
@@ -450,6 +473,37 @@ csa_status csa_index_topk(const csa_index_desc* d, const void* qI, const float* 
     ta.scores = nullptr; ta.q_begin = 0; ta.q_count = static_cast<int>(Q); ta.score_row_offset = 0;
     e = csa::launch_topk(ta, cand, stream, &launches);
     count(launches);
+    return from_cuda(e);
+  }
+  if (plan.sel && !score_out) {
+    // scores and selection in one kernel: the candidate lists sit where the score rows would
+    ia.idx_out = idx_out;
+    ia.k = d->k;
+    ia.cand = reinterpret_cast<unsigned long long*>(wsb + csa::kStatusBytes);
+    ia.cand_cap = csa::index_select_cap(d->N);
+    ia.cand_ctas = csa::index_select_ctas();
+    ia.score_row_offset = 0;
+    // one launch over every group; the low-precision indexer quantises its queries per chunk
+    const long long sstep = lowp ? plan.chunk : plan.groups;
+    for (long long g0 = 0; g0 < plan.groups && e == cudaSuccess; g0 += sstep) {
+      const long long g1 = (g0 + sstep < plan.groups) ? g0 + sstep : plan.groups;
+      ia.q_begin = static_cast<int>(g0);
+      ia.q_count = static_cast<int>(g1 - g0);
+      if (lowp) {
+        const long long q_first = (g0 / gpb) * d->Tq + (g0 % gpb) * plan.G;
+        const long long gl = g1 - 1;
+        const long long q_last = (gl / gpb) * d->Tq + (gl % gpb) * plan.G +
+                                 ((d->Tq - (gl % gpb) * plan.G) < plan.G ? (d->Tq - (gl % gpb) * plan.G) : plan.G);
+        const long long row0 = q_first * d->n_heads;
+        e = csa::launch_quant_q(qI, w, q8, wp, row0, (q_last - q_first) * d->n_heads, stream, &launches);
+        if (e != cudaSuccess) break;
+        ia.qI = q8 - row0 * 128;
+        ia.w = wp - row0;
+      }
+      e = csa::launch_index_select(ia, grouping, stream, &launches);
+    }
+    count(launches);
+    if (e == cudaErrorInvalidValue) return CSA_ERR_UNSUPPORTED;
     return from_cuda(e);
   }
   const long long step = plan.chunk;

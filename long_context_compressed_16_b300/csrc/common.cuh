@@ -23,6 +23,13 @@ constexpr size_t kStatusBytes = 256;
 // Adds to the library's count of kernel launches (csa_launch_count).
 void note_launches(int n);
 
+// Order-preserving 32-bit key of an fp32 score (unsigned comparison of keys = comparison of the
+// scores); -0 and +0 map to the same key, so equal scores tie by entry index.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // Closed compressed blocks visible to position t: s < floor((t+1)/m), clipped to [0, N].
 __host__ __device__ __forceinline__ int n_visible(int t, int m, int N) {
   const long long v = (static_cast<long long>(t) + 1) / m;
@@ -213,6 +220,12 @@ struct IndexArgs {
   int bf16_scores;          // round each score to bf16 (RNE) before it is stored
   int q_begin, q_count;     // range of query GROUPS (G consecutive queries of one sequence)
   int score_row_offset;     // flattened query q (= b*Tq + i) owns score row q - score_row_offset
+  // fused selection (launch_index_select): the top-k rows, k, and the candidate lists (two
+  // buffers of G lists of cand_cap (key, entry) slots per CTA, for cand_ctas CTAs; a list is four
+  // sub-lists of cand_cap / 4 slots)
+  int32_t* idx_out;
+  unsigned long long* cand;
+  int cand_cap, cand_ctas, k;
 };
 
 // How the indexer packs queries into one tensor-core N dimension: heads padded to NHP (a power
@@ -240,6 +253,15 @@ cudaError_t launch_quant_q(const void* qI, const float* w, void* q8, float* wp, 
                            cudaStream_t s, int* launches);
 cudaError_t launch_index_score_groups(const IndexArgs& a, const IndexGrouping& gr, int fill_invisible,
                                       cudaStream_t s, int* launches);
+// Scores and top-k in one kernel (the selection fused into the score kernel's epilogue): only for
+// groupings of 4 queries x 64 heads (256 MMA columns), rows of at most 32768 entries, bf16 keys
+// or the low-precision indexer.  index_select_supported says whether a call of this shape takes it;
+// index_select_bytes is the candidate-list workspace it needs on the current device.
+bool index_select_supported(const IndexGrouping& gr, int dI, int fp8, int lowp, int N);
+size_t index_select_bytes(const IndexGrouping& gr, int N);
+int index_select_cap(int N);
+int index_select_ctas();
+cudaError_t launch_index_select(const IndexArgs& a, const IndexGrouping& gr, cudaStream_t s, int* launches);
 
 struct TopkArgs {
   const float* scores;

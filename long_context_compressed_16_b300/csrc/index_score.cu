@@ -44,7 +44,19 @@ constexpr int kMaxSmem = 232448;        // dynamic shared memory per block on sm
 // FP8: e4m3 keys with per-row scales.  LP (low-precision indexer): the query is e4m3 too and the
 // contraction runs on the FP8 tensor cores (kind::f8f6f4, K = 32 per instruction); otherwise FP8
 // keys are widened to bf16 in shared memory by converter warps.
-template <int DI, int NCOL, bool FP8, bool LP = false>
+// Fused selection (CAND): the epilogue keeps, per query, the (key, entry) pairs above a running
+// lower bound of the k-th largest score seen so far, and two selector warps pick each finished
+// group's top-k from those lists (see the selector and the candidate epilogue below).
+constexpr int kCandG = 4;          // queries per group the fused selection holds
+constexpr int kCandBins = 256;     // histogram bins per query (bin 0 collects everything below)
+constexpr int kClassShift = 17;    // key class = key >> 17: sign, exponent, 6 mantissa bits (64 per octave)
+constexpr int kCandHead = 64;      // classes of headroom above the first tile's largest key (one octave)
+constexpr int kSelWarps = 2;       // selector warps (warps 2 and 3, idle otherwise)
+constexpr int kSelMembers = 512;   // keys of the k-th entry's class a selector warp holds
+constexpr int kSelBitmap = 1024;   // words of a selector warp's entry bitmap (rows of up to 32768 entries)
+constexpr int kSelU = 8;           // candidate-list loads in flight per lane
+
+template <int DI, int NCOL, bool FP8, bool LP = false, bool CAND = false>
 struct Cfg {
   static constexpr bool WIDEN = FP8 && !LP;               // converter warps widen e4m3 to bf16
   static constexpr int ESIZE = LP ? 1 : 2;                // operand bytes per element
@@ -65,17 +77,30 @@ struct Cfg {
   // FP8 keys with N <= 128: the widening to bf16 is the busiest role, so 8 converter warps and
   // one set of 4 epilogue warps; otherwise 8 epilogue warps (two sets of four) and 4 converters
   static constexpr bool CONV_HEAVY = WIDEN && NCOL <= 128;
-  static constexpr int EW = (CONV_HEAVY || CTAS == 2) ? 4 : 8;   // epilogue warps
+  // 256 columns without widening (the prefill groupings): 16 epilogue warps, four per SM
+  // sub-partition, so that more tensor-memory loads are in flight (one warp's loads are serial,
+  // about 44 bytes per clock each) and each warp sums one query of 64 heads per tile
+  static constexpr int EW = (CONV_HEAVY || CTAS == 2) ? 4 : (NCOL == 256 && !WIDEN) ? 16 : 8;   // epilogue warps
   // NCOL <= 128: the two sets take alternate tiles; wider: they split the group's queries
   static constexpr bool TSPLIT = EW == 8 && NCOL <= 128;
   static constexpr int ACC_ARRIVALS = 32 * (TSPLIT ? EW / 2 : EW);   // epilogue threads per tile
   static constexpr int CW = WIDEN ? (CONV_HEAVY ? 8 : 4) : 0;   // converter warps
   static constexpr int THREADS = 32 * (4 + EW + CW);
-  static constexpr int W_FLOATS = EW * NCOL;              // per-epilogue-warp copy of the head weights
+  static constexpr int SPLIT = TSPLIT ? 1 : EW / 4;        // warp sets splitting a group's queries
+  static constexpr int QW = NCOL / 64 / SPLIT > 0 ? NCOL / 64 / SPLIT : 1;   // queries per warp with 64 heads
+  static constexpr int W_FLOATS = EW * (NCOL / SPLIT);    // per-epilogue-warp copy of its queries' head weights
   static constexpr int GMAX = 16;                         // queries per group (NCOL / 16 heads at most)
   static constexpr int NV_INTS = EW * GMAX;               // per-epilogue-warp visible counts of the group
   static constexpr int MISC = 1024;                       // barriers, TMEM address, flags
-  static constexpr int FIXED = 1024 /*alignment slack*/ + QB * Q_BYTES + W_FLOATS * 4 + NV_INTS * 4 + MISC;
+  // fused selection: per-query histograms (two group buffers), the per-tile ballot and maximum
+  // exchange (two tile buffers), thresholds / bases / counts, the handoff barriers, and the
+  // selector warps' histograms and class-member keys
+  static constexpr int CAND_SMEM =
+      CAND ? (2 * kCandG * kCandBins + 2 * kCandG * 4 /*maxima*/ + 2 * kCandG * 2 /*thr, lo*/ +
+              2 * kCandG * 4 /*counts*/) * 4 + 4 * 8 + kSelWarps * (kCandBins + kSelMembers + kSelBitmap) * 4
+           : 0;
+  static constexpr int FIXED =
+      1024 /*alignment slack*/ + QB * Q_BYTES + W_FLOATS * 4 + NV_INTS * 4 + MISC + CAND_SMEM;
   static constexpr int S_RAW = (SMEM_CAP - FIXED) / (STAGE_BYTES + STAGED_BYTES);
   static constexpr int STAGES = S_RAW > CSA_IDX_MAX_STAGES ? CSA_IDX_MAX_STAGES : S_RAW;
   static constexpr int SMEM = FIXED + STAGES * (STAGE_BYTES + STAGED_BYTES);
@@ -86,6 +111,8 @@ struct Cfg {
   static_assert(SMEM <= SMEM_CAP, "shared memory budget");
   static_assert(CTAS == 1 || TMEM_COLS <= 256, "two CTAs per SM must share the 512 TMEM columns");
   static_assert(NCOL % 16 == 0 && NCOL >= 16 && NCOL <= 256, "UMMA N for M = 128");
+  // the candidate epilogue needs every tile seen by both warp sets (each owns half the queries)
+  static_assert(!CAND || (!WIDEN && EW == 16 && !TSPLIT && QW == 1), "fused selection layout");
 };
 
 struct TcParams {
@@ -218,11 +245,291 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf162(uint16_t v) {
   return pack_bf16x2(f.x, f.y);
 }
 
-template <int DI, int NCOL, bool FP8, bool LP>
-__global__ void __launch_bounds__(Cfg<DI, NCOL, FP8, LP>::THREADS, Cfg<DI, NCOL, FP8, LP>::CTAS)
+// ------------------------------------------------------------------ fused selection: selector
+//
+// The selection is the TopK_k equation of the CSA path ("DeepSeek V4 模型技术大全") with ties to
+// the smaller entry.  It reads the query's candidates (every entry that can still be among its
+// top k: four sub-lists, one per quarter of each tile's keys, each in increasing entry order, of
+// key << 32 | entry) instead of the whole score row.
+
+constexpr uint32_t kEntryMax = 0x3FFFFu;   // entries are below 2^18: kEntryMax - entry orders them reversed
+
+struct CandLists {
+  const unsigned long long* base;   // sub-list q at base + q * sub_cap
+  int sub_cap;
+  int n[4];
+};
+
+// f(e, valid) for every candidate, warp-uniform: 32 consecutive entries of a sub-list per call
+// round, kSelU rounds of loads in flight
+template <typename F>
+__device__ __forceinline__ void for_each_cand(const CandLists& cl, F f) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll 1
+  for (int q = 0; q < 4; ++q) {
+    const unsigned long long* sub = cl.base + static_cast<long long>(q) * cl.sub_cap;
+    const int n = cl.n[q];
+    for (int b = 0; b < n; b += 32 * kSelU) {
+      unsigned long long e[kSelU];
+#pragma unroll
+      for (int u = 0; u < kSelU; ++u) {
+        const int i = b + u * 32 + lane;
+        e[u] = i < n ? sub[i] : 0ull;
+      }
+#pragma unroll
+      for (int u = 0; u < kSelU; ++u) f(e[u], b + u * 32 + lane < n);
+    }
+  }
+}
+
+// Warp-wide radix select, 8 bits at a time.  each(g) calls g(key, valid) for every element
+// (warp-uniform).  Among the valid keys whose bits at and above `pos` equal `prefix`, finds the
+// rem-th largest.  On return prefix holds the threshold's bits at and above cmp_shift, rem how
+// many keys equal to it at that level are taken, and eq how many there are (eq = rem when the
+// threshold bin is taken whole; unchanged when no pass ran).  wh: kCandBins zeroed shared bins,
+// zeroed again on return.  False when the counts cannot hold the rem-th key.
+template <typename Each>
+__device__ bool warp_radix(Each each, int pos, uint32_t& prefix, int& rem, int& cmp_shift, uint32_t& eq, uint32_t* wh) {
+  const int lane = threadIdx.x & 31;
+  cmp_shift = pos;
+  while (pos > 0) {
+    const int nbits = pos < 8 ? pos : 8;
+    const int sh = pos - nbits;
+    const uint32_t dmask = (1u << nbits) - 1u;
+    const uint32_t hmask = pos >= 32 ? 0u : ~((1u << pos) - 1u);
+    const uint32_t pf = prefix;
+    each([&](uint32_t kk, bool v) {
+      if (v && (kk & hmask) == pf) atomicAdd(&wh[(kk >> sh) & dmask], 1u);
+    });
+    __syncwarp();
+    // lane owns 8 bins at descending positions and clears them for the next pass
+    const int nb = 1 << nbits;
+    uint32_t c[8];
+    uint32_t csum = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int bin = nb - 1 - (8 * lane + u);
+      c[u] = 0u;
+      if (bin >= 0) {
+        c[u] = wh[bin];
+        wh[bin] = 0u;
+      }
+      csum += c[u];
+    }
+    uint32_t incl = csum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    uint32_t above = incl - csum;
+    const uint32_t r = static_cast<uint32_t>(rem);
+    int fb = -1;
+    uint32_t fa = 0, fc = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (above < r && r <= above + c[u]) {
+        fb = nb - 1 - (8 * lane + u);
+        fa = above;
+        fc = c[u];
+      }
+      above += c[u];
+    }
+    const uint32_t fm = __ballot_sync(0xffffffffu, fb >= 0);
+    __syncwarp();
+    if (fm == 0u) return false;
+    const int src = __ffs(fm) - 1;
+    fb = __shfl_sync(0xffffffffu, fb, src);
+    fa = __shfl_sync(0xffffffffu, fa, src);
+    fc = __shfl_sync(0xffffffffu, fc, src);
+    prefix |= static_cast<uint32_t>(fb) << sh;
+    rem -= static_cast<int>(fa);
+    eq = fc;
+    pos = sh;
+    cmp_shift = sh;
+    if (fc == static_cast<uint32_t>(rem)) break;   // the threshold bin is taken whole
+  }
+  return true;
+}
+
+// Top-k row of query qi from its candidates and the final histogram of their key classes (bins
+// 1 .. kCandBins-2 hold the single class lo + bin - 1).  The k-th largest key is found first: when
+// its class is one of those bins and holds at most kSelMembers keys, only that class is resolved
+// (its low key bits, in shared memory; two passes over the lists), otherwise the lists are radix-
+// selected whole.  Keys equal to the threshold beyond what is taken go by smallest entry (a radix
+// select on kEntryMax - entry).  The selected entries are marked in a bitmap of the row, which is
+// read in order: the output lists them in increasing entry, as the TopK definition's ties need.
+__device__ void select_query(const IndexArgs& a, long long qi, const CandLists& cl, const uint32_t* hist, int lo,
+                             int shift, uint32_t* wh, uint32_t* mem, uint32_t* bm) {
+  const int lane = threadIdx.x & 31;
+  const int K = a.k;
+  int32_t* out = a.idx_out + qi * K;
+  const int nv = n_visible(a.q_pos[qi], a.m, a.N);
+  if (nv <= K) {
+    for (int i = lane; i < K; i += 32) out[i] = i < nv ? i : -1;
+    return;
+  }
+  const int L = cl.n[0] + cl.n[1] + cl.n[2] + cl.n[3];
+  if (L < K || (nv + 31) / 32 > kSelBitmap) {   // cannot happen: the lists hold the row's top k
+    if (lane == 0) report_error(a.status, CSA_ERR_DEVICE_CHECK, -2000);
+    return;
+  }
+  uint32_t c[8];
+  uint32_t csum = 0;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    c[u] = hist[kCandBins - 1 - (8 * lane + u)];
+    csum += c[u];
+  }
+  uint32_t incl = csum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  uint32_t above = incl - csum;
+  int fb = -1;
+  uint32_t fa = 0, fc = 0;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    if (above < static_cast<uint32_t>(K) && static_cast<uint32_t>(K) <= above + c[u]) {
+      fb = kCandBins - 1 - (8 * lane + u);
+      fa = above;
+      fc = c[u];
+    }
+    above += c[u];
+  }
+  const uint32_t fm = __ballot_sync(0xffffffffu, fb >= 0);
+  if (fm != 0u) {
+    const int src = __ffs(fm) - 1;
+    fb = __shfl_sync(0xffffffffu, fb, src);
+    fa = __shfl_sync(0xffffffffu, fa, src);
+    fc = __shfl_sync(0xffffffffu, fc, src);
+  } else {
+    fb = -1;
+  }
+  const uint32_t lt = (1u << lane) - 1u;
+  uint32_t thr = 0, eq = 0;
+  int rem = K, cmp = 0;
+  bool ok = true;
+  const int lowb = kClassShift - shift;        // key bits below the class
+  if (fb >= 1 && fb <= kCandBins - 2 && fc <= static_cast<uint32_t>(kSelMembers)) {
+    const uint32_t cls = static_cast<uint32_t>(lo + fb - 1);
+    const uint32_t lmask = (1u << lowb) - 1u;
+    uint32_t m = 0;
+    for_each_cand(cl, [&](unsigned long long e, bool v) {
+      const uint32_t ks = static_cast<uint32_t>(e >> 32);
+      const bool hit = v && (ks >> lowb) == cls;
+      const uint32_t hm = __ballot_sync(0xffffffffu, hit);
+      if (hit) {
+        const uint32_t q = m + __popc(hm & lt);
+        if (q < static_cast<uint32_t>(kSelMembers)) mem[q] = ks & lmask;
+      }
+      m += __popc(hm);
+    });
+    __syncwarp();
+    if (m != fc) {
+      if (lane == 0) report_error(a.status, CSA_ERR_DEVICE_CHECK, -2001);
+      return;
+    }
+    rem = K - static_cast<int>(fa);
+    uint32_t pre = 0;
+    eq = fc;
+    if (fc == static_cast<uint32_t>(rem)) {
+      cmp = lowb;                                // the whole class is taken
+    } else {
+      const int nm = static_cast<int>(fc);
+      ok = warp_radix([&](auto g) {
+        for (int b = 0; b < nm; b += 32) g(b + lane < nm ? mem[b + lane] : 0u, b + lane < nm);
+      }, lowb, pre, rem, cmp, eq, wh);
+    }
+    thr = (cls << lowb) | pre;
+  } else {
+    uint32_t kmax = 0u, kmin = 0xFFFFFFFFu;
+    for_each_cand(cl, [&](unsigned long long e, bool v) {
+      if (v) {
+        const uint32_t ks = static_cast<uint32_t>(e >> 32);
+        kmax = max(kmax, ks);
+        kmin = min(kmin, ks);
+      }
+    });
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+      kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+    }
+    const int pos = kmax == kmin ? 0 : 32 - __clz(kmax ^ kmin);
+    uint32_t pre = pos >= 32 ? 0u : (kmax >> pos) << pos;
+    rem = K;
+    eq = static_cast<uint32_t>(L);               // no pass: every key equals kmax
+    ok = warp_radix([&](auto g) {
+      for_each_cand(cl, [&](unsigned long long e, bool v) { g(static_cast<uint32_t>(e >> 32), v); });
+    }, pos, pre, rem, cmp, eq, wh);
+    thr = pre;
+  }
+  // keys equal to the threshold, more of them than are taken: the smallest entries go first
+  const bool ties = ok && cmp == 0 && eq > static_cast<uint32_t>(rem);
+  uint32_t tpre = 0;
+  int tcmp_shift = 0;
+  if (ties) {
+    int trem = rem;
+    uint32_t teq = 0;
+    const uint32_t t = thr;
+    ok = warp_radix([&](auto g) {
+      for_each_cand(cl, [&](unsigned long long e, bool v) {
+        g(kEntryMax - static_cast<uint32_t>(e & 0xFFFFFFFFull), v && static_cast<uint32_t>(e >> 32) == t);
+      });
+    }, 18, tpre, trem, tcmp_shift, teq, wh);
+  }
+  if (!ok) {
+    if (lane == 0) report_error(a.status, CSA_ERR_DEVICE_CHECK, -2002);
+    return;
+  }
+  const int nwords = (nv + 31) / 32;
+  for (int i = lane; i < nwords; i += 32) bm[i] = 0u;
+  __syncwarp();
+  const uint32_t tc_ = cmp >= 32 ? 0u : thr >> cmp;
+  for_each_cand(cl, [&](unsigned long long e, bool v) {
+    const uint32_t ks = static_cast<uint32_t>(e >> 32);
+    const uint32_t entry = static_cast<uint32_t>(e & 0xFFFFFFFFull);
+    const uint32_t kt = cmp >= 32 ? 0u : ks >> cmp;
+    bool sel = v && kt >= tc_;
+    if (sel && kt == tc_ && ties) sel = ((kEntryMax - entry) >> tcmp_shift) >= (tpre >> tcmp_shift);
+    if (sel && entry < static_cast<uint32_t>(nv)) atomicOr(&bm[entry >> 5], 1u << (entry & 31));
+  });
+  __syncwarp();
+  // the marked entries in increasing order: lane l reads words [l W, (l + 1) W)
+  const int W = (nwords + 31) / 32;
+  const int w0 = min(nwords, lane * W), w1 = min(nwords, w0 + W);
+  uint32_t cnt = 0;
+  for (int i = w0; i < w1; ++i) cnt += __popc(bm[i]);
+  uint32_t ex = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, ex, o);
+    if (lane >= o) ex += y;
+  }
+  const uint32_t total = __shfl_sync(0xffffffffu, ex, 31);
+  if (total != static_cast<uint32_t>(K)) {
+    if (lane == 0) report_error(a.status, CSA_ERR_DEVICE_CHECK, -2003);
+    return;
+  }
+  uint32_t o = ex - cnt;
+  for (int i = w0; i < w1; ++i) {
+    uint32_t bits = bm[i];
+    while (bits != 0u) {
+      const int b = __ffs(bits) - 1;
+      out[o++] = i * 32 + b;
+      bits &= bits - 1u;
+    }
+  }
+}
+
+template <int DI, int NCOL, bool FP8, bool LP, bool CAND>
+__global__ void __launch_bounds__(Cfg<DI, NCOL, FP8, LP, CAND>::THREADS, Cfg<DI, NCOL, FP8, LP, CAND>::CTAS)
 k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
               const TcParams p) {
-  using C = Cfg<DI, NCOL, FP8, LP>;
+  using C = Cfg<DI, NCOL, FP8, LP, CAND>;
   constexpr int S = C::STAGES;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // TMA destinations and the 128-byte swizzle atoms need 1024-byte alignment of the shared-window
@@ -231,7 +538,7 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
   unsigned char* qbuf = smem;                                         // QB x Q_BYTES
   unsigned char* kbuf = qbuf + C::QB * C::Q_BYTES;                    // S x STAGE_BYTES
   unsigned char* sbuf = kbuf + S * C::STAGE_BYTES;                    // S x STAGED_BYTES (FP8)
-  float* wsm = reinterpret_cast<float*>(sbuf + S * C::STAGED_BYTES);  // [EW][NCOL]
+  float* wsm = reinterpret_cast<float*>(sbuf + S * C::STAGED_BYTES);  // [EW][NCOL / SPLIT]
   int* nvsm = reinterpret_cast<int*>(wsm + C::W_FLOATS);                // [EW][GMAX]
   uint64_t* bars = reinterpret_cast<uint64_t*>(nvsm + C::NV_INTS);
   uint64_t* full = bars;              // [S] operand ready (TMA bytes, or converters)
@@ -245,6 +552,18 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
   uint64_t* drain = accempty + 4;     // [1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // fused selection (CAND only; past the barriers' area).  Index [buf] is the group buffer (group
+  // parity), [G] the query in the group, [4] the quarter of the tile's keys (epilogue warp).
+  uint32_t* chist = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(bars) + C::MISC);  // [2][G][bins]
+  uint32_t* cwmax = chist + 2 * kCandG * kCandBins;   // [2][G][4] largest key of a group's first tile
+  volatile uint32_t* cthr = cwmax + 2 * kCandG * 4;   // [2][G] emit when key >= thr
+  int* clo = reinterpret_cast<int*>(cwmax + 2 * kCandG * 4 + 2 * kCandG);   // [2][G] class of bin 1
+  int* ccnt = clo + 2 * kCandG;                        // [2][G][4] sub-list lengths
+  uint64_t* gdone = reinterpret_cast<uint64_t*>(ccnt + 2 * kCandG * 4);   // [2] group's lists complete
+  uint64_t* gfree = gdone + 2;                         // [2] selectors done with a buffer
+  uint32_t* selh = reinterpret_cast<uint32_t*>(gfree + 2);   // [kSelWarps][bins]
+  uint32_t* selm = selh + kSelWarps * kCandBins;             // [kSelWarps][kSelMembers]
+  uint32_t* selb = selm + kSelWarps * kSelMembers;           // [kSelWarps][kSelBitmap]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ngroups = a.q_count;
@@ -253,11 +572,16 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
 
   // alignment the TMA / tensor-core path relies on; a violation is reported, never executed
   {
-    const uint32_t bad = (tc::sptr(smem) & 1023u) | (tc::sptr(bars) & 7u) |
+    const uint32_t bad = (tc::sptr(smem) & 1023u) | (tc::sptr(bars) & 7u) | (CAND ? tc::sptr(gdone) & 7u : 0u) |
                          static_cast<uint32_t>(reinterpret_cast<uintptr_t>(&kmap) & 63u) |
                          static_cast<uint32_t>(reinterpret_cast<uintptr_t>(&qmap) & 63u);
     if (bad != 0u) {
       if (threadIdx.x == 0) report_error(a.status, CSA_ERR_DEVICE_CHECK, -1000 - static_cast<int>(bad));
+      return;
+    }
+    // the candidate lists were sized for cand_ctas CTAs of at most kCandG queries per group
+    if (CAND && (static_cast<int>(blockIdx.x) >= a.cand_ctas || p.G > kCandG || p.mode != 1)) {
+      if (threadIdx.x == 0) report_error(a.status, CSA_ERR_DEVICE_CHECK, -1100);
       return;
     }
   }
@@ -278,6 +602,12 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
       tc::mbar_init(&accempty[i], C::ACC_ARRIVALS);
     }
     tc::mbar_init(drain, 1);
+    if (CAND) {
+      for (int i = 0; i < 2; ++i) {
+        tc::mbar_init(&gdone[i], 32 * C::EW);
+        tc::mbar_init(&gfree[i], kSelWarps);
+      }
+    }
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -416,12 +746,92 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
     const int quarter = warp & 3;                 // TMEM lanes [32*quarter, +32)
     const int set = ew >> 2;                      // warp set: its tile parity or its query half
     const int half = C::TSPLIT ? 0 : set;
-    constexpr int SPLIT = C::TSPLIT ? 1 : C::EW / 4;
+    constexpr int SPLIT = C::SPLIT;
     const int NHP = p.NHP, G = p.G;
     const int qs_per = (G + SPLIT - 1) / SPLIT;
     const int j_lo = half * qs_per, j_hi = min(G, j_lo + qs_per);
-    float* wb = wsm + ew * NCOL;                  // this warp's copy of the group's head weights
+    float* wb = wsm + ew * (NCOL / SPLIT);        // this warp's copy of its queries' head weights
     int* nvb = nvsm + ew * C::GMAX;               // and of its queries' visible entry counts
+    const int jn = j_hi - j_lo;                  // this warp's queries j_lo + jj, jj < jn (<= C::QW for 64 heads)
+    // w-weighted ReLU head sums of the warp's queries at this thread's key (TMEM lane) of the tile
+    // in tbase: per query four independent partial sums in a fixed order, sum = (p0 + p1) +
+    // (p2 + p3); head h always feeds partial sum h % 4, in increasing h, whatever the load width.
+    // 64 heads (at most C::QW queries per warp): 32-column loads, the next one in flight while the
+    // current one is summed, and the pairs (p0, p1), (p2, p3) updated by packed fused
+    // multiply-adds (the same roundings as one at a time).
+    auto head_sums = [&](uint32_t tbase, float (&sums)[C::QW]) {
+      float ps[C::QW][4];
+#pragma unroll
+      for (int jj = 0; jj < C::QW; ++jj) ps[jj][0] = ps[jj][1] = ps[jj][2] = ps[jj][3] = 0.f;
+      uint32_t ra[32], rb[32];
+      const int nch = 2 * jn;
+      tc::tmem_ld32_issue(tbase + j_lo * 64, ra);
+      tc::tmem_ld_wait();
+      tc::reg_fence32(ra);
+#pragma unroll
+      for (int c = 0; c < 2 * C::QW; ++c) {
+        if (c < nch) {
+          if (c + 1 < nch) {
+            const uint32_t col = static_cast<uint32_t>((j_lo + ((c + 1) >> 1)) * 64 + ((c + 1) & 1) * 32);
+            if (c & 1) tc::tmem_ld32_issue(tbase + col, ra);
+            else tc::tmem_ld32_issue(tbase + col, rb);
+          }
+          const uint32_t(&cur)[32] = (c & 1) ? rb : ra;
+          const float4* w4 = reinterpret_cast<const float4*>(wb + (c >> 1) * 64 + (c & 1) * 32);
+#pragma unroll
+          for (int h = 0; h < 32; h += 4) {
+            const float4 ww = w4[h >> 2];
+            tc::fma_f32x2(ps[c >> 1][0], ps[c >> 1][1], ww.x, ww.y, fmaxf(__uint_as_float(cur[h]), 0.f),
+                          fmaxf(__uint_as_float(cur[h + 1]), 0.f));
+            tc::fma_f32x2(ps[c >> 1][2], ps[c >> 1][3], ww.z, ww.w, fmaxf(__uint_as_float(cur[h + 2]), 0.f),
+                          fmaxf(__uint_as_float(cur[h + 3]), 0.f));
+          }
+          if (c + 1 < nch) {
+            tc::tmem_ld_wait();
+            if (c & 1) tc::reg_fence32(ra);
+            else tc::reg_fence32(rb);
+          }
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < C::QW; ++jj) sums[jj] = (ps[jj][0] + ps[jj][1]) + (ps[jj][2] + ps[jj][3]);
+    };
+    // 16 or 32 heads: one query at a time, one load of its columns
+    auto head_sum1 = [&](uint32_t tbase, int j) -> float {
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      auto accum = [&](const float* v, const float* wrow, int cnt) {
+        const float4* w4 = reinterpret_cast<const float4*>(wrow);
+#pragma unroll
+        for (int h = 0; h < cnt; h += 4) {
+          const float4 ww = w4[h >> 2];
+          ps[0] = fmaf(ww.x, fmaxf(v[h], 0.f), ps[0]);
+          ps[1] = fmaf(ww.y, fmaxf(v[h + 1], 0.f), ps[1]);
+          ps[2] = fmaf(ww.z, fmaxf(v[h + 2], 0.f), ps[2]);
+          ps[3] = fmaf(ww.w, fmaxf(v[h + 3], 0.f), ps[3]);
+        }
+      };
+      if (NHP == 16) {
+        float v[16];
+        tc::tmem_ld16_wait(tbase + j * NHP, v);
+        accum(v, wb + (j - j_lo) * NHP, 16);
+      } else {
+        float v[32];
+        tc::tmem_ld32_wait(tbase + j * NHP, v);
+        accum(v, wb + (j - j_lo) * NHP, 32);
+      }
+      return (ps[0] + ps[1]) + (ps[2] + ps[3]);
+    };
+    // fused selection state.  Every warp keeps its own sub-list per query (its quarter of each
+    // tile's keys, in entry order) and its length; the set agrees on each group's histogram base
+    const int tis = quarter * 32 + lane;          // thread index inside the warp set
+    const int cshift = a.bf16_scores ? 16 : 0;
+    const int sub_cap = a.cand_cap / 4;
+    int gce = -1, cbuf = 0;
+    int ccount[C::QW], clos[C::QW];
+#pragma unroll
+    for (int jj = 0; jj < C::QW; ++jj) ccount[jj] = clos[jj] = 0;
+    unsigned long long* csub = nullptr;           // this warp's sub-list of query j_lo
+    bool dead = false;                            // a wait of this warp gave up: walk on, do nothing
     Walker wk;
     wk.init(p, ngroups);
     long long n = 0;
@@ -435,12 +845,31 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
           float v = 0.f;
           if (j < wk.gi.nq && h < a.nI)
             v = a.w[(static_cast<size_t>(wk.gi.b) * a.Tq + wk.gi.i0 + j) * a.nI + h];
-          wb[c] = v;
+          wb[c - j_lo * NHP] = v;
         }
         for (int j = j_lo + lane; j < j_hi; j += 32)
           nvb[j] = j < wk.gi.nq ? n_visible(a.q_pos[static_cast<size_t>(wk.gi.b) * a.Tq + wk.gi.i0 + j], a.m, a.N)
                                 : 0;
         __syncwarp();
+        if (CAND) {
+          // the selectors are done with this buffer (it held group gce - 2); clear this set's
+          // histograms and thresholds (ordered before any use by the first tile's barrier)
+          ++gce;
+          cbuf = gce & 1;
+          if (!dead && !__all_sync(0xffffffffu, tc::mbar_wait(&gfree[cbuf], ((gce >> 1) & 1) ^ 1, abort_flag))) {
+            dead = true;
+            fail(12);
+          }
+          if (!dead) {
+            uint32_t* hb = chist + (cbuf * kCandG + j_lo) * kCandBins;
+            for (int i = tis; i < jn * kCandBins; i += 128) hb[i] = 0u;
+            if (tis < jn) cthr[cbuf * kCandG + j_lo + tis] = 0u;
+          }
+#pragma unroll
+          for (int jj = 0; jj < C::QW; ++jj) ccount[jj] = 0;
+          csub = a.cand + ((static_cast<long long>(blockIdx.x) * 2 + cbuf) * p.G + j_lo) *
+                              static_cast<long long>(a.cand_cap) + static_cast<long long>(quarter) * sub_cap;
+        }
       }
       if (C::TSPLIT && static_cast<int>(n & 1) != set) {   // the other set's tile
         ++n;
@@ -450,42 +879,153 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
       const int key = wk.t * KT + quarter * 32 + lane;
       float kscale = 1.f;                         // issued before the wait so its latency overlaps it
       if (FP8 && key < a.N) kscale = a.kI_scale[static_cast<size_t>(wk.gi.b) * a.N + key];
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * NCOL;
+      if (CAND) {
+        // ---- candidate epilogue.  Per query, each warp appends the visible entries of its
+        // quarter whose key is at least the query's threshold to its sub-list, and counts them in
+        // the query's histogram of key classes (the key's top 15 bits: 64 classes per octave; bin 0
+        // collects the classes below the range, the top bin those above).  One warp of the set per
+        // tile raises one query's threshold to just above the lowest edge of a class whose bins at
+        // and above it already hold k entries: every entry of a later tile at or below that edge
+        // is beaten by those k (smaller entries, keys at least as large), so the lists keep every
+        // entry of the row's top k.  Any partial view of the histogram undercounts, so a threshold
+        // read early, or computed while other warps still add to the bins, is still a valid bound.
+        const bool first = wk.t == 0, last = wk.t == wk.gi.nt - 1;
+        float sv[C::QW];
+#pragma unroll
+        for (int jj = 0; jj < C::QW; ++jj) sv[jj] = 0.f;
+        if (!dead) {
+          if (__all_sync(0xffffffffu, tc::mbar_wait(&accfull[acc], (n / C::ACC) & 1, abort_flag))) {
+            tc::tc_fence_after();
+            head_sums(tbase, sv);
+            tc::tc_fence_before();
+            tc::mbar_arrive(&accempty[acc]);      // tensor memory is free for the next tile
+          } else {
+            dead = true;
+            fail(6);
+          }
+        }
+        uint32_t k32[C::QW];
+        bool vis[C::QW];
+#pragma unroll
+        for (int jj = 0; jj < C::QW; ++jj) {
+          k32[jj] = 0u;
+          vis[jj] = false;
+        }
+#pragma unroll
+        for (int jj = 0; jj < C::QW; ++jj) {
+          if (jj < jn) {
+            const int j = j_lo + jj;
+            const int nv = nvb[j];
+            float v = sv[jj] * kscale;
+            if (a.bf16_scores) v = __bfloat162float(__float2bfloat16_rn(v));
+            vis[jj] = j < wk.gi.nq && key < nv && nv > a.k;
+            k32[jj] = order_key(v);
+          }
+        }
+        if (first) {
+          // the histogram base of each query: the largest key of the group's first tile, agreed by
+          // the set (the only barrier of the group; a warp that gave up makes the set leave here)
+          if (!dead) {
+#pragma unroll
+            for (int jj = 0; jj < C::QW; ++jj) {
+              if (jj < jn) {
+                uint32_t mx = vis[jj] ? k32[jj] : 0u;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                if (lane == 0) cwmax[(cbuf * kCandG + j_lo + jj) * 4 + quarter] = mx;
+              }
+            }
+          }
+          if (tc::named_bar_or(1 + set, 128, dead)) break;
+#pragma unroll
+          for (int jj = 0; jj < C::QW; ++jj) {
+            if (jj < jn) {
+              const uint32_t* wm = cwmax + (cbuf * kCandG + j_lo + jj) * 4;
+              const uint32_t mx = max(max(wm[0], wm[1]), max(wm[2], wm[3]));
+              clos[jj] = static_cast<int>(mx >> kClassShift) + kCandHead - (kCandBins - 2);
+              if (tis == 0) clo[cbuf * kCandG + j_lo + jj] = clos[jj];
+            }
+          }
+        }
+        if (dead) {
+          ++n;
+          continue;
+        }
+#pragma unroll
+        for (int jj = 0; jj < C::QW; ++jj) {
+          if (jj < jn) {
+            const int j = j_lo + jj;
+            const uint32_t thr = first ? 0u : cthr[cbuf * kCandG + j];
+            const bool pass = vis[jj] && (k32[jj] >> cshift) >= thr;
+            const uint32_t m = __ballot_sync(0xffffffffu, pass);
+            if (pass) {
+              const int pos = ccount[jj] + __popc(m & ((1u << lane) - 1u));
+              if (pos < sub_cap)
+                csub[static_cast<long long>(jj) * a.cand_cap + pos] =
+                    (static_cast<unsigned long long>(k32[jj] >> cshift) << 32) | static_cast<uint32_t>(key);
+              const int bin = min(max(static_cast<int>(k32[jj] >> kClassShift) - clos[jj] + 1, 0), kCandBins - 1);
+              atomicAdd(&chist[(cbuf * kCandG + j) * kCandBins + bin], 1u);
+            }
+            ccount[jj] += __popc(m);
+          }
+        }
+        if (!last) {
+          // tile t: query t % jn, refreshed by warp (t / jn) % 4 of the set
+          const int jj = wk.t % jn;
+          if (((wk.t / jn) & 3) == quarter) {
+            const int j = j_lo + jj;
+            int lo_q = clos[0];
+#pragma unroll
+            for (int u = 1; u < C::QW; ++u)
+              if (jj == u) lo_q = clos[u];
+            const uint32_t* h = chist + (cbuf * kCandG + j) * kCandBins;
+            uint32_t cc[8];
+            uint32_t csum = 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              cc[u] = h[kCandBins - 1 - (8 * lane + u)];
+              csum += cc[u];
+            }
+            uint32_t incl = csum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+              if (lane >= o) incl += y;
+            }
+            uint32_t above = incl - csum;
+            const uint32_t K = static_cast<uint32_t>(a.k);
+            int fb = -1;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int bin = kCandBins - 1 - (8 * lane + u);
+              if (bin >= 1 && above < K && K <= above + cc[u]) fb = bin;
+              above += cc[u];
+            }
+            const uint32_t fm = __ballot_sync(0xffffffffu, fb >= 0);
+            if (fm != 0u) {
+              const int b = __shfl_sync(0xffffffffu, fb, __ffs(fm) - 1);
+              if (lane == 0)
+                cthr[cbuf * kCandG + j] = ((static_cast<uint32_t>(lo_q + b - 1) << kClassShift) >> cshift) + 1u;
+            }
+          }
+        } else {
+          // the group's sub-lists are complete: hand them to the selectors
+          if (lane == 0) {
+#pragma unroll
+            for (int jj = 0; jj < C::QW; ++jj)
+              if (jj < jn) ccnt[(cbuf * kCandG + j_lo + jj) * 4 + quarter] = ccount[jj];
+          }
+          tc::mbar_arrive(&gdone[cbuf]);
+        }
+        ++n;
+        continue;
+      }
       // the warp leaves together: a wait that gave up on any lane ends the loop for all lanes
       const bool got = tc::mbar_wait(&accfull[acc], (n / C::ACC) & 1, abort_flag);
       if (!__all_sync(0xffffffffu, got)) { fail(6); break; }
       tc::tc_fence_after();
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * NCOL;
-      for (int j = j_lo; j < j_hi; ++j) {
-        // four independent partial sums (fixed order: sum = (p0 + p1) + (p2 + p3))
-        // head h always feeds partial sum h % 4, in increasing h, whatever the load width
-        float ps[4] = {0.f, 0.f, 0.f, 0.f};
-        auto accum = [&](const float* v, const float* wrow, int cnt) {
-          const float4* w4 = reinterpret_cast<const float4*>(wrow);
-#pragma unroll
-          for (int h = 0; h < cnt; h += 4) {
-            const float4 ww = w4[h >> 2];
-            ps[0] = fmaf(ww.x, fmaxf(v[h], 0.f), ps[0]);
-            ps[1] = fmaf(ww.y, fmaxf(v[h + 1], 0.f), ps[1]);
-            ps[2] = fmaf(ww.z, fmaxf(v[h + 2], 0.f), ps[2]);
-            ps[3] = fmaf(ww.w, fmaxf(v[h + 3], 0.f), ps[3]);
-          }
-        };
-        if (NHP == 16) {
-          float v[16];
-          tc::tmem_ld16_wait(tbase + j * NHP, v);
-          accum(v, wb + j * NHP, 16);
-        } else if (NHP == 32) {
-          float v[32];
-          tc::tmem_ld32_wait(tbase + j * NHP, v);
-          accum(v, wb + j * NHP, 32);
-        } else {
-          for (int c0 = 0; c0 < NHP; c0 += 64) {
-            float v[64];
-            tc::tmem_ld64_wait(tbase + j * NHP + c0, v);
-            accum(v, wb + j * NHP + c0, 64);
-          }
-        }
-        const float sum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      auto store = [&](int j, float sum) {
         if (j < wk.gi.nq && key < a.N) {
           const size_t qi = static_cast<size_t>(wk.gi.b) * a.Tq + wk.gi.i0 + j;
           const int nv = nvb[j];
@@ -496,6 +1036,15 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
           }
           else if (p.fill_invisible) dst[key] = -INFINITY;
         }
+      };
+      if (NHP == 64) {                            // at most C::QW queries per warp
+        float sv[C::QW];
+        head_sums(tbase, sv);
+#pragma unroll
+        for (int jj = 0; jj < C::QW; ++jj)
+          if (jj < jn) store(j_lo + jj, sv[jj]);
+      } else {
+        for (int j = j_lo; j < j_hi; ++j) store(j, head_sum1(tbase, j));
       }
       tc::tc_fence_before();
       tc::mbar_arrive(&accempty[acc]);
@@ -532,6 +1081,50 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
       tc::mbar_arrive(&sempty[s]);
       ++n;
     }
+  } else if (CAND && (warp == 2 || warp == 3)) {
+    // ------------------------------------------------------------ selectors (fused selection)
+    // Walk this CTA's groups in the producer's order (groups no query of which sees an entry are
+    // skipped by the other roles: their rows are all padding), wait for each group's lists, and
+    // select the top k of queries sw, sw + 2, ... of the group.
+    const int sw = warp - 2;
+    uint32_t* wh = selh + sw * kCandBins;
+    uint32_t* mem = selm + sw * kSelMembers;
+    uint32_t* bm = selb + sw * kSelBitmap;
+    for (int i = lane; i < kCandBins; i += 32) wh[i] = 0u;
+    __syncwarp();
+    const int shift = a.bf16_scores ? 16 : 0;
+    const int sub_cap = a.cand_cap / 4;
+    const int P = gridDim.x, c = blockIdx.x;
+    int gcs = 0;
+    for (int round = 0;; ++round) {
+      const long long base = static_cast<long long>(round) * P;
+      if (base >= ngroups) break;
+      const long long gg = base + ((round & 1) ? (P - 1 - c) : c);
+      if (gg >= ngroups) continue;
+      const GroupInfo gi = group_info(a, p, static_cast<int>(gg));
+      if (gi.nt == 0) {
+        for (int j = sw; j < gi.nq; j += kSelWarps) {
+          int32_t* out = a.idx_out + (static_cast<long long>(gi.b) * a.Tq + gi.i0 + j) * a.k;
+          for (int i = lane; i < a.k; i += 32) out[i] = -1;
+        }
+        continue;
+      }
+      const int buf = gcs & 1;
+      const bool got = tc::mbar_wait(&gdone[buf], (gcs >> 1) & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) { fail(13); break; }
+      for (int j = sw; j < gi.nq; j += kSelWarps) {
+        CandLists cl;
+        cl.base = a.cand + ((static_cast<long long>(blockIdx.x) * 2 + buf) * p.G + j) * static_cast<long long>(a.cand_cap);
+        cl.sub_cap = sub_cap;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) cl.n[q] = ccnt[(buf * kCandG + j) * 4 + q];
+        select_query(a, static_cast<long long>(gi.b) * a.Tq + gi.i0 + j, cl, chist + (buf * kCandG + j) * kCandBins,
+                     clo[buf * kCandG + j], shift, wh, mem, bm);
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&gfree[buf]);
+      ++gcs;
+    }
   }
 
   // ------------------------------------------------------------ teardown
@@ -556,10 +1149,10 @@ int sm_count() {
   return n;
 }
 
-template <int DI, int NCOL, bool FP8, bool LP>
+template <int DI, int NCOL, bool FP8, bool LP, bool CAND = false>
 cudaError_t launch_t(const IndexArgs& a, const IndexGrouping& gr, int fill_invisible, cudaStream_t s,
                      int* launches) {
-  using C = Cfg<DI, NCOL, FP8, LP>;
+  using C = Cfg<DI, NCOL, FP8, LP, CAND>;
   CUtensorMap kmap, qmap;
   bool ok;
   if (LP)
@@ -585,16 +1178,18 @@ cudaError_t launch_t(const IndexArgs& a, const IndexGrouping& gr, int fill_invis
   p.fill_invisible = fill_invisible;
   const int sms = sm_count();
   const long long groups = a.q_count;
-  p.mode = groups >= 4LL * sms ? 1 : (CSA_IDX_WALK_CHUNK > 0 ? 2 : 0);
+  // fused selection: whole groups per CTA in tile order (the lists are built in entry order)
+  p.mode = (CAND || groups >= 4LL * sms) ? 1 : (CSA_IDX_WALK_CHUNK > 0 ? 2 : 0);
   p.chunk = CSA_IDX_WALK_CHUNK > 0 ? CSA_IDX_WALK_CHUNK : 1;
   p.F = groups * p.tiles_max;
   long long grid = static_cast<long long>(sms) * C::CTAS;
   if (p.mode != 1 && p.F < grid) grid = p.F;
+  if (CAND && grid > a.cand_ctas) grid = a.cand_ctas;
   if (grid < 1) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(k_index_score<DI, NCOL, FP8, LP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(k_index_score<DI, NCOL, FP8, LP, CAND>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  e = launch_k(k_index_score<DI, NCOL, FP8, LP>, dim3(static_cast<unsigned>(grid)), dim3(C::THREADS),
+  e = launch_k(k_index_score<DI, NCOL, FP8, LP, CAND>, dim3(static_cast<unsigned>(grid)), dim3(C::THREADS),
                static_cast<size_t>(C::SMEM), s, a, kmap, qmap, p);
   ++*launches;
   return e;
@@ -649,6 +1244,35 @@ cudaError_t launch_index_score_groups(const IndexArgs& a, const IndexGrouping& g
   if (a.dI == 64) return a.fp8 ? launch_di<64, true, false>(a, gr, fill_invisible, s, launches)
                                : launch_di<64, false, false>(a, gr, fill_invisible, s, launches);
   return cudaErrorInvalidValue;
+}
+
+bool index_select_supported(const IndexGrouping& gr, int dI, int fp8, int lowp, int N) {
+  if (gr.NCOL != 256 || gr.G > kCandG || gr.NHP != 64) return false;
+  if (N < 1 || N > 32 * kSelBitmap) return false;   // the selector's entry bitmap
+  if (fp8 && !lowp) return false;             // widened FP8 keys: no shared memory left for the lists' state
+  return lowp ? dI == 128 : (dI == 64 || dI == 128);
+}
+
+int index_select_ctas() { return sm_count(); }
+
+// per query: four sub-lists of (tiles x 32) slots, one per quarter of each tile's keys
+int index_select_cap(int N) { return (N + KT - 1) / KT * KT; }
+
+size_t index_select_bytes(const IndexGrouping& gr, int N) {
+  return static_cast<size_t>(index_select_ctas()) * 2 * gr.G * static_cast<size_t>(index_select_cap(N)) *
+         sizeof(unsigned long long);
+}
+
+// a.cand: index_select_bytes(gr, a.N) bytes; a.cand_cap = index_select_cap(N); a.cand_ctas = the SM count those
+// bytes were sized for.  Writes a.idx_out for the queries of groups [q_begin, q_begin + q_count).
+cudaError_t launch_index_select(const IndexArgs& a, const IndexGrouping& gr, cudaStream_t s, int* launches) {
+  if (a.q_count <= 0 || a.N <= 0) return cudaErrorInvalidValue;
+  if (!index_select_supported(gr, a.dI, a.fp8, a.lowp, a.N) || a.cand == nullptr || a.idx_out == nullptr ||
+      a.cand_cap != index_select_cap(a.N) || a.cand_ctas < 1 || a.k < 1)
+    return cudaErrorInvalidValue;
+  if (a.lowp) return launch_t<128, 256, true, true, true>(a, gr, 0, s, launches);
+  if (a.dI == 128) return launch_t<128, 256, false, false, true>(a, gr, 0, s, launches);
+  return launch_t<64, 256, false, false, true>(a, gr, 0, s, launches);
 }
 
 // rows [row0, row0 + rows) of qI [.., 128] bf16 / w -> q8 [rows, 128] e4m3 / wp [rows] (rows

@@ -157,6 +157,39 @@ __device__ __forceinline__ void tc_fence_after() {
 // 32 lanes x 32 bits, N consecutive columns, followed by the wait in the same asm statement so
 // that no use of the destination registers can be scheduled before the data has arrived.
 // Thread i of the warp gets TMEM lane (lane field of taddr) + i.
+// tcgen05.ld of 32 columns without the wait: the registers are undefined until tmem_ld_wait()
+// and reg_fence32() on them (the fence makes every later use depend on the wait's completion,
+// so the compiler cannot read them earlier).
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 8)
+    asm volatile("" : "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]), "+r"(r[i + 5]),
+                 "+r"(r[i + 6]), "+r"(r[i + 7]) :: "memory");
+}
+
+// (a0, a1) += (w0, w1) * (x0, x1): two independent fp32 fused multiply-adds, round to nearest
+// even, in one packed instruction
+__device__ __forceinline__ void fma_f32x2(float& a0, float& a1, float w0, float w1, float x0, float x1) {
+  asm("{\n\t.reg .b64 acc, ww, xx;\n\t"
+      "mov.b64 acc, {%0, %1};\n\tmov.b64 ww, {%2, %3};\n\tmov.b64 xx, {%4, %5};\n\t"
+      "fma.rn.f32x2 acc, ww, xx, acc;\n\tmov.b64 {%0, %1}, acc;\n\t}"
+      : "+f"(a0), "+f"(a1) : "f"(w0), "f"(w1), "f"(x0), "f"(x1));
+}
+
 __device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, float* v) {
   uint32_t r[16];
   asm volatile(

@@ -49,12 +49,6 @@ constexpr int kBins = 1 << kDigit;          // one warp scans them: kBins / 32 p
 constexpr int kBinsPerLane = kBins / 32;
 constexpr uint32_t kNoIndex = 0xFFFFFFFFu;
 
-// Order-preserving key of a score; -0 and +0 map to the same key (equal scores tie by index).
-__device__ __forceinline__ uint32_t order_key(float f) {
-  const uint32_t u = __float_as_uint(f + 0.0f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
 // Exclusive block-wide scan of 64-bit values.  ws: 33 slots of shared memory.
 __device__ __forceinline__ unsigned long long block_excl_scan(unsigned long long v, unsigned long long* ws,
                                                               unsigned long long* total) {
