@@ -254,6 +254,61 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf162(uint16_t v) {
 
 constexpr uint32_t kEntryMax = 0x3FFFFu;   // entries are below 2^18: kEntryMax - entry orders them reversed
 
+// The bin of a kCandBins-bin histogram (bins in increasing key order) where the count of entries
+// in it and in the bins above first reaches K, in every lane: returns the bin (-1 when the whole
+// histogram holds fewer than K), with the count above it (fa) and its own count (fc).  Lane l
+// reads bins 8l .. 8l+7 as two 16-byte loads (no bank conflicts) and the counts above come from a
+// suffix sum across the lanes.  The loads are volatile: other warps may still be adding to the
+// bins, and any partial view only undercounts.
+__device__ __forceinline__ int hist_kth_bin(const uint32_t* h, uint32_t K, uint32_t& fa, uint32_t& fc) {
+  const int lane = threadIdx.x & 31;
+  uint32_t c[8];
+  asm volatile("ld.volatile.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(c[0]), "=r"(c[1]), "=r"(c[2]), "=r"(c[3]) : "r"(tc::sptr(h + 8 * lane)));
+  asm volatile("ld.volatile.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(c[4]), "=r"(c[5]), "=r"(c[6]), "=r"(c[7]) : "r"(tc::sptr(h + 8 * lane + 4)));
+  uint32_t csum = 0;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) csum += c[u];
+  uint32_t suf = csum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_down_sync(0xffffffffu, suf, o);
+    if (lane + o < 32) suf += y;
+  }
+  uint32_t above = suf - csum;                 // entries in the bins above 8l + 7
+  int fb = -1;
+  uint32_t a0 = 0, c0 = 0;
+#pragma unroll
+  for (int u = 7; u >= 0; --u) {
+    if (above < K && K <= above + c[u]) {
+      fb = 8 * lane + u;
+      a0 = above;
+      c0 = c[u];
+    }
+    above += c[u];
+  }
+  const uint32_t fm = __ballot_sync(0xffffffffu, fb >= 0);
+  if (fm == 0u) {
+    fa = fc = 0;
+    return -1;
+  }
+  const int src = __ffs(fm) - 1;
+  fa = __shfl_sync(0xffffffffu, a0, src);
+  fc = __shfl_sync(0xffffffffu, c0, src);
+  return __shfl_sync(0xffffffffu, fb, src);
+}
+
+// The smallest score whose order key (order_key) is at least T, so that order_key(s) >= T exactly
+// when s >= key_floor_float(T) (non-NaN s): the inverse of order_key.  A T above every finite
+// key's range decodes to a NaN (nothing compares >= it, as nothing has such a key); a T below
+// every finite key gives -inf (everything passes).
+__device__ __forceinline__ float key_floor_float(uint32_t T) {
+  if (T & 0x80000000u) return __uint_as_float(T & 0x7FFFFFFFu);
+  const float f = __uint_as_float(~T);
+  return (f != f) ? -INFINITY : f;
+}
+
 struct CandLists {
   const unsigned long long* base;   // sub-list q at base + q * sub_cap
   int sub_cap;
@@ -374,40 +429,8 @@ __device__ void select_query(const IndexArgs& a, long long qi, const CandLists& 
     if (lane == 0) report_error(a.status, CSA_ERR_DEVICE_CHECK, -2000);
     return;
   }
-  uint32_t c[8];
-  uint32_t csum = 0;
-#pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    c[u] = hist[kCandBins - 1 - (8 * lane + u)];
-    csum += c[u];
-  }
-  uint32_t incl = csum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  uint32_t above = incl - csum;
-  int fb = -1;
   uint32_t fa = 0, fc = 0;
-#pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    if (above < static_cast<uint32_t>(K) && static_cast<uint32_t>(K) <= above + c[u]) {
-      fb = kCandBins - 1 - (8 * lane + u);
-      fa = above;
-      fc = c[u];
-    }
-    above += c[u];
-  }
-  const uint32_t fm = __ballot_sync(0xffffffffu, fb >= 0);
-  if (fm != 0u) {
-    const int src = __ffs(fm) - 1;
-    fb = __shfl_sync(0xffffffffu, fb, src);
-    fa = __shfl_sync(0xffffffffu, fa, src);
-    fc = __shfl_sync(0xffffffffu, fc, src);
-  } else {
-    fb = -1;
-  }
+  const int fb = hist_kth_bin(hist, static_cast<uint32_t>(K), fa, fc);
   const uint32_t lt = (1u << lane) - 1u;
   uint32_t thr = 0, eq = 0;
   int rem = K, cmp = 0;
@@ -556,7 +579,7 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
   // parity), [G] the query in the group, [4] the quarter of the tile's keys (epilogue warp).
   uint32_t* chist = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(bars) + C::MISC);  // [2][G][bins]
   uint32_t* cwmax = chist + 2 * kCandG * kCandBins;   // [2][G][4] largest key of a group's first tile
-  volatile uint32_t* cthr = cwmax + 2 * kCandG * 4;   // [2][G] emit when key >= thr
+  volatile uint32_t* cthr = cwmax + 2 * kCandG * 4;   // [2][G] bits of the float t: emit scores >= t
   int* clo = reinterpret_cast<int*>(cwmax + 2 * kCandG * 4 + 2 * kCandG);   // [2][G] class of bin 1
   int* ccnt = clo + 2 * kCandG;                        // [2][G][4] sub-list lengths
   uint64_t* gdone = reinterpret_cast<uint64_t*>(ccnt + 2 * kCandG * 4);   // [2] group's lists complete
@@ -572,7 +595,8 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
 
   // alignment the TMA / tensor-core path relies on; a violation is reported, never executed
   {
-    const uint32_t bad = (tc::sptr(smem) & 1023u) | (tc::sptr(bars) & 7u) | (CAND ? tc::sptr(gdone) & 7u : 0u) |
+    const uint32_t bad = (tc::sptr(smem) & 1023u) | (tc::sptr(bars) & 7u) |
+                         (CAND ? (tc::sptr(gdone) & 7u) | (tc::sptr(chist) & 15u) : 0u) |
                          static_cast<uint32_t>(reinterpret_cast<uintptr_t>(&kmap) & 63u) |
                          static_cast<uint32_t>(reinterpret_cast<uintptr_t>(&qmap) & 63u);
     if (bad != 0u) {
@@ -706,13 +730,16 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
         if (!tc::mbar_wait(&full[s], ph, abort_flag)) { fail(4); break; }
         if (!tc::mbar_wait(&accempty[acc], ((n / C::ACC) & 1) ^ 1, abort_flag)) { fail(5); break; }
         tc::tc_fence_after();
-        const uint32_t kaddr = tc::sptr(kbuf + s * C::STAGE_BYTES);
-        const uint32_t qaddr = tc::sptr(qbuf + (gc % C::QB) * C::Q_BYTES);
+        // descriptors of the tile's first K step; a later step only moves the start address
+        // (its 16-byte units fill the descriptor's low 14 bits, and every operand address of the
+        // kernel stays below 256 KB, so the sum never carries out of that field)
+        const uint64_t ad0 = tc::umma_desc_sw128(tc::sptr(kbuf + s * C::STAGE_BYTES));
+        const uint64_t bd0 = tc::umma_desc_sw128(tc::sptr(qbuf + (gc % C::QB) * C::Q_BYTES));
 #pragma unroll
         for (int k = 0; k < C::KSTEPS; ++k) {               // 32 bytes of K per instruction
           const int r = k >> 2, off = (k & 3) * 32;
-          const uint64_t ad = tc::umma_desc_sw128(kaddr + r * C::KEY_REGION + off);
-          const uint64_t bd = tc::umma_desc_sw128(qaddr + r * C::Q_REGION + off);
+          const uint64_t ad = ad0 + static_cast<uint64_t>((r * C::KEY_REGION + off) >> 4);
+          const uint64_t bd = bd0 + static_cast<uint64_t>((r * C::Q_REGION + off) >> 4);
           if (LP) tc::umma_e4m3(tmem + acc * NCOL, ad, bd, idesc, k > 0 ? 1u : 0u);
           else tc::umma_bf16(tmem + acc * NCOL, ad, bd, idesc, k > 0 ? 1u : 0u);
         }
@@ -781,10 +808,10 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
 #pragma unroll
           for (int h = 0; h < 32; h += 4) {
             const float4 ww = w4[h >> 2];
+            const float x2 = __uint_as_float(cur[h + 2]), x3 = __uint_as_float(cur[h + 3]);
             tc::fma_f32x2(ps[c >> 1][0], ps[c >> 1][1], ww.x, ww.y, fmaxf(__uint_as_float(cur[h]), 0.f),
                           fmaxf(__uint_as_float(cur[h + 1]), 0.f));
-            tc::fma_f32x2(ps[c >> 1][2], ps[c >> 1][3], ww.z, ww.w, fmaxf(__uint_as_float(cur[h + 2]), 0.f),
-                          fmaxf(__uint_as_float(cur[h + 3]), 0.f));
+            tc::fma_f32x2(ps[c >> 1][2], ps[c >> 1][3], ww.z, ww.w, x2 + fabsf(x2), x3 + fabsf(x3));
           }
           if (c + 1 < nch) {
             tc::tmem_ld_wait();
@@ -806,8 +833,8 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
           const float4 ww = w4[h >> 2];
           ps[0] = fmaf(ww.x, fmaxf(v[h], 0.f), ps[0]);
           ps[1] = fmaf(ww.y, fmaxf(v[h + 1], 0.f), ps[1]);
-          ps[2] = fmaf(ww.z, fmaxf(v[h + 2], 0.f), ps[2]);
-          ps[3] = fmaf(ww.w, fmaxf(v[h + 3], 0.f), ps[3]);
+          ps[2] = fmaf(ww.z, v[h + 2] + fabsf(v[h + 2]), ps[2]);
+          ps[3] = fmaf(ww.w, v[h + 3] + fabsf(v[h + 3]), ps[3]);
         }
       };
       if (NHP == 16) {
@@ -832,6 +859,13 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
     for (int jj = 0; jj < C::QW; ++jj) ccount[jj] = clos[jj] = 0;
     unsigned long long* csub = nullptr;           // this warp's sub-list of query j_lo
     bool dead = false;                            // a wait of this warp gave up: walk on, do nothing
+    float* srow[C::QW];                           // 64 heads: this warp's score rows of the group
+    int snv[C::QW];                               // and their visible entry counts
+#pragma unroll
+    for (int jj = 0; jj < C::QW; ++jj) {
+      srow[jj] = nullptr;
+      snv[jj] = 0;
+    }
     Walker wk;
     wk.init(p, ngroups);
     long long n = 0;
@@ -845,12 +879,26 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
           float v = 0.f;
           if (j < wk.gi.nq && h < a.nI)
             v = a.w[(static_cast<size_t>(wk.gi.b) * a.Tq + wk.gi.i0 + j) * a.nI + h];
-          wb[c - j_lo * NHP] = v;
+          // heads 2 and 3 of every four take ReLU(x) as (x + |x|) / 2 on the FMA pipe (the fmax
+          // of the other two runs on the ALU pipe): their weight is stored halved, and
+          // (w / 2) (x + |x|) = w ReLU(x) exactly, so each product and sum rounds as before
+          wb[c - j_lo * NHP] = (h & 2) ? 0.5f * v : v;
         }
         for (int j = j_lo + lane; j < j_hi; j += 32)
           nvb[j] = j < wk.gi.nq ? n_visible(a.q_pos[static_cast<size_t>(wk.gi.b) * a.Tq + wk.gi.i0 + j], a.m, a.N)
                                 : 0;
         __syncwarp();
+        if (!CAND && NHP == 64) {
+#pragma unroll
+          for (int jj = 0; jj < C::QW; ++jj) {
+            const int j = j_lo + jj;
+            const bool live = jj < jn && j < wk.gi.nq;
+            srow[jj] = live ? a.scores + (static_cast<long long>(wk.gi.b) * a.Tq + wk.gi.i0 + j - a.score_row_offset) *
+                                             static_cast<long long>(a.N)
+                            : nullptr;
+            snv[jj] = live ? nvb[j] : 0;
+          }
+        }
         if (CAND) {
           // the selectors are done with this buffer (it held group gce - 2); clear this set's
           // histograms and thresholds (ordered before any use by the first tile's barrier)
@@ -863,10 +911,15 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
           if (!dead) {
             uint32_t* hb = chist + (cbuf * kCandG + j_lo) * kCandBins;
             for (int i = tis; i < jn * kCandBins; i += 128) hb[i] = 0u;
-            if (tis < jn) cthr[cbuf * kCandG + j_lo + tis] = 0u;
+            if (tis < jn) cthr[cbuf * kCandG + j_lo + tis] = __float_as_uint(-INFINITY);
           }
 #pragma unroll
           for (int jj = 0; jj < C::QW; ++jj) ccount[jj] = 0;
+#pragma unroll
+          for (int jj = 0; jj < C::QW; ++jj) {    // entries a query's list takes: none at most k visible
+            const int j = j_lo + jj;
+            snv[jj] = (jj < jn && j < wk.gi.nq && nvb[j] > a.k) ? nvb[j] : 0;
+          }
           csub = a.cand + ((static_cast<long long>(blockIdx.x) * 2 + cbuf) * p.G + j_lo) *
                               static_cast<long long>(a.cand_cap) + static_cast<long long>(quarter) * sub_cap;
         }
@@ -905,23 +958,14 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
             fail(6);
           }
         }
-        uint32_t k32[C::QW];
+        float scv[C::QW];                         // the scores, as the unfused path stores them
         bool vis[C::QW];
 #pragma unroll
         for (int jj = 0; jj < C::QW; ++jj) {
-          k32[jj] = 0u;
-          vis[jj] = false;
-        }
-#pragma unroll
-        for (int jj = 0; jj < C::QW; ++jj) {
-          if (jj < jn) {
-            const int j = j_lo + jj;
-            const int nv = nvb[j];
-            float v = sv[jj] * kscale;
-            if (a.bf16_scores) v = __bfloat162float(__float2bfloat16_rn(v));
-            vis[jj] = j < wk.gi.nq && key < nv && nv > a.k;
-            k32[jj] = order_key(v);
-          }
+          float v = sv[jj] * kscale;
+          if (a.bf16_scores) v = __bfloat162float(__float2bfloat16_rn(v));
+          scv[jj] = v;
+          vis[jj] = jj < jn && key < snv[jj];
         }
         if (first) {
           // the histogram base of each query: the largest key of the group's first tile, agreed by
@@ -930,7 +974,7 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
 #pragma unroll
             for (int jj = 0; jj < C::QW; ++jj) {
               if (jj < jn) {
-                uint32_t mx = vis[jj] ? k32[jj] : 0u;
+                uint32_t mx = vis[jj] ? order_key(scv[jj]) : 0u;
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
                 if (lane == 0) cwmax[(cbuf * kCandG + j_lo + jj) * 4 + quarter] = mx;
@@ -956,58 +1000,37 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
         for (int jj = 0; jj < C::QW; ++jj) {
           if (jj < jn) {
             const int j = j_lo + jj;
-            const uint32_t thr = first ? 0u : cthr[cbuf * kCandG + j];
-            const bool pass = vis[jj] && (k32[jj] >> cshift) >= thr;
+            // key(s) >= T exactly when s >= the float T encodes (the key order is the score order)
+            const float thr = first ? -INFINITY : __uint_as_float(cthr[cbuf * kCandG + j]);
+            const bool pass = vis[jj] && scv[jj] >= thr;
             const uint32_t m = __ballot_sync(0xffffffffu, pass);
             if (pass) {
+              const uint32_t kk = order_key(scv[jj]);
               const int pos = ccount[jj] + __popc(m & ((1u << lane) - 1u));
               if (pos < sub_cap)
                 csub[static_cast<long long>(jj) * a.cand_cap + pos] =
-                    (static_cast<unsigned long long>(k32[jj] >> cshift) << 32) | static_cast<uint32_t>(key);
-              const int bin = min(max(static_cast<int>(k32[jj] >> kClassShift) - clos[jj] + 1, 0), kCandBins - 1);
+                    (static_cast<unsigned long long>(kk >> cshift) << 32) | static_cast<uint32_t>(key);
+              const int bin = min(max(static_cast<int>(kk >> kClassShift) - clos[jj] + 1, 0), kCandBins - 1);
               atomicAdd(&chist[(cbuf * kCandG + j) * kCandBins + bin], 1u);
             }
             ccount[jj] += __popc(m);
           }
         }
         if (!last) {
-          // tile t: query t % jn, refreshed by warp (t / jn) % 4 of the set
-          const int jj = wk.t % jn;
-          if (((wk.t / jn) & 3) == quarter) {
+          // tile t: query t % jn, refreshed by warp (t / jn) % 4 of the set (one query per warp
+          // set when the selection is fused: query 0, warp t % 4)
+          const int jj = C::QW == 1 ? 0 : wk.t % jn;
+          if (((C::QW == 1 ? wk.t : wk.t / jn) & 3) == quarter) {
             const int j = j_lo + jj;
             int lo_q = clos[0];
 #pragma unroll
             for (int u = 1; u < C::QW; ++u)
               if (jj == u) lo_q = clos[u];
-            const uint32_t* h = chist + (cbuf * kCandG + j) * kCandBins;
-            uint32_t cc[8];
-            uint32_t csum = 0;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              cc[u] = h[kCandBins - 1 - (8 * lane + u)];
-              csum += cc[u];
-            }
-            uint32_t incl = csum;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-              if (lane >= o) incl += y;
-            }
-            uint32_t above = incl - csum;
-            const uint32_t K = static_cast<uint32_t>(a.k);
-            int fb = -1;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int bin = kCandBins - 1 - (8 * lane + u);
-              if (bin >= 1 && above < K && K <= above + cc[u]) fb = bin;
-              above += cc[u];
-            }
-            const uint32_t fm = __ballot_sync(0xffffffffu, fb >= 0);
-            if (fm != 0u) {
-              const int b = __shfl_sync(0xffffffffu, fb, __ffs(fm) - 1);
-              if (lane == 0)
-                cthr[cbuf * kCandG + j] = ((static_cast<uint32_t>(lo_q + b - 1) << kClassShift) >> cshift) + 1u;
-            }
+            uint32_t fa, fc;
+            const int b = hist_kth_bin(chist + (cbuf * kCandG + j) * kCandBins, static_cast<uint32_t>(a.k), fa, fc);
+            if (b >= 1 && lane == 0)
+              cthr[cbuf * kCandG + j] = __float_as_uint(
+                  key_floor_float((static_cast<uint32_t>(lo_q + b - 1) << kClassShift) + (1u << cshift)));
           }
         } else {
           // the group's sub-lists are complete: hand them to the selectors
@@ -1040,14 +1063,24 @@ k_index_score(const IndexArgs a, const __grid_constant__ CUtensorMap kmap, const
       if (NHP == 64) {                            // at most C::QW queries per warp
         float sv[C::QW];
         head_sums(tbase, sv);
+        tc::tc_fence_before();
+        tc::mbar_arrive(&accempty[acc]);          // tensor memory is free before the stores
 #pragma unroll
-        for (int jj = 0; jj < C::QW; ++jj)
-          if (jj < jn) store(j_lo + jj, sv[jj]);
+        for (int jj = 0; jj < C::QW; ++jj) {
+          if (srow[jj] != nullptr && key < a.N) {
+            if (key < snv[jj]) {
+              const float v = sv[jj] * kscale;
+              srow[jj][key] = a.bf16_scores ? __bfloat162float(__float2bfloat16_rn(v)) : v;
+            } else if (p.fill_invisible) {
+              srow[jj][key] = -INFINITY;
+            }
+          }
+        }
       } else {
         for (int j = j_lo; j < j_hi; ++j) store(j, head_sum1(tbase, j));
+        tc::tc_fence_before();
+        tc::mbar_arrive(&accempty[acc]);
       }
-      tc::tc_fence_before();
-      tc::mbar_arrive(&accempty[acc]);
       ++n;
     }
   } else if (C::WIDEN && warp >= 4 + C::EW) {
