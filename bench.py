@@ -30,7 +30,7 @@ sys.path.insert(0, ROOT)
 # DRAM traffic of the indexer score kernel per launch, taken with ncu on the workload below; the
 # figure is reported only while the kernel source still hashes to the value it was taken with.
 TRAFFIC = {
-    "csa_decode_128k_b32": {"kernel": "k_index_score", "bytes_per_launch": 276261888, "source_sha": "ef4143193fc0bd19",
+    "csa_decode_128k_b32": {"kernel": "k_index_score", "bytes_per_launch": 273702528, "source_sha": "73239b0175b9b709",
                             "profile": "profiles/k_index_score_csa_decode_128k_b32.md"},
 }
 
@@ -50,7 +50,8 @@ def parse():
     ap.add_argument("--prefill-steps", type=int, default=3)
     ap.add_argument("--lowp", action="store_true",
                     help="FP8 workloads: the low-precision indexer (query quantised to e4m3, FP8 tensor cores)")
-    ap.add_argument("--case", choices=["compress", "out_proj", "attend", "index_prefill", "index_topk_prefill"],
+    ap.add_argument("--case", choices=["compress", "out_proj", "attend", "index_prefill", "index_topk_prefill",
+                                       "index_topk_prefill_split"],
                     default=None,
                     help="time one library call on a profiler-sized input and exit (no contract line)")
     ap.add_argument("--case-tokens", type=int, default=65536, help="tokens of the --case input")
@@ -777,14 +778,15 @@ def run_case(args):
     """One library call on a small input, repeated: the command the ncu summaries under profiles/
     capture.  compress: the CSA main-stream compressor (T tokens of four [T, 512] bf16 streams);
     out_proj: the grouped output projection at Flash widths (O [T, 64, 512]); attend /
-    index_prefill / index_topk_prefill: the sparse attention / the indexer scores / the fused
-    indexer scores + top-k selection of a CSA prefill chunk of T tokens."""
+    index_prefill / index_topk_prefill / index_topk_prefill_split: the sparse attention / the
+    indexer scores / the fused indexer scores + top-k selection / the scores stored and then
+    selected (two calls) of a CSA prefill chunk of T tokens."""
     import torch
     from long_context_compressed_16_b300 import pipeline as P
     from long_context_compressed_16_b300 import synth as S
     dev = torch.device("cuda", 0)
     T = args.case_tokens
-    if args.case in ("attend", "index_prefill", "index_topk_prefill"):
+    if args.case in ("attend", "index_prefill", "index_topk_prefill", "index_topk_prefill_split"):
         # the CSA prefill shapes at T tokens (N = T / 4 entries, 64 heads x 512, k = 512): the
         # attention over seeded random selections, or the indexer scores of every causal pair
         from long_context_compressed_16_b300 import capi as C
@@ -802,6 +804,19 @@ def run_case(args):
             fn = lambda: C.check(C.csa_attend(adesc, inp["q"], kv, idx, inp["win"], inp["sink"], inp["q_pos"], out,
                                               None, ws), "csa_attend")
             _, flops = prefill_flops(w)
+        elif args.case == "index_topk_prefill_split":
+            kI = S.normal_bf16((1, w.N, w.dI), 3, S.TID["kI"], dev)
+            idesc = P.index_desc(1, w.T, w.N, w.nI, w.dI, w.k, w.m)
+            ws = torch.zeros(max(256, C.csa_index_score_workspace(idesc), C.csa_topk_workspace(idesc)),
+                             dtype=torch.uint8, device=dev)
+            scores = torch.empty((1, w.T, w.N), dtype=torch.float32, device=dev)
+            idx = torch.empty((1, w.T, w.k), dtype=torch.int32, device=dev)
+
+            def fn():
+                C.check(C.csa_index_score(idesc, inp["qI"], inp["w"], kI, None, inp["q_pos"], scores, ws),
+                        "csa_index_score")
+                C.check(C.csa_topk(idesc, scores, inp["q_pos"], idx, ws), "csa_topk")
+            flops, _ = prefill_flops(w)
         elif args.case == "index_topk_prefill":
             kI = S.normal_bf16((1, w.N, w.dI), 3, S.TID["kI"], dev)
             idesc = P.index_desc(1, w.T, w.N, w.nI, w.dI, w.k, w.m)

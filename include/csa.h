@@ -143,13 +143,28 @@ csa_status csa_compress(const csa_compress_desc* desc, const void* Ca, const voi
  * FP8 row scale; the stored values (score_out, workspace rows) are those rounded values in fp32,
  * and the top-k selects on them with the same rule (ties, which rounding makes frequent, go to
  * the smaller s).  CSA_SCORE_FP32 (0, the default of a zeroed descriptor) keeps fp32 scores.
+ *
+ * select_mode: where the top-k selection runs (the result is the same bit for bit):
+ *   CSA_SELECT_AUTO (0, the default): fused into the score kernel when the call qualifies (below)
+ *     and its rows are long, N >= 16 k (there it is faster: 65536-token prefill, N = 16384,
+ *     k = 512: 7.8 ms against 9.1 ms for the stored path); the stored path otherwise.
+ *   CSA_SELECT_FUSED: fused whenever the call qualifies.
+ *   CSA_SELECT_STORED: score rows stored in the workspace (in chunks of at most 256 MiB) and
+ *     selected by the top-k kernels.
+ * The fused selection keeps, per query, the entries that can still be among its top k (above a
+ * running lower bound of the k-th score) and selects from those; the score rows are never
+ * stored.  It qualifies when score_out is NULL, groups of 4 queries x 64 indexer heads fill the
+ * tensor-core tile (n_heads in 33..64, Tq >= 4), the keys are bf16 or the low-precision indexer's,
+ * N <= 32768, and the batch holds at least 4 groups per SM of the device.
  * ------------------------------------------------------------------------------------------- */
 enum { CSA_SCORE_FP32 = 0, CSA_SCORE_BF16 = 1 };
+enum { CSA_SELECT_AUTO = 0, CSA_SELECT_FUSED = 1, CSA_SELECT_STORED = 2 };
 
 typedef struct {
   int B, Tq, N, n_heads, head_dim, k, m;
   csa_format key_fmt;      /* CSA_FMT_BF16, CSA_FMT_FP8_ROWSCALE or CSA_FMT_FP8_ROWSCALE_LOWP */
   int score_fmt;           /* CSA_SCORE_FP32 (0) or CSA_SCORE_BF16 */
+  int select_mode;         /* CSA_SELECT_AUTO (0), CSA_SELECT_FUSED or CSA_SELECT_STORED */
 } csa_index_desc;
 
 size_t csa_index_topk_workspace(const csa_index_desc* desc);

@@ -31,6 +31,10 @@ CSA_FP8_MIXED_ROW_BYTES = 608
 # csa_index_desc.score_fmt
 CSA_SCORE_FP32 = 0
 CSA_SCORE_BF16 = 1
+# csa_index_desc.select_mode
+CSA_SELECT_AUTO = 0
+CSA_SELECT_FUSED = 1
+CSA_SELECT_STORED = 2
 CSA_NOALLOC_SCRATCH_BYTES = 8 << 20
 # flags
 CSA_COMPRESS_NORM = 1
@@ -54,7 +58,7 @@ class csa_compress_desc(ctypes.Structure):
 
 class csa_index_desc(ctypes.Structure):
     _fields_ = [("B", c_int), ("Tq", c_int), ("N", c_int), ("n_heads", c_int), ("head_dim", c_int),
-                ("k", c_int), ("m", c_int), ("key_fmt", c_int), ("score_fmt", c_int)]
+                ("k", c_int), ("m", c_int), ("key_fmt", c_int), ("score_fmt", c_int), ("select_mode", c_int)]
 
 
 class csa_attend_desc(ctypes.Structure):

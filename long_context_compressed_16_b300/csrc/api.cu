@@ -136,6 +136,8 @@ bool index_desc_ok(const csa_index_desc* d) {
     return false;
   if (d->key_fmt == CSA_FMT_FP8_ROWSCALE_LOWP && d->head_dim != 128) return false;
   if (d->score_fmt != CSA_SCORE_FP32 && d->score_fmt != CSA_SCORE_BF16) return false;
+  if (d->select_mode != CSA_SELECT_AUTO && d->select_mode != CSA_SELECT_FUSED && d->select_mode != CSA_SELECT_STORED)
+    return false;
   return true;
 }
 
@@ -171,9 +173,11 @@ IndexPlan plan_index(const csa_index_desc* d) {
   // persistent grid; its lists take the place of the score rows (below about 28K entries per row
   // they are the smaller of the two)
   const csa::IndexGrouping gr = csa::index_grouping(d->n_heads, d->Tq);
-  p.sel = CSA_INDEX_FUSED_SELECT && d->N > 0 &&
+  // (AUTO: only rows of at least 16 k entries, where it measured faster than storing the rows)
+  p.sel = CSA_INDEX_FUSED_SELECT && d->select_mode != CSA_SELECT_STORED && d->N > 0 &&
           csa::index_select_supported(gr, d->head_dim, fp8_keys(d), is_lowp(d), d->N) &&
-          p.groups >= 4LL * csa::index_select_ctas();
+          p.groups >= 4LL * csa::index_select_ctas() &&
+          (d->select_mode == CSA_SELECT_FUSED || static_cast<long long>(d->N) >= 16LL * d->k);
   p.sel_bytes = p.sel ? round256(csa::index_select_bytes(gr, d->N)) : 0;
   return p;
 }

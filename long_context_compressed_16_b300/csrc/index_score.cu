@@ -407,13 +407,42 @@ __device__ bool warp_radix(Each each, int pos, uint32_t& prefix, int& rem, int& 
   return true;
 }
 
+// Writes the entries marked in the bitmap bm (nwords words) to out in increasing entry order; lane
+// l reads words [l W, (l + 1) W).  False (nothing written) unless exactly K entries are marked.
+__device__ bool emit_bitmap(const uint32_t* bm, int nwords, int32_t* out, int K) {
+  const int lane = threadIdx.x & 31;
+  const int W = (nwords + 31) / 32;
+  const int w0 = min(nwords, lane * W), w1 = min(nwords, w0 + W);
+  uint32_t cnt = 0;
+  for (int i = w0; i < w1; ++i) cnt += __popc(bm[i]);
+  uint32_t ex = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, ex, o);
+    if (lane >= o) ex += y;
+  }
+  const uint32_t total = __shfl_sync(0xffffffffu, ex, 31);
+  if (total != static_cast<uint32_t>(K)) return false;
+  uint32_t o = ex - cnt;
+  for (int i = w0; i < w1; ++i) {
+    uint32_t bits = bm[i];
+    while (bits != 0u) {
+      const int b = __ffs(bits) - 1;
+      out[o++] = i * 32 + b;
+      bits &= bits - 1u;
+    }
+  }
+  return true;
+}
+
 // Top-k row of query qi from its candidates and the final histogram of their key classes (bins
-// 1 .. kCandBins-2 hold the single class lo + bin - 1).  The k-th largest key is found first: when
-// its class is one of those bins and holds at most kSelMembers keys, only that class is resolved
-// (its low key bits, in shared memory; two passes over the lists), otherwise the lists are radix-
-// selected whole.  Keys equal to the threshold beyond what is taken go by smallest entry (a radix
-// select on kEntryMax - entry).  The selected entries are marked in a bitmap of the row, which is
-// read in order: the output lists them in increasing entry, as the TopK definition's ties need.
+// 1 .. kCandBins-2 hold the single class lo + bin - 1).  The class of the k-th largest key comes
+// from the histogram.  When it is one of those bins and holds at most kSelMembers keys, one pass
+// over the lists decides every entry (see below); otherwise the lists are radix-selected whole,
+// keys equal to the threshold beyond what is taken going by smallest entry (a radix select on
+// kEntryMax - entry).  The selected entries are marked in a bitmap of the row, which is read in
+// order: the output lists them in increasing entry, as the TopK definition's ties need, and the
+// lists may be visited in any order.
 __device__ void select_query(const IndexArgs& a, long long qi, const CandLists& cl, const uint32_t* hist, int lo,
                              int shift, uint32_t* wh, uint32_t* mem, uint32_t* bm) {
   const int lane = threadIdx.x & 31;
@@ -436,17 +465,27 @@ __device__ void select_query(const IndexArgs& a, long long qi, const CandLists& 
   int rem = K, cmp = 0;
   bool ok = true;
   const int lowb = kClassShift - shift;        // key bits below the class
+  const int nwords = (nv + 31) / 32;
   if (fb >= 1 && fb <= kCandBins - 2 && fc <= static_cast<uint32_t>(kSelMembers)) {
+    // one pass over the lists: entries of the classes above the k-th one are marked at once;
+    // the k-th class's keys go to shared memory as (low key bits, kEntryMax15 - entry), one
+    // 32-bit value each (entries are below 2^15), whose larger values are exactly the better
+    // entries (larger key, or equal key and smaller entry): its rem largest are marked next
     const uint32_t cls = static_cast<uint32_t>(lo + fb - 1);
     const uint32_t lmask = (1u << lowb) - 1u;
+    for (int i = lane; i < nwords; i += 32) bm[i] = 0u;
+    __syncwarp();
     uint32_t m = 0;
     for_each_cand(cl, [&](unsigned long long e, bool v) {
       const uint32_t ks = static_cast<uint32_t>(e >> 32);
-      const bool hit = v && (ks >> lowb) == cls;
+      const uint32_t entry = static_cast<uint32_t>(e & 0xFFFFFFFFull);
+      const uint32_t c = ks >> lowb;
+      if (v && c > cls && entry < static_cast<uint32_t>(nv)) atomicOr(&bm[entry >> 5], 1u << (entry & 31));
+      const bool hit = v && c == cls;
       const uint32_t hm = __ballot_sync(0xffffffffu, hit);
       if (hit) {
         const uint32_t q = m + __popc(hm & lt);
-        if (q < static_cast<uint32_t>(kSelMembers)) mem[q] = ks & lmask;
+        if (q < static_cast<uint32_t>(kSelMembers)) mem[q] = ((ks & lmask) << 15) | (0x7FFFu - (entry & 0x7FFFu));
       }
       m += __popc(hm);
     });
@@ -455,18 +494,33 @@ __device__ void select_query(const IndexArgs& a, long long qi, const CandLists& 
       if (lane == 0) report_error(a.status, CSA_ERR_DEVICE_CHECK, -2001);
       return;
     }
-    rem = K - static_cast<int>(fa);
-    uint32_t pre = 0;
-    eq = fc;
-    if (fc == static_cast<uint32_t>(rem)) {
-      cmp = lowb;                                // the whole class is taken
-    } else {
-      const int nm = static_cast<int>(fc);
+    int rem1 = K - static_cast<int>(fa);
+    uint32_t pre = 0, eq1 = fc;
+    int cmp1 = lowb + 15;                        // every member taken: compare nothing below the class
+    const int nm = static_cast<int>(fc);
+    if (fc != static_cast<uint32_t>(rem1)) {
       ok = warp_radix([&](auto g) {
         for (int b = 0; b < nm; b += 32) g(b + lane < nm ? mem[b + lane] : 0u, b + lane < nm);
-      }, lowb, pre, rem, cmp, eq, wh);
+      }, lowb + 15, pre, rem1, cmp1, eq1, wh);
+      if (!ok) {
+        if (lane == 0) report_error(a.status, CSA_ERR_DEVICE_CHECK, -2002);
+        return;
+      }
     }
-    thr = (cls << lowb) | pre;
+    // the member values are distinct, so every value at or above the threshold is taken
+    const uint32_t tcm = cmp1 >= 32 ? 0u : pre >> cmp1;
+    for (int b = 0; b < nm; b += 32) {
+      if (b + lane < nm) {
+        const uint32_t val = mem[b + lane];
+        if ((cmp1 >= 32 ? 0u : val >> cmp1) >= tcm) {
+          const uint32_t entry = 0x7FFFu - (val & 0x7FFFu);
+          if (entry < static_cast<uint32_t>(nv)) atomicOr(&bm[entry >> 5], 1u << (entry & 31));
+        }
+      }
+    }
+    __syncwarp();
+    if (!emit_bitmap(bm, nwords, out, K) && lane == 0) report_error(a.status, CSA_ERR_DEVICE_CHECK, -2003);
+    return;
   } else {
     uint32_t kmax = 0u, kmin = 0xFFFFFFFFu;
     for_each_cand(cl, [&](unsigned long long e, bool v) {
@@ -508,7 +562,6 @@ __device__ void select_query(const IndexArgs& a, long long qi, const CandLists& 
     if (lane == 0) report_error(a.status, CSA_ERR_DEVICE_CHECK, -2002);
     return;
   }
-  const int nwords = (nv + 31) / 32;
   for (int i = lane; i < nwords; i += 32) bm[i] = 0u;
   __syncwarp();
   const uint32_t tc_ = cmp >= 32 ? 0u : thr >> cmp;
@@ -521,31 +574,7 @@ __device__ void select_query(const IndexArgs& a, long long qi, const CandLists& 
     if (sel && entry < static_cast<uint32_t>(nv)) atomicOr(&bm[entry >> 5], 1u << (entry & 31));
   });
   __syncwarp();
-  // the marked entries in increasing order: lane l reads words [l W, (l + 1) W)
-  const int W = (nwords + 31) / 32;
-  const int w0 = min(nwords, lane * W), w1 = min(nwords, w0 + W);
-  uint32_t cnt = 0;
-  for (int i = w0; i < w1; ++i) cnt += __popc(bm[i]);
-  uint32_t ex = cnt;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, ex, o);
-    if (lane >= o) ex += y;
-  }
-  const uint32_t total = __shfl_sync(0xffffffffu, ex, 31);
-  if (total != static_cast<uint32_t>(K)) {
-    if (lane == 0) report_error(a.status, CSA_ERR_DEVICE_CHECK, -2003);
-    return;
-  }
-  uint32_t o = ex - cnt;
-  for (int i = w0; i < w1; ++i) {
-    uint32_t bits = bm[i];
-    while (bits != 0u) {
-      const int b = __ffs(bits) - 1;
-      out[o++] = i * 32 + b;
-      bits &= bits - 1u;
-    }
-  }
+  if (!emit_bitmap(bm, nwords, out, K) && lane == 0) report_error(a.status, CSA_ERR_DEVICE_CHECK, -2003);
 }
 
 template <int DI, int NCOL, bool FP8, bool LP, bool CAND>

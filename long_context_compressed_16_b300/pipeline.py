@@ -36,23 +36,27 @@ def compress(Ca, Za, m, Cb=None, Zb=None, bias_a=None, bias_b=None, gamma=None, 
     return out
 
 
-def index_desc(B, Tq, N, nI, dI, k, m, fp8=False, lowp=False, bf16_scores=False):
+def index_desc(B, Tq, N, nI, dI, k, m, fp8=False, lowp=False, bf16_scores=False, select_mode=0):
+    """select_mode: C.CSA_SELECT_AUTO (0), C.CSA_SELECT_FUSED or C.CSA_SELECT_STORED."""
     fmt = C.CSA_FMT_FP8_ROWSCALE_LOWP if lowp else (C.CSA_FMT_FP8_ROWSCALE if fp8 else C.CSA_FMT_BF16)
     return C.csa_index_desc(B=B, Tq=Tq, N=N, n_heads=nI, head_dim=dI, k=k, m=m, key_fmt=fmt,
-                            score_fmt=C.CSA_SCORE_BF16 if bf16_scores else C.CSA_SCORE_FP32)
+                            score_fmt=C.CSA_SCORE_BF16 if bf16_scores else C.CSA_SCORE_FP32,
+                            select_mode=select_mode)
 
 
 def index_topk(qI, w, kI, q_pos, m, k, kI_scale=None, score_out=None, idx_out=None, workspace=None,
-               stream=None, lowp=False, bf16_scores=False):
+               stream=None, lowp=False, bf16_scores=False, select_mode=0):
     """Lightning-indexer scores + per-query top-k. Returns int32 [B, Tq, k] (-1 padded).
     lowp: the low-precision indexer (FP8 keys with kI_scale, the query quantised to e4m3).
-    bf16_scores: scores rounded to bf16 before the selection."""
+    bf16_scores: scores rounded to bf16 before the selection.
+    select_mode: where the selection runs (same result): C.CSA_SELECT_AUTO, _FUSED or _STORED."""
     _dev_check(qI, w, kI, q_pos, kI_scale, score_out)
     B, Tq, nI, dI = qI.shape
     N = kI.shape[1]
     if lowp and kI_scale is None:
         raise ValueError("the low-precision indexer takes e4m3 keys with row scales")
-    desc = index_desc(B, Tq, N, nI, dI, k, m, fp8=kI_scale is not None, lowp=lowp, bf16_scores=bf16_scores)
+    desc = index_desc(B, Tq, N, nI, dI, k, m, fp8=kI_scale is not None, lowp=lowp, bf16_scores=bf16_scores,
+                      select_mode=select_mode)
     if idx_out is None:
         idx_out = torch.empty((B, Tq, k), dtype=torch.int32, device=qI.device)
     if workspace is None:

@@ -113,7 +113,14 @@ def test_index_validation_and_workspace():
     assert call(_idesc(), ws_bytes=100) == C.CSA_ERR_WORKSPACE
     assert call(_idesc(key_fmt=C.CSA_FMT_FP8_ROWSCALE)) == C.CSA_ERR_INVALID_ARG   # scales missing
     assert call(_idesc(score_fmt=2)) == C.CSA_ERR_INVALID_ARG                       # unknown score format
+    assert call(_idesc(select_mode=3)) == C.CSA_ERR_INVALID_ARG                     # unknown selection mode
     assert C.lib.csa_index_topk_workspace(ctypes.byref(_idesc(score_fmt=C.CSA_SCORE_BF16))) == ws
+    # the fused selection's candidate lists take the place of the score rows, so a call that may
+    # take it never needs less workspace than one that stores the rows
+    kw = dict(B=1, Tq=2400, N=32768, k=512)
+    stored = C.lib.csa_index_topk_workspace(ctypes.byref(_idesc(select_mode=C.CSA_SELECT_STORED, **kw)))
+    fused = C.lib.csa_index_topk_workspace(ctypes.byref(_idesc(select_mode=C.CSA_SELECT_FUSED, **kw)))
+    assert stored > 0 and fused >= stored
     assert call(_idesc(B=0)) == C.CSA_OK
 
 

@@ -8,6 +8,8 @@ list; the score rows are never stored.  The selection is exact, so the result mu
 bit, the unfused path (csa_index_score, then csa_topk on the stored rows), which the oracle pins in
 test_parity_gpu; a few rows per case are also checked against the oracle directly.
 
+The cases force the fused path (select_mode CSA_SELECT_FUSED) on shapes small enough to check
+quickly; CSA_SELECT_AUTO takes it only for rows of at least 16 k entries, which one test checks.
 The cases reach both selector paths: the common one (the class of the k-th key holds few keys:
 resolve only that class) and the general radix select over the whole list (heavy ties, or keys
 that climb past the histogram's range), plus rows with nothing visible (groups the score kernel
@@ -95,7 +97,7 @@ def test_fused_select_equals_unfused(B, Tq, N, nI, dI, k, fused):
     w = S.uniform_f64((B, Tq, nI), 41, S.TID["w"], DEV).float()
     kI = S.normal_bf16((B, N, dI), 41, S.TID["kI"], DEV)
     q_pos = _causal_pos(B, Tq, N)
-    desc = P.index_desc(B, Tq, N, nI, dI, k, M)
+    desc = P.index_desc(B, Tq, N, nI, dI, k, M, select_mode=C.CSA_SELECT_FUSED)
     got = _fused(desc, qI, w, kI, None, q_pos, expect_launches=1, fused=fused)
     ref = _unfused(desc, qI, w, kI, None, q_pos)
     assert torch.equal(got, ref)
@@ -115,7 +117,7 @@ def test_fused_select_heavy_ties():
     base = S.normal_bf16((B, 3, dI), 43, S.TID["kI"], DEV)
     kI = base[:, torch.arange(N, device=DEV) % 3].contiguous()
     q_pos = _causal_pos(B, Tq, N)
-    desc = P.index_desc(B, Tq, N, nI, dI, k, M)
+    desc = P.index_desc(B, Tq, N, nI, dI, k, M, select_mode=C.CSA_SELECT_FUSED)
     fused = _fused(desc, qI, w, kI, None, q_pos, expect_launches=1)
     ref = _unfused(desc, qI, w, kI, None, q_pos)
     assert torch.equal(fused, ref)
@@ -136,7 +138,7 @@ def test_fused_select_climbing_scores():
     scale = torch.pow(2.0, torch.arange(N, device=DEV, dtype=torch.float32) / 48.0)
     kI = (kI0 * scale[None, :, None]).to(torch.bfloat16).contiguous()
     q_pos = _causal_pos(B, Tq, N)
-    desc = P.index_desc(B, Tq, N, nI, dI, k, M)
+    desc = P.index_desc(B, Tq, N, nI, dI, k, M, select_mode=C.CSA_SELECT_FUSED)
     fused = _fused(desc, qI, w, kI, None, q_pos, expect_launches=1)
     ref = _unfused(desc, qI, w, kI, None, q_pos)
     assert torch.equal(fused, ref)
@@ -149,7 +151,7 @@ def test_fused_select_bf16_scores():
     w = S.uniform_f64((B, Tq, nI), 45, S.TID["w"], DEV).float()
     kI = S.normal_bf16((B, N, dI), 45, S.TID["kI"], DEV)
     q_pos = _causal_pos(B, Tq, N)
-    desc = P.index_desc(B, Tq, N, nI, dI, k, M, bf16_scores=True)
+    desc = P.index_desc(B, Tq, N, nI, dI, k, M, bf16_scores=True, select_mode=C.CSA_SELECT_FUSED)
     fused = _fused(desc, qI, w, kI, None, q_pos, expect_launches=1)
     ref = _unfused(desc, qI, w, kI, None, q_pos)
     assert torch.equal(fused, ref)
@@ -164,7 +166,7 @@ def test_fused_select_lowp():
     kI8, kI_scale = S.quantize_rows_e4m3(kf)
     kI8, kI_scale = kI8.to(DEV), kI_scale.to(DEV)
     q_pos = _causal_pos(B, Tq, N)
-    desc = P.index_desc(B, Tq, N, nI, dI, k, M, lowp=True)
+    desc = P.index_desc(B, Tq, N, nI, dI, k, M, lowp=True, select_mode=C.CSA_SELECT_FUSED)
     fused = _fused(desc, qI, w, kI8, kI_scale, q_pos, expect_launches=2)   # query quantisation + scores
     ref = _unfused(desc, qI, w, kI8, kI_scale, q_pos)
     assert torch.equal(fused, ref)
@@ -178,11 +180,31 @@ def test_fused_select_is_deterministic_and_batch_invariant():
     w = S.uniform_f64((B, Tq, nI), 47, S.TID["w"], DEV).float()
     kI = S.normal_bf16((B, N, dI), 47, S.TID["kI"], DEV)
     q_pos = (M * N - M * Tq + M * torch.arange(Tq, dtype=torch.int32, device=DEV)).repeat(B, 1).contiguous()
-    a = P.index_topk(qI, w, kI, q_pos, M, k)
-    b = P.index_topk(qI, w, kI, q_pos, M, k)
+    F = C.CSA_SELECT_FUSED
+    a = P.index_topk(qI, w, kI, q_pos, M, k, select_mode=F)
+    b = P.index_topk(qI, w, kI, q_pos, M, k, select_mode=F)
     # sequence 1 alone (350 groups: too few for the fused path, so stored scores and the
     # selector kernels) and inside the batch (700 groups: fused)
-    c = P.index_topk(qI[1:].contiguous(), w[1:].contiguous(), kI[1:].contiguous(), q_pos[1:].contiguous(), M, k)
+    c = P.index_topk(qI[1:].contiguous(), w[1:].contiguous(), kI[1:].contiguous(), q_pos[1:].contiguous(), M, k,
+                     select_mode=F)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
     assert torch.equal(a[1:], c)
+
+
+@pytest.mark.parametrize("N,auto_fused", [(8192, True), (8191, False)])
+def test_select_mode_auto_and_stored(N, auto_fused):
+    """CSA_SELECT_AUTO fuses the selection for rows of at least 16 k entries (k = 512: N >= 8192),
+    where it is faster, and stores the rows otherwise; CSA_SELECT_STORED always stores them.  All
+    give the same rows."""
+    B, Tq, nI, dI, k = 1, 2400, 64, 128, 512
+    qI = S.normal_bf16((B, Tq, nI, dI), 48, S.TID["qI"], DEV)
+    w = S.uniform_f64((B, Tq, nI), 48, S.TID["w"], DEV).float()
+    kI = S.normal_bf16((B, N, dI), 48, S.TID["kI"], DEV)
+    q_pos = _causal_pos(B, Tq, N)
+    auto = _fused(P.index_desc(B, Tq, N, nI, dI, k, M), qI, w, kI, None, q_pos, expect_launches=1, fused=auto_fused)
+    stored = _fused(P.index_desc(B, Tq, N, nI, dI, k, M, select_mode=C.CSA_SELECT_STORED), qI, w, kI, None, q_pos,
+                    expect_launches=1, fused=False)
+    forced = _fused(P.index_desc(B, Tq, N, nI, dI, k, M, select_mode=C.CSA_SELECT_FUSED), qI, w, kI, None, q_pos,
+                    expect_launches=1, fused=True)
+    assert torch.equal(auto, stored) and torch.equal(auto, forced)
