@@ -322,6 +322,39 @@ def test_attend_decode_1m_fp8_full():
     _decode_attend_case("csa_decode_1m_b4_fp8", fp8=True)
 
 
+@pytest.mark.parametrize("k,splits", [(60, 1), (100, 2), (320, 3), (1024, 6)])
+def test_attend_decode_split_counts(k, splits):
+    """Decode with k + 128 window slots cut into 192-slot splits: one split (no merge) and 2, 3, 6
+    splits merged in a thread-block cluster (each CTA owns whole dim pairs of the output, so a
+    rotated pair is merged and turned back in one place; 3 and 6 do not divide the 256 pairs
+    evenly).  Selections are seeded random rows; a few queries see fewer entries than k."""
+    assert (k + 128 + 191) // 192 == splits
+    B, H, d, N, m = 4, 64, 512, 4096, 4
+    q_pos = torch.tensor([[4 * N - 1], [4 * N - 77], [4 * k // 2], [4 * N // 3]], dtype=torch.int32, device=DEV)
+    q = S.normal_bf16((B, 1, H, d), 17, 1, DEV)
+    kv = S.normal_bf16((B, N, d), 17, 2, DEV)
+    win = S.normal_bf16((B, 128, d), 17, 3, DEV)
+    sink = S.normal_f64((H,), 17, 4).float().to(DEV)
+    rng = np.random.default_rng(k)
+    idx_np = np.full((B, 1, k), -1, dtype=np.int64)
+    for b in range(B):
+        nv = nvis_of(int(q_pos[b, 0]), m, N)
+        take = min(k, nv)
+        idx_np[b, 0, :take] = np.sort(rng.permutation(nv)[:take])
+    idx = torch.from_numpy(idx_np.astype(np.int32)).to(DEV)
+    out, lse, ws = P.csa_attend(q, kv, idx, win, sink, q_pos, want_lse=True)
+    torch.cuda.synchronize()
+    assert C.csa_read_device_status(ws)[0] == C.CSA_OK
+    inp = dict(q=q, kv=kv, win=win, sink=sink, q_pos=q_pos)
+    ref, lref = _oracle_attend_rows(inp, idx_np, m, 128, [(b, 0) for b in range(B)])
+    assert_close(out[:, 0], ref, f"decode, {splits} splits")
+    assert_lse(lse[:, 0], lref, "lse")
+    # the same call again gives the same bits (fixed split order)
+    out2, lse2, _ = P.csa_attend(q, kv, idx, win, sink, q_pos, want_lse=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
 def test_attend_tiny_prefill_all_queries():
     w = S.WORKLOADS["tiny_csa_prefill_t2048"]
     inp = S.make_inputs(w, DEV)
