@@ -331,7 +331,8 @@ def run_other(args, dev, stream):
     ad = P.attend_desc(1, w.T, w.N, w.H, w.d, k=0, m=w.m, Wcap=w.T, window=w.window)
     ws = torch.zeros(max(256, C.hca_attend_workspace(ad)), dtype=torch.uint8, device=dev)
     out = torch.empty((1, w.T, w.H, w.d), dtype=torch.bfloat16, device=dev)
-    ms_c = graph_ms([lambda sp: P.compress(inp["C"], inp["Z"], w.m, out=kv, stream=sp)], 5)
+    ms_c = graph_ms([lambda sp: P.compress(inp["C"], inp["Z"], w.m, bias_a=inp["B"], gamma=inp["gamma"], out=kv,
+                                           stream=sp)], 5)
     ms_a = graph_ms([lambda sp: C.check(C.hca_attend(ad, inp["q"], kv, inp["win"], inp["sink"], inp["q_pos"], out, None,
                                                      ws, stream=sp), "hca_attend")], 3)
     rows = sum(min(w.N, (t + 1) // w.m) + min(w.window, t + 1) for t in range(w.T))
@@ -351,9 +352,10 @@ def run_other(args, dev, stream):
     wsi = torch.zeros(max(256, C.csa_index_topk_workspace(idesc)), dtype=torch.uint8, device=dev)
     wsa = torch.zeros(max(256, C.csa_attend_workspace(ad)), dtype=torch.uint8, device=dev)
     ms = graph_ms([
-        lambda sp: P.compress(inp["Ca"], inp["Za"], w.m, Cb=inp["Cb"], Zb=inp["Zb"], out=kv, stream=sp),
-        lambda sp: P.compress(inp["Ca_I"], inp["Za_I"], w.m, Cb=inp["Cb_I"], Zb=inp["Zb_I"], rope=False, rope_dims=0,
-                              out=kI, stream=sp),
+        lambda sp: P.compress(inp["Ca"], inp["Za"], w.m, Cb=inp["Cb"], Zb=inp["Zb"], bias_a=inp["Ba"],
+                              bias_b=inp["Bb"], gamma=inp["gamma"], out=kv, stream=sp),
+        lambda sp: P.compress(inp["Ca_I"], inp["Za_I"], w.m, Cb=inp["Cb_I"], Zb=inp["Zb_I"], bias_a=inp["Ba_I"],
+                              bias_b=inp["Bb_I"], gamma=inp["gamma_I"], rope=False, rope_dims=0, out=kI, stream=sp),
         lambda sp: C.check(C.csa_index_topk(idesc, inp["qI"], inp["w"], kI, None, inp["q_pos"], idx, None, wsi,
                                             stream=sp), "csa_index_topk"),
         lambda sp: C.check(C.csa_attend(ad, inp["q"], kv, idx, inp["win"], inp["sink"], inp["q_pos"], out, None, wsa,
@@ -429,8 +431,10 @@ def run_prefill(args, dev, stream):
         # score rows are never stored)
         rec = (lambda i: evs[i].record(stream)) if evs else (lambda i: None)
         rec(0)
-        P.compress(inp["Ca"], inp["Za"], w.m, Cb=inp["Cb"], Zb=inp["Zb"], out=kv, stream=sptr)
-        P.compress(inp["Ca_I"], inp["Za_I"], w.m, Cb=inp["Cb_I"], Zb=inp["Zb_I"], rope=False, rope_dims=0, out=kI,
+        P.compress(inp["Ca"], inp["Za"], w.m, Cb=inp["Cb"], Zb=inp["Zb"], bias_a=inp["Ba"], bias_b=inp["Bb"],
+                   gamma=inp["gamma"], out=kv, stream=sptr)
+        P.compress(inp["Ca_I"], inp["Za_I"], w.m, Cb=inp["Cb_I"], Zb=inp["Zb_I"], bias_a=inp["Ba_I"],
+                   bias_b=inp["Bb_I"], gamma=inp["gamma_I"], rope=False, rope_dims=0, out=kI,
                    stream=sptr)
         rec(1)
         C.check(C.csa_index_topk(idesc, inp["qI"], inp["w"], kI, None, inp["q_pos"], idx, None, wsi, stream=sptr),
@@ -817,8 +821,8 @@ def run_case(args):
             adesc = P.attend_desc(1, w.T, w.N, w.H, w.d, k=w.k, m=w.m, Wcap=w.T, window=w.window)
             ws = torch.zeros(max(256, C.csa_attend_workspace(adesc)), dtype=torch.uint8, device=dev)
             out = torch.empty((1, w.T, w.H, w.d), dtype=torch.bfloat16, device=dev)
-            fn = lambda: C.check(C.csa_attend(adesc, inp["q"], kv, idx, inp["win"], inp["sink"], inp["q_pos"], out,
-                                              None, ws), "csa_attend")
+            fn = lambda sp: C.check(C.csa_attend(adesc, inp["q"], kv, idx, inp["win"], inp["sink"], inp["q_pos"], out,
+                                                 None, ws, stream=sp), "csa_attend")
             _, flops = prefill_flops(w)
         elif args.case == "index_topk_prefill_split":
             kI = S.normal_bf16((1, w.N, w.dI), 3, S.TID["kI"], dev)
@@ -828,17 +832,18 @@ def run_case(args):
             scores = torch.empty((1, w.T, w.N), dtype=torch.float32, device=dev)
             idx = torch.empty((1, w.T, w.k), dtype=torch.int32, device=dev)
 
-            def fn():
-                C.check(C.csa_index_score(idesc, inp["qI"], inp["w"], kI, None, inp["q_pos"], scores, ws),
-                        "csa_index_score")
-                C.check(C.csa_topk(idesc, scores, inp["q_pos"], idx, ws), "csa_topk")
+            def fn(sp):
+                C.check(C.csa_index_score(idesc, inp["qI"], inp["w"], kI, None, inp["q_pos"], scores, ws,
+                                          stream=sp), "csa_index_score")
+                C.check(C.csa_topk(idesc, scores, inp["q_pos"], idx, ws, stream=sp), "csa_topk")
             flops, _ = prefill_flops(w)
         elif args.case == "index_topk_prefill":
             kI = S.normal_bf16((1, w.N, w.dI), 3, S.TID["kI"], dev)
             idesc = P.index_desc(1, w.T, w.N, w.nI, w.dI, w.k, w.m)
             ws = torch.zeros(max(256, C.csa_index_topk_workspace(idesc)), dtype=torch.uint8, device=dev)
             idx = torch.empty((1, w.T, w.k), dtype=torch.int32, device=dev)
-            fn = lambda: C.check(C.csa_index_topk(idesc, inp["qI"], inp["w"], kI, None, inp["q_pos"], idx, None, ws),
+            fn = lambda sp: C.check(C.csa_index_topk(idesc, inp["qI"], inp["w"], kI, None, inp["q_pos"], idx, None, ws,
+                                                     stream=sp),
                                  "csa_index_topk")
             flops, _ = prefill_flops(w)
         else:
@@ -846,14 +851,18 @@ def run_case(args):
             idesc = P.index_desc(1, w.T, w.N, w.nI, w.dI, w.k, w.m)
             ws = torch.zeros(max(256, C.csa_index_score_workspace(idesc)), dtype=torch.uint8, device=dev)
             scores = torch.empty((1, w.T, w.N), dtype=torch.float32, device=dev)
-            fn = lambda: C.check(C.csa_index_score(idesc, inp["qI"], inp["w"], kI, None, inp["q_pos"], scores, ws),
+            fn = lambda sp: C.check(C.csa_index_score(idesc, inp["qI"], inp["w"], kI, None, inp["q_pos"], scores, ws,
+                                                      stream=sp),
                                  "csa_index_score")
             flops, _ = prefill_flops(w)
         unit = ("TFLOP/s", lambda ms: flops / (ms * 1e-3) / 1e12)
     elif args.case == "compress":
         x = {n: S.normal_bf16((1, T, 512), 3, S.TID[n], dev) for n in ("Ca", "Cb", "Za", "Zb")}
+        prm = {n: (0.5 * S.normal_f64((4, 512), 3, S.TID[n], dev)).float() for n in ("Ba", "Bb")}
+        prm["gamma"] = (1.0 + 0.1 * S.normal_f64((512,), 3, S.TID["gamma"], dev)).float()
         out = torch.empty((1, T // 4, 512), dtype=torch.bfloat16, device=dev)
-        fn = lambda: P.compress(x["Ca"], x["Za"], 4, Cb=x["Cb"], Zb=x["Zb"], out=out)
+        fn = lambda sp: P.compress(x["Ca"], x["Za"], 4, Cb=x["Cb"], Zb=x["Zb"], bias_a=prm["Ba"], bias_b=prm["Bb"],
+                                   gamma=prm["gamma"], out=out, stream=sp)
         byts = 4 * T * 512 * 2 + (T // 4) * 512 * 2
         unit = ("GB/s", lambda ms: byts / (ms * 1e-3) / 1e9)
     else:
@@ -865,19 +874,28 @@ def run_case(args):
         z = torch.empty((T, g * r_o), dtype=torch.bfloat16, device=dev)
         y = torch.empty((T, d_out), dtype=torch.bfloat16, device=dev)
         ws = torch.zeros(256, dtype=torch.uint8, device=dev)
-        fn = lambda: P.out_proj(Oa, Wd, g, W_proj=Wp, z=z, y=y, workspace=ws)
+        fn = lambda sp: P.out_proj(Oa, Wd, g, W_proj=Wp, z=z, y=y, workspace=ws, stream=sp)
         flops = 2.0 * T * (n_h * d_h * r_o + g * r_o * d_out)
         unit = ("TFLOP/s", lambda ms: flops / (ms * 1e-3) / 1e12)
-    for _ in range(max(1, args.warmup)):
-        fn()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(max(1, args.steps)):
-        fn()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / max(1, args.steps)
+    # the calls back to back in one CUDA graph (no host time between them), after warm-up calls
+    stream = torch.cuda.Stream()
+    n = max(1, args.steps)
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            fn(stream.cuda_stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(n):
+                fn(stream.cuda_stream)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
     print(json.dumps({"case": args.case, "tokens": T, "ms_per_call": ms, unit[0]: unit[1](ms)}), flush=True)
 
 

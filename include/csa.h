@@ -104,8 +104,9 @@ typedef struct {
   int overlap;             /* 1: CSA (Cb, Zb used, block i-1 overlaps); 0: HCA single stream */
   int rope_dims;           /* r; 0 = no rotation */
   float rope_theta;        /* base used when inv_freq is NULL (160000 on the compressed branch) */
-  const float* inv_freq;   /* HOST pointer to r/2 values (e.g. a YaRN table) or NULL:
-                              inv_freq_j = theta^(-2j/r) */
+  const float* inv_freq;   /* HOST pointer to r/2 finite values (e.g. a YaRN table) or
+                              NULL: inv_freq_j = theta^(-2j/r); a non-finite value is
+                              CSA_ERR_INVALID_ARG */
   int pos_shift;           /* entry i sits at position m*i + pos_shift */
   float eps;               /* RMSNorm epsilon (1e-6) */
   unsigned flags;          /* CSA_COMPRESS_NORM | CSA_COMPRESS_ROPE */
@@ -269,7 +270,7 @@ typedef struct {
   int Wcap, window;        /* ring capacity and window length (128) */
   float scale;             /* 0 => 1/sqrt(d) */
   float rope_theta;        /* base used when inv_freq is NULL */
-  const float* inv_freq;   /* HOST pointer to rope_dims/2 values or NULL */
+  const float* inv_freq;   /* HOST pointer to rope_dims/2 finite values or NULL */
   float eps;               /* RMSNorm epsilon for q */
   csa_format kv_fmt;       /* CSA_FMT_BF16 or CSA_FMT_FP8_MIXED */
   unsigned flags;          /* CSA_ATTEND_* */

@@ -36,9 +36,17 @@ bool make_rope(int r, float theta, const float* inv_freq, csa::RopeParams* rp) {
   if (r < 0 || (r & 1) || r / 2 > csa::kMaxRopePairs) return false;
   std::memset(rp, 0, sizeof(*rp));
   rp->r = r;
+  const long double two_pi = 2.0L * std::acos(-1.0L);
+  const long double two64 = std::ldexp(1.0L, 64);
   for (int j = 0; j < r / 2; ++j) {
-    rp->inv_freq[j] = inv_freq ? static_cast<double>(inv_freq[j])
-                               : std::pow(static_cast<double>(theta), -2.0 * j / static_cast<double>(r));
+    const double f = inv_freq ? static_cast<double>(inv_freq[j])
+                              : std::pow(static_cast<double>(theta), -2.0 * j / static_cast<double>(r));
+    if (!std::isfinite(f)) return false;
+    // the turn per position as a fraction of a revolution, mod 1, in 64-bit fixed point
+    long double x = static_cast<long double>(f) / two_pi;
+    x -= std::floor(x);
+    x = std::floor(x * two64 + 0.5L);
+    rp->phase[j] = x >= two64 ? 0ull : static_cast<unsigned long long>(x);
   }
   return true;
 }

@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(AttnCfg<D, NG, FP8>::THREADS, 1) k_attend(Atte
   const int r16 = (a.q_norm_rope && !FP8) ? ((a.rp.r + 15) & ~15) : 0;   // dims of the lo block
   if (tid < a.rp.r / 2) {
     float cs, sn;
-    rope_cos_sin(static_cast<double>(t), a.rp.inv_freq[tid], cs, sn);
+    rope_cos_sin(t, a.rp.phase[tid], cs, sn);
     rope_tab[tid] = make_float2(cs, sn);
   }
   __syncthreads();
@@ -629,7 +629,7 @@ __global__ void __launch_bounds__(128 * kCombineHeads) k_attend_combine(AttendAr
   const int tid = threadIdx.x;
   if (tid < a.rp.r / 2) {
     float cs, sn;
-    rope_cos_sin(static_cast<double>(t), a.rp.inv_freq[tid], cs, sn);
+    rope_cos_sin(t, a.rp.phase[tid], cs, sn);
     tab[tid] = make_float2(cs, -sn);                                              // rotation by -t
   }
   if (tid < kCombineHeads) {

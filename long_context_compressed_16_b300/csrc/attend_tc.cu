@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
       }
       if (ct < a.rp.r / 2) {
         float cs, sn;
-        rope_cos_sin(static_cast<double>(J.t), a.rp.inv_freq[ct], cs, sn);
+        rope_cos_sin(J.t, a.rp.phase[ct], cs, sn);
         rope[par * 32 + ct] = make_float2(cs, sn);
       }
       // the copies land whatever happened elsewhere: wait for them without the abort flag
@@ -781,7 +781,7 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
       if (rank == 0 && a.lse != nullptr) a.lse[I.qi * a.H + hgl] = (M + log2f(L)) * kLn2;
     } else if (tid >= 128 && tid - 128 < a.rp.r / 2) {
       float cs, sn;
-      rope_cos_sin(static_cast<double>(I.t), a.rp.inv_freq[tid - 128], cs, sn);
+      rope_cos_sin(I.t, a.rp.phase[tid - 128], cs, sn);
       rope[32 + tid - 128] = make_float2(cs, -sn);                // rotation by -t
     }
     __syncthreads();

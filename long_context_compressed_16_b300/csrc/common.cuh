@@ -11,10 +11,13 @@ namespace csa {
 
 constexpr int kMaxRopePairs = 64;   // rope_dims <= 128
 
-// RoPE frequencies are computed on the host in double and passed by value.
+// RoPE frequencies, computed on the host and passed by value.  Pair j turns by inv_freq_j radians
+// per position; phase[j] is that turn as a 64-bit binary fraction of a revolution,
+// round(inv_freq_j / (2 pi) * 2^64) mod 2^64, so the angle of an integer position reduces modulo
+// 2 pi exactly in integer arithmetic (no FP64 on the device).
 struct RopeParams {
   int r;                    // rotated dims (even), the last r dims of each vector
-  double inv_freq[kMaxRopePairs];
+  unsigned long long phase[kMaxRopePairs];
 };
 
 // Status word at the start of every workspace: {code, detail, pad, pad}.
@@ -69,13 +72,13 @@ __device__ __forceinline__ void report_error(int32_t* status, int32_t code, int3
 // positions up to 2^20 and beyond keep full fp32 accuracy in the angle; the reduced angle lies in
 // [-pi, pi], where the hardware sine/cosine (__sincosf, absolute error about 2^-21) is far more
 // accurate than the bf16 values it rotates and needs no general-range reduction.
-__device__ __forceinline__ void rope_cos_sin(double pos, double inv_freq, float& c, float& s) {
-  const double kTwoPi = 6.283185307179586476925286766559;
-  const double kInvTwoPi = 0.15915494309189533576888376337251;
-  double a = pos * inv_freq;
-  double n = rint(a * kInvTwoPi);
-  double red = fma(-n, kTwoPi, a);
-  __sincosf(static_cast<float>(red), &s, &c);
+// cos and sin of the RoPE angle pos * inv_freq: pos * phase mod 2^64 is the angle's fraction of a
+// revolution (to 2^-64 per unit of pos); its top 32 bits, read as a signed fraction, give the angle
+// reduced to [-pi, pi) for the fast sine and cosine.
+__device__ __forceinline__ void rope_cos_sin(long long pos, unsigned long long phase, float& c, float& s) {
+  const unsigned long long turn = static_cast<unsigned long long>(pos) * phase;
+  const float ang = __fmul_rn(static_cast<float>(static_cast<int>(turn >> 32)), 1.46291807926715968e-9f);  // 2 pi / 2^32
+  __sincosf(ang, &s, &c);
 }
 
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }

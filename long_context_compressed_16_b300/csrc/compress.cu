@@ -82,104 +82,169 @@ __device__ __forceinline__ void softmax_step(const uint4* zv, const uint4* cv, c
   }
 }
 
-// CSA entry with m = 4 (R = 4 rows for entry 0, 8 otherwise), exact two-pass softmax per channel:
-// the maximum over all R logits first, then one exp2 per logit and the weighted sum, with no
-// rescaling.  fetch(r, zv, cv) returns row r (a-rows 0..3, then b-rows 4..7) for this thread's 8
-// channels; it is called in both passes.  Both kernels that compress m = 4 CSA entries (the
-// staged whole-sequence kernel and the cache-append path of k_compress) run exactly this code.
-template <int R, class Fetch>
-__device__ __forceinline__ void csa4_entry(Fetch fetch, const float* bias_a, const float* bias_b, int d, int c0,
-                                           float* outv) {
-  auto logits = [&](int r, const uint4& zv, float* z) {
-    const float* bp = r < 4 ? bias_a : bias_b;
-    float4 b0 = make_float4(0.f, 0.f, 0.f, 0.f), b1 = b0;
-    if (bp != nullptr) {
-      b0 = __ldg(reinterpret_cast<const float4*>(bp + static_cast<size_t>(r & 3) * d + c0));
-      b1 = __ldg(reinterpret_cast<const float4*>(bp + static_cast<size_t>(r & 3) * d + c0 + 4));
-    }
-    z[0] = (bf16lo(zv.x) + b0.x) * kLog2e; z[1] = (bf16hi(zv.x) + b0.y) * kLog2e;
-    z[2] = (bf16lo(zv.y) + b0.z) * kLog2e; z[3] = (bf16hi(zv.y) + b0.w) * kLog2e;
-    z[4] = (bf16lo(zv.z) + b1.x) * kLog2e; z[5] = (bf16hi(zv.z) + b1.y) * kLog2e;
-    z[6] = (bf16lo(zv.w) + b1.z) * kLog2e; z[7] = (bf16hi(zv.w) + b1.w) * kLog2e;
-  };
-  float mx[8];
-#pragma unroll
-  for (int c = 0; c < 8; ++c) mx[c] = -INFINITY;
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    uint4 zv, cv;
-    fetch(r, zv, cv);
-    float z[8];
-    logits(r, zv, z);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) mx[c] = fmaxf(mx[c], z[c]);
-  }
-  float sm[8], ac[8];
-#pragma unroll
-  for (int c = 0; c < 8; ++c) { sm[c] = 0.f; ac[c] = 0.f; }
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    uint4 zv, cv;
-    fetch(r, zv, cv);
-    float z[8];
-    logits(r, zv, z);
-    const float cvals[8] = {bf16lo(cv.x), bf16hi(cv.x), bf16lo(cv.y), bf16hi(cv.y),
-                            bf16lo(cv.z), bf16hi(cv.z), bf16lo(cv.w), bf16hi(cv.w)};
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const float p = ex2_approx(z[c] - mx[c]);
-      sm[c] += p;
-      ac[c] = fmaf(p, cvals[c], ac[c]);
-    }
-  }
-#pragma unroll
-  for (int c = 0; c < 8; ++c) outv[c] = ac[c] / sm[c];
+// Pairs of fp32 lanes (channels 2p, 2p+1), each lane rounded to nearest by its own scalar
+// instruction.  (The packed f32x2 forms of these were tried: the same source then gave results
+// that differed in the last bit between the two kernels that inline the entry routine, so the
+// whole-sequence and cache-append paths no longer agreed bit for bit.)
+__device__ __forceinline__ float2 f2_add(float2 a, float2 b) {
+  return make_float2(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y));
+}
+__device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
+  return make_float2(__fmul_rn(a.x, b.x), __fmul_rn(a.y, b.y));
+}
+// a * b + c, one rounding per lane
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
+  return make_float2(__fmaf_rn(a.x, b.x, c.x), __fmaf_rn(a.y, b.y, c.y));
+}
+// maximum of three (a NaN operand is ignored, as by fmaxf)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
+// (lo + bx, hi + by) for the two bf16 halves of w, each one mixed-precision add (bf16 + fp32,
+// rounded to nearest): the same bits as widening first and adding in fp32, without the widening
+__device__ __forceinline__ float2 bf16x2_add(uint32_t w, float bx, float by) {
+  float2 r;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "add.rn.f32.bf16 %0, l, %3;\n\tadd.rn.f32.bf16 %1, h, %4;\n\t}"
+      : "=f"(r.x), "=f"(r.y) : "r"(w), "f"(bx), "f"(by));
+  return r;
 }
 
-// RMSNorm over the entry's d channels (the TPE threads of one entry; every thread of the block
-// takes part), gamma, RoPE at position m*i + pos_shift, bf16 store.  `writer`: this thread holds
-// a finished outv.  `red`: shared scratch of one float per warp (used when TPE > 32).
+// CSA entry with m = 4: softmax over the entry's R rows per channel (R = 4 for entry 0: the a-block
+// only; 8 otherwise: the a-block, then the b-block of the previous block of m tokens), in two
+// chunks of 4 rows.  Each chunk takes its maximum, rescales what the chunk before it summed by
+// 2^(nmx_new - nmx_old), where nmx = -max log2 e, and adds one exp2 per logit:
+// every row is read once.  The maximum starts at -FLT_MAX / 2 rather than -inf, so a chunk whose
+// logits are all -inf contributes zero weights instead of NaN.  The weighted sum is scaled by the
+// correctly rounded reciprocal of the sum.  Every floating-point step here and in the epilogue is
+// an explicit instruction or an intrinsic with a fixed rounding, never a contraction left to the
+// compiler, so each kernel that inlines it computes the same bits.  fetch_z(r) and
+// fetch_c(r) return the logits and the values of row r (a-rows 0..3, then b-rows 4..7) for this
+// thread's 8 channels, fetch_bias(r, lo, hi) the row's 8 position biases (read only when kBias);
+// the values are fetched only when the weights are known.  Both kernels that
+// compress m = 4 CSA entries (the staged whole-sequence kernel and the cache-append path of
+// k_compress) run exactly this code, so their results agree bit for bit.
+template <int R, bool kBias, class FetchZ, class FetchC, class FetchB>
+__device__ __forceinline__ void csa4_entry(FetchZ fetch_z, FetchC fetch_c, FetchB fetch_bias, float* outv) {
+  const float2 kL = make_float2(kLog2e, kLog2e);
+  const float2 kNegL = make_float2(-kLog2e, -kLog2e);
+  float2 mx[4], nm[4], sm[4], ac[4];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    mx[p] = make_float2(-1.7014117e38f, -1.7014117e38f);
+    sm[p] = make_float2(0.f, 0.f);
+    ac[p] = make_float2(0.f, 0.f);
+  }
+#pragma unroll
+  for (int ch = 0; ch < R / 4; ++ch) {
+    float2 t[4][4];       // [row][pair]: logit + bias
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint4 zv = fetch_z(ch * 4 + u);
+      if (kBias) {
+        float4 b0, b1;
+        fetch_bias(ch * 4 + u, b0, b1);
+        t[u][0] = bf16x2_add(zv.x, b0.x, b0.y);
+        t[u][1] = bf16x2_add(zv.y, b0.z, b0.w);
+        t[u][2] = bf16x2_add(zv.z, b1.x, b1.y);
+        t[u][3] = bf16x2_add(zv.w, b1.z, b1.w);
+      } else {
+        t[u][0] = bf16x2_to_f2(zv.x); t[u][1] = bf16x2_to_f2(zv.y);
+        t[u][2] = bf16x2_to_f2(zv.z); t[u][3] = bf16x2_to_f2(zv.w);
+      }
+    }
+    float2 nnew[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      mx[p].x = fmax3(fmax3(mx[p].x, t[0][p].x, t[1][p].x), t[2][p].x, t[3][p].x);
+      mx[p].y = fmax3(fmax3(mx[p].y, t[0][p].y, t[1][p].y), t[2][p].y, t[3][p].y);
+      nnew[p] = f2_mul(mx[p], kNegL);
+    }
+    if (ch > 0) {
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const float2 dl = f2_fma(nm[p], make_float2(-1.f, -1.f), nnew[p]);
+        const float2 al = make_float2(ex2_approx(dl.x), ex2_approx(dl.y));
+        sm[p] = f2_mul(sm[p], al);
+        ac[p] = f2_mul(ac[p], al);
+      }
+    }
+#pragma unroll
+    for (int p = 0; p < 4; ++p) nm[p] = nnew[p];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint4 cw = fetch_c(ch * 4 + u);
+      const float2 cv[4] = {bf16x2_to_f2(cw.x), bf16x2_to_f2(cw.y), bf16x2_to_f2(cw.z), bf16x2_to_f2(cw.w)};
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const float2 g = f2_fma(t[u][p], kL, nm[p]);
+        const float2 w = make_float2(ex2_approx(g.x), ex2_approx(g.y));
+        sm[p] = f2_add(sm[p], w);
+        ac[p] = f2_fma(w, cv[p], ac[p]);
+      }
+    }
+  }
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    outv[2 * p] = __fmul_rn(ac[p].x, __frcp_rn(sm[p].x));
+    outv[2 * p + 1] = __fmul_rn(ac[p].y, __frcp_rn(sm[p].y));
+  }
+}
+
+// RMSNorm over the entry's d channels (the TPE threads of one entry; every thread of the sync
+// domain takes part), gamma, RoPE at position m*i + pos_shift, bf16 store.  `writer`: this thread
+// holds a finished outv.  `lt`: the thread's index in the sync domain, whose barrier is sync();
+// `red`: the domain's shared scratch of one float per warp (used when TPE > 32).  `gam`: this
+// thread's 8 RMSNorm weights already in registers, or null to read them from a.gamma.
+template <class Sync>
 __device__ __forceinline__ void norm_rope_store(const CompressArgs& a, float* outv, bool writer, int b, int i,
-                                                int c0, int TPE, float* red) {
-  const int tid = threadIdx.x;
+                                                int c0, int TPE, int lt, float* red, const float* gam, Sync sync) {
   const int d = a.d;
   if (a.norm) {
     float ss = 0.f;
     if (writer) {
 #pragma unroll
-      for (int c = 0; c < 8; ++c) ss = fmaf(outv[c], outv[c], ss);
+      for (int c = 0; c < 8; c += 2) ss = fmaf(outv[c], outv[c], fmaf(outv[c + 1], outv[c + 1], ss));
     }
     const int lanes = TPE < 32 ? TPE : 32;
-    for (int o = lanes >> 1; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    for (int o = lanes >> 1; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
     if (TPE > 32) {
-      __syncthreads();
-      if ((tid & 31) == 0) red[tid >> 5] = ss;
-      __syncthreads();
-      const int w0 = (tid / TPE) * (TPE >> 5);
+      sync();
+      if ((lt & 31) == 0) red[lt >> 5] = ss;
+      sync();
+      const int w0 = (lt / TPE) * (TPE >> 5);
       ss = 0.f;
-      for (int k = 0; k < (TPE >> 5); ++k) ss += red[w0 + k];
+      for (int k = 0; k < (TPE >> 5); ++k) ss = __fadd_rn(ss, red[w0 + k]);
     }
-    const float inv = 1.0f / sqrtf(ss / static_cast<float>(d) + a.eps);
+    // d is a power of two, so 1/d is exact
+    const float inv = rsqrtf(fmaf(ss, 1.0f / static_cast<float>(d), a.eps));
 #pragma unroll
-    for (int c = 0; c < 8; ++c) outv[c] *= inv;
+    for (int c = 0; c < 8; ++c) outv[c] = __fmul_rn(outv[c], inv);
   }
   if (!writer) return;
-  if (a.gamma != nullptr) {
+  if (gam != nullptr) {
+#pragma unroll
+    for (int c = 0; c < 8; ++c) outv[c] = __fmul_rn(outv[c], gam[c]);
+  } else if (a.gamma != nullptr) {
     const float4 g0 = __ldg(reinterpret_cast<const float4*>(a.gamma + c0));
     const float4 g1 = __ldg(reinterpret_cast<const float4*>(a.gamma + c0 + 4));
-    outv[0] *= g0.x; outv[1] *= g0.y; outv[2] *= g0.z; outv[3] *= g0.w;
-    outv[4] *= g1.x; outv[5] *= g1.y; outv[6] *= g1.z; outv[7] *= g1.w;
+    const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+    for (int c = 0; c < 8; ++c) outv[c] = __fmul_rn(outv[c], gv[c]);
   }
   if (a.rope && c0 >= d - a.rp.r) {
-    const double pos = static_cast<double>(static_cast<long long>(a.m) * i + a.pos_shift);
+    const long long pos = static_cast<long long>(a.m) * i + a.pos_shift;
     const int j0 = (c0 - (d - a.rp.r)) >> 1;
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
       float cs, sn;
-      rope_cos_sin(pos, a.rp.inv_freq[j0 + p], cs, sn);
+      rope_cos_sin(pos, a.rp.phase[j0 + p], cs, sn);
       const float x0 = outv[2 * p], x1 = outv[2 * p + 1];
-      outv[2 * p] = x0 * cs - x1 * sn;
-      outv[2 * p + 1] = x0 * sn + x1 * cs;
+      outv[2 * p] = fmaf(x0, cs, -__fmul_rn(x1, sn));
+      outv[2 * p + 1] = fmaf(x0, sn, __fmul_rn(x1, cs));
     }
   }
   uint4 o;
@@ -225,25 +290,36 @@ __global__ void __launch_bounds__(256) k_compress(CompressArgs a, int RS, int EP
     const __nv_bfloat16* rCa = static_cast<const __nv_bfloat16*>(a.ring.Ca);
     const __nv_bfloat16* rZb = static_cast<const __nv_bfloat16*>(a.ring.Zb);
     const __nv_bfloat16* rCb = static_cast<const __nv_bfloat16*>(a.ring.Cb);
-    auto fetch = [&](int r, uint4& zv, uint4& cv) {
+    // row r of this entry (a-rows 0..3, b-rows 4..7): this call's chunk, or the tail ring for a
+    // token before it.  Token indices stay below 2^31 (checked by the host), so 32-bit
+    // arithmetic: a 64-bit remainder is a long software sequence on the GPU.
+    auto row_ptr = [&](int r, const __nv_bfloat16* X, const __nv_bfloat16* Y, const __nv_bfloat16* rX,
+                       const __nv_bfloat16* rY) {
       const bool isb = r >= 4;
-      // token indices stay below 2^31 (checked by the host), so 32-bit arithmetic: a 64-bit
-      // remainder is a long software sequence on the GPU
       const int tok = isb ? 4 * (i - 1) + (r - 4) : 4 * i + r;
-      if (tok >= a.t0) {
-        const size_t off = (static_cast<size_t>(b) * a.T + (tok - a.t0)) * d + c0;
-        zv = ldg_nc((isb ? Zb : Za) + off);
-        cv = ldg_nc((isb ? Cb : Ca) + off);
-      } else {
-        const uint32_t slot = static_cast<uint32_t>(tok) % static_cast<uint32_t>(a.ring.R);
-        const size_t off = (static_cast<size_t>(b) * a.ring.R + slot) * d + c0;
-        zv = ldg_nc((isb ? rZb : rZa) + off);
-        cv = ldg_nc((isb ? rCb : rCa) + off);
+      if (tok >= a.t0) return (isb ? Y : X) + (static_cast<size_t>(b) * a.T + (tok - a.t0)) * d + c0;
+      const uint32_t slot = static_cast<uint32_t>(tok) % static_cast<uint32_t>(a.ring.R);
+      return (isb ? rY : rX) + (static_cast<size_t>(b) * a.ring.R + slot) * d + c0;
+    };
+    auto fetch_z = [&](int r) { return ldg_nc(row_ptr(r, Za, Zb, rZa, rZb)); };
+    auto fetch_c = [&](int r) { return ldg_nc(row_ptr(r, Ca, Cb, rCa, rCb)); };
+    auto fetch_bias = [&](int r, float4& lo, float4& hi) {
+      const float* bp = r < 4 ? a.bias_a : a.bias_b;
+      lo = hi = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (bp != nullptr) {
+        lo = __ldg(reinterpret_cast<const float4*>(bp + static_cast<size_t>(r & 3) * d + c0));
+        hi = __ldg(reinterpret_cast<const float4*>(bp + static_cast<size_t>(r & 3) * d + c0 + 4));
       }
     };
     float o4[8];
-    if (i >= 1) csa4_entry<8>(fetch, a.bias_a, a.bias_b, d, c0, o4);
-    else csa4_entry<4>(fetch, a.bias_a, a.bias_b, d, c0, o4);
+    const bool hb = a.bias_a != nullptr || a.bias_b != nullptr;
+    if (i >= 1) {
+      if (hb) csa4_entry<8, true>(fetch_z, fetch_c, fetch_bias, o4);
+      else csa4_entry<8, false>(fetch_z, fetch_c, fetch_bias, o4);
+    } else {
+      if (hb) csa4_entry<4, true>(fetch_z, fetch_c, fetch_bias, o4);
+      else csa4_entry<4, false>(fetch_z, fetch_c, fetch_bias, o4);
+    }
 #pragma unroll
     for (int c = 0; c < 8; ++c) { mx[c] = 0.f; sm[c] = 1.f; acc[c] = o4[c]; }   // outv = acc / sm below
   } else if (active) {
@@ -326,78 +402,196 @@ __global__ void __launch_bounds__(256) k_compress(CompressArgs a, int RS, int EP
   }
 
   float* red = smem + (RS > 1 ? static_cast<size_t>(EPC) * RS * TPE * 24 : 0);
-  norm_rope_store(a, outv, active && rg == 0, b, i, c0, TPE, red);
+  norm_rope_store(a, outv, active && rg == 0, b, i, c0, TPE, tid, red, nullptr, [] { __syncthreads(); });
 }
 
-// Whole-sequence CSA compression (overlap, m = 4), staged: a CTA owns EPC consecutive entries
-// i0 .. i1-1 of one sequence, whose a-rows (tokens m i0 .. m i1 - 1 of Ca, Za) and b-rows (tokens
-// m (i0-1) .. m (i1-1) - 1 of Cb, Zb) are four contiguous runs.  One thread issues four bulk
-// copies into shared memory on one mbarrier, so a whole block's rows are in flight at once (the
-// per-thread loads of k_compress leave too few bytes in flight to reach HBM bandwidth); then every
-// thread runs csa4_entry and the same epilogue as the cache-append path of k_compress, so the
-// results agree bit for bit.
-// Shared layout: [Za | Ca | Zb | Cb] regions of EPC*m rows x d bf16 (b-region slot e holds the
-// b-block of entry i0 + e), then one float per warp for the norm, then the mbarrier.
-__global__ void __launch_bounds__(256) k_compress_staged(CompressArgs a, int EPC) {
+// Whole-sequence CSA compression (overlap, m = 4), streamed: one persistent CTA per SM walks a
+// contiguous range of stages.  A stage is EPG consecutive entries i0 .. i1-1 of one sequence,
+// whose a-rows (tokens m i0 .. m i1 - 1 of Ca, Za) and b-rows (tokens m (i0-1) .. m (i1-1) - 1 of
+// Cb, Zb) are four contiguous runs: 16 KB for d <= 512.  G groups of GT = max(64, d/8) threads
+// take the CTA's stages from a shared counter (the next unclaimed stage of the CTA's range), each
+// group with two shared-memory buffers of its own: while the group computes one stage, the bulk
+// copies of its next stage land in the other buffer.  Each thread first reads its entry's rows into registers; one thread per
+// group then issues the group's next copies into the buffer just read (four per stage, on the
+// buffer's mbarrier) as soon as the group's named barrier shows every thread done with it, so a
+// buffer is held only while it is read, both buffers are mostly in flight, the copies are spread
+// over G issuing threads and a slow group never holds up another.  The position biases are copied into shared memory
+// once per CTA, the RMSNorm weights into registers once per thread (a thread keeps its 8
+// channels for the whole kernel).  Every wait is bounded; a group that gives up waits (bounded)
+// for its own copies in flight before the CTA exits.
+// Shared layout: [bias_a | bias_b] fp32 m x d each (zeros where null), 2G stage buffers of
+// [Za | Ca | Zb | Cb] regions of EPG*m rows x d bf16 (b-region slot e holds the b-block of entry
+// i0 + e), one float per warp for the norm, the mbarriers, the stage counter and the stage index
+// held by each buffer (-1: the range is exhausted).
+struct StreamShape {
+  int GT, EPG, G;
+  uint32_t stage_bytes, bias_bytes;
+  size_t smem;
+};
+
+inline StreamShape stream_shape(int d) {
+  StreamShape h;
+  const int TPE = d / 8;
+  h.GT = TPE > 64 ? TPE : 64;
+  h.EPG = h.GT / TPE;
+  h.G = 384 / h.GT;                                                   // 12 warps
+  h.stage_bytes = static_cast<uint32_t>(h.EPG) * 4 * 4 * d * 2;      // 4 arrays x m = 4 rows x d bf16
+  h.bias_bytes = 2u * 4u * d * 4u;
+  // biases, 2G buffers, the norm scratch (one float per warp), barriers (2G + 1), the counter and
+  // the buffers' stage indices
+  h.smem = h.bias_bytes + 2 * static_cast<size_t>(h.G) * h.stage_bytes + 12 * 4 + 8 * (2 * h.G + 1) + 4 * (1 + 2 * h.G);
+  return h;
+}
+
+template <bool kBias>
+__global__ void __launch_bounds__(384, 1) k_compress_stream(CompressArgs a, StreamShape h, int n_stages) {
   extern __shared__ __align__(128) unsigned char sraw[];
   grid_dep_wait();
   grid_dep_launch();
-  const int TPE = a.d >> 3;
+  const int d = a.d, m = a.m;
+  const int TPE = d >> 3;
   const int tid = threadIdx.x;
-  const int cg = tid % TPE;
-  const int e = tid / TPE;
-  const int m = a.m, d = a.d;
-  const int nblk = (a.N + EPC - 1) / EPC;
-  const int b = static_cast<int>(blockIdx.x / nblk);
-  const int i0 = static_cast<int>(blockIdx.x % nblk) * EPC;
-  const int i1 = min(a.N, i0 + EPC);
-  const size_t region = static_cast<size_t>(EPC) * m * d;          // elements per region
-  __nv_bfloat16* sZa = reinterpret_cast<__nv_bfloat16*>(sraw);
-  __nv_bfloat16* sCa = sZa + region;
-  __nv_bfloat16* sZb = sCa + region;
-  __nv_bfloat16* sCb = sZb + region;
-  float* red = reinterpret_cast<float*>(sCb + region);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(red + 8);
+  const int nblk = (a.N + h.EPG - 1) / h.EPG;                      // stages per sequence
+  const int j0 = static_cast<int>(static_cast<long long>(n_stages) * blockIdx.x / gridDim.x);
+  const int j1 = static_cast<int>(static_cast<long long>(n_stages) * (blockIdx.x + 1) / gridDim.x);
+  float* sBa = reinterpret_cast<float*>(sraw);
+  float* sBb = sBa + 4 * d;
+  unsigned char* stage0 = sraw + h.bias_bytes;
+  float* red = reinterpret_cast<float*>(stage0 + 2 * static_cast<size_t>(h.G) * h.stage_bytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + 12);           // after one float per warp (8-byte aligned)
+  uint64_t* pbar = full + 2 * h.G;
+  int* sctr = reinterpret_cast<int*>(pbar + 1);
+  volatile int* sidx = sctr + 1;
+  const size_t region = static_cast<size_t>(h.EPG) * m * d;          // elements per region
+  const int g = tid / h.GT;
+  const int lt = tid - g * h.GT;                                     // thread index in the group
   if (tid == 0) {
-    tc::mbar_init(bar, 1);
+    for (int s = 0; s < 2 * h.G; ++s) tc::mbar_init(&full[s], 1);
+    tc::mbar_init(pbar, 1);
     tc::fence_barrier_init();
+    *sctr = 0;
+  }
+  // a null bias reads as zeros
+  if (kBias) {
+    for (int k = tid; k < 4 * d; k += blockDim.x) {
+      if (a.bias_a == nullptr) sBa[k] = 0.f;
+      if (a.bias_b == nullptr) sBb[k] = 0.f;
+    }
   }
   __syncthreads();
-  if (tid == 0) {
+  if (kBias && tid == 0) {
+    const uint32_t bb = 4u * d * 4u;
+    tc::mbar_arrive_expect_tx(pbar, (a.bias_a != nullptr ? bb : 0u) + (a.bias_b != nullptr ? bb : 0u));
+    if (a.bias_a != nullptr) tc::bulk_load(sBa, a.bias_a, bb, pbar);
+    if (a.bias_b != nullptr) tc::bulk_load(sBb, a.bias_b, bb, pbar);
+  }
+
+  // claims the CTA's next stage for buffer s and bulk-copies its rows there; when the range is
+  // exhausted it records -1 and completes the buffer's phase with a plain arrival
+  const int ncta = j1 - j0;
+  auto issue = [&](int s) {
+    const int k = atomicAdd(sctr, 1);
+    if (k >= ncta) {
+      sidx[s] = -1;
+      tc::mbar_arrive(&full[s]);
+      return;
+    }
+    sidx[s] = k;
+    const int j = j0 + k;
+    const int b = j / nblk;
+    const int i0 = (j % nblk) * h.EPG;
+    const int i1 = min(a.N, i0 + h.EPG);
+    const int e_lo = i0 == 0 ? 1 : 0;                                // entry 0 has no b-block
     const uint32_t rowb = static_cast<uint32_t>(d) * 2;
-    const int e_lo = i0 == 0 ? 1 : 0;                  // entry 0 has no b-block
     const uint32_t abytes = static_cast<uint32_t>(i1 - i0) * m * rowb;
     const uint32_t bbytes = static_cast<uint32_t>(i1 - i0 - e_lo) * m * rowb;
-    tc::mbar_arrive_expect_tx(bar, 2 * abytes + 2 * bbytes);
+    __nv_bfloat16* sZa = reinterpret_cast<__nv_bfloat16*>(stage0 + static_cast<size_t>(s) * h.stage_bytes);
+    tc::mbar_arrive_expect_tx(&full[s], 2 * abytes + 2 * bbytes);
     const size_t aoff = (static_cast<size_t>(b) * a.T + static_cast<size_t>(m) * i0) * d;
-    tc::bulk_load(sZa, static_cast<const __nv_bfloat16*>(a.Za) + aoff, abytes, bar);
-    tc::bulk_load(sCa, static_cast<const __nv_bfloat16*>(a.Ca) + aoff, abytes, bar);
+    tc::bulk_load(sZa, static_cast<const __nv_bfloat16*>(a.Za) + aoff, abytes, &full[s]);
+    tc::bulk_load(sZa + region, static_cast<const __nv_bfloat16*>(a.Ca) + aoff, abytes, &full[s]);
     if (bbytes > 0) {
       const size_t boff = (static_cast<size_t>(b) * a.T + static_cast<size_t>(m) * (i0 + e_lo - 1)) * d;
       const size_t soff = static_cast<size_t>(e_lo) * m * d;
-      tc::bulk_load(sZb + soff, static_cast<const __nv_bfloat16*>(a.Zb) + boff, bbytes, bar);
-      tc::bulk_load(sCb + soff, static_cast<const __nv_bfloat16*>(a.Cb) + boff, bbytes, bar);
+      tc::bulk_load(sZa + 2 * region + soff, static_cast<const __nv_bfloat16*>(a.Zb) + boff, bbytes, &full[s]);
+      tc::bulk_load(sZa + 3 * region + soff, static_cast<const __nv_bfloat16*>(a.Cb) + boff, bbytes, &full[s]);
     }
+  };
+  const bool issuer = lt == 0;
+  if (issuer) {
+    issue(2 * g);
+    issue(2 * g + 1);
   }
-  // every thread observes the copies' completion; the block leaves together if any wait gave up
-  const bool got = tc::mbar_wait(bar, 0, nullptr, 1000000000ull);
-  if (!__syncthreads_and(got)) return;
 
-  const int i = i0 + e;
-  const bool active = e < EPC && i < i1;
+  const int e = lt / TPE;
+  const int cg = lt % TPE;
   const int c0 = cg * 8;
-  float outv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  if (active) {
-    const uint32_t base = (static_cast<uint32_t>(e) * 4) * d + c0;     // element offset of row 0
-    auto fetch = [&](int r, uint4& zv, uint4& cv) {
-      const uint32_t off = base + static_cast<uint32_t>(r & 3) * d;
-      zv = *reinterpret_cast<const uint4*>((r < 4 ? sZa : sZb) + off);
-      cv = *reinterpret_cast<const uint4*>((r < 4 ? sCa : sCb) + off);
-    };
-    if (i >= 1) csa4_entry<8>(fetch, a.bias_a, a.bias_b, d, c0, outv);
-    else csa4_entry<4>(fetch, a.bias_a, a.bias_b, d, c0, outv);
+  float gam[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) gam[c] = 1.f;
+  if (a.gamma != nullptr) {
+    const float4 g0 = __ldg(reinterpret_cast<const float4*>(a.gamma + c0));
+    const float4 g1 = __ldg(reinterpret_cast<const float4*>(a.gamma + c0 + 4));
+    gam[0] = g0.x; gam[1] = g0.y; gam[2] = g0.z; gam[3] = g0.w;
+    gam[4] = g1.x; gam[5] = g1.y; gam[6] = g1.z; gam[7] = g1.w;
   }
-  norm_rope_store(a, outv, active, b, i, c0, TPE, red);
+  // the group leaves together if any of its threads' bounded waits gave up
+  bool ok = !tc::named_bar_or(1 + g, h.GT, kBias && !tc::mbar_wait(pbar, 0, nullptr));
+  auto gsync = [&] { tc::named_bar_sync(1 + g, h.GT); };
+  // the group's n-th stage sits in buffer 2g + (n & 1), in that buffer's phase n >> 1
+  int n = 0;
+  for (; ok; ++n) {
+    const int s = 2 * g + (n & 1);
+    const bool got = tc::mbar_wait(&full[s], (n >> 1) & 1, nullptr);
+    const int k = got ? sidx[s] : -1;
+    const int j = j0 + k;
+    const int b = k >= 0 ? j / nblk : 0;
+    const int i0 = k >= 0 ? (j % nblk) * h.EPG : 0;
+    const int i1 = k >= 0 ? min(a.N, i0 + h.EPG) : 0;
+    const int i = i0 + e;
+    const bool active = i < i1;
+    // the entry's rows into registers at once
+    const __nv_bfloat16* sZa =
+        reinterpret_cast<const __nv_bfloat16*>(stage0 + static_cast<size_t>(s) * h.stage_bytes);
+    const uint32_t base = (static_cast<uint32_t>(e) * 4) * d + c0;     // element offset of row 0
+    uint4 zr[8], cr[8];
+    if (active) {
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        if (r < 4 || i >= 1) {
+          const size_t off = (r < 4 ? 0 : 2 * region) + base + static_cast<uint32_t>(r & 3) * d;
+          zr[r] = *reinterpret_cast<const uint4*>(sZa + off);
+          cr[r] = *reinterpret_cast<const uint4*>(sZa + region + off);
+        }
+      }
+    }
+    // every thread of the group has read the buffer (the group leaves together if a wait gave
+    // up, or when the range is exhausted: every thread read the same index): refill it with the
+    // next unclaimed stage while the rows are reduced from registers
+    if (tc::named_bar_or(1 + g, h.GT, !got) || k < 0) break;
+    if (issuer) issue(s);
+    float outv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (active) {
+      auto fetch_z = [&](int r) { return zr[r]; };
+      auto fetch_c = [&](int r) { return cr[r]; };
+      auto fetch_bias = [&](int r, float4& lo, float4& hi) {
+        const float* bp = (r < 4 ? sBa : sBb) + (r & 3) * d + c0;
+        lo = *reinterpret_cast<const float4*>(bp);
+        hi = *reinterpret_cast<const float4*>(bp + 4);
+      };
+      if (i >= 1) csa4_entry<8, kBias>(fetch_z, fetch_c, fetch_bias, outv);
+      else csa4_entry<4, kBias>(fetch_z, fetch_c, fetch_bias, outv);
+    }
+    norm_rope_store(a, outv, active, b, i, c0, TPE, lt, red + g * (h.GT / 32), gam, gsync);
+  }
+  // before the CTA exits, nothing this group issued is still in flight (at once, unless a wait
+  // gave up): the pending phases of both its buffers have completed
+  if (issuer) {
+    tc::mbar_wait(&full[2 * g + (n & 1)], (n >> 1) & 1, nullptr);
+    tc::mbar_wait(&full[2 * g + ((n + 1) & 1)], ((n + 1) >> 1) & 1, nullptr);
+    if (kBias && g == 0) tc::mbar_wait(pbar, 0, nullptr);
+  }
+  __syncthreads();
 }
 
 // One 16-byte vector per thread; blockIdx.y is the job.  Every job's row width is a multiple
@@ -442,18 +636,21 @@ cudaError_t launch_ring_rows(const RingArgs& a, cudaStream_t s, int* launches) {
 cudaError_t launch_compress(const CompressArgs& a, cudaStream_t s, int* launches) {
   const int TPE = a.d / 8;
   if (a.overlap && a.m == 4 && a.t0 == 0 && a.i_begin == 0 && a.out_N == a.N && a.ring.R == 0) {
-    // whole-sequence CSA call: the staged kernel (64 KB of rows per CTA)
-    const int EPC = 256 / TPE;
-    const long long blocks = static_cast<long long>(a.B) * ((a.N + EPC - 1) / EPC);
-    if (blocks == 0) return cudaSuccess;
-    const size_t smem = 4 * static_cast<size_t>(EPC) * a.m * a.d * 2 + 8 * sizeof(float) + 16;
-    if (smem > 48 * 1024) {
-      const cudaError_t e = cudaFuncSetAttribute(k_compress_staged, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(smem));
-      if (e != cudaSuccess) return e;
-    }
-    const cudaError_t e = launch_k(k_compress_staged, dim3(static_cast<unsigned>(blocks)), dim3(EPC * TPE), smem, s,
-                                   a, EPC);
+    // whole-sequence CSA call: the streamed kernel, one CTA per SM
+    const StreamShape h = stream_shape(a.d);
+    const int nblk = (a.N + h.EPG - 1) / h.EPG;
+    const long long n_stages = static_cast<long long>(a.B) * nblk;
+    if (n_stages == 0) return cudaSuccess;
+    const bool hb = a.bias_a != nullptr || a.bias_b != nullptr;
+    auto kern = hb ? k_compress_stream<true> : k_compress_stream<false>;
+    const cudaError_t e0 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                static_cast<int>(h.smem));
+    if (e0 != cudaSuccess) return e0;
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long grid = n_stages < sms ? n_stages : sms;
+    const cudaError_t e = launch_k(kern, dim3(static_cast<unsigned>(grid)), dim3(h.G * h.GT), h.smem, s, a, h,
+                                   static_cast<int>(n_stages));
     ++*launches;
     return e;
   }

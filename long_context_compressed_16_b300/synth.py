@@ -33,6 +33,7 @@ TID = {
     "q": 11, "qI": 12, "w": 13, "kv": 14, "kI": 15, "win": 16, "sink": 17,
     "outlier_kv": 18, "outlier_kI": 19,
     "O": 20, "W_down": 21, "W_proj": 22,
+    "Ba": 23, "Bb": 24, "Ba_I": 25, "Bb_I": 26, "gamma": 27, "gamma_I": 28, "B": 29,
 }
 
 
@@ -277,7 +278,9 @@ def make_inputs(w: Workload, device="cpu") -> dict:
 
     prefill: per-token streams Ca/Cb/Za/Zb [B,T,d] (CSA; HCA: C/Z), indexer streams [B,T,dI],
              q [B,T,H,d], qI [B,T,nI,dI], w [B,T,nI], win [B,T,d] (per-token window KV, slot=position),
-             q_pos [B,T] = 0..T-1.
+             q_pos [B,T] = 0..T-1; the compressor's parameters: position biases Ba/Bb [m,d] (CSA; HCA: B)
+             and Ba_I/Bb_I [m,dI] ~ 0.5 N(0,1), RMSNorm weights gamma [d], gamma_I [dI] ~ 1 + 0.1 N(0,1),
+             all fp32.
     decode:  kv [B,N,d] (bf16, or packed mixed FP8 rows), kI [B,N,dI] (bf16, or e4m3 + row scales),
              q [B,1,H,d], qI [B,1,nI,dI], w [B,1,nI], win ring [B,128,d] (slot = position mod 128),
              q_pos [B,1] = m*N (the new token's index).
@@ -285,6 +288,7 @@ def make_inputs(w: Workload, device="cpu") -> dict:
     s = w.seed
     out = {}
     g = lambda name, shape: normal_bf16(shape, s, TID[name], device)
+    f32 = lambda name, shape, scale, shift: (shift + scale * normal_f64(shape, s, TID[name], device)).to(torch.float32)
     out["sink"] = normal_f64((w.H,), s, TID["sink"], device).to(torch.float32)
     if w.kind == "csa_prefill":
         B, T = w.B, w.T
@@ -297,6 +301,9 @@ def make_inputs(w: Workload, device="cpu") -> dict:
         out["w"] = uniform_f64((B, T, w.nI), s, TID["w"], device).to(torch.float32)
         out["win"] = g("win", (B, T, w.d))
         out["q_pos"] = torch.arange(T, dtype=torch.int32, device=device).repeat(B, 1)
+        out["Ba"], out["Bb"] = f32("Ba", (w.m, w.d), 0.5, 0.0), f32("Bb", (w.m, w.d), 0.5, 0.0)
+        out["Ba_I"], out["Bb_I"] = f32("Ba_I", (w.m, w.dI), 0.5, 0.0), f32("Bb_I", (w.m, w.dI), 0.5, 0.0)
+        out["gamma"], out["gamma_I"] = f32("gamma", (w.d,), 0.1, 1.0), f32("gamma_I", (w.dI,), 0.1, 1.0)
     elif w.kind == "hca_prefill":
         B, T = w.B, w.T
         out["C"] = g("C", (B, T, w.d))
@@ -304,6 +311,8 @@ def make_inputs(w: Workload, device="cpu") -> dict:
         out["q"] = g("q", (B, T, w.H, w.d))
         out["win"] = g("win", (B, T, w.d))
         out["q_pos"] = torch.arange(T, dtype=torch.int32, device=device).repeat(B, 1)
+        out["B"] = f32("B", (w.m, w.d), 0.5, 0.0)
+        out["gamma"] = f32("gamma", (w.d,), 0.1, 1.0)
     elif w.kind in ("csa_decode", "hca_decode"):
         B, N = w.B, w.N
         if w.fp8:
