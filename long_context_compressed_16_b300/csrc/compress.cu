@@ -4,11 +4,11 @@
 //
 // Pure HBM stream: every input row is read exactly once (entry i owns a-block i and b-block i-1),
 // in 16-byte vectors of 8 channels; a thread owns 8 channels of one entry.
-//   - CSA with m = 4 (the method's ratio): an exact two-pass softmax per channel over the entry's
-//     8 rows (4 for entry 0): the maximum first, then one hardware exp2 per logit (csa4_entry).
-//     Whole sequences run in k_compress_staged, which bulk-copies a block of entries' rows into
-//     shared memory first; cache appends run the same routine in k_compress, so both agree bit
-//     for bit.
+//   - CSA with m = 4 (the method's ratio): a one-pass softmax per channel over the entry's 8 rows
+//     (4 for entry 0) in two chunks of 4, one hardware exp2 per logit (csa4_entry).  Whole
+//     sequences run in k_compress_stream, a persistent kernel that bulk-copies stages of entries'
+//     rows into double-buffered shared memory; cache appends run the same routine in k_compress,
+//     so both agree bit for bit.
 //   - Other cases (HCA, m' = 128; other m): the softmax runs online over chunks of 2 (CSA) or 4
 //     (HCA) rows in k_compress; long blocks are split over row groups whose partial (max, sum,
 //     acc) are merged in shared memory in fixed order, so results are deterministic.
@@ -125,7 +125,7 @@ __device__ __forceinline__ float2 bf16x2_add(uint32_t w, float bx, float by) {
 // fetch_c(r) return the logits and the values of row r (a-rows 0..3, then b-rows 4..7) for this
 // thread's 8 channels, fetch_bias(r, lo, hi) the row's 8 position biases (read only when kBias);
 // the values are fetched only when the weights are known.  Both kernels that
-// compress m = 4 CSA entries (the staged whole-sequence kernel and the cache-append path of
+// compress m = 4 CSA entries (the streamed whole-sequence kernel and the cache-append path of
 // k_compress) run exactly this code, so their results agree bit for bit.
 template <int R, bool kBias, class FetchZ, class FetchC, class FetchB>
 __device__ __forceinline__ void csa4_entry(FetchZ fetch_z, FetchC fetch_c, FetchB fetch_bias, float* outv) {
