@@ -589,7 +589,14 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
           if (lane == 0) tc::mbar_arrive(&bars[B_OFREE]);   // the next item's PV may overwrite O^T
         }
         const int dim = mt * 128 + quarter * 32 + lane;
-        if (a.n_splits == 1) {
+        if (a.n_splits == 1 && !(a.out_unrotate && (dim & ~1) >= D - a.rp.r)) {
+          // dims that are not rotated back (warp-uniform: the rotated dims are the last r of the
+          // row, r a multiple of 32): one bf16 per (head, dim), a warp storing 64 contiguous bytes
+          // of one head's row
+          __nv_bfloat16* op = outp + (I.qi * a.H + I.h0 + hb) * static_cast<long long>(D) + dim;
+#pragma unroll
+          for (int h = 0; h < 32; ++h) op[static_cast<size_t>(h) * D] = __float2bfloat16_rn(o[h] * efac[hb + h]);
+        } else if (a.n_splits == 1) {
           // lanes 2i and 2i+1 swap one value per head pair, so that each lane holds two adjacent
           // dims of one head: the even lane head hb + 2hp, the odd lane head hb + 2hp + 1
           const int dd = dim & ~1;

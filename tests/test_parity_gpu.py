@@ -39,6 +39,12 @@ def _to_dev_bf16(x64: np.ndarray) -> torch.Tensor:
     (1, 1000, 128, 1, True, True, True),        # m = 1 (two-row logistic mix)
     (2, 4096 + 77, 512, 128, False, True, True),  # HCA, ragged
     (1, 640, 1024, 8, True, True, False),       # widest supported row
+    # whole-sequence m = 4 calls at every stage shape of the streamed kernel: d = 1024 (one entry
+    # of 32 KB per stage, 3 groups), d = 256 (two entries per stage), a null b-bias read as zeros,
+    # gamma without biases, and batch 2 with ~55 stages per CTA crossing the sequence boundary
+    (3, 4096 + 8, 1024, 4, True, True, "a_only"),
+    (2, 8192 + 4, 256, 4, True, True, "gamma_only"),
+    (2, 16384 + 12, 512, 4, True, True, True),
 ])
 def test_compress_parity(B, T, d, m, overlap, rope, bias):
     g = torch.Generator().manual_seed(T + d)
@@ -50,8 +56,12 @@ def test_compress_parity(B, T, d, m, overlap, rope, bias):
         ba = torch.randn(m, d, generator=g).float().to(DEV)
         bb = torch.randn(m, d, generator=g).float().to(DEV)
         gam = (1 + 0.1 * torch.randn(d, generator=g)).float().to(DEV)
-        kw = dict(bias_a=ba.double().cpu().numpy(), bias_b=bb.double().cpu().numpy() if overlap else None,
-                  gamma=gam.double().cpu().numpy())
+        if bias == "a_only":
+            bb = None
+        if bias == "gamma_only":
+            ba = bb = None
+        np_ = lambda t: None if t is None else t.double().cpu().numpy()
+        kw = dict(bias_a=np_(ba), bias_b=np_(bb) if overlap else None, gamma=np_(gam))
     out = P.compress(inp["Ca"], inp["Za"], m, Cb=inp["Cb"] if overlap else None, Zb=inp["Zb"] if overlap else None,
                      bias_a=ba, bias_b=bb if overlap else None, gamma=gam, rope=rope,
                      rope_dims=64 if rope else 0, theta=THETA)
