@@ -426,9 +426,6 @@ def run_prefill(args, dev, stream):
     ws_t = torch.zeros(max(256, C.csa_topk_workspace(idesc)), dtype=torch.uint8, device=dev)
     ws_a = torch.zeros(max(256, C.csa_attend_workspace(adesc)), dtype=torch.uint8, device=dev)
 
-    side = torch.cuda.Stream()
-    fork, join = torch.cuda.Event(), torch.cuda.Event()
-
     def step(evs=None):
         # the prefill path: the indexer scores and the top-k selection in one fused call (the
         # score rows are never stored)
@@ -439,17 +436,11 @@ def run_prefill(args, dev, stream):
             with torch.cuda.stream(stream):
                 torch.cuda._sleep(2_000_000)
         rec(0)
-        # the two compressor calls are independent: the indexer stream's runs on a second stream,
-        # so its kernel starts on the SMs the main stream's kernel leaves at its tail
-        fork.record(stream)
-        side.wait_event(fork)
         P.compress(inp["Ca"], inp["Za"], w.m, Cb=inp["Cb"], Zb=inp["Zb"], bias_a=inp["Ba"], bias_b=inp["Bb"],
                    gamma=inp["gamma"], out=kv, stream=sptr)
         P.compress(inp["Ca_I"], inp["Za_I"], w.m, Cb=inp["Cb_I"], Zb=inp["Zb_I"], bias_a=inp["Ba_I"],
                    bias_b=inp["Bb_I"], gamma=inp["gamma_I"], rope=False, rope_dims=0, out=kI,
-                   stream=side.cuda_stream)
-        join.record(side)
-        stream.wait_event(join)
+                   stream=sptr)
         rec(1)
         C.check(C.csa_index_topk(idesc, inp["qI"], inp["w"], kI, None, inp["q_pos"], idx, None, wsi, stream=sptr),
                 "csa_index_topk")
@@ -471,25 +462,22 @@ def run_prefill(args, dev, stream):
         torch.cuda.synchronize()
         times.append([evs[i].elapsed_time(evs[i + 1]) for i in range(3)])
     comp, ind, att = (statistics.median(x[i] for x in times) for i in range(3))
-    # the two compressor calls are ~0.07 ms of GPU time, so their eager timing above carries
-    # stream-event and launch latencies of the same order; their breakdown entry is the same pair
-    # replayed back to back from one CUDA graph (the main stream on `stream`, the indexer stream on
-    # a second captured stream), as the decode breakdown is
+    # the two compressor calls are ~0.07 ms of GPU time, so their eager timing above carries launch
+    # latencies of the same order; their breakdown entry is the same pair replayed back to back
+    # from one CUDA graph on one stream, as the decode breakdown is.  (The pair on two streams
+    # measured slower: each kernel wants every SM's shared memory, so they cannot overlap, and the
+    # cross-stream events cost more than the dependent launch on one stream.)
     reps = 10
     cap = torch.cuda.Stream()                  # graphs are captured on a non-default stream
     g = torch.cuda.CUDAGraph()
     torch.cuda.synchronize()
     with torch.cuda.graph(g, stream=cap):
         for _ in range(reps):
-            fork.record(cap)
-            side.wait_event(fork)
             P.compress(inp["Ca"], inp["Za"], w.m, Cb=inp["Cb"], Zb=inp["Zb"], bias_a=inp["Ba"], bias_b=inp["Bb"],
                        gamma=inp["gamma"], out=kv, stream=cap.cuda_stream)
             P.compress(inp["Ca_I"], inp["Za_I"], w.m, Cb=inp["Cb_I"], Zb=inp["Zb_I"], bias_a=inp["Ba_I"],
                        bias_b=inp["Bb_I"], gamma=inp["gamma_I"], rope=False, rope_dims=0, out=kI,
-                       stream=side.cuda_stream)
-            join.record(side)
-            cap.wait_event(join)
+                       stream=cap.cuda_stream)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(cap):                # a replay runs on the current stream
         g.replay()
