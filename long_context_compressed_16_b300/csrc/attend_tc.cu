@@ -104,6 +104,15 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_barrier() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Four floats at the same shared-memory offset as p (16-byte aligned) in CTA `rank` of the cluster.
+__device__ __forceinline__ float4 ld_peer4f(const float* p, uint32_t rank) {
+  const uint32_t la = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(la), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(ra));
+  return v;
+}
 // Two floats at the same shared-memory offset as p (8-byte aligned) in CTA `rank` of the cluster.
 __device__ __forceinline__ float2 ld_peer2(const float* p, uint32_t rank) {
   const uint32_t la = static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -754,8 +763,9 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
   if (a.cluster_merge) {
     // ---------------- the splits of one query are the CTAs of this cluster (one item each, split =
     // cluster rank).  Each staged its (m, l) and fp32 accumulator; CTA r merges output units
-    // [r U / S, (r + 1) U / S) of the U = 64 heads x 256 dim pairs, reading every split's staged
-    // accumulator over distributed shared memory in fixed split order:
+    // [r U / S, (r + 1) U / S) of the U = 64 heads x 128 groups of 4 dims, reading every split's
+    // staged accumulator over distributed shared memory (one 16-byte load per split and unit) in
+    // fixed split order:
     //   out = sum_s O_s 2^(m_s - M) / (sum_s l_s 2^(m_s - M) + 2^(a_h - M)),  M = max(a_h, max_s m_s)
     cluster_barrier();
     const int S = a.n_splits;
@@ -794,27 +804,32 @@ __global__ void __launch_bounds__(NT, 1) k_attend_tc(const AttendArgs a, const _
     __syncthreads();
     const float* stage = reinterpret_cast<const float*>(kvs);
     __nv_bfloat16* outp = static_cast<__nv_bfloat16*>(a.out);
-    constexpr int U = HG * (D / 2);
+    constexpr int U = HG * (D / 4);
     const int u1 = static_cast<int>((rank + 1) * static_cast<long long>(U) / S);
     for (int u = static_cast<int>(rank * static_cast<long long>(U) / S) + tid; u < u1; u += NT) {
-      const int h = u / (D / 2), d = 2 * (u % (D / 2));
-      float x0 = 0.f, x1 = 0.f;
+      const int h = u / (D / 4), d = 4 * (u % (D / 4));
+      float x[4] = {0.f, 0.f, 0.f, 0.f};
       for (int sp = 0; sp < S; ++sp) {
         const float f = facm[sp * HG + h];       // 0 for a split without rows (nothing staged)
         if (f != 0.f) {
-          const float2 v = ld_peer2(stage + h * D + d, static_cast<uint32_t>(sp));
-          x0 = fmaf(v.x, f, x0);
-          x1 = fmaf(v.y, f, x1);
+          const float4 v = ld_peer4f(stage + h * D + d, static_cast<uint32_t>(sp));
+          x[0] = fmaf(v.x, f, x[0]);
+          x[1] = fmaf(v.y, f, x[1]);
+          x[2] = fmaf(v.z, f, x[2]);
+          x[3] = fmaf(v.w, f, x[3]);
         }
       }
       if (a.out_unrotate && d >= D - a.rp.r) {
-        const float2 cssn = rope[32 + ((d - (D - a.rp.r)) >> 1)];
-        const float y0 = x0 * cssn.x - x1 * cssn.y, y1 = x0 * cssn.y + x1 * cssn.x;
-        x0 = y0;
-        x1 = y1;
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+          const float2 cssn = rope[32 + ((d + 2 * p - (D - a.rp.r)) >> 1)];
+          const float y0 = x[2 * p] * cssn.x - x[2 * p + 1] * cssn.y, y1 = x[2 * p] * cssn.y + x[2 * p + 1] * cssn.x;
+          x[2 * p] = y0;
+          x[2 * p + 1] = y1;
+        }
       }
-      *reinterpret_cast<uint32_t*>(outp + (I.qi * a.H + I.h0 + h) * static_cast<long long>(D) + d) =
-          pack_bf16x2(x0, x1);
+      *reinterpret_cast<uint2*>(outp + (I.qi * a.H + I.h0 + h) * static_cast<long long>(D) + d) =
+          make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
     }
     cluster_barrier();                                           // no CTA leaves while a peer reads it
   }
