@@ -75,6 +75,23 @@ def test_compress_parity(B, T, d, m, overlap, rope, bias):
     assert_close(out, ref, f"compress B{B} T{T} d{d} m{m}")
 
 
+def test_compress_rope_far_positions_and_table():
+    """RoPE angles reduced in 64-bit integer phase: entries at positions past 2^21 (pos_shift),
+    and a host frequency table with values above one radian per position (the reduction modulo a
+    revolution) and far below it, against the oracle's fp64 angles."""
+    B, T, d, m = 2, 2048 + 12, 512, 4
+    g = torch.Generator().manual_seed(77)
+    inp = {n: S.normal_bf16((B, T, d), 9, S.TID[n], DEV) for n in ("Ca", "Cb", "Za", "Zb")}
+    inv = [3.7, 1.0, 0.5, 2.0 ** -0.5] + [float(160000.0 ** (-2.0 * j / 64)) for j in range(4, 32)]
+    inv = [float(np.float32(v)) for v in inv]                 # the table is fp32 on the host side
+    shift = 3 * (1 << 20) + 5
+    out = P.compress(inp["Ca"], inp["Za"], m, Cb=inp["Cb"], Zb=inp["Zb"], inv_freq=inv, pos_shift=shift)
+    torch.cuda.synchronize()
+    ref = O.compress(f64(inp["Ca"]), f64(inp["Za"]), m, Cb=f64(inp["Cb"]), Zb=f64(inp["Zb"]),
+                     inv_freq=np.asarray(inv, np.float64), pos_shift=shift)
+    assert_close(out, ref, "compress, far positions, frequency table")
+
+
 def test_compress_degenerate_sizes():
     x = S.normal_bf16((1, 3, 128), 0, 1, DEV)
     out = P.compress(x, x, 4, Cb=x, Zb=x)             # T < m: no closed block
