@@ -332,7 +332,7 @@ typedef struct {
   int N_cap;               /* entries the kv / kI buffers hold per sequence */
   int rope_dims;           /* RoPE on the main entries, as csa_compress */
   float rope_theta;
-  const float* inv_freq;   /* HOST pointer or NULL */
+  const float* inv_freq;   /* HOST pointer to rope_dims/2 finite values or NULL */
   float eps;
   unsigned flags;          /* CSA_COMPRESS_* for the main entries */
   unsigned index_flags;    /* CSA_COMPRESS_* for the indexer keys (rotation not supported) */
