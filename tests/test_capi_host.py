@@ -87,6 +87,10 @@ def test_compress_validation():
     assert call(_cdesc(), Cb=None) == C.CSA_ERR_INVALID_ARG
     assert call(_cdesc(), Ca=FAKE + 4) == C.CSA_ERR_INVALID_ARG                # misaligned
     assert call(_cdesc(T=3)) == C.CSA_OK                                       # no closed block: nothing to do
+    bad = C.float_table([float("nan")] + [0.5] * 31)                           # a non-finite frequency
+    assert call(_cdesc(inv_freq=bad)) == C.CSA_ERR_INVALID_ARG
+    inf = C.float_table([0.5] * 31 + [float("inf")])
+    assert call(_cdesc(inv_freq=inf)) == C.CSA_ERR_INVALID_ARG
 
 
 def _idesc(**kw):
