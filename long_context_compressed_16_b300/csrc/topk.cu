@@ -12,7 +12,7 @@
 // increasing entry index: entries above the threshold bin and, inside it, the smallest indices
 // first.
 //
-// Rows longer than one slice: up to 8 x 32768 entries, one thread-block cluster per row selects
+// Rows longer than one slice: up to 16 x 32768 entries, one thread-block cluster per row selects
 // in one stage (k_topk_cluster, below: the slices' histograms are summed over distributed shared
 // memory).  Longer rows run in two stages: every slice writes its own top-k (key, index)
 // candidates in index order, and a merge CTA selects the top-k of the concatenation.  This is
@@ -41,7 +41,8 @@ constexpr int kMergeCap = 16384;     // candidates one merge CTA holds (keys + i
 #ifndef CSA_TOPK_CLUSTER_NT
 #define CSA_TOPK_CLUSTER_NT 1024     // threads per CTA of the cluster selection
 #endif
-constexpr int kClusterMax = 8;       // portable cluster size
+constexpr int kClusterMax = 16;      // clusters of up to 16 CTAs (above 8: the non-portable size)
+constexpr int kPeerBatch = 8;         // peers whose histogram words are loaded together
 constexpr int kTargetCtas = CSA_TOPK_TARGET_CTAS;   // split rows until the first stage has about this many CTAs
 constexpr int kMergeRounds = 16;     // 32-candidate rounds per merge warp (registers per thread)
 constexpr int kDigit = 8;
@@ -327,7 +328,7 @@ __global__ void __launch_bounds__(NT) k_topk_slice(TopkArgs a, int S, int slice_
 }
 
 // ------------------------------------------------------------------ one-stage cluster selection
-// A row of S <= 8 slices is selected by one thread-block cluster of S CTAs (CTA r = slice r)
+// A row of S <= 16 slices is selected by one thread-block cluster of S CTAs (CTA r = slice r)
 // instead of slices plus a merge: every radix pass adds the slices' local histograms through
 // distributed shared memory, so all CTAs see the row's histogram and take the same decisions.
 // Each CTA then counts its keys above the threshold and its ties, the CTAs exchange these counts,
@@ -463,16 +464,20 @@ __global__ void __launch_bounds__(NT) k_topk_cluster(TopkArgs a, int S, int slic
       const int lo8 = nb - kBinsPerLane * (lane + 1);
       if (lo8 >= 0) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {                  // 4 bins at a time: all CTAs' loads in flight
-          uint4 v[kClusterMax];
+        for (int h = 0; h < 2; ++h) {                  // 4 bins at a time, 8 CTAs' loads in flight
 #pragma unroll
-          for (int r = 0; r < kClusterMax; ++r)
-            if (r < S) v[r] = ld_peer4(&hist[lo8 + 4 * h], r);
+          for (int r0 = 0; r0 < kClusterMax; r0 += kPeerBatch) {
+            if (r0 >= S) break;
+            uint4 v[kPeerBatch];
 #pragma unroll
-          for (int r = 0; r < kClusterMax; ++r) {
-            if (r < S) {
-              c[7 - 4 * h] += v[r].x; c[6 - 4 * h] += v[r].y;
-              c[5 - 4 * h] += v[r].z; c[4 - 4 * h] += v[r].w;
+            for (int r = 0; r < kPeerBatch; ++r)
+              if (r0 + r < S) v[r] = ld_peer4(&hist[lo8 + 4 * h], r0 + r);
+#pragma unroll
+            for (int r = 0; r < kPeerBatch; ++r) {
+              if (r0 + r < S) {
+                c[7 - 4 * h] += v[r].x; c[6 - 4 * h] += v[r].y;
+                c[5 - 4 * h] += v[r].z; c[4 - 4 * h] += v[r].w;
+              }
             }
           }
         }
@@ -710,7 +715,7 @@ cudaError_t launch_merge(const TopkArgs& a, int S, int cap, const unsigned long 
   return launch_k(k_topk_merge<NT>, dim3(static_cast<unsigned>(a.q_count)), dim3(NT), smem, s, a, S, cap, cand);
 }
 
-// One cluster of S CTAs per query (S <= 8).  Returns cudaErrorNotSupported, before launching,
+// One cluster of S CTAs per query (S <= 16).  Returns cudaErrorNotSupported, before launching,
 // when the device cannot hold such a cluster.
 template <int NT>
 cudaError_t launch_cluster(const TopkArgs& a, int S, int len, cudaStream_t s) {
@@ -718,6 +723,13 @@ cudaError_t launch_cluster(const TopkArgs& a, int S, int len, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(k_topk_cluster<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
+  if (S > 8) {                       // above the portable size; a device that cannot is not asked
+    e = cudaFuncSetAttribute(k_topk_cluster<NT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      return cudaErrorNotSupported;
+    }
+  }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(a.q_count) * S);
   cfg.blockDim = dim3(NT);
@@ -745,8 +757,8 @@ cudaError_t launch_topk(const TopkArgs& a, void* cand_ws, cudaStream_t s, int* l
   const int len = topk_slice_len(a.q_count, a.N, a.k);
   const int S = topk_slices(a.q_count, a.N, a.k);
   if (S > 1 && CSA_TOPK_CLUSTER && a.N <= kClusterMax * kSlice) {
-    // one-stage selection by a cluster per query (at most 8 slices: rows cut for the two-stage
-    // path into more are re-cut into 8 of at most 32768); falls through to the two stages only
+    // one-stage selection by a cluster per query (at most 16 slices: rows cut for the two-stage
+    // path into more are re-cut into 16 of at most 32768); falls through to the two stages only
     // when the device cannot hold the cluster (the result is the same either way)
     int cl_len = len, cl_S = S;
     if (S > kClusterMax && CSA_TOPK_CLUSTER_LONG) {
